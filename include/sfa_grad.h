@@ -1,0 +1,172 @@
+/*
+ * sfa_grad.h -- C ABI of the GB300 (sm_103a) top-k sparse flash-attention
+ * backward library (libsfa.so), plus the companion forward that produces the
+ * backward's saved inputs.
+ *
+ * Operation (aclnnSparseFlashAttentionGrad doc, section 功能说明 and stages
+ * 阶段1-3): every query token t carries K int32 indices into its KV sequence;
+ * index r selects keys r .. r + sparseBlockSize - 1.  With
+ *   x_j  = scale * ([q || qRope]_t . [k || kRope]_j)            (per head)
+ *   P_j  = exp(x_j - softmaxMax) / softmaxSum                   (masked keys: 0)
+ *   Dsum = rowsum(dOut_t * out_t)                               (FlashSoftmaxGrad)
+ *   dP_j = dOut_t . v_j,     dS_j = P_j (dP_j - Dsum)
+ * the outputs are
+ *   [dQ || dQRope]_t  = scale * sum_j dS_j [k || kRope]_j
+ *   [dK || dKRope]_j += scale * dS_j [q || qRope]_t,     dV_j += P_j dOut_t
+ * summed over every head and every (token, slot) that selects key j.
+ * softmaxMax is the max of the scaled scores x over the selected keys and
+ * softmaxSum = sum_j exp(x_j - softmaxMax) (the MindSpore
+ * flash_attention_bwd.py page, compute_Pij, uses exactly these two saved
+ * statistics).
+ *
+ * Conventions
+ *  - Two phases, as on the documentation page (函数原型): ask for the workspace
+ *    size, allocate it, then call.  The caller owns every buffer; the library
+ *    allocates nothing, keeps no state between calls and is thread-safe.
+ *  - All tensor pointers are DEVICE pointers to contiguous row-major data
+ *    (16-byte aligned).  Shapes use the page's names (参数说明 table):
+ *      BSND: q, dOut, out (B,S1,N1,D); k, v (B,S2,1,D); indices (B,S1,1,K);
+ *            softmaxMax/Sum (B,1,S1,N1); qRope (B,S1,N1,Dr); kRope (B,S2,1,Dr)
+ *      TND:  q, dOut, out (T1,N1,D); k, v (T2,1,D); indices (T1,1,K);
+ *            softmaxMax/Sum (1,T1,N1); actualSeqLengths{Query,Kv} int32 (B,)
+ *            of per-batch lengths summing to T1 / T2.
+ *    Outputs have the shape and dtype of the matching input and are fully
+ *    overwritten (never accumulated into).
+ *  - Calls are asynchronous on `stream`; a SFA_OK return means the work was
+ *    enqueued.  Device-side problems (TND lengths that are negative or do not
+ *    sum to T1/T2, an internal pipeline wait that timed out) are recorded in
+ *    an error word inside the workspace, readable with sfa_read_device_error.
+ *  - Indices need no host inspection: negative, out-of-range and (sparseMode
+ *    3) future positions are masked and contribute nothing; duplicates count
+ *    once per occurrence.
+ *  - With deterministic = 0 the key-side sums use fp32 atomics (order varies
+ *    run to run, as on the page: "默认非确定性实现"); with deterministic = 1
+ *    they are reduced in a fixed order and the outputs are bitwise
+ *    reproducible (约束说明, 确定性计算).
+ */
+#ifndef SFA_GRAD_H_
+#define SFA_GRAD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes: the page's 返回值 table (aclnn status values). */
+typedef enum {
+  SFA_OK = 0,
+  SFA_ERR_NULLPTR = 161001,       /* a required pointer is null */
+  SFA_ERR_PARAM_INVALID = 161002, /* dtype / layout enum out of range, workspace too small */
+  SFA_ERR_RUNTIME = 361001,       /* a CUDA launch or runtime call failed */
+  SFA_ERR_SHAPE = 561002          /* a size or attribute outside the supported range */
+} sfa_status;
+
+typedef enum { SFA_DTYPE_BF16 = 0, SFA_DTYPE_FP16 = 1 } sfa_dtype;
+typedef enum { SFA_LAYOUT_BSND = 0, SFA_LAYOUT_TND = 1 } sfa_layout;
+
+/* Device error word values (sfa_read_device_error). */
+#define SFA_DEVERR_NONE 0
+#define SFA_DEVERR_TIMEOUT 1  /* a kernel abandoned a pipeline wait (no hang) */
+#define SFA_DEVERR_SEQLENS 2  /* TND lengths negative or not summing to T1/T2: every key was masked */
+
+/*
+ * Problem description (replaces the page's aclTensor shape metadata and the
+ * scalar attributes of the first-phase call).
+ *   layout             SFA_LAYOUT_BSND or SFA_LAYOUT_TND ("layout")
+ *   dtype              element type of q, k, v, dOut, out, rope tensors and outputs
+ *   B                  batch count (TND: number of actual-length entries)
+ *   S1, S2             BSND query / kv sequence lengths (ignored for TND)
+ *   T1, T2             TND total query / kv tokens (ignored for BSND)
+ *   N1                 query heads, 1..128 (G = N1 / N2)
+ *   N2                 kv heads; must be 1 (the op is MQA)
+ *   D                  head dim; must be 512
+ *   Dr                 rope dim: 64, or 0 when the rope tensors are absent
+ *   K                  indices per query token (>= 1)
+ *   scale              scaleValue (suggested 1/sqrt(d))
+ *   sparse_block_size  1, 8, 16, 32 or 64 keys per index
+ *   sparse_mode        0 (no mask) or 3 (rightDownCausal)
+ *   deterministic      0 or 1
+ */
+typedef struct sfa_params {
+  int32_t layout;
+  int32_t dtype;
+  int64_t B, S1, S2, T1, T2;
+  int64_t N1, N2, D, Dr, K;
+  double scale;
+  int64_t sparse_block_size;
+  int64_t sparse_mode;
+  int32_t deterministic;
+  int32_t reserved;
+} sfa_params;
+
+/*
+ * Phase 1 (aclnnSparseFlashAttentionGradGetWorkspaceSize): validates *p and
+ * writes the device workspace size in bytes to *bytes.
+ * Errors: SFA_ERR_NULLPTR (p or bytes null), SFA_ERR_PARAM_INVALID (dtype or
+ * layout out of range), SFA_ERR_SHAPE (N2 != 1, D != 512, Dr not in {0,64},
+ * N1 not in 1..128, sparse_mode not in {0,3}, block size not in
+ * {1,8,16,32,64}, K < 1, negative sizes, non-finite scale, sizes overflowing
+ * 32-bit row counts).
+ */
+sfa_status sfa_grad_workspace_size(const sfa_params* p, size_t* bytes);
+
+/*
+ * Phase 2 (aclnnSparseFlashAttentionGrad): computes dq, dk, dv, dq_rope,
+ * dk_rope.  act_seq_q / act_seq_kv are device int32 arrays of length B (TND
+ * only; ignored for BSND).  q_rope, k_rope, dq_rope, dk_rope are required when
+ * Dr = 64 and ignored when Dr = 0.  `workspace` is a device buffer of at
+ * least the phase-1 size, 256-byte aligned, owned by the caller; its contents
+ * need no initialisation and are scratch after the call.  An empty query
+ * (T1 = 0 or S1 = 0, 约束说明: "query为空Tensor：直接返回") returns SFA_OK after
+ * zeroing dk, dv, dk_rope.  Returns SFA_ERR_NULLPTR for a missing required
+ * pointer, SFA_ERR_PARAM_INVALID for a short workspace, SFA_ERR_RUNTIME when
+ * a launch fails, and the phase-1 codes.
+ */
+sfa_status sfa_grad(const sfa_params* p, const void* q, const void* k, const void* v, const int32_t* indices,
+                    const void* d_out, const void* out, const float* softmax_max, const float* softmax_sum,
+                    const int32_t* act_seq_q, const int32_t* act_seq_kv, const void* q_rope, const void* k_rope,
+                    void* dq, void* dk, void* dv, void* dq_rope, void* dk_rope, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/*
+ * Companion forward that produces the backward's saved inputs (the page lists
+ * out, softmaxMax and softmaxSum as inputs of the backward; it does not
+ * specify the forward).  out = sum_j P_j v_j with P and the statistics defined
+ * as above; a row with no valid key gets out = 0, softmaxMax = -inf,
+ * softmaxSum = 0.  Same conventions, shapes and error codes as sfa_grad
+ * (p->deterministic is ignored: the forward is always deterministic).
+ */
+sfa_status sfa_fwd_workspace_size(const sfa_params* p, size_t* bytes);
+sfa_status sfa_fwd(const sfa_params* p, const void* q, const void* k, const void* v, const int32_t* indices,
+                   const int32_t* act_seq_q, const int32_t* act_seq_kv, const void* q_rope, const void* k_rope,
+                   void* out, float* softmax_max, float* softmax_sum, void* workspace, size_t workspace_bytes,
+                   void* stream);
+
+/*
+ * Index decode as the kernels see it (功能说明 gather with block expansion,
+ * Mask table for sparseMode 3): writes, for every query token t and every
+ * expanded slot s < K * sparse_block_size, the global kv row the slot reads
+ * (BSND: b * S2 + key; TND: kv segment start + key) or -1 when the slot is
+ * masked.  rows_out: device int32 (T1, K * sparse_block_size).  Needs the same
+ * workspace as sfa_grad.
+ */
+sfa_status sfa_decode_keys(const sfa_params* p, const int32_t* indices, const int32_t* act_seq_q,
+                           const int32_t* act_seq_kv, int32_t* rows_out, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/*
+ * Synchronises `stream` and copies the workspace error word (SFA_DEVERR_*) to
+ * *code, then clears it.  Returns SFA_ERR_RUNTIME if the copy fails.
+ */
+sfa_status sfa_read_device_error(void* workspace, void* stream, int32_t* code);
+
+/* Static description of a status code. */
+const char* sfa_status_string(int32_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SFA_GRAD_H_ */

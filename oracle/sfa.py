@@ -189,14 +189,19 @@ def _scores(prob: Problem, t: int, rows):
     return prob.scale * x
 
 
-def token_terms(prob: Problem, t: int, d_out, out, smax, ssum):
+def token_terms(prob: Problem, t: int, d_out, out, smax, ssum, keep=None):
     """All intermediate terms of token t over its valid key columns.
 
     d_out, out: (T1, G, Dv) float64; smax, ssum: (T1, G) float64.
+    keep (optional, bool per global kv row) restricts the columns to those rows;
+    every term of a column depends only on that column and the token's row
+    statistics, so a subset is exact.
     Returns dict(rows, x, P, dP, D, dS) where rows are global kv rows.
     """
     j, valid, kv0 = token_keys(prob, t)
     rows = kv0 + j[valid]
+    if keep is not None:
+        rows = rows[keep[rows]]
     x = _scores(prob, t, rows)
     m = smax[t][:, None]
     l = ssum[t][:, None]
@@ -209,18 +214,25 @@ def token_terms(prob: Problem, t: int, d_out, out, smax, ssum):
 
 
 def sfa_fwd(q, k, v, indices, scale, sparse_block_size=1, layout="BSND", sparse_mode=0,
-            act_seq_q=None, act_seq_kv=None, q_rope=None, k_rope=None):
+            act_seq_q=None, act_seq_kv=None, q_rope=None, k_rope=None, token_rows=None):
     """Forward: out, softmaxMax, softmaxSum (float64), shaped like the pages'
     tensors: out like q (last dim = v's), stats (B,1,S1,G) or (1,T1,G).
 
-    Rows with no valid key: out = 0, max = -inf, sum = 0 (reading 6)."""
+    Rows with no valid key: out = 0, max = -inf, sum = 0 (reading 6).
+    token_rows (optional) computes only those query tokens; other rows are NaN."""
     prob = Problem(q, k, v, indices, scale, sparse_block_size, layout, sparse_mode,
                    act_seq_q, act_seq_kv, q_rope, k_rope)
     Dv = prob.v.shape[1]
     out = np.zeros((prob.T1, prob.G, Dv))
     smax = np.full((prob.T1, prob.G), -np.inf)
     ssum = np.zeros((prob.T1, prob.G))
-    for t in range(prob.T1):
+    visit = range(prob.T1)
+    if token_rows is not None:
+        visit = sorted(set(int(x) for x in token_rows))
+        keep = np.zeros(prob.T1, bool)
+        keep[visit] = True
+        out[~keep], smax[~keep], ssum[~keep] = np.nan, np.nan, np.nan
+    for t in visit:
         j, valid, kv0 = token_keys(prob, t)
         rows = kv0 + j[valid]
         if rows.size == 0:
@@ -288,7 +300,7 @@ def sfa_bwd(q, k, v, indices, d_out, out, softmax_max, softmax_sum, scale,
             j, valid, kv0 = token_keys(prob, t)
             if not np.any(want_key[(kv0 + j[valid])]):
                 continue
-        terms = token_terms(prob, t, dO, O, smax, ssum)
+        terms = token_terms(prob, t, dO, O, smax, ssum, keep=None if (full or want_tok[t]) else want_key)
         rows, P, dS = terms["rows"], terms["P"], terms["dS"]
         if want_tok[t]:
             dq[t] = prob.scale * (dS @ prob.k[rows])                  # [SFAG] 阶段3 dQ

@@ -1,0 +1,209 @@
+"""Python binding of libsfa.so (include/sfa_grad.h): argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; this module
+builds the parameter block from tensor shapes, allocates outputs/workspace
+with torch when the caller does not pass them, and calls the C ABI on the
+current CUDA stream.  There is no fallback: if the library is missing or a
+tensor is not on a CUDA device, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsfa.so")
+
+SFA_OK = 0
+SFA_ERR_NULLPTR = 161001
+SFA_ERR_PARAM_INVALID = 161002
+SFA_ERR_RUNTIME = 361001
+SFA_ERR_SHAPE = 561002
+
+LAYOUTS = {"BSND": 0, "TND": 1}
+DTYPES = {torch.bfloat16: 0, torch.float16: 1}
+
+EXPORTS = ("sfa_grad_workspace_size", "sfa_grad", "sfa_fwd_workspace_size", "sfa_fwd", "sfa_decode_keys",
+           "sfa_read_device_error", "sfa_status_string")
+
+
+class SfaParams(ctypes.Structure):
+    _fields_ = [
+        ("layout", ctypes.c_int32), ("dtype", ctypes.c_int32),
+        ("B", ctypes.c_int64), ("S1", ctypes.c_int64), ("S2", ctypes.c_int64),
+        ("T1", ctypes.c_int64), ("T2", ctypes.c_int64),
+        ("N1", ctypes.c_int64), ("N2", ctypes.c_int64), ("D", ctypes.c_int64),
+        ("Dr", ctypes.c_int64), ("K", ctypes.c_int64),
+        ("scale", ctypes.c_double),
+        ("sparse_block_size", ctypes.c_int64), ("sparse_mode", ctypes.c_int64),
+        ("deterministic", ctypes.c_int32), ("reserved", ctypes.c_int32),
+    ]
+
+
+class SfaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} ({code})")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libsfa.so (built in-tree by sfa_grad_gb300.build); raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m sfa_grad_gb300.build`")
+    L = ctypes.CDLL(LIB_PATH)
+    P = ctypes.POINTER(SfaParams)
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    L.sfa_grad_workspace_size.argtypes = [P, ctypes.POINTER(sz)]
+    L.sfa_fwd_workspace_size.argtypes = [P, ctypes.POINTER(sz)]
+    L.sfa_grad.argtypes = [P] + [vp] * 18 + [sz, vp]
+    L.sfa_fwd.argtypes = [P] + [vp] * 12 + [sz, vp]
+    L.sfa_decode_keys.argtypes = [P, vp, vp, vp, vp, vp, sz, vp]
+    L.sfa_read_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
+    L.sfa_status_string.argtypes = [ctypes.c_int32]
+    L.sfa_status_string.restype = ctypes.c_char_p
+    for name in ("sfa_grad_workspace_size", "sfa_fwd_workspace_size", "sfa_grad", "sfa_fwd", "sfa_decode_keys",
+                 "sfa_read_device_error"):
+        getattr(L, name).restype = ctypes.c_int32
+    _lib = L
+    return L
+
+
+def status_string(code: int) -> str:
+    return lib().sfa_status_string(int(code)).decode()
+
+
+def _check(code: int, where: str):
+    if code != SFA_OK:
+        raise SfaError(code, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def make_params(q: torch.Tensor, k: torch.Tensor, indices: torch.Tensor, scale: float, *, layout: str = "BSND",
+                sparse_block_size: int = 1, sparse_mode: int = 0, deterministic: bool = False,
+                has_rope: bool = True, batch: Optional[int] = None) -> SfaParams:
+    p = SfaParams()
+    p.layout = LAYOUTS[layout.upper()]
+    if q.dtype not in DTYPES:
+        raise ValueError("q must be bfloat16 or float16")
+    p.dtype = DTYPES[q.dtype]
+    if p.layout == 0:
+        p.B, p.S1, p.N1, p.D = q.shape
+        p.S2, p.N2 = k.shape[1], k.shape[2]
+        p.T1, p.T2 = p.B * p.S1, p.B * p.S2
+    else:
+        p.T1, p.N1, p.D = q.shape
+        p.T2, p.N2 = k.shape[0], k.shape[1]
+        p.B = int(batch) if batch is not None else 1
+    p.Dr = 64 if has_rope else 0
+    p.K = indices.shape[-1]
+    p.scale = float(scale)
+    p.sparse_block_size = int(sparse_block_size)
+    p.sparse_mode = int(sparse_mode)
+    p.deterministic = 1 if deterministic else 0
+    return p
+
+
+def grad_workspace_size(p: SfaParams) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().sfa_grad_workspace_size(ctypes.byref(p), ctypes.byref(n)), "sfa_grad_workspace_size")
+    return n.value
+
+
+def fwd_workspace_size(p: SfaParams) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().sfa_fwd_workspace_size(ctypes.byref(p), ctypes.byref(n)), "sfa_fwd_workspace_size")
+    return n.value
+
+
+def _stream(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]) -> torch.Tensor:
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError("workspace too small")
+        return workspace
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def grad(q, k, v, indices, d_out, out, softmax_max, softmax_sum, scale, *, q_rope=None, k_rope=None,
+         sparse_block_size=1, layout="BSND", sparse_mode=0, deterministic=False, act_seq_q=None, act_seq_kv=None,
+         outputs=None, workspace=None, stream=None):
+    """sfa_grad on torch CUDA tensors; returns (dq, dk, dv, dq_rope, dk_rope)."""
+    has_rope = q_rope is not None
+    batch = act_seq_q.numel() if act_seq_q is not None else None
+    p = make_params(q, k, indices, scale, layout=layout, sparse_block_size=sparse_block_size,
+                    sparse_mode=sparse_mode, deterministic=deterministic, has_rope=has_rope, batch=batch)
+    if outputs is None:
+        outputs = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v),
+                   torch.empty_like(q_rope) if has_rope else None, torch.empty_like(k_rope) if has_rope else None)
+    dq, dk, dv, dqr, dkr = outputs
+    ws = _workspace(grad_workspace_size(p), q.device, workspace)
+    rc = lib().sfa_grad(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(indices), _ptr(d_out), _ptr(out),
+                        _ptr(softmax_max), _ptr(softmax_sum), _ptr(act_seq_q), _ptr(act_seq_kv), _ptr(q_rope),
+                        _ptr(k_rope), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dqr), _ptr(dkr), _ptr(ws),
+                        ws.numel() * ws.element_size(), _stream(stream))
+    _check(rc, "sfa_grad")
+    return dq, dk, dv, dqr, dkr
+
+
+def fwd(q, k, v, indices, scale, *, q_rope=None, k_rope=None, sparse_block_size=1, layout="BSND", sparse_mode=0,
+        act_seq_q=None, act_seq_kv=None, workspace=None, stream=None):
+    """sfa_fwd on torch CUDA tensors; returns (out, softmax_max, softmax_sum)."""
+    has_rope = q_rope is not None
+    batch = act_seq_q.numel() if act_seq_q is not None else None
+    p = make_params(q, k, indices, scale, layout=layout, sparse_block_size=sparse_block_size,
+                    sparse_mode=sparse_mode, has_rope=has_rope, batch=batch)
+    out = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    if p.layout == 0:
+        st_shape = (p.B, 1, p.S1, p.N1)
+    else:
+        st_shape = (1, p.T1, p.N1)
+    smax = torch.empty(st_shape, dtype=torch.float32, device=q.device)
+    ssum = torch.empty(st_shape, dtype=torch.float32, device=q.device)
+    ws = _workspace(fwd_workspace_size(p), q.device, workspace)
+    rc = lib().sfa_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(indices), _ptr(act_seq_q),
+                       _ptr(act_seq_kv), _ptr(q_rope), _ptr(k_rope), _ptr(out), _ptr(smax), _ptr(ssum), _ptr(ws),
+                       ws.numel() * ws.element_size(), _stream(stream))
+    _check(rc, "sfa_fwd")
+    return out, smax, ssum
+
+
+def decode_keys(q, k, indices, *, sparse_block_size=1, layout="BSND", sparse_mode=0, act_seq_q=None,
+                act_seq_kv=None, has_rope=True, workspace=None, stream=None):
+    """sfa_decode_keys: the global kv row (or -1) of every expanded slot, int32 (T1, K*bs)."""
+    batch = act_seq_q.numel() if act_seq_q is not None else None
+    p = make_params(q, k, indices, 1.0, layout=layout, sparse_block_size=sparse_block_size,
+                    sparse_mode=sparse_mode, has_rope=has_rope, batch=batch)
+    rows = torch.empty((p.T1, p.K * p.sparse_block_size), dtype=torch.int32, device=q.device)
+    ws = _workspace(grad_workspace_size(p), q.device, workspace)
+    rc = lib().sfa_decode_keys(ctypes.byref(p), _ptr(indices), _ptr(act_seq_q), _ptr(act_seq_kv), _ptr(rows),
+                               _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    _check(rc, "sfa_decode_keys")
+    return rows, ws
+
+
+def read_device_error(workspace: torch.Tensor, stream=None) -> int:
+    code = ctypes.c_int32(0)
+    _check(lib().sfa_read_device_error(_ptr(workspace), _stream(stream), ctypes.byref(code)), "sfa_read_device_error")
+    return code.value

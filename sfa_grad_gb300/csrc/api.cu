@@ -1,0 +1,342 @@
+// C-ABI entry points (include/sfa_grad.h): validation, workspace plan and the
+// launch sequence of the backward and the companion forward.
+//
+// aclnnSparseFlashAttentionGrad doc: 函数原型 (two-phase call), 参数说明
+// (shapes, dtypes), 返回值 (status codes), 约束说明 (empty query, determinism),
+// 规格约束 (supported ranges).
+#include <cmath>
+#include <cstring>
+
+#include "../../include/sfa_grad.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace sfa {
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr size_t kPdsCap = size_t(8) << 30;    // P + dS staging per token chunk
+constexpr size_t kPartCap = size_t(8) << 30;   // deterministic partial rows per chunk
+constexpr int kAccRow = 1088;
+constexpr int kDetMaxKeff = 16384;             // per-token sort runs in shared memory
+
+size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Plan {
+  int layout, B, S1, S2, T1, T2, G, Gp, Kidx, bs, Keff, Kpad, mode, has_rope, det, is_f16;
+  float scale;
+  int chunk;
+  size_t off_err, off_batch, off_meta, off_dsum, off_acc, off_P, off_dS, off_part, off_skey, off_sslot, off_tstats;
+  size_t total;
+};
+
+sfa_status validate(const sfa_params* p, bool fwd, Plan* out) {
+  if (!p) return SFA_ERR_NULLPTR;
+  if (p->dtype != SFA_DTYPE_BF16 && p->dtype != SFA_DTYPE_FP16) return SFA_ERR_PARAM_INVALID;
+  if (p->layout != SFA_LAYOUT_BSND && p->layout != SFA_LAYOUT_TND) return SFA_ERR_PARAM_INVALID;
+  if (p->N2 != 1 || p->D != 512 || (p->Dr != 64 && p->Dr != 0)) return SFA_ERR_SHAPE;
+  if (p->N1 < 1 || p->N1 > 128) return SFA_ERR_SHAPE;
+  if (p->sparse_mode != 0 && p->sparse_mode != 3) return SFA_ERR_SHAPE;
+  const int64_t bs = p->sparse_block_size;
+  if (bs != 1 && bs != 8 && bs != 16 && bs != 32 && bs != 64) return SFA_ERR_SHAPE;
+  if (p->K < 1 || p->K > (1 << 20)) return SFA_ERR_SHAPE;
+  if (!std::isfinite(p->scale)) return SFA_ERR_SHAPE;
+  if (p->deterministic != 0 && p->deterministic != 1) return SFA_ERR_PARAM_INVALID;
+  if (p->B < 1) return SFA_ERR_SHAPE;
+  int64_t T1, T2;
+  if (p->layout == SFA_LAYOUT_BSND) {
+    if (p->S1 < 0 || p->S2 < 0) return SFA_ERR_SHAPE;
+    T1 = p->B * p->S1;
+    T2 = p->B * p->S2;
+  } else {
+    if (p->T1 < 0 || p->T2 < 0) return SFA_ERR_SHAPE;
+    T1 = p->T1;
+    T2 = p->T2;
+  }
+  const int64_t keff = p->K * bs;
+  if (keff > (1 << 24) || T1 > INT32_MAX / 2 || T2 > INT32_MAX / 2 || T1 * p->N1 > INT32_MAX / 2)
+    return SFA_ERR_SHAPE;
+  if (!fwd && p->deterministic && keff > kDetMaxKeff) return SFA_ERR_SHAPE;
+  Plan& P = *out;
+  std::memset(&P, 0, sizeof(P));
+  P.layout = (int)p->layout;
+  P.B = (int)p->B;
+  P.S1 = (int)p->S1;
+  P.S2 = (int)p->S2;
+  P.T1 = (int)T1;
+  P.T2 = (int)T2;
+  P.G = (int)p->N1;
+  P.Gp = P.G <= 64 ? 64 : 128;
+  P.Kidx = (int)p->K;
+  P.bs = (int)bs;
+  P.Keff = (int)keff;
+  P.Kpad = (int)((keff + 127) / 128 * 128);
+  P.mode = (int)p->sparse_mode;
+  P.has_rope = p->Dr == 64;
+  P.det = fwd ? 0 : p->deterministic;
+  P.is_f16 = p->dtype == SFA_DTYPE_FP16;
+  P.scale = (float)p->scale;
+  // token chunking keeps the per-chunk staging bounded
+  const size_t pds_per_tok = (size_t)P.Kpad * P.Gp * 2 * (fwd ? 1 : 2);
+  size_t chunk = kPdsCap / pds_per_tok;
+  if (P.det) {
+    const size_t part_per_tok = (size_t)P.Kpad * kAccRow * 4;
+    const size_t c2 = kPartCap / part_per_tok;
+    if (c2 < chunk) chunk = c2;
+  }
+  if (chunk < 1) chunk = 1;
+  if (chunk > (size_t)P.T1) chunk = P.T1 > 0 ? P.T1 : 1;
+  P.chunk = (int)chunk;
+  size_t o = 0;
+  P.off_err = o; o += up(16);
+  P.off_batch = o; o += up((size_t)(2 * P.B + 2) * 4);
+  P.off_meta = o; o += up((size_t)P.T1 * sizeof(TokMeta));
+  P.off_dsum = o; o += fwd ? 0 : up((size_t)P.T1 * P.G * 4);
+  P.off_acc = o; o += fwd ? 0 : up((size_t)P.T2 * kAccRow * 4);
+  P.off_P = o; o += up(chunk * P.Kpad * P.Gp * 2);
+  P.off_dS = o; o += fwd ? 0 : up(chunk * P.Kpad * P.Gp * 2);
+  P.off_part = o; o += P.det ? up(chunk * P.Kpad * kAccRow * 4) : 0;
+  P.off_skey = o; o += P.det ? up(chunk * P.Kpad * 4) : 0;
+  P.off_sslot = o; o += P.det ? up(chunk * P.Kpad * 4) : 0;
+  P.off_tstats = o; o += fwd ? up(chunk * (P.Kpad / 128) * P.G * 2 * 4) : 0;
+  P.total = o;
+  return SFA_OK;
+}
+
+Prob make_prob(const Plan& P, uint8_t* ws) {
+  Prob pr;
+  std::memset(&pr, 0, sizeof(pr));
+  pr.T1 = P.T1;
+  pr.T2 = P.T2;
+  pr.G = P.G;
+  pr.Gp = P.Gp;
+  pr.Kidx = P.Kidx;
+  pr.bs = P.bs;
+  pr.Keff = P.Keff;
+  pr.Kpad = P.Kpad;
+  pr.has_rope = P.has_rope;
+  pr.scale = P.scale;
+  pr.meta = reinterpret_cast<const TokMeta*>(ws + P.off_meta);
+  return pr;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  return n;
+}
+
+#define SFA_CK(x)                                   \
+  do {                                              \
+    if ((x) != cudaSuccess) {                       \
+      (void)cudaGetLastError();                     \
+      return SFA_ERR_RUNTIME;                       \
+    }                                               \
+  } while (0)
+
+__global__ void decode_kernel(Prob p, int* rows_out) {
+  const long long n = (long long)p.T1 * p.Keff;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(i / p.Keff), s = (int)(i - (long long)t * p.Keff);
+    rows_out[i] = slot_row(p, p.meta[t], t, s);
+  }
+}
+
+template <typename T>
+sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const void* k, const void* v,
+                    const int32_t* idx, const void* dO, const void* out, const float* smax, const float* ssum,
+                    const int32_t* aq, const int32_t* akv, const void* qr, const void* kr, void* dq, void* dk, void* dv,
+                    void* dqr, void* dkr, uint8_t* ws, cudaStream_t st) {
+  int* gerr = reinterpret_cast<int*>(ws + P.off_err);
+  Prob pr = make_prob(P, ws);
+  pr.q = q; pr.k = k; pr.v = v; pr.dO = dO; pr.out = out; pr.idx = idx;
+  pr.qr = P.has_rope ? qr : nullptr;
+  pr.kr = P.has_rope ? kr : nullptr;
+  pr.smax = smax; pr.ssum = ssum;
+  pr.dsum = reinterpret_cast<const float*>(ws + P.off_dsum);
+  const int nsm = sm_count();
+  SFA_CK(cudaMemsetAsync(gerr, 0, 16, st));
+  SFA_CK(cudaMemsetAsync(ws + P.off_acc, 0, (size_t)P.T2 * kAccRow * 4, st));
+  SFA_CK(launch_meta(pr, P.layout, P.B, P.S1, P.S2, P.mode, aq, akv, reinterpret_cast<int*>(ws + P.off_batch),
+                     reinterpret_cast<TokMeta*>(ws + P.off_meta), gerr, st));
+  SFA_CK(launch_dsum<T>(pr, reinterpret_cast<float*>(ws + P.off_dsum), st));
+  float* acc = reinterpret_cast<float*>(ws + P.off_acc);
+  for (int t0 = 0; t0 < P.T1; t0 += P.chunk) {
+    pr.tok0 = t0;
+    pr.ntok = (P.T1 - t0) < P.chunk ? (P.T1 - t0) : P.chunk;
+    void* Pst = ws + P.off_P;
+    void* dSst = ws + P.off_dS;
+    SFA_CK(launch_sdp<T>(pr, kModeBwd, Pst, dSst, nullptr, gerr, nsm, st));
+    if (P.det) {
+      int* skey = reinterpret_cast<int*>(ws + P.off_skey);
+      int* sslot = reinterpret_cast<int*>(ws + P.off_sslot);
+      float* part = reinterpret_cast<float*>(ws + P.off_part);
+      SFA_CK(launch_sort_keys(pr, skey, sslot, st));
+      SFA_CK(launch_dkv<T>(pr, Pst, dSst, acc, part, gerr, nsm, st));
+      SFA_CK(launch_det_reduce(pr, skey, sslot, part, acc, st));
+    } else {
+      SFA_CK(launch_dkv<T>(pr, Pst, dSst, acc, nullptr, gerr, nsm, st));
+    }
+    SFA_CK(launch_dq<T>(pr, 0, dSst, dq, P.has_rope ? dqr : nullptr, gerr, nsm, st));
+  }
+  SFA_CK(launch_cast<T>(acc, P.T2, dk, P.has_rope ? dkr : nullptr, dv, P.has_rope, st));
+  (void)prm;
+  return SFA_OK;
+}
+
+template <typename T>
+sfa_status run_fwd(const Plan& P, const void* q, const void* k, const void* v, const int32_t* idx, const int32_t* aq,
+                   const int32_t* akv, const void* qr, const void* kr, void* out, float* smax, float* ssum, uint8_t* ws,
+                   cudaStream_t st) {
+  int* gerr = reinterpret_cast<int*>(ws + P.off_err);
+  Prob pr = make_prob(P, ws);
+  pr.q = q; pr.k = k; pr.v = v; pr.idx = idx;
+  pr.qr = P.has_rope ? qr : nullptr;
+  pr.kr = P.has_rope ? kr : nullptr;
+  pr.smax = smax; pr.ssum = ssum;
+  const int nsm = sm_count();
+  SFA_CK(cudaMemsetAsync(gerr, 0, 16, st));
+  SFA_CK(launch_meta(pr, P.layout, P.B, P.S1, P.S2, P.mode, aq, akv, reinterpret_cast<int*>(ws + P.off_batch),
+                     reinterpret_cast<TokMeta*>(ws + P.off_meta), gerr, st));
+  float* ts = reinterpret_cast<float*>(ws + P.off_tstats);
+  for (int t0 = 0; t0 < P.T1; t0 += P.chunk) {
+    pr.tok0 = t0;
+    pr.ntok = (P.T1 - t0) < P.chunk ? (P.T1 - t0) : P.chunk;
+    SFA_CK(launch_sdp<T>(pr, kModeFwdStats, nullptr, nullptr, ts, gerr, nsm, st));
+    SFA_CK(launch_stats_combine(pr, ts, smax, ssum, st));
+    SFA_CK(launch_sdp<T>(pr, kModeFwdP, ws + P.off_P, nullptr, nullptr, gerr, nsm, st));
+    SFA_CK(launch_dq<T>(pr, 1, ws + P.off_P, out, nullptr, gerr, nsm, st));
+  }
+  return SFA_OK;
+}
+
+}  // namespace
+}  // namespace sfa
+
+using sfa::Plan;
+
+extern "C" {
+
+sfa_status sfa_grad_workspace_size(const sfa_params* p, size_t* bytes) {
+  if (!p || !bytes) return SFA_ERR_NULLPTR;
+  Plan P;
+  sfa_status s = sfa::validate(p, false, &P);
+  if (s != SFA_OK) return s;
+  *bytes = P.total;
+  return SFA_OK;
+}
+
+sfa_status sfa_fwd_workspace_size(const sfa_params* p, size_t* bytes) {
+  if (!p || !bytes) return SFA_ERR_NULLPTR;
+  Plan P;
+  sfa_status s = sfa::validate(p, true, &P);
+  if (s != SFA_OK) return s;
+  *bytes = P.total;
+  return SFA_OK;
+}
+
+sfa_status sfa_grad(const sfa_params* p, const void* q, const void* k, const void* v, const int32_t* indices,
+                    const void* d_out, const void* out, const float* softmax_max, const float* softmax_sum,
+                    const int32_t* act_seq_q, const int32_t* act_seq_kv, const void* q_rope, const void* k_rope,
+                    void* dq, void* dk, void* dv, void* dq_rope, void* dk_rope, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  if (!p) return SFA_ERR_NULLPTR;
+  Plan P;
+  sfa_status s = sfa::validate(p, false, &P);
+  if (s != SFA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool rope = P.has_rope;
+  if (!dk || !dv || (rope && !dk_rope)) return SFA_ERR_NULLPTR;
+  if (P.T1 == 0) {  // empty query: nothing selects any key
+    if (P.T2 > 0) {
+      const size_t esz = 2;
+      SFA_CK(cudaMemsetAsync(dk, 0, (size_t)P.T2 * 512 * esz, st));
+      SFA_CK(cudaMemsetAsync(dv, 0, (size_t)P.T2 * 512 * esz, st));
+      if (rope) SFA_CK(cudaMemsetAsync(dk_rope, 0, (size_t)P.T2 * 64 * esz, st));
+    }
+    return SFA_OK;
+  }
+  if (!q || !k || !v || !indices || !d_out || !out || !softmax_max || !softmax_sum || !dq || !workspace)
+    return SFA_ERR_NULLPTR;
+  if (rope && (!q_rope || !k_rope || !dq_rope)) return SFA_ERR_NULLPTR;
+  if (P.layout == SFA_LAYOUT_TND && (!act_seq_q || !act_seq_kv)) return SFA_ERR_NULLPTR;
+  if (workspace_bytes < P.total) return SFA_ERR_PARAM_INVALID;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (P.is_f16)
+    return sfa::run_grad<__half>(P, p, q, k, v, indices, d_out, out, softmax_max, softmax_sum, act_seq_q, act_seq_kv,
+                                 q_rope, k_rope, dq, dk, dv, dq_rope, dk_rope, ws, st);
+  return sfa::run_grad<__nv_bfloat16>(P, p, q, k, v, indices, d_out, out, softmax_max, softmax_sum, act_seq_q,
+                                      act_seq_kv, q_rope, k_rope, dq, dk, dv, dq_rope, dk_rope, ws, st);
+}
+
+sfa_status sfa_fwd(const sfa_params* p, const void* q, const void* k, const void* v, const int32_t* indices,
+                   const int32_t* act_seq_q, const int32_t* act_seq_kv, const void* q_rope, const void* k_rope,
+                   void* out, float* softmax_max, float* softmax_sum, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+  if (!p) return SFA_ERR_NULLPTR;
+  Plan P;
+  sfa_status s = sfa::validate(p, true, &P);
+  if (s != SFA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (P.T1 == 0) return SFA_OK;
+  if (!q || !k || !v || !indices || !out || !softmax_max || !softmax_sum || !workspace) return SFA_ERR_NULLPTR;
+  if (P.has_rope && (!q_rope || !k_rope)) return SFA_ERR_NULLPTR;
+  if (P.layout == SFA_LAYOUT_TND && (!act_seq_q || !act_seq_kv)) return SFA_ERR_NULLPTR;
+  if (workspace_bytes < P.total) return SFA_ERR_PARAM_INVALID;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (P.is_f16)
+    return sfa::run_fwd<__half>(P, q, k, v, indices, act_seq_q, act_seq_kv, q_rope, k_rope, out, softmax_max,
+                                softmax_sum, ws, st);
+  return sfa::run_fwd<__nv_bfloat16>(P, q, k, v, indices, act_seq_q, act_seq_kv, q_rope, k_rope, out, softmax_max,
+                                     softmax_sum, ws, st);
+}
+
+sfa_status sfa_decode_keys(const sfa_params* p, const int32_t* indices, const int32_t* act_seq_q,
+                           const int32_t* act_seq_kv, int32_t* rows_out, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  if (!p) return SFA_ERR_NULLPTR;
+  Plan P;
+  sfa_status s = sfa::validate(p, false, &P);
+  if (s != SFA_OK) return s;
+  if (P.T1 == 0) return SFA_OK;
+  if (!indices || !rows_out || !workspace) return SFA_ERR_NULLPTR;
+  if (P.layout == SFA_LAYOUT_TND && (!act_seq_q || !act_seq_kv)) return SFA_ERR_NULLPTR;
+  if (workspace_bytes < P.total) return SFA_ERR_PARAM_INVALID;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* gerr = reinterpret_cast<int*>(ws + P.off_err);
+  sfa::Prob pr = sfa::make_prob(P, ws);
+  pr.idx = indices;
+  SFA_CK(cudaMemsetAsync(gerr, 0, 16, st));
+  SFA_CK(sfa::launch_meta(pr, P.layout, P.B, P.S1, P.S2, P.mode, act_seq_q, act_seq_kv,
+                          reinterpret_cast<int*>(ws + P.off_batch), reinterpret_cast<sfa::TokMeta*>(ws + P.off_meta),
+                          gerr, st));
+  sfa::decode_kernel<<<1024, 256, 0, st>>>(pr, rows_out);
+  SFA_CK(cudaGetLastError());
+  return SFA_OK;
+}
+
+sfa_status sfa_read_device_error(void* workspace, void* stream, int32_t* code) {
+  if (!workspace || !code) return SFA_ERR_NULLPTR;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  SFA_CK(cudaMemcpyAsync(&v, workspace, 4, cudaMemcpyDeviceToHost, st));
+  SFA_CK(cudaStreamSynchronize(st));
+  SFA_CK(cudaMemsetAsync(workspace, 0, 4, st));
+  *code = v;
+  return SFA_OK;
+}
+
+const char* sfa_status_string(int32_t s) {
+  switch (s) {
+    case SFA_OK: return "SFA_OK";
+    case SFA_ERR_NULLPTR: return "SFA_ERR_NULLPTR: a required pointer is null";
+    case SFA_ERR_PARAM_INVALID: return "SFA_ERR_PARAM_INVALID: dtype/layout out of range or workspace too small";
+    case SFA_ERR_RUNTIME: return "SFA_ERR_RUNTIME: a CUDA call failed";
+    case SFA_ERR_SHAPE: return "SFA_ERR_SHAPE: size or attribute outside the supported range";
+    default: return "unknown sfa status";
+  }
+}
+
+}  // extern "C"

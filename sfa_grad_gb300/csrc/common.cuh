@@ -1,0 +1,223 @@
+// Shared device helpers for the sm_103a kernels of the sparse flash-attention
+// backward: mbarrier waits with a spin limit, tcgen05 (TMEM allocation, MMA,
+// commit, TMEM loads), cp.async with zero fill, and the 128-byte-swizzled
+// shared-memory operand layouts the tensor-core descriptors describe.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+namespace sfa {
+
+// ------------------------------------------------------------------ limits
+// Every mbarrier wait gives up after this many polls; the kernel then records
+// an error code and returns instead of hanging.
+constexpr uint32_t kSpinLimit = 1u << 25;
+
+// Kernels that allocate all 512 TMEM columns request at least this much
+// dynamic shared memory so that no two of their CTAs share an SM.
+constexpr int kOneCtaSmem = 120 * 1024;
+
+// Device error codes written to the workspace error word.
+constexpr int kErrTimeout = 1;       // a pipeline wait ran out
+constexpr int kErrSeqLens = 2;       // TND lengths negative or not summing to T1/T2
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ------------------------------------------------------------------ mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on phase `parity`.  `abort` is a shared flag any warp may raise;
+// `gerr` is the global error word.  Returns false when the wait was abandoned.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* gerr) {
+  const uint32_t a = smem_u32(bar);
+  for (uint32_t it = 0; it < kSpinLimit; ++it) {
+    if (mbar_test(a, parity)) return true;
+    if ((it & 255u) == 255u && *abort) return false;
+  }
+  *abort = 1;
+  atomicExch(gerr, kErrTimeout);
+  return false;
+}
+
+// ------------------------------------------------------------------ cp.async
+// 16-byte global -> shared copy; src_bytes = 0 fills the destination with zeros
+// without reading the source.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+// Makes this thread's completed generic-proxy shared writes visible to the
+// tensor core (async proxy).
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// ------------------------------------------------------------------ operand layouts
+// All tensor-core operands live in shared memory as 128-byte swizzled rows:
+// a "panel" holds R rows of 64 consecutive 16-bit elements (128 B per row),
+// rows contiguous, 8-row atoms of 1024 B, and the 16-byte chunk c of row r is
+// stored at chunk position c ^ (r & 7).  A K-major operand (K contiguous) with
+// K > 64 is a sequence of panels along K; an MN-major operand (M or N
+// contiguous) is a sequence of panels along MN whose rows are indexed by K.
+__host__ __device__ __forceinline__ uint32_t swz_chunk(uint32_t row, uint32_t chunk16) {
+  return row * 128u + (((chunk16 ^ (row & 7u)) & 7u) << 4);
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): start address, leading and
+// stride byte offsets (16-byte units), descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  d |= 2ull << 61;
+  return d;
+}
+// K-major panel of R rows starting at `panel`: K step ks (16 elements) inside
+// the 64-wide panel advances the start by 32 B.
+__device__ __forceinline__ uint64_t sdesc_kmajor(uint32_t panel, int ks) {
+  return sdesc(panel + (uint32_t)ks * 32u, 16u, 1024u);
+}
+// MN-major operand made of panels of `krows` K-rows each (panel stride
+// krows*128 B): K step ks (16 rows) advances the start by 2048 B.
+__device__ __forceinline__ uint64_t sdesc_mnmajor(uint32_t base, int ks, uint32_t krows) {
+  return sdesc(base + (uint32_t)ks * 2048u, krows * 128u, 1024u);
+}
+
+// Instruction descriptor for kind::f16 with fp32 accumulation.
+// is_f16: operands are fp16 (else bf16); a_mn / b_mn: operand is MN-major.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool is_f16, bool a_mn, bool b_mn) {
+  return (1u << 4) | ((is_f16 ? 0u : 1u) << 7) | ((is_f16 ? 0u : 1u) << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ------------------------------------------------------------------ tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D(tmem) (+)= A(smem desc) * B(smem desc)
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrives on `bar` once every MMA issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// 32 lanes x 32 consecutive fp32 columns: thread i of the warp gets lane
+// (warp quadrant base + i), columns [col, col+32).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ------------------------------------------------------------------ element types
+template <typename T>
+struct Elt;
+template <>
+struct Elt<__nv_bfloat16> {
+  static constexpr bool is_f16 = false;
+  __device__ static __forceinline__ uint32_t pack(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __device__ static __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+  __device__ static __forceinline__ __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
+};
+template <>
+struct Elt<__half> {
+  static constexpr bool is_f16 = true;
+  __device__ static __forceinline__ uint32_t pack(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __device__ static __forceinline__ float to_f(__half x) { return __half2float(x); }
+  __device__ static __forceinline__ __half from_f(float x) { return __float2half_rn(x); }
+};
+
+// ------------------------------------------------------------------ problem view
+// Per-token metadata built by the prep kernel: start row of the token's KV
+// segment, and the largest key position the token may attend (-1: none).
+struct TokMeta {
+  int kv_start;
+  int limit;
+};
+
+// Everything a kernel needs about one call (device pointers, sizes).
+struct Prob {
+  const void* q;    // (T1, G, 512)
+  const void* qr;   // (T1, G, 64) or null
+  const void* k;    // (T2, 512)
+  const void* kr;   // (T2, 64) or null
+  const void* v;    // (T2, 512)
+  const void* dO;   // (T1, G, 512)
+  const void* out;  // (T1, G, 512)
+  const int* idx;   // (T1, Kidx)
+  const float* smax;  // (T1, G)
+  const float* ssum;  // (T1, G)
+  const TokMeta* meta;  // (T1)
+  const float* dsum;    // (T1, G)
+  int T1, T2, G, Gp, Kidx, bs, Keff, Kpad;
+  int has_rope;
+  float scale;
+  int tok0, ntok;  // token chunk processed by this launch
+};
+
+// Expanded key position of slot s of token t (64-bit: index + block offset
+// cannot overflow) and whether it is attendable.
+__device__ __forceinline__ int slot_row(const Prob& p, const TokMeta& m, int t, int s) {
+  if (s >= p.Keff) return -1;
+  const int r = __ldg(p.idx + (size_t)t * p.Kidx + s / p.bs);
+  const long long j = (long long)r + (s % p.bs);
+  if (j < 0 || j > (long long)m.limit) return -1;
+  return m.kv_start + (int)j;
+}
+
+}  // namespace sfa

@@ -1,0 +1,42 @@
+// Internal launcher declarations shared by the C-ABI host code and the kernels.
+#pragma once
+#include "common.cuh"
+
+namespace sfa {
+
+constexpr int kModeBwd = 0;       // S and dP -> P, dS
+constexpr int kModeFwdStats = 1;  // S -> per-tile max / sum partials
+constexpr int kModeFwdP = 2;      // S -> P from final statistics
+
+// Score / softmax-gradient kernel (sdp.cu).
+template <typename T>
+cudaError_t launch_sdp(const Prob& p, int mode, void* out_p, void* out_ds, float* tile_stats, int* gerr, int nsm,
+                       cudaStream_t st);
+
+// Key-side gradients (dkv.cu): dV = P^T dO, [dK || dKRope] = dS^T [q || qRope],
+// reduced into the fp32 accumulator acc (T2 x 1088) with atomics, or written
+// as per-(token, slot) partial rows when `partials` is non-null.
+template <typename T>
+cudaError_t launch_dkv(const Prob& p, const void* P, const void* dS, float* acc, float* partials, int* gerr, int nsm,
+                       cudaStream_t st);
+
+// Query-side contraction (dq.cu): dQ = dS K (mode 0) or O = P V (mode 1).
+template <typename T>
+cudaError_t launch_dq(const Prob& p, int mode, const void* A, void* out_main, void* out_rope, int* gerr, int nsm,
+                      cudaStream_t st);
+
+// Small kernels (prep.cu).
+cudaError_t launch_meta(const Prob& p, int layout, int B, int S1, int S2, int mode, const int* act_q, const int* act_kv,
+                        int* batch_ofs, TokMeta* meta, int* gerr, cudaStream_t st);
+template <typename T>
+cudaError_t launch_dsum(const Prob& p, float* dsum, cudaStream_t st);
+template <typename T>
+cudaError_t launch_cast(const float* acc, int T2, void* dk, void* dkr, void* dv, int has_rope, cudaStream_t st);
+cudaError_t launch_stats_combine(const Prob& p, const float* tile_stats, float* smax, float* ssum, cudaStream_t st);
+
+// Deterministic key-side reduction (det.cu).
+cudaError_t launch_sort_keys(const Prob& p, int* sorted_key, int* sorted_slot, cudaStream_t st);
+cudaError_t launch_det_reduce(const Prob& p, const int* sorted_key, const int* sorted_slot, const float* partials,
+                              float* acc, cudaStream_t st);
+
+}  // namespace sfa

@@ -1,0 +1,199 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle on the
+same seeded bytes.  Index decode is compared bit for bit; float outputs with
+the relative-Frobenius / max-abs tolerances of parity_util."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sfa_grad_gb300 as sfa
+from parity_util import OUT_NAMES, compare, gpu_call_kwargs, oracle_kwargs, oracle_saved, to_cuda
+from workloads import WORKLOADS, make_inputs, small_workload, with_
+
+pytestmark = pytest.mark.gpu
+
+# Small cases that span several key tiles and a ragged tail.
+SMALL = {
+    "tiny": WORKLOADS["tiny"],
+    "g16_ragged": small_workload(N1=16, S1=8, S2=512, K=300, seed=11),
+    "g128_causal": small_workload(N1=128, S1=4, S2=1024, K=640, mode=3, seed=12),
+    "g64_tnd": small_workload(name="tnd_small", layout="TND", B=3, N1=64, K=200, mode=3, index_kind="causal",
+                              kv_extra=150, T1=8, act_q=(3, 0, 5), seed=13),
+    "g16_block_fp16": small_workload(N1=16, S1=6, S2=1024, K=40, block_size=8, index_kind="block",
+                                     dtype="fp16", std=0.5, seed=14),
+    "g32_padding_dups": small_workload(N1=32, S1=5, S2=300, K=160, index_kind="random_any", seed=15),
+    "g64_norope": small_workload(N1=64, S1=4, S2=700, K=256, Dr=0, seed=16),
+    "g128_fp16": small_workload(N1=128, S1=3, S2=600, K=384, dtype="fp16", seed=17),
+    "g4_bs64": small_workload(N1=4, S1=4, S2=4096, K=5, block_size=64, index_kind="block", seed=18),
+}
+
+
+def _run(w, det, inp=None, saved=None):
+    inp = inp or make_inputs(w)
+    out, smax, ssum = saved or oracle_saved(w, inp)
+    dev = {k: to_cuda(v) for k, v in inp.items()}
+    g = sfa.grad(dev["q"], dev["k"], dev["v"], dev["indices"], dev["d_out"], out.cuda(), smax.cuda(), ssum.cuda(),
+                 w.scale_value, deterministic=det, **gpu_call_kwargs(w, dev))
+    torch.cuda.synchronize()
+    return inp, (out, smax, ssum), g
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("det", [False, True])
+def test_grad_small(name, det):
+    w = SMALL[name]
+    inp, (out, smax, ssum), g = _run(w, det)
+    ref = oracle.sfa_bwd(d_out=inp["d_out"], out=out, softmax_max=smax, softmax_sum=ssum, **oracle_kwargs(w, inp))
+    for n, x in zip(OUT_NAMES, g):
+        if ref[n] is None:
+            assert x is None
+            continue
+        compare(f"{name}/{n}", x, ref[n], w.dtype)
+
+
+@pytest.mark.parametrize("name", ["tiny", "g16_ragged", "g64_tnd", "g16_block_fp16", "g32_padding_dups"])
+def test_decode_bit_exact(name):
+    w = SMALL[name]
+    inp = make_inputs(w)
+    dev = {k: to_cuda(v) for k, v in inp.items()}
+    kw = gpu_call_kwargs(w, dev)
+    rows, _ = sfa.decode_keys(dev["q"], dev["k"], dev["indices"], sparse_block_size=w.block_size, layout=w.layout,
+                              sparse_mode=w.mode, act_seq_q=kw.get("act_seq_q"), act_seq_kv=kw.get("act_seq_kv"),
+                              has_rope=dev.get("q_rope") is not None)
+    got = rows.cpu().numpy()
+    prob = oracle.make_problem(**{k: v for k, v in oracle_kwargs(w, inp).items() if k not in ("sparse_block_size", "layout", "sparse_mode")},
+                               block_size=w.block_size, layout=w.layout, mode=w.mode)
+    exp = np.full_like(got, -1)
+    for t in range(prob.T1):
+        j, valid, kv0 = oracle.token_keys(prob, t)
+        exp[t, valid] = kv0 + j[valid]
+    assert np.array_equal(got, exp)
+
+
+@pytest.mark.parametrize("name", ["tiny", "g128_causal", "g64_tnd", "g16_block_fp16", "g64_norope"])
+def test_fwd_small(name):
+    w = SMALL[name]
+    inp = make_inputs(w)
+    dev = {k: to_cuda(v) for k, v in inp.items()}
+    kw = gpu_call_kwargs(w, dev)
+    out, smax, ssum = sfa.fwd(dev["q"], dev["k"], dev["v"], dev["indices"], w.scale_value, **kw)
+    torch.cuda.synchronize()
+    ro, rm, rl = oracle.sfa_fwd(**oracle_kwargs(w, inp))
+    compare(f"{name}/out", out, ro, w.dtype)
+    m = smax.cpu().double().numpy()
+    fin = np.isfinite(rm)
+    assert np.array_equal(np.isfinite(m), fin)
+    np.testing.assert_allclose(m[fin], rm[fin], rtol=1e-4, atol=1e-4)
+    np.testing.assert_allclose(ssum.cpu().double().numpy(), rl, rtol=2e-4, atol=1e-6)
+
+
+def test_deterministic_bitwise():
+    w = SMALL["g128_causal"]
+    inp, saved, g1 = _run(w, True)
+    _, _, g2 = _run(w, True, inp, saved)
+    for a, b in zip(g1, g2):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_doc_example_closed_form_on_gpu():
+    """The documentation page's example (fp16 0x0001 everywhere, constant stats 3.0):
+    dS is exactly zero, so dQ, dK and the rope gradients are zero; dV is 16 *
+    exp(x - 3) / 3 * 2^-24 per element, below half the smallest fp16 subnormal,
+    so it rounds to zero as well."""
+    T1, N1, T2, K = 1, 16, 2048, 2048
+    c = torch.tensor([1], dtype=torch.int16).view(torch.float16)
+    q = c.repeat(T1 * N1 * 512).reshape(T1, N1, 512).cuda()
+    k = c.repeat(T2 * 512).reshape(T2, 1, 512).cuda()
+    qr = c.repeat(T1 * N1 * 64).reshape(T1, N1, 64).cuda()
+    kr = c.repeat(T2 * 64).reshape(T2, 1, 64).cuda()
+    idx = torch.arange(K, dtype=torch.int32).reshape(T1, 1, K).cuda()
+    st = torch.full((1, T1, N1), 3.0, device="cuda")
+    aq = torch.tensor([1], dtype=torch.int32, device="cuda")
+    akv = torch.tensor([2048], dtype=torch.int32, device="cuda")
+    g = sfa.grad(q, k, k.clone(), idx, q.clone(), q.clone(), st, st.clone(), 0.088388, q_rope=qr, k_rope=kr,
+                 layout="TND", act_seq_q=aq, act_seq_kv=akv)
+    torch.cuda.synchronize()
+    for x in g:
+        assert torch.all(x == 0)
+
+
+def test_tnd_bad_lengths_reported():
+    w = SMALL["g64_tnd"]
+    inp = make_inputs(w)
+    out, smax, ssum = oracle_saved(w, inp)
+    dev = {k: to_cuda(v) for k, v in inp.items()}
+    kw = gpu_call_kwargs(w, dev)
+    kw["act_seq_kv"] = kw["act_seq_kv"] + 1   # no longer sums to T2
+    ws = torch.empty(sfa.grad_workspace_size(sfa.make_params(dev["q"], dev["k"], dev["indices"], 1.0, layout="TND",
+                                                             batch=3)), dtype=torch.uint8, device="cuda")
+    g = sfa.grad(dev["q"], dev["k"], dev["v"], dev["indices"], dev["d_out"], out.cuda(), smax.cuda(), ssum.cuda(),
+                 w.scale_value, workspace=ws, **kw)
+    assert sfa.read_device_error(ws) == 2
+    for x in g:
+        assert torch.all(x == 0)
+
+
+# ------------------------------------------------------------------ full-size workloads, sampled rows
+FULL = ["mla", "tnd", "block", "long"]
+
+
+def _full_case(name, det):
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    dev = {k: to_cuda(v) for k, v in inp.items()}
+    kw = gpu_call_kwargs(w, dev)
+    out, smax, ssum = sfa.fwd(dev["q"], dev["k"], dev["v"], dev["indices"], w.scale_value, **kw)
+    g = sfa.grad(dev["q"], dev["k"], dev["v"], dev["indices"], dev["d_out"], out, smax, ssum, w.scale_value,
+                 deterministic=det, **kw)
+    torch.cuda.synchronize()
+    return w, inp, (out, smax, ssum), g
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(name):
+    w, inp, (out, smax, ssum), g = _full_case(name, det=False)
+    rng = np.random.default_rng(0)
+    T1 = inp["q"].reshape(-1, w.N1, 512).shape[0]
+    T2 = inp["k"].reshape(-1, 512).shape[0]
+    toks = np.sort(rng.choice(T1, size=6, replace=False))
+    # key rows: a few the sampled tokens select, plus random ones
+    idx = inp["indices"].reshape(T1, -1).numpy()
+    picks = [int(idx[toks[0], 0]), int(idx[toks[1], -1])]
+    if w.layout == "BSND":
+        b0 = toks[0] // w.S1
+        picks = [b0 * w.S2 + p for p in picks]
+    keys = np.unique(np.concatenate([picks, rng.choice(T2, size=6, replace=False)]))
+    keys = keys[(keys >= 0) & (keys < T2)]
+    o_c, m_c, l_c = out.cpu(), smax.cpu(), ssum.cpu()
+    # the companion forward on the sampled tokens
+    ro, rm, rl = oracle.sfa_fwd(**oracle_kwargs(w, inp), token_rows=toks)
+    compare(f"{name}/fwd_out", o_c.reshape(T1, w.N1, 512)[toks], ro.reshape(T1, w.N1, 512)[toks], w.dtype)
+    np.testing.assert_allclose(l_c.reshape(T1, w.N1)[toks].double().numpy(), rl.reshape(T1, w.N1)[toks], rtol=2e-4)
+    ref = oracle.sfa_bwd(d_out=inp["d_out"], out=o_c, softmax_max=m_c, softmax_sum=l_c, token_rows=toks,
+                         key_rows=keys, **oracle_kwargs(w, inp))
+    dq, dk, dv, dqr, dkr = g
+    compare(f"{name}/dq", dq.reshape(T1, -1)[toks], ref["dq"].reshape(T1, -1)[toks], w.dtype)
+    compare(f"{name}/dq_rope", dqr.reshape(T1, -1)[toks], ref["dq_rope"].reshape(T1, -1)[toks], w.dtype)
+    compare(f"{name}/dk", dk.reshape(T2, -1)[keys], ref["dk"].reshape(T2, -1)[keys], w.dtype)
+    compare(f"{name}/dv", dv.reshape(T2, -1)[keys], ref["dv"].reshape(T2, -1)[keys], w.dtype)
+    compare(f"{name}/dk_rope", dkr.reshape(T2, -1)[keys], ref["dk_rope"].reshape(T2, -1)[keys], w.dtype)
+    for x in g:
+        assert torch.isfinite(x.float()).all()
+
+
+@pytest.mark.parametrize("name", ["mla"])
+def test_full_size_deterministic(name):
+    w, inp, saved, g1 = _full_case(name, det=True)
+    dev = {k: to_cuda(v) for k, v in inp.items()}
+    out, smax, ssum = saved
+    g2 = sfa.grad(dev["q"], dev["k"], dev["v"], dev["indices"], dev["d_out"], out, smax, ssum, w.scale_value,
+                  deterministic=True, **gpu_call_kwargs(w, dev))
+    torch.cuda.synchronize()
+    for a, b in zip(g1, g2):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    # and it agrees with the atomic path within tolerance
+    g3 = sfa.grad(dev["q"], dev["k"], dev["v"], dev["indices"], dev["d_out"], out, smax, ssum, w.scale_value,
+                  deterministic=False, **gpu_call_kwargs(w, dev))
+    torch.cuda.synchronize()
+    for n, a, b in zip(OUT_NAMES, g1, g3):
+        compare(f"{name}/det_vs_atomic/{n}", a, b.float().cpu().double().numpy(), w.dtype)
