@@ -1,0 +1,390 @@
+#!/usr/bin/env python
+"""Benchmark of the top-k sparse flash-attention backward (sfa_grad) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl sfa|reference]
+                    [--workload mla] [--deterministic]
+
+One step is one sfa_grad call (phase 2: workspace zeroing, token metadata,
+Dsum, score/softmax-gradient, key-side and query-side contractions, output
+cast) over the whole workload, inputs already resident in HBM.  The metric is
+TFLOP/s with 2 * (3 * (D + Dr) + 2 * D) = 5504 flops per valid
+(query, head, key).  Each timed step is bracketed by CUDA events on the
+launching stream; L2 is flushed (a 256 MB write) between steps, outside the
+events.  Prints one JSON line (rank 0).
+
+Under torchrun (N > 1) every rank runs an independent replica of the
+workload on its own GPU (weak scaling, no collective); the time is the max
+over ranks and the value counts the work of all ranks.
+
+--impl reference times the fp64 CPU oracle instead, on a bounded token
+sample of the same workload per step (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from workloads import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "sparse-attn bwd TFLOP/s (1×GB300) and % of dense bf16 tensor peak"
+FLOPS_PER_QHK = 2 * (3 * (512 + 64) + 2 * 512)
+# Peaks used when MEASURED_PEAKS.json is absent (one earlier GB300 measurement).
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        out = dict(FALLBACK_PEAKS)
+        for k in FALLBACK_PEAKS:
+            for cand in (k, k.replace("_gbs", "_GBs")):
+                if cand in d and isinstance(d[cand], (int, float)):
+                    out[k] = float(d[cand])
+        return out, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def valid_pairs(w, inp) -> int:
+    """Valid (query, key) slot count; every workload here draws in-range keys,
+    and mode-3 workloads draw them below each query's limit."""
+    idx = inp["indices"].reshape(-1, w.K)
+    return int((idx >= 0).sum().item()) * w.block_size
+
+
+class ClockSampler:
+    """nvidia-smi SM clocks and throttle reasons sampled during the timed region."""
+
+    def __init__(self, dev_index: int):
+        self.proc = None
+        self.lines = []
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={dev_index}", f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_oracle_sample(w, inp, n_tokens: int):
+    """Runs the fp64 oracle backward on the first n_tokens query tokens of the
+    workload (full K/V); returns (seconds, flops, sample description)."""
+    import oracle
+    sub = {}
+    B, S1 = w.B, w.S1
+    n = min(n_tokens, S1)
+    sl = slice(0, n)
+    sub["q"] = inp["q"][:1, sl]
+    sub["q_rope"] = inp["q_rope"][:1, sl]
+    sub["d_out"] = inp["d_out"][:1, sl]
+    sub["indices"] = inp["indices"][:1, sl]
+    kw = dict(k=inp["k"][:1], v=inp["v"][:1], k_rope=inp["k_rope"][:1], scale=w.scale_value,
+              sparse_block_size=w.block_size, layout="BSND", sparse_mode=w.mode)
+    out, smax, ssum = oracle.sfa_fwd(q=sub["q"], indices=sub["indices"], q_rope=sub["q_rope"], **kw)
+    t0 = time.perf_counter()
+    oracle.sfa_bwd(q=sub["q"], indices=sub["indices"], q_rope=sub["q_rope"], d_out=sub["d_out"], out=out,
+                   softmax_max=smax, softmax_sum=ssum, **kw)
+    dt = time.perf_counter() - t0
+    pairs = int((sub["indices"] >= 0).sum().item()) * w.block_size
+    return dt, pairs * w.N1 * FLOPS_PER_QHK, f"first {n} query tokens of {w.name} (full K/V), fp64 numpy"
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return 0
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w)
+    per_step = 2
+    times, flops = [], 0
+    for i in range(args.warmup + args.steps):
+        dt, fl, sample = cpu_oracle_sample(w, inp, per_step)
+        if i >= args.warmup:
+            times.append(dt)
+            flops = fl
+    ms = 1e3 * statistics.mean(times)
+    value = flops / (ms * 1e-3) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(w, False), "sample_tokens_per_step": per_step},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_desc(w, det):
+    return (f"{w.name}: {w.layout} B={w.B} S1={w.S1} S2={w.S2} N1={w.N1} N2=1 D=512 Dr=64 K={w.K} "
+            f"sparseBlockSize={w.block_size} sparseMode={w.mode} {w.dtype} deterministic={int(det)}")
+
+
+def kernel_names(p, det):
+    names = []
+    if p.layout == 1:
+        names.append("batch_prefix")
+    names += ["meta", "dsum"]
+    import sfa_grad_gb300 as sfa
+    chunk, _ = sfa.plan_info(p)
+    nch = (p.T1 + chunk - 1) // chunk
+    for _ in range(nch):
+        names += (["sdp", "sort_keys", "dkv", "det_reduce", "dq"] if det else ["sdp", "dkv", "dq"])
+    names.append("cast")
+    return names
+
+
+def run_sfa(args):
+    import sfa_grad_gb300 as sfa
+    world, rank, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    det = args.deterministic
+    inp = make_inputs(w)
+    d = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
+    kw = dict(q_rope=d["q_rope"], k_rope=d["k_rope"], sparse_block_size=w.block_size, layout=w.layout,
+              sparse_mode=w.mode, act_seq_q=d.get("act_seq_q"), act_seq_kv=d.get("act_seq_kv"))
+    out, smax, ssum = sfa.fwd(d["q"], d["k"], d["v"], d["indices"], w.scale_value, **kw)
+    p = sfa.make_params(d["q"], d["k"], d["indices"], w.scale_value, layout=w.layout,
+                        sparse_block_size=w.block_size, sparse_mode=w.mode, deterministic=det,
+                        batch=w.B if w.layout == "TND" else None)
+    _, launches = sfa.plan_info(p)
+    names = kernel_names(p, det)
+    ws = torch.empty(sfa.grad_workspace_size(p), dtype=torch.uint8, device=dev)
+    outs = (torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"]),
+            torch.empty_like(d["q_rope"]), torch.empty_like(d["k_rope"]))
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    pairs = valid_pairs(w, inp)
+    flops = pairs * w.N1 * FLOPS_PER_QHK
+
+    def step(events=None):
+        sfa.grad(d["q"], d["k"], d["v"], d["indices"], d["d_out"], out, smax, ssum, w.scale_value,
+                 deterministic=det, outputs=outs, workspace=ws, events=events, **kw)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    nev = launches + 1
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    for row in ev:
+        for e in row:
+            e.record(stream)   # materialise the event handles
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xff)
+        step(ev[i])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    step_ms = [ev[i][0].elapsed_time(ev[i][-1]) for i in range(args.steps)]
+    per_launch = [statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
+                  for j in range(launches)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms = total_ms / args.steps
+    value = world * flops / (ms * 1e-3) / 1e12
+    err = sfa.read_device_error(ws)
+    if err != 0:
+        raise RuntimeError(f"device error word {err}")
+
+    # ---- end to end through the C ABI from pinned host buffers
+    host = {k: (v.pin_memory() if v is not None else None) for k, v in inp.items()}
+    h_out, h_m, h_l = out.cpu().pin_memory(), smax.cpu().pin_memory(), ssum.cpu().pin_memory()
+    res_host = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    in_list = [host["q"], host["k"], host["v"], host["indices"], host["d_out"], h_out, h_m, h_l, host["q_rope"],
+               host["k_rope"]]
+    dev_in = [x.to(dev) for x in in_list]
+    h2d = sum(x.numel() * x.element_size() for x in in_list)
+    d2h = sum(x.numel() * x.element_size() for x in res_host)
+    e2e_steps = max(3, min(args.steps, 10))
+    e2e_ms = []
+    for i in range(e2e_steps + 2):
+        flush.fill_(2)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for dst, src in zip(dev_in, in_list):
+            dst.copy_(src, non_blocking=True)
+        q_, k_, v_, idx_, do_, o_, m_, l_, qr_, kr_ = dev_in
+        sfa.grad(q_, k_, v_, idx_, do_, o_, m_, l_, w.scale_value, q_rope=qr_, k_rope=kr_,
+                 sparse_block_size=w.block_size, layout=w.layout, sparse_mode=w.mode, deterministic=det,
+                 outputs=outs, workspace=ws)
+        for dst, src in zip(res_host, outs):
+            dst.copy_(src, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= 2:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_mean = statistics.mean(e2e_ms)
+    if world > 1:
+        t = torch.tensor([e2e_mean], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_mean = float(t.item())
+    e2e_value = world * flops / (e2e_mean * 1e-3) / 1e12
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.barrier()
+            torch.distributed.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    # dominant kernel and its roofline
+    dom = max(range(launches), key=lambda j: per_launch[j])
+    dname = names[dom] if dom < len(names) else f"launch{dom}"
+    G, Kp = w.N1, w.keff
+    if dname in ("sdp", "dq"):
+        fl = pairs * G * 2 * ((576 + 512) if dname == "sdp" else 576)
+        achieved = fl / (per_launch[dom] * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak}
+    else:
+        # key-side contraction: algorithmic bytes = the fp32 key-row reductions
+        # (1088 floats per valid pair) + reading P/dS (2 * G * 2 B per slot) + q/dO per token
+        T1 = p.T1
+        by = pairs * 1088 * 4 + T1 * Kp * 2 * 2 * (64 if G <= 64 else 128) + T1 * G * (576 + 512) * 2
+        if dname != "dkv":
+            by = pairs * 1088 * 4
+        achieved = by / (per_launch[dom] * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak}
+    roof["traffic"] = args.traffic
+    roof["kernel"] = dname
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        # bounded sample: grow the token count until ~10 s of oracle work
+        n, dt, fl, sample = 1, 0.0, 0, ""
+        while True:
+            dt, fl, sample = cpu_oracle_sample(w, inp, n)
+            if dt > 4.0 or n >= 64:
+                break
+            n = max(n * 2, int(n * 8.0 / max(dt, 1e-3)))
+            n = min(n, 64)
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": sample, "seconds": dt}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": workload_desc(w, det), "l2": "flushed between steps (256 MB write, outside the events)",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "valid_query_head_key": pairs * G},
+        "frac_of_dense_bf16_peak": value / world / peaks["bf16_tflops"],
+        "peak_source": peak_src,
+        "per_kernel_ms": {f"{j}:{names[j] if j < len(names) else j}": round(per_launch[j], 4) for j in range(launches)},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_mean},
+        "gpu_launches": launches * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": t_wall,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["sfa", "reference"], default="sfa")
+    ap.add_argument("--workload", default="mla", choices=list(WORKLOADS))
+    ap.add_argument("--deterministic", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="dram bytes per launch of the dominant kernel from an ncu capture")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_sfa(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -131,6 +131,29 @@ sfa_status sfa_grad(const sfa_params* p, const void* q, const void* k, const voi
                     size_t workspace_bytes, void* stream);
 
 /*
+ * sfa_grad with per-launch timing: identical work; additionally, when
+ * `events` is non-null, records events[0] on `stream` before the first
+ * launch and events[i] after the i-th kernel launch (i = 1 .. n_events - 1;
+ * later launches record nothing).  events[] are caller-created cudaEvent_t
+ * handles.  The launch order is the one sfa_grad_plan_info describes.
+ */
+sfa_status sfa_grad_profile(const sfa_params* p, const void* q, const void* k, const void* v, const int32_t* indices,
+                            const void* d_out, const void* out, const float* softmax_max, const float* softmax_sum,
+                            const int32_t* act_seq_q, const int32_t* act_seq_kv, const void* q_rope,
+                            const void* k_rope, void* dq, void* dk, void* dv, void* dq_rope, void* dk_rope,
+                            void* workspace, size_t workspace_bytes, void* stream, void** events, int32_t n_events);
+
+/*
+ * Static plan of one sfa_grad call: *chunk_tokens = query tokens processed
+ * per chunk of the staging buffers, *kernel_launches = number of kernels the
+ * call launches (in order: [batch prefix (TND)], token metadata, Dsum, then
+ * per chunk: score/softmax-gradient, [key sort (deterministic)], key-side
+ * contraction, [fixed-order reduction (deterministic)], query-side
+ * contraction; finally the output cast).  Either output pointer may be null.
+ */
+sfa_status sfa_grad_plan_info(const sfa_params* p, int64_t* chunk_tokens, int64_t* kernel_launches);
+
+/*
  * Companion forward that produces the backward's saved inputs (the page lists
  * out, softmaxMax and softmaxSum as inputs of the backward; it does not
  * specify the forward).  out = sum_j P_j v_j with P and the statistics defined

@@ -26,8 +26,8 @@ SFA_ERR_SHAPE = 561002
 LAYOUTS = {"BSND": 0, "TND": 1}
 DTYPES = {torch.bfloat16: 0, torch.float16: 1}
 
-EXPORTS = ("sfa_grad_workspace_size", "sfa_grad", "sfa_fwd_workspace_size", "sfa_fwd", "sfa_decode_keys",
-           "sfa_read_device_error", "sfa_status_string")
+EXPORTS = ("sfa_grad_workspace_size", "sfa_grad", "sfa_grad_profile", "sfa_grad_plan_info",
+           "sfa_fwd_workspace_size", "sfa_fwd", "sfa_decode_keys", "sfa_read_device_error", "sfa_status_string")
 
 
 class SfaParams(ctypes.Structure):
@@ -65,13 +65,15 @@ def lib() -> ctypes.CDLL:
     L.sfa_grad_workspace_size.argtypes = [P, ctypes.POINTER(sz)]
     L.sfa_fwd_workspace_size.argtypes = [P, ctypes.POINTER(sz)]
     L.sfa_grad.argtypes = [P] + [vp] * 18 + [sz, vp]
+    L.sfa_grad_profile.argtypes = [P] + [vp] * 18 + [sz, vp, ctypes.POINTER(vp), ctypes.c_int32]
+    L.sfa_grad_plan_info.argtypes = [P, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]
     L.sfa_fwd.argtypes = [P] + [vp] * 12 + [sz, vp]
     L.sfa_decode_keys.argtypes = [P, vp, vp, vp, vp, vp, sz, vp]
     L.sfa_read_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
     L.sfa_status_string.argtypes = [ctypes.c_int32]
     L.sfa_status_string.restype = ctypes.c_char_p
-    for name in ("sfa_grad_workspace_size", "sfa_fwd_workspace_size", "sfa_grad", "sfa_fwd", "sfa_decode_keys",
-                 "sfa_read_device_error"):
+    for name in ("sfa_grad_workspace_size", "sfa_fwd_workspace_size", "sfa_grad", "sfa_grad_profile",
+                 "sfa_grad_plan_info", "sfa_fwd", "sfa_decode_keys", "sfa_read_device_error"):
         getattr(L, name).restype = ctypes.c_int32
     _lib = L
     return L
@@ -133,6 +135,13 @@ def fwd_workspace_size(p: SfaParams) -> int:
     return n.value
 
 
+def plan_info(p: SfaParams):
+    """(tokens per staging chunk, kernel launches per call) of sfa_grad."""
+    c, n = ctypes.c_int64(0), ctypes.c_int64(0)
+    _check(lib().sfa_grad_plan_info(ctypes.byref(p), ctypes.byref(c), ctypes.byref(n)), "sfa_grad_plan_info")
+    return c.value, n.value
+
+
 def _stream(stream) -> int:
     s = stream if stream is not None else torch.cuda.current_stream()
     return s.cuda_stream
@@ -148,8 +157,11 @@ def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]) -> torch.
 
 def grad(q, k, v, indices, d_out, out, softmax_max, softmax_sum, scale, *, q_rope=None, k_rope=None,
          sparse_block_size=1, layout="BSND", sparse_mode=0, deterministic=False, act_seq_q=None, act_seq_kv=None,
-         outputs=None, workspace=None, stream=None):
-    """sfa_grad on torch CUDA tensors; returns (dq, dk, dv, dq_rope, dk_rope)."""
+         outputs=None, workspace=None, stream=None, events=None):
+    """sfa_grad on torch CUDA tensors; returns (dq, dk, dv, dq_rope, dk_rope).
+
+    events: optional list of torch.cuda.Event; when given, sfa_grad_profile
+    records events[0] before the first launch and events[i] after launch i."""
     has_rope = q_rope is not None
     batch = act_seq_q.numel() if act_seq_q is not None else None
     p = make_params(q, k, indices, scale, layout=layout, sparse_block_size=sparse_block_size,
@@ -159,11 +171,14 @@ def grad(q, k, v, indices, d_out, out, softmax_max, softmax_sum, scale, *, q_rop
                    torch.empty_like(q_rope) if has_rope else None, torch.empty_like(k_rope) if has_rope else None)
     dq, dk, dv, dqr, dkr = outputs
     ws = _workspace(grad_workspace_size(p), q.device, workspace)
-    rc = lib().sfa_grad(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(indices), _ptr(d_out), _ptr(out),
-                        _ptr(softmax_max), _ptr(softmax_sum), _ptr(act_seq_q), _ptr(act_seq_kv), _ptr(q_rope),
-                        _ptr(k_rope), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dqr), _ptr(dkr), _ptr(ws),
-                        ws.numel() * ws.element_size(), _stream(stream))
-    _check(rc, "sfa_grad")
+    args = (ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(indices), _ptr(d_out), _ptr(out), _ptr(softmax_max),
+            _ptr(softmax_sum), _ptr(act_seq_q), _ptr(act_seq_kv), _ptr(q_rope), _ptr(k_rope), _ptr(dq), _ptr(dk),
+            _ptr(dv), _ptr(dqr), _ptr(dkr), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    if events:
+        handles = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+        _check(lib().sfa_grad_profile(*args, handles, len(events)), "sfa_grad_profile")
+    else:
+        _check(lib().sfa_grad(*args), "sfa_grad")
     return dq, dk, dv, dqr, dkr
 
 

@@ -143,11 +143,26 @@ __global__ void decode_kernel(Prob p, int* rows_out) {
   }
 }
 
+// Records the caller's timing events between launches (sfa_grad_profile).
+struct Marks {
+  void** ev = nullptr;
+  int n = 0, next = 0;
+  cudaError_t mark(cudaStream_t st) {
+    if (!ev || next >= n) return cudaSuccess;
+    return cudaEventRecord(static_cast<cudaEvent_t>(ev[next++]), st);
+  }
+};
+
+int64_t launch_count(const Plan& P) {
+  const int64_t chunks = P.T1 > 0 ? (P.T1 + P.chunk - 1) / P.chunk : 0;
+  return (P.layout == SFA_LAYOUT_TND ? 1 : 0) + 2 + chunks * (P.det ? 5 : 3) + 1;
+}
+
 template <typename T>
 sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const void* k, const void* v,
                     const int32_t* idx, const void* dO, const void* out, const float* smax, const float* ssum,
                     const int32_t* aq, const int32_t* akv, const void* qr, const void* kr, void* dq, void* dk, void* dv,
-                    void* dqr, void* dkr, uint8_t* ws, cudaStream_t st) {
+                    void* dqr, void* dkr, uint8_t* ws, cudaStream_t st, Marks mk) {
   int* gerr = reinterpret_cast<int*>(ws + P.off_err);
   Prob pr = make_prob(P, ws);
   pr.q = q; pr.k = k; pr.v = v; pr.dO = dO; pr.out = out; pr.idx = idx;
@@ -156,11 +171,18 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
   pr.smax = smax; pr.ssum = ssum;
   pr.dsum = reinterpret_cast<const float*>(ws + P.off_dsum);
   const int nsm = sm_count();
+  SFA_CK(mk.mark(st));
   SFA_CK(cudaMemsetAsync(gerr, 0, 16, st));
   SFA_CK(cudaMemsetAsync(ws + P.off_acc, 0, (size_t)P.T2 * kAccRow * 4, st));
+  if (P.layout == SFA_LAYOUT_TND) {
+    SFA_CK(launch_batch_prefix(pr, P.B, aq, akv, reinterpret_cast<int*>(ws + P.off_batch), gerr, st));
+    SFA_CK(mk.mark(st));
+  }
   SFA_CK(launch_meta(pr, P.layout, P.B, P.S1, P.S2, P.mode, aq, akv, reinterpret_cast<int*>(ws + P.off_batch),
                      reinterpret_cast<TokMeta*>(ws + P.off_meta), gerr, st));
+  SFA_CK(mk.mark(st));
   SFA_CK(launch_dsum<T>(pr, reinterpret_cast<float*>(ws + P.off_dsum), st));
+  SFA_CK(mk.mark(st));
   float* acc = reinterpret_cast<float*>(ws + P.off_acc);
   for (int t0 = 0; t0 < P.T1; t0 += P.chunk) {
     pr.tok0 = t0;
@@ -168,19 +190,26 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
     void* Pst = ws + P.off_P;
     void* dSst = ws + P.off_dS;
     SFA_CK(launch_sdp<T>(pr, kModeBwd, Pst, dSst, nullptr, gerr, nsm, st));
+    SFA_CK(mk.mark(st));
     if (P.det) {
       int* skey = reinterpret_cast<int*>(ws + P.off_skey);
       int* sslot = reinterpret_cast<int*>(ws + P.off_sslot);
       float* part = reinterpret_cast<float*>(ws + P.off_part);
       SFA_CK(launch_sort_keys(pr, skey, sslot, st));
+      SFA_CK(mk.mark(st));
       SFA_CK(launch_dkv<T>(pr, Pst, dSst, acc, part, gerr, nsm, st));
+      SFA_CK(mk.mark(st));
       SFA_CK(launch_det_reduce(pr, skey, sslot, part, acc, st));
+      SFA_CK(mk.mark(st));
     } else {
       SFA_CK(launch_dkv<T>(pr, Pst, dSst, acc, nullptr, gerr, nsm, st));
+      SFA_CK(mk.mark(st));
     }
     SFA_CK(launch_dq<T>(pr, 0, dSst, dq, P.has_rope ? dqr : nullptr, gerr, nsm, st));
+    SFA_CK(mk.mark(st));
   }
   SFA_CK(launch_cast<T>(acc, P.T2, dk, P.has_rope ? dkr : nullptr, dv, P.has_rope, st));
+  SFA_CK(mk.mark(st));
   (void)prm;
   return SFA_OK;
 }
@@ -197,6 +226,8 @@ sfa_status run_fwd(const Plan& P, const void* q, const void* k, const void* v, c
   pr.smax = smax; pr.ssum = ssum;
   const int nsm = sm_count();
   SFA_CK(cudaMemsetAsync(gerr, 0, 16, st));
+  if (P.layout == SFA_LAYOUT_TND)
+    SFA_CK(launch_batch_prefix(pr, P.B, aq, akv, reinterpret_cast<int*>(ws + P.off_batch), gerr, st));
   SFA_CK(launch_meta(pr, P.layout, P.B, P.S1, P.S2, P.mode, aq, akv, reinterpret_cast<int*>(ws + P.off_batch),
                      reinterpret_cast<TokMeta*>(ws + P.off_meta), gerr, st));
   float* ts = reinterpret_cast<float*>(ws + P.off_tstats);
@@ -241,6 +272,25 @@ sfa_status sfa_grad(const sfa_params* p, const void* q, const void* k, const voi
                     const int32_t* act_seq_q, const int32_t* act_seq_kv, const void* q_rope, const void* k_rope,
                     void* dq, void* dk, void* dv, void* dq_rope, void* dk_rope, void* workspace,
                     size_t workspace_bytes, void* stream) {
+  return sfa_grad_profile(p, q, k, v, indices, d_out, out, softmax_max, softmax_sum, act_seq_q, act_seq_kv, q_rope,
+                          k_rope, dq, dk, dv, dq_rope, dk_rope, workspace, workspace_bytes, stream, nullptr, 0);
+}
+
+sfa_status sfa_grad_plan_info(const sfa_params* p, int64_t* chunk_tokens, int64_t* kernel_launches) {
+  if (!p) return SFA_ERR_NULLPTR;
+  Plan P;
+  sfa_status s = sfa::validate(p, false, &P);
+  if (s != SFA_OK) return s;
+  if (chunk_tokens) *chunk_tokens = P.chunk;
+  if (kernel_launches) *kernel_launches = P.T1 == 0 ? 0 : sfa::launch_count(P);
+  return SFA_OK;
+}
+
+sfa_status sfa_grad_profile(const sfa_params* p, const void* q, const void* k, const void* v, const int32_t* indices,
+                            const void* d_out, const void* out, const float* softmax_max, const float* softmax_sum,
+                            const int32_t* act_seq_q, const int32_t* act_seq_kv, const void* q_rope,
+                            const void* k_rope, void* dq, void* dk, void* dv, void* dq_rope, void* dk_rope,
+                            void* workspace, size_t workspace_bytes, void* stream, void** events, int32_t n_events) {
   if (!p) return SFA_ERR_NULLPTR;
   Plan P;
   sfa_status s = sfa::validate(p, false, &P);
@@ -263,11 +313,14 @@ sfa_status sfa_grad(const sfa_params* p, const void* q, const void* k, const voi
   if (P.layout == SFA_LAYOUT_TND && (!act_seq_q || !act_seq_kv)) return SFA_ERR_NULLPTR;
   if (workspace_bytes < P.total) return SFA_ERR_PARAM_INVALID;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  sfa::Marks mk;
+  mk.ev = events;
+  mk.n = events ? n_events : 0;
   if (P.is_f16)
     return sfa::run_grad<__half>(P, p, q, k, v, indices, d_out, out, softmax_max, softmax_sum, act_seq_q, act_seq_kv,
-                                 q_rope, k_rope, dq, dk, dv, dq_rope, dk_rope, ws, st);
+                                 q_rope, k_rope, dq, dk, dv, dq_rope, dk_rope, ws, st, mk);
   return sfa::run_grad<__nv_bfloat16>(P, p, q, k, v, indices, d_out, out, softmax_max, softmax_sum, act_seq_q,
-                                      act_seq_kv, q_rope, k_rope, dq, dk, dv, dq_rope, dk_rope, ws, st);
+                                      act_seq_kv, q_rope, k_rope, dq, dk, dv, dq_rope, dk_rope, ws, st, mk);
 }
 
 sfa_status sfa_fwd(const sfa_params* p, const void* q, const void* k, const void* v, const int32_t* indices,
@@ -309,6 +362,8 @@ sfa_status sfa_decode_keys(const sfa_params* p, const int32_t* indices, const in
   sfa::Prob pr = sfa::make_prob(P, ws);
   pr.idx = indices;
   SFA_CK(cudaMemsetAsync(gerr, 0, 16, st));
+  if (P.layout == SFA_LAYOUT_TND)
+    SFA_CK(sfa::launch_batch_prefix(pr, P.B, act_seq_q, act_seq_kv, reinterpret_cast<int*>(ws + P.off_batch), gerr, st));
   SFA_CK(sfa::launch_meta(pr, P.layout, P.B, P.S1, P.S2, P.mode, act_seq_q, act_seq_kv,
                           reinterpret_cast<int*>(ws + P.off_batch), reinterpret_cast<sfa::TokMeta*>(ws + P.off_meta),
                           gerr, st));

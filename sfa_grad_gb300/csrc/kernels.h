@@ -26,6 +26,8 @@ cudaError_t launch_dq(const Prob& p, int mode, const void* A, void* out_main, vo
                       cudaStream_t st);
 
 // Small kernels (prep.cu).
+cudaError_t launch_batch_prefix(const Prob& p, int B, const int* act_q, const int* act_kv, int* batch_ofs, int* gerr,
+                                cudaStream_t st);
 cudaError_t launch_meta(const Prob& p, int layout, int B, int S1, int S2, int mode, const int* act_q, const int* act_kv,
                         int* batch_ofs, TokMeta* meta, int* gerr, cudaStream_t st);
 template <typename T>

@@ -146,13 +146,15 @@ __global__ void stats_combine_kernel(const float* ts, int ntok, int ntiles, int 
 
 }  // namespace
 
+cudaError_t launch_batch_prefix(const Prob& p, int B, const int* act_q, const int* act_kv, int* batch_ofs, int* gerr,
+                                cudaStream_t st) {
+  batch_prefix_kernel<<<1, 1, 0, st>>>(act_q, act_kv, B, p.T1, p.T2, batch_ofs, gerr);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_meta(const Prob& p, int layout, int B, int S1, int S2, int mode, const int* act_q, const int* act_kv,
                         int* batch_ofs, TokMeta* meta, int* gerr, cudaStream_t st) {
-  if (layout == 1) {
-    batch_prefix_kernel<<<1, 1, 0, st>>>(act_q, act_kv, B, p.T1, p.T2, batch_ofs, gerr);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
+  (void)gerr;
   if (p.T1 > 0) meta_kernel<<<(p.T1 + 255) / 256, 256, 0, st>>>(layout, p.T1, B, S1, S2, mode, batch_ofs, act_q, act_kv, meta);
   return cudaGetLastError();
 }
