@@ -193,7 +193,7 @@ def kernel_names(p, det):
     chunk, _ = sfa.plan_info(p)
     nch = (p.T1 + chunk - 1) // chunk
     for _ in range(nch):
-        names += (["sdp", "sort_keys", "dkv", "det_reduce", "dq"] if det else ["sdp", "dkv", "dq"])
+        names += (["rowtab", "sdp", "sort_keys", "dkv", "det_reduce", "dq"] if det else ["rowtab", "sdp", "dkv", "dq"])
     names.append("cast")
     return names
 

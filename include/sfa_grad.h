@@ -147,7 +147,7 @@ sfa_status sfa_grad_profile(const sfa_params* p, const void* q, const void* k, c
  * Static plan of one sfa_grad call: *chunk_tokens = query tokens processed
  * per chunk of the staging buffers, *kernel_launches = number of kernels the
  * call launches (in order: [batch prefix (TND)], token metadata, Dsum, then
- * per chunk: score/softmax-gradient, [key sort (deterministic)], key-side
+ * per chunk: row table, score/softmax-gradient, [key sort (deterministic)], key-side
  * contraction, [fixed-order reduction (deterministic)], query-side
  * contraction; finally the output cast).  Either output pointer may be null.
  */
@@ -184,6 +184,13 @@ sfa_status sfa_decode_keys(const sfa_params* p, const int32_t* indices, const in
  * *code, then clears it.  Returns SFA_ERR_RUNTIME if the copy fails.
  */
 sfa_status sfa_read_device_error(void* workspace, void* stream, int32_t* code);
+
+/*
+ * Human-readable detail of the most recent SFA_ERR_RUNTIME returned on the
+ * calling thread (the failing CUDA call's error text and location); empty if
+ * none.  The pointer stays valid until the thread's next library call.
+ */
+const char* sfa_last_error_message(void);
 
 /* Static description of a status code. */
 const char* sfa_status_string(int32_t status);

@@ -27,7 +27,8 @@ LAYOUTS = {"BSND": 0, "TND": 1}
 DTYPES = {torch.bfloat16: 0, torch.float16: 1}
 
 EXPORTS = ("sfa_grad_workspace_size", "sfa_grad", "sfa_grad_profile", "sfa_grad_plan_info",
-           "sfa_fwd_workspace_size", "sfa_fwd", "sfa_decode_keys", "sfa_read_device_error", "sfa_status_string")
+           "sfa_fwd_workspace_size", "sfa_fwd", "sfa_decode_keys", "sfa_read_device_error", "sfa_status_string",
+           "sfa_last_error_message")
 
 
 class SfaParams(ctypes.Structure):
@@ -46,7 +47,10 @@ class SfaParams(ctypes.Structure):
 class SfaError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
-        super().__init__(f"{where}: {status_string(code)} ({code})")
+        detail = ""
+        if code == SFA_ERR_RUNTIME:
+            detail = " - " + lib().sfa_last_error_message().decode()
+        super().__init__(f"{where}: {status_string(code)} ({code}){detail}")
 
 
 _lib = None
@@ -70,6 +74,8 @@ def lib() -> ctypes.CDLL:
     L.sfa_fwd.argtypes = [P] + [vp] * 12 + [sz, vp]
     L.sfa_decode_keys.argtypes = [P, vp, vp, vp, vp, vp, sz, vp]
     L.sfa_read_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
+    L.sfa_last_error_message.argtypes = []
+    L.sfa_last_error_message.restype = ctypes.c_char_p
     L.sfa_status_string.argtypes = [ctypes.c_int32]
     L.sfa_status_string.restype = ctypes.c_char_p
     for name in ("sfa_grad_workspace_size", "sfa_fwd_workspace_size", "sfa_grad", "sfa_grad_profile",

@@ -5,7 +5,10 @@
 // (shapes, dtypes), 返回值 (status codes), 约束说明 (empty query, determinism),
 // 规格约束 (supported ranges).
 #include <cmath>
+#include <cstdio>
 #include <cstring>
+
+#include <cudaTypedefs.h>
 
 #include "../../include/sfa_grad.h"
 #include "common.cuh"
@@ -26,7 +29,7 @@ struct Plan {
   int layout, B, S1, S2, T1, T2, G, Gp, Kidx, bs, Keff, Kpad, mode, has_rope, det, is_f16;
   float scale;
   int chunk;
-  size_t off_err, off_batch, off_meta, off_dsum, off_acc, off_P, off_dS, off_part, off_skey, off_sslot, off_tstats;
+  size_t off_err, off_batch, off_meta, off_dsum, off_acc, off_P, off_dS, off_rows, off_part, off_skey, off_sslot, off_tstats;
   size_t total;
 };
 
@@ -95,6 +98,7 @@ sfa_status validate(const sfa_params* p, bool fwd, Plan* out) {
   P.off_acc = o; o += fwd ? 0 : up((size_t)P.T2 * kAccRow * 4);
   P.off_P = o; o += up(chunk * P.Kpad * P.Gp * 2);
   P.off_dS = o; o += fwd ? 0 : up(chunk * P.Kpad * P.Gp * 2);
+  P.off_rows = o; o += up(chunk * P.Kpad * 4);
   P.off_part = o; o += P.det ? up(chunk * P.Kpad * kAccRow * 4) : 0;
   P.off_skey = o; o += P.det ? up(chunk * P.Kpad * 4) : 0;
   P.off_sslot = o; o += P.det ? up(chunk * P.Kpad * 4) : 0;
@@ -117,7 +121,57 @@ Prob make_prob(const Plan& P, uint8_t* ws) {
   pr.has_rope = P.has_rope;
   pr.scale = P.scale;
   pr.meta = reinterpret_cast<const TokMeta*>(ws + P.off_meta);
+  pr.rowtab = reinterpret_cast<int*>(ws + P.off_rows);
   return pr;
+}
+
+// ---------------------------------------------------------------- tensor maps
+using EncodeTiled = PFN_cuTensorMapEncodeTiled_v12000;
+
+// The driver's tensor-map encoder, looked up once through the runtime (no
+// link-time dependency on libcuda).
+EncodeTiled encoder() {
+  static EncodeTiled fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(ptr);
+  }
+  return fn;
+}
+
+// 2-D row-major map over `rows` x `cols` 16-bit elements, 128-byte swizzle,
+// box of 64 columns x box_rows rows.
+bool encode2d(CUtensorMap* m, bool f16, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  EncodeTiled fn = encoder();
+  if (!fn) return false;
+  if (rows == 0) rows = 1;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+            strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Maps of one call.  Tensors a call does not use (dO and dS in the forward,
+// the rope pair without rope) alias a used tensor and are never read.
+bool make_maps(Maps* M, const Plan& P, const void* q, const void* qr, const void* dO, const void* k, const void* kr,
+               const void* v, const void* Pst, const void* dSst) {
+  const bool f = P.is_f16;
+  const uint64_t TG = (uint64_t)P.T1 * P.G, T2 = (uint64_t)P.T2, R = (uint64_t)P.chunk * P.Kpad;
+  bool ok = encode2d(&M->q, f, q, 512, TG, P.Gp);
+  ok = ok && encode2d(&M->qr, f, qr ? qr : q, qr ? 64 : 512, TG, P.Gp);
+  ok = ok && encode2d(&M->dO, f, dO ? dO : q, 512, TG, P.Gp);
+  ok = ok && encode2d(&M->k, f, k, 512, T2, 1);
+  ok = ok && encode2d(&M->kr, f, kr ? kr : k, kr ? 64 : 512, T2, 1);
+  ok = ok && encode2d(&M->v, f, v, 512, T2, 1);
+  ok = ok && encode2d(&M->P, f, Pst, P.Gp, R, 64);
+  ok = ok && encode2d(&M->dS, f, dSst ? dSst : Pst, P.Gp, R, 64);
+  return ok;
 }
 
 int sm_count() {
@@ -127,12 +181,19 @@ int sm_count() {
   return n;
 }
 
+// Text of the last failing CUDA call on this thread (sfa_last_error_message).
+thread_local char g_last_error[256] = "";
+
+sfa_status fail(cudaError_t e, int line) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s (CUDA error %d) at api.cu:%d", cudaGetErrorString(e), (int)e, line);
+  (void)cudaGetLastError();
+  return SFA_ERR_RUNTIME;
+}
+
 #define SFA_CK(x)                                   \
   do {                                              \
-    if ((x) != cudaSuccess) {                       \
-      (void)cudaGetLastError();                     \
-      return SFA_ERR_RUNTIME;                       \
-    }                                               \
+    const cudaError_t sfa_e_ = (x);                 \
+    if (sfa_e_ != cudaSuccess) return ::sfa::fail(sfa_e_, __LINE__); \
   } while (0)
 
 __global__ void decode_kernel(Prob p, int* rows_out) {
@@ -155,7 +216,7 @@ struct Marks {
 
 int64_t launch_count(const Plan& P) {
   const int64_t chunks = P.T1 > 0 ? (P.T1 + P.chunk - 1) / P.chunk : 0;
-  return (P.layout == SFA_LAYOUT_TND ? 1 : 0) + 2 + chunks * (P.det ? 5 : 3) + 1;
+  return (P.layout == SFA_LAYOUT_TND ? 1 : 0) + 2 + chunks * (P.det ? 6 : 4) + 1;
 }
 
 template <typename T>
@@ -171,6 +232,11 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
   pr.smax = smax; pr.ssum = ssum;
   pr.dsum = reinterpret_cast<const float*>(ws + P.off_dsum);
   const int nsm = sm_count();
+  Maps maps;
+  if (!make_maps(&maps, P, q, pr.qr, dO, k, pr.kr, v, ws + P.off_P, ws + P.off_dS)) {
+    snprintf(g_last_error, sizeof(g_last_error), "tensor map encoding failed");
+    return SFA_ERR_RUNTIME;
+  }
   SFA_CK(mk.mark(st));
   SFA_CK(cudaMemsetAsync(gerr, 0, 16, st));
   SFA_CK(cudaMemsetAsync(ws + P.off_acc, 0, (size_t)P.T2 * kAccRow * 4, st));
@@ -189,7 +255,9 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
     pr.ntok = (P.T1 - t0) < P.chunk ? (P.T1 - t0) : P.chunk;
     void* Pst = ws + P.off_P;
     void* dSst = ws + P.off_dS;
-    SFA_CK(launch_sdp<T>(pr, kModeBwd, Pst, dSst, nullptr, gerr, nsm, st));
+    SFA_CK(launch_rowtab(pr, st));
+    SFA_CK(mk.mark(st));
+    SFA_CK(launch_sdp<T>(maps, pr, kModeBwd, Pst, dSst, nullptr, gerr, nsm, st));
     SFA_CK(mk.mark(st));
     if (P.det) {
       int* skey = reinterpret_cast<int*>(ws + P.off_skey);
@@ -197,15 +265,15 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
       float* part = reinterpret_cast<float*>(ws + P.off_part);
       SFA_CK(launch_sort_keys(pr, skey, sslot, st));
       SFA_CK(mk.mark(st));
-      SFA_CK(launch_dkv<T>(pr, Pst, dSst, acc, part, gerr, nsm, st));
+      SFA_CK(launch_dkv<T>(maps, pr, acc, part, gerr, nsm, st));
       SFA_CK(mk.mark(st));
       SFA_CK(launch_det_reduce(pr, skey, sslot, part, acc, st));
       SFA_CK(mk.mark(st));
     } else {
-      SFA_CK(launch_dkv<T>(pr, Pst, dSst, acc, nullptr, gerr, nsm, st));
+      SFA_CK(launch_dkv<T>(maps, pr, acc, nullptr, gerr, nsm, st));
       SFA_CK(mk.mark(st));
     }
-    SFA_CK(launch_dq<T>(pr, 0, dSst, dq, P.has_rope ? dqr : nullptr, gerr, nsm, st));
+    SFA_CK(launch_dq<T>(maps, pr, 0, dq, P.has_rope ? dqr : nullptr, gerr, nsm, st));
     SFA_CK(mk.mark(st));
   }
   SFA_CK(launch_cast<T>(acc, P.T2, dk, P.has_rope ? dkr : nullptr, dv, P.has_rope, st));
@@ -225,6 +293,11 @@ sfa_status run_fwd(const Plan& P, const void* q, const void* k, const void* v, c
   pr.kr = P.has_rope ? kr : nullptr;
   pr.smax = smax; pr.ssum = ssum;
   const int nsm = sm_count();
+  Maps maps;
+  if (!make_maps(&maps, P, q, pr.qr, nullptr, k, pr.kr, v, ws + P.off_P, nullptr)) {
+    snprintf(g_last_error, sizeof(g_last_error), "tensor map encoding failed");
+    return SFA_ERR_RUNTIME;
+  }
   SFA_CK(cudaMemsetAsync(gerr, 0, 16, st));
   if (P.layout == SFA_LAYOUT_TND)
     SFA_CK(launch_batch_prefix(pr, P.B, aq, akv, reinterpret_cast<int*>(ws + P.off_batch), gerr, st));
@@ -234,10 +307,11 @@ sfa_status run_fwd(const Plan& P, const void* q, const void* k, const void* v, c
   for (int t0 = 0; t0 < P.T1; t0 += P.chunk) {
     pr.tok0 = t0;
     pr.ntok = (P.T1 - t0) < P.chunk ? (P.T1 - t0) : P.chunk;
-    SFA_CK(launch_sdp<T>(pr, kModeFwdStats, nullptr, nullptr, ts, gerr, nsm, st));
+    SFA_CK(launch_rowtab(pr, st));
+    SFA_CK(launch_sdp<T>(maps, pr, kModeFwdStats, nullptr, nullptr, ts, gerr, nsm, st));
     SFA_CK(launch_stats_combine(pr, ts, smax, ssum, st));
-    SFA_CK(launch_sdp<T>(pr, kModeFwdP, ws + P.off_P, nullptr, nullptr, gerr, nsm, st));
-    SFA_CK(launch_dq<T>(pr, 1, ws + P.off_P, out, nullptr, gerr, nsm, st));
+    SFA_CK(launch_sdp<T>(maps, pr, kModeFwdP, ws + P.off_P, nullptr, nullptr, gerr, nsm, st));
+    SFA_CK(launch_dq<T>(maps, pr, 1, out, nullptr, gerr, nsm, st));
   }
   return SFA_OK;
 }
@@ -382,6 +456,8 @@ sfa_status sfa_read_device_error(void* workspace, void* stream, int32_t* code) {
   *code = v;
   return SFA_OK;
 }
+
+const char* sfa_last_error_message(void) { return sfa::g_last_error; }
 
 const char* sfa_status_string(int32_t s) {
   switch (s) {

@@ -4,6 +4,7 @@
 // shared-memory operand layouts the tensor-core descriptors describe.
 #pragma once
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -74,6 +75,47 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // Makes this thread's completed generic-proxy shared writes visible to the
 // tensor core (async proxy).
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// ------------------------------------------------------------------ TMA
+// Tensor maps of one call (2-D, 16-bit elements, 64-element = 128-byte inner
+// box, 128-byte swizzle, so a box lands in shared memory exactly in the panel
+// layout below).  Rows outside a map's extent (negative or past the end) are
+// filled with zeros.
+struct Maps {
+  CUtensorMap q;    // (T1*G, 512), box 64 x GP
+  CUtensorMap qr;   // (T1*G, 64),  box 64 x GP
+  CUtensorMap dO;   // (T1*G, 512), box 64 x GP
+  CUtensorMap k;    // (T2, 512),   box 64 x 1 (row gathers)
+  CUtensorMap kr;   // (T2, 64),    box 64 x 1
+  CUtensorMap v;    // (T2, 512),   box 64 x 1
+  CUtensorMap P;    // (chunk*Kpad, GP) staged P^T,  box 64 x 64
+  CUtensorMap dS;   // (chunk*Kpad, GP) staged dS^T, box 64 x 64
+};
+
+// Arrive once on `bar` and add `bytes` to the transaction count the phase
+// waits for.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+// One box at (x = column, y = row) into shared memory at `dst`.
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+// Four one-row boxes (rows r0..r3, columns x .. x+63) into four consecutive
+// 128-byte rows at `dst`.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int r0, int r1, int r2, int r3,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+      "%5, %6}], [%7];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+      : "memory");
+}
 
 // ------------------------------------------------------------------ operand layouts
 // All tensor-core operands live in shared memory as 128-byte swizzled rows:
@@ -158,6 +200,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 2^x on the special-function unit (ex2.approx, flush-to-zero); 2^-inf = 0.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;
+
 // ------------------------------------------------------------------ element types
 template <typename T>
 struct Elt;
@@ -204,6 +254,7 @@ struct Prob {
   const float* ssum;  // (T1, G)
   const TokMeta* meta;  // (T1)
   const float* dsum;    // (T1, G)
+  int* rowtab;          // (ntok, Kpad): kv row of every slot of the chunk, -1 if masked
   int T1, T2, G, Gp, Kidx, bs, Keff, Kpad;
   int has_rope;
   float scale;

@@ -18,9 +18,10 @@ namespace sfa {
 namespace {
 
 constexpr int kKeys = 128;
-constexpr int kStages = 4;
-constexpr int kProducerWarps = 3;
-constexpr int kThreads = 256;
+constexpr int kStages = 3;
+constexpr int kDrainThreads = 256;           // warps 4-11
+constexpr int kThreads = 128 + kDrainThreads;
+constexpr int kStgRow = 36;                   // floats per staged row (32 + pad)
 constexpr int kChunks = 5;        // dK 3 x 192, dV 2 x 256
 constexpr int kAccRow = 1088;     // fp32 accumulator row: dK | dKRope | dV
 
@@ -33,7 +34,8 @@ template <int GP>
 struct DkvSmem {
   static constexpr int kB = 4 * GP * 128;           // up to 4 feature panels of GP head rows
   static constexpr int kA = (GP / 64) * kKeys * 128;  // head panels of 128 slot rows
-  static constexpr int kBytes = kB + kStages * kA + 1024;
+  static constexpr int kStg = (kDrainThreads / 32) * 32 * kStgRow * 4;  // per-warp transpose buffers
+  static constexpr int kBytes = kB + kStages * kA + kStg + 1024;
 };
 
 __device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
@@ -41,14 +43,15 @@ __device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c
 }
 
 template <typename T, int GP, bool DET>
-__global__ void __launch_bounds__(kThreads, 1) dkv_kernel(Prob p, const T* Pst, const T* dSst, float* acc,
+__global__ void __launch_bounds__(kThreads, 1) dkv_kernel(const __grid_constant__ Maps maps, Prob p, float* acc,
                                                           float* partials, int* gerr) {
   using E = Elt<T>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sB = smem;
   uint8_t* sA = smem + DkvSmem<GP>::kB;
-  __shared__ uint64_t full_bar[kStages], empty_bar[kStages], tfull_bar[2], tempty_bar[2], bempty_bar;
+  float* sStg = reinterpret_cast<float*>(sA + kStages * DkvSmem<GP>::kA);
+  __shared__ uint64_t full_bar[kStages], empty_bar[kStages], tfull_bar[2], tempty_bar[2], bempty_bar, bfull_bar;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
@@ -58,14 +61,15 @@ __global__ void __launch_bounds__(kThreads, 1) dkv_kernel(Prob p, const T* Pst, 
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&full_bar[i], kProducerWarps * 32);
+      mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull_bar[i], 1);
-      mbar_init(&tempty_bar[i], 128);
+      mbar_init(&tempty_bar[i], kDrainThreads);
     }
     mbar_init(&bempty_bar, 1);
+    mbar_init(&bfull_bar, 1);
     abort_flag = 0;
     mbar_fence_init();
   }
@@ -86,6 +90,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkv_kernel(Prob p, const T* Pst, 
         chunk_geom(ch, ncol, col0);
         const uint32_t idesc = idesc_f16(kKeys, ncol, E::is_f16, false, true);
         const uint32_t b = smem_u32(sB);
+        if (!mbar_wait(&bfull_bar, icount & 1, &abort_flag, gerr)) break;
         for (int kt = 0; kt < ntiles; ++kt, ++tcount) {
           const int set = tcount & 1;
           if (!mbar_wait(&tempty_bar[set], ((tcount >> 1) & 1) ^ 1, &abort_flag, gerr)) break;
@@ -105,115 +110,101 @@ __global__ void __launch_bounds__(kThreads, 1) dkv_kernel(Prob p, const T* Pst, 
       }
     }
     __syncwarp();
-  } else if (warp <= kProducerWarps) {
-    // ---------------------------------------------------------------- producers
-    const int pt = threadIdx.x - 32;
-    constexpr int kNP = kProducerWarps * 32;
-    const T* q = static_cast<const T*>(p.q);
-    const T* qr = static_cast<const T*>(p.qr);
-    const T* dO = static_cast<const T*>(p.dO);
-    int stage = 0, issued = 0, signalled = 0, sig_stage = 0, icount = 0;
-    uint32_t phase = 0;
-    constexpr int kLag = 2;
-    constexpr int kHP = GP / 64;
-    for (int item = blockIdx.x; item < nitems && !abort_flag; item += gridDim.x, ++icount) {
-      const int tl = item / kChunks, ch = item % kChunks;
-      const int t = p.tok0 + tl;
-      int ncol, col0;
-      chunk_geom(ch, ncol, col0);
-      // flush: every issued tile must be signalled before waiting for the
-      // previous item's MMAs to release the B panels
-      cp_async_wait<0>();
-      fence_async_smem();
-      while (signalled < issued) {
-        mbar_arrive(&full_bar[sig_stage]);
-        if (++sig_stage == kStages) sig_stage = 0;
-        ++signalled;
-      }
-      if (icount > 0 && !mbar_wait(&bempty_bar, (icount - 1) & 1, &abort_flag, gerr)) break;
-      // B panels: GP head rows x ncol features, MN-major (feature panels)
-      {
-        const uint32_t b = smem_u32(sB);
-        const int npan = ncol / 64;
-        for (int r = pt; r < GP * npan; r += kNP) {
-          const int h = r % GP, pb = r / GP;
-          const int f = (ch < 3 ? col0 : col0 - 576) + pb * 64;   // feature in the source tensor
-          const T* src;
-          if (ch < 3) src = (f < 512 || !p.has_rope) ? q + ((size_t)t * p.G + (h < p.G ? h : 0)) * 512 + (f < 512 ? f : 0)
-                                                     : qr + ((size_t)t * p.G + (h < p.G ? h : 0)) * 64 + (f - 512);
-          else src = dO + ((size_t)t * p.G + (h < p.G ? h : 0)) * 512 + f;
-          uint32_t nb = h < p.G ? 16u : 0u;
-          if (ch < 3 && f >= 512 && !p.has_rope) { src = q; nb = 0u; }
-          const uint32_t dst = b + pb * (GP * 128);
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- producer (TMA, lane 0)
+    // Per item: the token's head rows of q / qRope / dO for the chunk's
+    // feature panels (B, kept for the whole item); per key tile: the staged
+    // P^T or dS^T rows as 64x64 boxes (A).
+    if (lane == 0) {
+      int stage = 0, icount = 0;
+      uint32_t phase = 0;
+      constexpr int kHP = GP / 64;
+      bool ok = true;
+      for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++icount) {
+        const int tl = item / kChunks, ch = item % kChunks;
+        const int t = p.tok0 + tl;
+        int ncol, col0;
+        chunk_geom(ch, ncol, col0);
+        if (icount > 0) ok = mbar_wait(&bempty_bar, (icount - 1) & 1, &abort_flag, gerr);
+        if (!ok) break;
+        {
+          const uint32_t b = smem_u32(sB);
+          const int npan = ncol / 64;
+          mbar_expect_tx(&bfull_bar, npan * GP * 128);
+          for (int pb = 0; pb < npan; ++pb) {
+            const CUtensorMap* mp;
+            int x, y = t * p.G;
+            if (ch >= 3) { mp = &maps.dO; x = col0 - 576 + pb * 64; }
+            else {
+              const int f = col0 + pb * 64;
+              if (f < 512) { mp = &maps.q; x = f; }
+              else if (p.has_rope) { mp = &maps.qr; x = f - 512; }
+              else { mp = &maps.q; x = 0; y = -2 * GP; }   // no rope part: rows outside the map read as zeros
+            }
+            tma_2d(b + pb * (GP * 128), mp, x, y, &bfull_bar);
+          }
+        }
+        const CUtensorMap* mA = ch < 3 ? &maps.dS : &maps.P;
+        for (int kt = 0; kt < ntiles && ok; ++kt) {
+          ok = mbar_wait(&empty_bar[stage], phase ^ 1, &abort_flag, gerr);
+          if (!ok) break;
+          const uint32_t a = smem_u32(sA + stage * DkvSmem<GP>::kA);
+          mbar_expect_tx(&full_bar[stage], DkvSmem<GP>::kA);
+          const int y0 = tl * p.Kpad + kt * kKeys;
 #pragma unroll
-          for (int cc = 0; cc < 8; ++cc) cp_async16(dst + swz_chunk(h, cc), src + cc * 8, nb);
+          for (int hp = 0; hp < kHP; ++hp) {
+            tma_2d(a + hp * (kKeys * 128), mA, hp * 64, y0, &full_bar[stage]);
+            tma_2d(a + hp * (kKeys * 128) + 64 * 128, mA, hp * 64, y0 + 64, &full_bar[stage]);
+          }
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
-      }
-      const T* Ast = ch < 3 ? dSst : Pst;
-      for (int kt = 0; kt < ntiles; ++kt) {
-        if (!mbar_wait(&empty_bar[stage], phase ^ 1, &abort_flag, gerr)) break;
-        const uint32_t a = smem_u32(sA + stage * DkvSmem<GP>::kA);
-        const T* tile = Ast + ((size_t)tl * p.Kpad + (size_t)kt * kKeys) * GP;
-        for (int r = pt; r < kKeys * kHP; r += kNP) {
-          const int s = r % kKeys, hp = r / kKeys;
-          const T* src = tile + (size_t)s * GP + hp * 64;
-          const uint32_t dst = a + hp * (kKeys * 128);
-#pragma unroll
-          for (int cc = 0; cc < 8; ++cc) cp_async16(dst + swz_chunk(s, cc), src + cc * 8, 16u);
-        }
-        cp_async_commit();
-        ++issued;
-        if (issued - signalled > kLag) {
-          cp_async_wait<kLag>();
-          fence_async_smem();
-          mbar_arrive(&full_bar[sig_stage]);
-          if (++sig_stage == kStages) sig_stage = 0;
-          ++signalled;
-        }
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
       }
     }
-    cp_async_wait<0>();
-    fence_async_smem();
-    while (signalled < issued) {
-      mbar_arrive(&full_bar[sig_stage]);
-      if (++sig_stage == kStages) sig_stage = 0;
-      ++signalled;
-    }
-  } else {
-    // ---------------------------------------------------------------- drain (thread = slot)
-    const int ew = warp - 4;
-    const int key = ew * 32 + lane;
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- drain
+    // Eight warps: warp w reads TMEM lanes (slots) 32*(w%4) .. +31 and one
+    // half of the chunk's columns.  Each 32-column slice is transposed through
+    // a per-warp shared buffer so that one reduction instruction covers four
+    // key rows x 128 contiguous bytes.
+    const int q = warp & 3;
+    const int half = (warp - 4) >> 2;
+    const int key = q * 32 + lane;
+    float* stg = sStg + (warp - 4) * 32 * kStgRow;
     int tcount = 0;
     for (int item = blockIdx.x; item < nitems && !abort_flag; item += gridDim.x) {
       const int tl = item / kChunks, ch = item % kChunks;
-      const int t = p.tok0 + tl;
-      const TokMeta m = p.meta[t];
       int ncol, col0;
       chunk_geom(ch, ncol, col0);
+      const int cbeg = half * (ncol / 2), cend = cbeg + ncol / 2;
       for (int kt = 0; kt < ntiles; ++kt, ++tcount) {
         const int set = tcount & 1;
         const int slot = kt * kKeys + key;
-        const int row = slot_row(p, m, t, slot);
-        if (!mbar_wait(&tfull_bar[set], (tcount >> 1) & 1, &abort_flag, gerr)) break;
+        const int row = p.rowtab[(size_t)tl * p.Kpad + slot];
+        const bool ok = mbar_wait(&tfull_bar[set], (tcount >> 1) & 1, &abort_flag, gerr);
+        if (!__all_sync(0xffffffffu, ok)) break;
         tc_fence_after();
-        const uint32_t td = tbase + set * 256 + ((uint32_t)(ew * 32) << 16);
-        float* dst;
-        if (DET) dst = partials + ((size_t)tl * p.Kpad + slot) * kAccRow + col0;
-        else dst = acc + (size_t)(row < 0 ? 0 : row) * kAccRow + col0;
-        for (int c = 0; c < ncol; c += 32) {
+        const uint32_t td = tbase + set * 256 + ((uint32_t)(q * 32) << 16);
+        for (int c = cbeg; c < cend; c += 32) {
           float v[32];
           tmem_ld32(td + c, v);
-          if (DET) {
-            float4* d4 = reinterpret_cast<float4*>(dst + c);
+          float4* mine = reinterpret_cast<float4*>(stg + lane * kStgRow);
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-              d4[u] = row >= 0 ? make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3])
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-          } else if (row >= 0) {
+          for (int u = 0; u < 8; ++u) mine[u] = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+          __syncwarp();
 #pragma unroll
-            for (int u = 0; u < 8; ++u) red_add_v4(dst + c + 4 * u, v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+          for (int rr = 0; rr < 8; ++rr) {
+            const int rl = rr * 4 + (lane >> 3), c4 = lane & 7;
+            const float4 x = reinterpret_cast<const float4*>(stg + rl * kStgRow)[c4];
+            const int grow = __shfl_sync(0xffffffffu, row, rl);
+            if (DET) {
+              float* dst = partials + ((size_t)tl * p.Kpad + kt * kKeys + q * 32 + rl) * kAccRow + col0 + c + c4 * 4;
+              *reinterpret_cast<float4*>(dst) = grow >= 0 ? x : make_float4(0.f, 0.f, 0.f, 0.f);
+            } else if (grow >= 0) {
+              red_add_v4(acc + (size_t)grow * kAccRow + col0 + c + c4 * 4, x.x, x.y, x.z, x.w);
+            }
           }
+          __syncwarp();
         }
         tc_fence_before();
         mbar_arrive(&tempty_bar[set]);
@@ -229,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1) dkv_kernel(Prob p, const T* Pst, 
 }
 
 template <typename T, int GP>
-cudaError_t launch_gp(const Prob& p, const void* P, const void* dS, float* acc, float* partials, int* gerr, int nsm,
+cudaError_t launch_gp(const Maps& maps, const Prob& p, float* acc, float* partials, int* gerr, int nsm,
                       cudaStream_t st) {
   const int smem = DkvSmem<GP>::kBytes > kOneCtaSmem ? DkvSmem<GP>::kBytes : kOneCtaSmem;
   const int nitems = p.ntok * kChunks;
@@ -239,12 +230,12 @@ cudaError_t launch_gp(const Prob& p, const void* P, const void* dS, float* acc, 
     auto kern = dkv_kernel<T, GP, true>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, smem, st>>>(p, static_cast<const T*>(P), static_cast<const T*>(dS), acc, partials, gerr);
+    kern<<<grid, kThreads, smem, st>>>(maps, p, acc, partials, gerr);
   } else {
     auto kern = dkv_kernel<T, GP, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, smem, st>>>(p, static_cast<const T*>(P), static_cast<const T*>(dS), acc, partials, gerr);
+    kern<<<grid, kThreads, smem, st>>>(maps, p, acc, partials, gerr);
   }
   return cudaGetLastError();
 }
@@ -252,14 +243,13 @@ cudaError_t launch_gp(const Prob& p, const void* P, const void* dS, float* acc, 
 }  // namespace
 
 template <typename T>
-cudaError_t launch_dkv(const Prob& p, const void* P, const void* dS, float* acc, float* partials, int* gerr, int nsm,
+cudaError_t launch_dkv(const Maps& maps, const Prob& p, float* acc, float* partials, int* gerr, int nsm,
                        cudaStream_t st) {
-  if (p.Gp == 64) return launch_gp<T, 64>(p, P, dS, acc, partials, gerr, nsm, st);
-  return launch_gp<T, 128>(p, P, dS, acc, partials, gerr, nsm, st);
+  if (p.Gp == 64) return launch_gp<T, 64>(maps, p, acc, partials, gerr, nsm, st);
+  return launch_gp<T, 128>(maps, p, acc, partials, gerr, nsm, st);
 }
 
-template cudaError_t launch_dkv<__nv_bfloat16>(const Prob&, const void*, const void*, float*, float*, int*, int,
-                                               cudaStream_t);
-template cudaError_t launch_dkv<__half>(const Prob&, const void*, const void*, float*, float*, int*, int, cudaStream_t);
+template cudaError_t launch_dkv<__nv_bfloat16>(const Maps&, const Prob&, float*, float*, int*, int, cudaStream_t);
+template cudaError_t launch_dkv<__half>(const Maps&, const Prob&, float*, float*, int*, int, cudaStream_t);
 
 }  // namespace sfa

@@ -16,8 +16,7 @@ namespace sfa {
 namespace {
 
 constexpr int kSlots = 64;         // keys per pipeline stage (MMA K extent)
-constexpr int kStages = 4;
-constexpr int kProducerWarps = 3;
+constexpr int kStages = 3;        // stage slots = producer warps 1-3
 constexpr int kThreads = 256;
 
 template <int NCOL>
@@ -29,7 +28,8 @@ struct DqSmem {
 };
 
 template <typename T, int GP, int MODE>
-__global__ void __launch_bounds__(kThreads, 1) dq_kernel(Prob p, const T* Ast, T* out_main, T* out_rope, int* gerr) {
+__global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__ Maps maps, Prob p, T* out_main, T* out_rope,
+                                                         int* gerr) {
   using E = Elt<T>;
   constexpr int NCOL = MODE == 0 ? 192 : 256;
   constexpr int NPART = MODE == 0 ? 3 : 2;
@@ -39,6 +39,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(Prob p, const T* Ast, T
   __shared__ uint64_t full_bar[kStages], empty_bar[kStages], tfull_bar[2], tempty_bar[2];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
+  __shared__ __align__(16) int rows_s[kStages][kSlots];   // read and written as int2
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nchunks = p.Kpad / kSlots;
@@ -54,7 +55,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(Prob p, const T* Ast, T
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&full_bar[i], kProducerWarps * 32);
+      mbar_init(&full_bar[i], 32 + 1);   // the owning warp's lanes + the TMA transaction arrive
       mbar_init(&empty_bar[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -73,93 +74,85 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(Prob p, const T* Ast, T
   if (warp == 0) {
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(128, NCOL, E::is_f16, true, true);
-      int stage = 0, it = 0;
-      uint32_t phase = 0;
-      for (int item = blockIdx.x; item < nitems && !abort_flag; item += gridDim.x, ++it) {
+      int it = 0, g = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++it) {
         const int set = it & 1;
-        if (!mbar_wait(&tempty_bar[set], ((it >> 1) & 1) ^ 1, &abort_flag, gerr)) break;
+        ok = mbar_wait(&tempty_bar[set], ((it >> 1) & 1) ^ 1, &abort_flag, gerr);
+        if (!ok) break;
         tc_fence_after();
         const uint32_t d = tbase + set * 256;
-        for (int c = 0; c < nchunks; ++c) {
-          if (!mbar_wait(&full_bar[stage], phase, &abort_flag, gerr)) break;
+        for (int c = 0; c < nchunks; ++c, ++g) {
+          const int slot = g % kStages;
+          ok = mbar_wait(&full_bar[slot], (g / kStages) & 1, &abort_flag, gerr);
+          if (!ok) break;
           tc_fence_after();
-          const uint32_t a = smem_u32(smem + stage * S::kStage);
+          const uint32_t a = smem_u32(smem + slot * S::kStage);
           const uint32_t b = a + S::kA;
 #pragma unroll
           for (int ks = 0; ks < kSlots / 16; ++ks)
             mma_ss(d, sdesc_mnmajor(a, ks, kSlots), sdesc_mnmajor(b, ks, kSlots), idesc, (c == 0 && ks == 0) ? 0u : 1u);
-          mma_commit(&empty_bar[stage]);
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
+          mma_commit(&empty_bar[slot]);
         }
+        if (!ok) break;
         mma_commit(&tfull_bar[set]);
       }
     }
     __syncwarp();
-  } else if (warp <= kProducerWarps) {
-    const int pt = threadIdx.x - 32;
-    constexpr int kNP = kProducerWarps * 32;
+  } else if (warp <= kStages) {
+    // ---------------------------------------------------------------- producers
+    // Warp w owns stage slot w-1 and takes every third stage of 64 keys: the
+    // staged dS^T (or P^T) rows as one TMA box per 64-head panel, and the
+    // keys' feature rows gathered by cp.async (NCOL contiguous features per
+    // row).  The warp waits only for its own copies, then fences them for the
+    // tensor core and arrives.
     constexpr int kHP = GP / 64;
-    constexpr int kFP = NCOL / 64;
-    const T* k = static_cast<const T*>(MODE == 0 ? p.k : p.v);
-    const T* kr = static_cast<const T*>(p.kr);
-    int stage = 0, issued = 0, signalled = 0, sig_stage = 0;
-    uint32_t phase = 0;
-    constexpr int kLag = 2;
-    for (int item = blockIdx.x; item < nitems && !abort_flag; item += gridDim.x) {
+    constexpr int kCpr = NCOL / 8;            // 16-byte pieces per gathered row
+    const int me = warp - 1;
+    const CUtensorMap* mA = MODE == 0 ? &maps.dS : &maps.P;
+    const T* kmain = static_cast<const T*>(MODE == 0 ? p.k : p.v);
+    const T* krope = static_cast<const T*>(p.kr);
+    const uint32_t a = smem_u32(smem + me * S::kStage);
+    const uint32_t b = a + S::kA;
+    int* rows = rows_s[me];
+    int g = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
       const int tl = item / NPART, part = item % NPART;
-      const int t = p.tok0 + tl;
-      const TokMeta m = p.meta[t];
       const int f0 = part * NCOL;
-      for (int c = 0; c < nchunks; ++c) {
-        if (!mbar_wait(&empty_bar[stage], phase ^ 1, &abort_flag, gerr)) break;
-        const uint32_t a = smem_u32(smem + stage * S::kStage);
-        const uint32_t b = a + S::kA;
-        const T* tile = Ast + ((size_t)tl * p.Kpad + (size_t)c * kSlots) * GP;
-        // A: stored rows [slot][GP heads] -> MN-major head panels
-        for (int r = pt; r < kSlots * kHP; r += kNP) {
-          const int s = r % kSlots, hp = r / kSlots;
-          const T* src = tile + (size_t)s * GP + hp * 64;
-          const uint32_t dst = a + hp * (kSlots * 128);
-#pragma unroll
-          for (int cc = 0; cc < 8; ++cc) cp_async16(dst + swz_chunk(s, cc), src + cc * 8, 16u);
+      for (int c = 0; c < nchunks; ++c, ++g) {
+        if (g % kStages != me) continue;
+        const int2 r2 = *reinterpret_cast<const int2*>(p.rowtab + (size_t)tl * p.Kpad + c * kSlots + 2 * lane);
+        if (lane == 0) ok = mbar_wait(&empty_bar[me], ((g / kStages) & 1) ^ 1, &abort_flag, gerr);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        *reinterpret_cast<int2*>(rows + 2 * lane) = r2;
+        __syncwarp();
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_expect_tx(&full_bar[me], kHP * kSlots * 128);
+          for (int hp = 0; hp < kHP; ++hp)
+            tma_2d(a + hp * (kSlots * 128), mA, hp * 64, tl * p.Kpad + c * kSlots, &full_bar[me]);
         }
-        // B: gathered key rows -> MN-major feature panels
-        for (int r = pt; r < kSlots * kFP; r += kNP) {
-          const int s = r % kSlots, fp = r / kSlots;
-          const int row = slot_row(p, m, t, c * kSlots + s);
-          const int f = f0 + fp * 64;
+        for (int e = lane; e < kSlots * kCpr; e += 32) {
+          const int r = e / kCpr, cc = e - r * kCpr;
+          const int row = rows[r];
+          const int f = f0 + cc * 8;
           const T* src;
           uint32_t nb = row >= 0 ? 16u : 0u;
-          const int rr = row < 0 ? 0 : row;
-          if (MODE == 1 || f < 512) src = k + (size_t)rr * 512 + f;
-          else {
-            src = p.has_rope ? kr + (size_t)rr * 64 + (f - 512) : k;
-            if (!p.has_rope) nb = 0u;
-          }
-          const uint32_t dst = b + fp * (kSlots * 128);
-#pragma unroll
-          for (int cc = 0; cc < 8; ++cc) cp_async16(dst + swz_chunk(s, cc), src + cc * 8, nb);
+          const size_t rr = (size_t)(row < 0 ? 0 : row);
+          if (MODE == 1 || f < 512) src = kmain + rr * 512 + f;
+          else if (p.has_rope) src = krope + rr * 64 + (f - 512);
+          else { src = kmain; nb = 0u; }
+          cp_async16(b + (cc >> 3) * (kSlots * 128) + swz_chunk(r, cc & 7), src, nb);
         }
         cp_async_commit();
-        ++issued;
-        if (issued - signalled > kLag) {
-          cp_async_wait<kLag>();
-          fence_async_smem();
-          mbar_arrive(&full_bar[sig_stage]);
-          if (++sig_stage == kStages) sig_stage = 0;
-          ++signalled;
-        }
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
+        cp_async_wait<0>();
+        fence_async_smem();
+        mbar_arrive(&full_bar[me]);
+        __syncwarp();
       }
     }
-    cp_async_wait<0>();
-    fence_async_smem();
-    while (signalled < issued) {
-      mbar_arrive(&full_bar[sig_stage]);
-      if (++sig_stage == kStages) sig_stage = 0;
-      ++signalled;
-    }
-  } else {
+  } else if (warp >= 4) {
     // ---------------------------------------------------------------- epilogue (thread = head)
     const int ew = warp - 4;
     const int h = ew * 32 + lane;
@@ -168,7 +161,8 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(Prob p, const T* Ast, T
       const int set = it & 1;
       const int tl = item / NPART, part = item % NPART;
       const int t = p.tok0 + tl;
-      if (!mbar_wait(&tfull_bar[set], (it >> 1) & 1, &abort_flag, gerr)) break;
+      const bool ok = mbar_wait(&tfull_bar[set], (it >> 1) & 1, &abort_flag, gerr);
+      if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const uint32_t td = tbase + set * 256 + ((uint32_t)(ew * 32) << 16);
       for (int c = 0; c < NCOL; c += 32) {
@@ -202,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(Prob p, const T* Ast, T
 }
 
 template <typename T, int GP, int MODE>
-cudaError_t launch_one(const Prob& p, const void* A, void* o1, void* o2, int* gerr, int nsm, cudaStream_t st) {
+cudaError_t launch_one(const Maps& maps, const Prob& p, void* o1, void* o2, int* gerr, int nsm, cudaStream_t st) {
   constexpr int NCOL = MODE == 0 ? 192 : 256;
   constexpr int NPART = MODE == 0 ? 3 : 2;
   auto kern = dq_kernel<T, GP, MODE>;
@@ -212,23 +206,23 @@ cudaError_t launch_one(const Prob& p, const void* A, void* o1, void* o2, int* ge
   const int nitems = p.ntok * NPART;
   const int grid = nitems < nsm ? nitems : nsm;
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, kThreads, smem, st>>>(p, static_cast<const T*>(A), static_cast<T*>(o1), static_cast<T*>(o2), gerr);
+  kern<<<grid, kThreads, smem, st>>>(maps, p, static_cast<T*>(o1), static_cast<T*>(o2), gerr);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 template <typename T>
-cudaError_t launch_dq(const Prob& p, int mode, const void* A, void* out_main, void* out_rope, int* gerr, int nsm,
+cudaError_t launch_dq(const Maps& maps, const Prob& p, int mode, void* out_main, void* out_rope, int* gerr, int nsm,
                       cudaStream_t st) {
   if (p.Gp == 64)
-    return mode == 0 ? launch_one<T, 64, 0>(p, A, out_main, out_rope, gerr, nsm, st)
-                     : launch_one<T, 64, 1>(p, A, out_main, out_rope, gerr, nsm, st);
-  return mode == 0 ? launch_one<T, 128, 0>(p, A, out_main, out_rope, gerr, nsm, st)
-                   : launch_one<T, 128, 1>(p, A, out_main, out_rope, gerr, nsm, st);
+    return mode == 0 ? launch_one<T, 64, 0>(maps, p, out_main, out_rope, gerr, nsm, st)
+                     : launch_one<T, 64, 1>(maps, p, out_main, out_rope, gerr, nsm, st);
+  return mode == 0 ? launch_one<T, 128, 0>(maps, p, out_main, out_rope, gerr, nsm, st)
+                   : launch_one<T, 128, 1>(maps, p, out_main, out_rope, gerr, nsm, st);
 }
 
-template cudaError_t launch_dq<__nv_bfloat16>(const Prob&, int, const void*, void*, void*, int*, int, cudaStream_t);
-template cudaError_t launch_dq<__half>(const Prob&, int, const void*, void*, void*, int*, int, cudaStream_t);
+template cudaError_t launch_dq<__nv_bfloat16>(const Maps&, const Prob&, int, void*, void*, int*, int, cudaStream_t);
+template cudaError_t launch_dq<__half>(const Maps&, const Prob&, int, void*, void*, int*, int, cudaStream_t);
 
 }  // namespace sfa

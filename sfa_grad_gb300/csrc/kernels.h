@@ -10,22 +10,23 @@ constexpr int kModeFwdP = 2;      // S -> P from final statistics
 
 // Score / softmax-gradient kernel (sdp.cu).
 template <typename T>
-cudaError_t launch_sdp(const Prob& p, int mode, void* out_p, void* out_ds, float* tile_stats, int* gerr, int nsm,
+cudaError_t launch_sdp(const Maps& maps, const Prob& p, int mode, void* out_p, void* out_ds, float* tile_stats, int* gerr, int nsm,
                        cudaStream_t st);
 
 // Key-side gradients (dkv.cu): dV = P^T dO, [dK || dKRope] = dS^T [q || qRope],
 // reduced into the fp32 accumulator acc (T2 x 1088) with atomics, or written
 // as per-(token, slot) partial rows when `partials` is non-null.
 template <typename T>
-cudaError_t launch_dkv(const Prob& p, const void* P, const void* dS, float* acc, float* partials, int* gerr, int nsm,
+cudaError_t launch_dkv(const Maps& maps, const Prob& p, float* acc, float* partials, int* gerr, int nsm,
                        cudaStream_t st);
 
 // Query-side contraction (dq.cu): dQ = dS K (mode 0) or O = P V (mode 1).
 template <typename T>
-cudaError_t launch_dq(const Prob& p, int mode, const void* A, void* out_main, void* out_rope, int* gerr, int nsm,
+cudaError_t launch_dq(const Maps& maps, const Prob& p, int mode, void* out_main, void* out_rope, int* gerr, int nsm,
                       cudaStream_t st);
 
 // Small kernels (prep.cu).
+cudaError_t launch_rowtab(const Prob& p, cudaStream_t st);
 cudaError_t launch_batch_prefix(const Prob& p, int B, const int* act_q, const int* act_kv, int* batch_ofs, int* gerr,
                                 cudaStream_t st);
 cudaError_t launch_meta(const Prob& p, int layout, int B, int S1, int S2, int mode, const int* act_q, const int* act_kv,

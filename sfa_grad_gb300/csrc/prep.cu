@@ -79,6 +79,17 @@ __global__ void meta_kernel(int layout, int T1, int B, int S1, int S2, int mode,
   meta[t] = TokMeta{kv_start, (int)lim};
 }
 
+// Row table of a token chunk: the kv row each (token, slot) reads, -1 if the
+// slot is masked (功能说明 gather with block expansion; Mask table).
+__global__ void rowtab_kernel(Prob p) {
+  const long long n = (long long)p.ntok * p.Kpad;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const int tl = (int)(i / p.Kpad), s = (int)(i - (long long)tl * p.Kpad);
+    const int t = p.tok0 + tl;
+    p.rowtab[i] = slot_row(p, p.meta[t], t, s);
+  }
+}
+
 // One warp per (token, head) row of 512 elements.
 template <typename T>
 __global__ void dsum_kernel(const T* dO, const T* out, int rows, float* dsum) {
@@ -156,6 +167,15 @@ cudaError_t launch_meta(const Prob& p, int layout, int B, int S1, int S2, int mo
                         int* batch_ofs, TokMeta* meta, int* gerr, cudaStream_t st) {
   (void)gerr;
   if (p.T1 > 0) meta_kernel<<<(p.T1 + 255) / 256, 256, 0, st>>>(layout, p.T1, B, S1, S2, mode, batch_ofs, act_q, act_kv, meta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rowtab(const Prob& p, cudaStream_t st) {
+  const long long n = (long long)p.ntok * p.Kpad;
+  if (n == 0) return cudaSuccess;
+  long long blocks = (n + 255) / 256;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  rowtab_kernel<<<(int)blocks, 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 

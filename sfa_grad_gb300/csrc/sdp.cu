@@ -9,6 +9,13 @@
 // contractions.  Forward modes reuse the score half: per-tile max/sum partials,
 // or P from final statistics.
 //
+// Pipeline: the contraction runs in stages of 128 features (64 for the rope
+// part).  Gathered key/value rows arrive by cp.async, 256 contiguous bytes per
+// row per stage (scattered 128-byte pieces halve the achievable gather rate);
+// three producer warps each own one shared-memory stage slot and take every
+// third stage, so up to three stages are in flight while each warp waits only
+// for its own copies.  The token's head rows (the other operand) arrive by TMA.
+//
 // aclnnSparseFlashAttentionGrad doc, 功能说明 (gather by topkIndices) and
 // 阶段1/阶段2 (dP, dS); MindSpore flash_attention_bwd.py, compute_Pij
 // (P from saved max and sum) and compute_dSij.
@@ -19,44 +26,61 @@ namespace sfa {
 
 namespace {
 
-constexpr int kKeys = 128;          // keys per work item (MMA M)
-constexpr int kStages = 5;
-constexpr int kProducerWarps = 3;
-constexpr int kThreads = 256;       // warp 0 MMA, 1-3 producers, 4-7 epilogue
+constexpr int kKeys = 128;           // keys per work item (MMA M)
+constexpr int kSlots = 3;            // shared-memory stage slots = producer warps
+constexpr int kEpiThreads = 256;     // warps 4-11
+constexpr int kThreads = 128 + kEpiThreads;  // warp 0 MMA, 1-3 producers, 4-11 epilogue
 
 template <int GP>
 struct SdpSmem {
-  static constexpr int kA = kKeys * 128;   // one 64-wide panel of 128 key rows
-  static constexpr int kB = GP * 128;      // one 64-wide panel of GP head rows
-  static constexpr int kStage = kA + kB;
-  static constexpr int kBytes = kStages * kStage + 1024;  // + alignment slack
+  static constexpr int kPanelA = kKeys * 128;   // 64 features x 128 key rows
+  static constexpr int kPanelB = GP * 128;      // 64 features x GP head rows
+  static constexpr int kA = 2 * kPanelA;
+  static constexpr int kSlot = kA + 2 * kPanelB;
+  static constexpr int kBytes = kSlots * kSlot + 1024;  // + alignment slack
 };
 
+// Stage c of an item: first source feature, 64-wide panel count, tensors.
+struct Chunk {
+  int f0;
+  int npan;    // 2, or 1 for the rope part
+  int kind;    // 0: k / q, 1: kRope / qRope, 2: v / dO
+};
+__device__ __forceinline__ Chunk chunk_of(int c, int nS) {
+  if (c < 4) return Chunk{c * 128, 2, 0};
+  if (c < nS) return Chunk{0, 1, 1};
+  return Chunk{(c - nS) * 128, 2, 2};
+}
+
 template <typename T, int GP, int MODE>
-__global__ void __launch_bounds__(kThreads, 1) sdp_kernel(Prob p, void* out_p, void* out_ds, float* tile_stats, int* gerr) {
+__global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant__ Maps maps, Prob p, void* out_p, void* out_ds,
+                                                          float* tile_stats, int* gerr) {
   using E = Elt<T>;
+  using S = SdpSmem<GP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t full_bar[kStages], empty_bar[kStages], tfull_bar[2], tempty_bar[2];
+  __shared__ uint64_t full_bar[kSlots], empty_bar[kSlots], tfull_bar[2], tempty_bar[2];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ float red_buf[4][GP][2];
+  __shared__ float stats_s[2][3 * GP];
+  __shared__ __align__(16) int rows_s[kSlots][kKeys];   // read and written as int4
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool bwd = (MODE == kModeBwd);
-  const int nS = p.has_rope ? 9 : 8;           // 64-wide chunks of the score contraction
-  const int nchunks = bwd ? nS + 8 : nS;      // + 8 chunks of dP
+  const int nS = p.has_rope ? 5 : 4;           // stages of the score contraction
+  const int nchunks = bwd ? nS + 4 : nS;      // + 4 stages of dP
   const int ntiles = p.Kpad / kKeys;
   const int nitems = p.ntok * ntiles;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&full_bar[i], kProducerWarps * 32);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&full_bar[i], 32 + 1);   // the owning warp's lanes + the TMA transaction arrive
       mbar_init(&empty_bar[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull_bar[i], 1);
-      mbar_init(&tempty_bar[i], 128);
+      mbar_init(&tempty_bar[i], kEpiThreads);
     }
     abort_flag = 0;
     mbar_fence_init();
@@ -71,210 +95,195 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(Prob p, void* out_p, v
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(kKeys, GP, E::is_f16, false, false);
-      int stage = 0;
-      uint32_t phase = 0;
-      int it = 0;
-      for (int item = blockIdx.x; item < nitems && !abort_flag; item += gridDim.x, ++it) {
+      int it = 0, g = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++it) {
         const int set = it & 1;
-        const uint32_t tph = (it >> 1) & 1;
-        if (!mbar_wait(&tempty_bar[set], tph ^ 1, &abort_flag, gerr)) break;
+        ok = mbar_wait(&tempty_bar[set], ((it >> 1) & 1) ^ 1, &abort_flag, gerr);
+        if (!ok) break;
         tc_fence_after();
         const uint32_t tS = tbase + set * (2 * GP);
         const uint32_t tP = tS + GP;
-        for (int c = 0; c < nchunks; ++c) {
-          if (!mbar_wait(&full_bar[stage], phase, &abort_flag, gerr)) break;
+        for (int c = 0; c < nchunks; ++c, ++g) {
+          const int slot = g % kSlots;
+          ok = mbar_wait(&full_bar[slot], (g / kSlots) & 1, &abort_flag, gerr);
+          if (!ok) break;
           tc_fence_after();
-          const uint32_t a = smem_u32(smem + stage * SdpSmem<GP>::kStage);
-          const uint32_t b = a + SdpSmem<GP>::kA;
+          const Chunk ck = chunk_of(c, nS);
+          const uint32_t a = smem_u32(smem + slot * S::kSlot);
+          const uint32_t b = a + S::kA;
           const uint32_t d = c < nS ? tS : tP;
           const bool first = (c == 0 || c == nS);
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_ss(d, sdesc_kmajor(a, ks), sdesc_kmajor(b, ks), idesc, (first && ks == 0) ? 0u : 1u);
-          mma_commit(&empty_bar[stage]);
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
+          for (int ks = 0; ks < ck.npan * 4; ++ks)
+            mma_ss(d, sdesc_kmajor(a + (ks >> 2) * S::kPanelA, ks & 3), sdesc_kmajor(b + (ks >> 2) * S::kPanelB, ks & 3),
+                   idesc, (first && ks == 0) ? 0u : 1u);
+          mma_commit(&empty_bar[slot]);
         }
+        if (!ok) break;
         mma_commit(&tfull_bar[set]);
       }
     }
     __syncwarp();
-  } else if (warp <= kProducerWarps) {
-    // ---------------------------------------------------------------- producers (cp.async gathers)
-    const int pt = threadIdx.x - 32;          // 0 .. 95
-    constexpr int kNP = kProducerWarps * 32;
-    constexpr int kRows = kKeys + GP;         // rows per stage
-    constexpr int kMine = (kRows + kNP - 1) / kNP;
-    const T* q = static_cast<const T*>(p.q);
-    const T* qr = static_cast<const T*>(p.qr);
+  } else if (warp <= kSlots) {
+    // ---------------------------------------------------------------- producers
+    const int me = warp - 1;                  // owned stage slot
     const T* k = static_cast<const T*>(p.k);
     const T* kr = static_cast<const T*>(p.kr);
     const T* v = static_cast<const T*>(p.v);
-    const T* dO = static_cast<const T*>(p.dO);
-    int stage = 0;
-    uint32_t phase = 0;
-    int issued = 0, signalled = 0;
-    int sig_stage = 0;
-    constexpr int kLag = 2;
-    for (int item = blockIdx.x; item < nitems && !abort_flag; item += gridDim.x) {
+    const uint32_t a = smem_u32(smem + me * S::kSlot);
+    const uint32_t b = a + S::kA;
+    int* rows = rows_s[me];
+    int g = 0, loaded_item = -1;
+    bool ok = true;
+    for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
       const int tl = item / ntiles, kt = item % ntiles;
       const int t = p.tok0 + tl;
-      const TokMeta m = p.meta[t];
-      int rowid[kMine];   // >= 0: kv row (A) ; for B rows: head index ; -1: zero fill
-#pragma unroll
-      for (int i = 0; i < kMine; ++i) {
-        const int r = pt + i * kNP;
-        if (r < kKeys) rowid[i] = slot_row(p, m, t, kt * kKeys + r);
-        else if (r < kRows) rowid[i] = (r - kKeys) < p.G ? (r - kKeys) : -1;
-        else rowid[i] = -1;
-      }
-      for (int c = 0; c < nchunks; ++c) {
-        if (!mbar_wait(&empty_bar[stage], phase ^ 1, &abort_flag, gerr)) break;
-        const uint32_t a = smem_u32(smem + stage * SdpSmem<GP>::kStage);
-        const uint32_t b = a + SdpSmem<GP>::kA;
-#pragma unroll
-        for (int i = 0; i < kMine; ++i) {
-          const int r = pt + i * kNP;
-          if (r >= kRows) continue;
-          const T* src;
-          uint32_t dst;
-          const int id = rowid[i];
-          if (r < kKeys) {
-            dst = a;
-            const int rr = id < 0 ? 0 : id;
-            if (c < 8) src = k + (size_t)rr * 512 + c * 64;
-            else if (c < nS) src = kr + (size_t)rr * 64;
-            else src = v + (size_t)rr * 512 + (c - nS) * 64;
-          } else {
-            const int h = r - kKeys;
-            dst = b;
-            const size_t tok = (size_t)t * p.G + (id < 0 ? 0 : id);
-            if (c < 8) src = q + tok * 512 + c * 64;
-            else if (c < nS) src = qr + tok * 64;
-            else src = dO + tok * 512 + (c - nS) * 64;
-          }
-          const uint32_t nb = id < 0 ? 0u : 16u;
-          const uint32_t row = (r < kKeys) ? r : (r - kKeys);
-#pragma unroll
-          for (int cc = 0; cc < 8; ++cc) cp_async16(dst + swz_chunk(row, cc), src + cc * 8, nb);
+      for (int c = 0; c < nchunks; ++c, ++g) {
+        if (g % kSlots != me) continue;
+        if (loaded_item != item) {   // the item's 128 kv rows (-1: masked)
+          const int4 r4 = *reinterpret_cast<const int4*>(p.rowtab + (size_t)tl * p.Kpad + kt * kKeys + 4 * lane);
+          *reinterpret_cast<int4*>(rows + 4 * lane) = r4;
+          loaded_item = item;
+        }
+        if (lane == 0) ok = mbar_wait(&empty_bar[me], ((g / kSlots) & 1) ^ 1, &abort_flag, gerr);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        __syncwarp();
+        if (!ok) break;
+        const Chunk ck = chunk_of(c, nS);
+        if (lane == 0) {
+          mbar_expect_tx(&full_bar[me], ck.npan * S::kPanelB);
+          const CUtensorMap* mq = ck.kind == 0 ? &maps.q : ck.kind == 1 ? &maps.qr : &maps.dO;
+          for (int pn = 0; pn < ck.npan; ++pn) tma_2d(b + pn * S::kPanelB, mq, ck.f0 + pn * 64, t * p.G, &full_bar[me]);
+        }
+        // gathered rows: 8 * npan 16-byte pieces per row, contiguous in global memory
+        const T* base = ck.kind == 0 ? k : ck.kind == 1 ? kr : v;
+        const int rlen = ck.kind == 1 ? 64 : 512;
+        const int cpr = ck.npan * 8;
+        for (int e = lane; e < kKeys * cpr; e += 32) {
+          const int r = e / cpr, cc = e - r * cpr;
+          const int row = rows[r];
+          const T* src = base + (size_t)(row < 0 ? 0 : row) * rlen + ck.f0 + cc * 8;
+          cp_async16(a + (cc >> 3) * S::kPanelA + swz_chunk(r, cc & 7), src, row < 0 ? 0u : 16u);
         }
         cp_async_commit();
-        ++issued;
-        if (issued - signalled > kLag) {
-          cp_async_wait<kLag>();
-          fence_async_smem();
-          mbar_arrive(&full_bar[sig_stage]);
-          if (++sig_stage == kStages) sig_stage = 0;
-          ++signalled;
-        }
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
+        cp_async_wait<0>();
+        fence_async_smem();
+        mbar_arrive(&full_bar[me]);
       }
     }
-    cp_async_wait<0>();
-    fence_async_smem();
-    while (signalled < issued) {
-      mbar_arrive(&full_bar[sig_stage]);
-      if (++sig_stage == kStages) sig_stage = 0;
-      ++signalled;
-    }
-  } else {
-    // ---------------------------------------------------------------- epilogue (thread = key)
-    const int ew = warp - 4;              // TMEM lane quadrant
-    const int key = ew * 32 + lane;
-    const float log2e = 1.4426950408889634f;
-    const float sl2 = p.scale * log2e;
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- epilogue
+    // Eight warps: warp w reads TMEM lanes (keys) 32*(w%4) .. +31 and the
+    // head half (w-4)/4, i.e. heads [half*GP/2, (half+1)*GP/2).  Named
+    // barriers between these warps run every item, so the trip count never
+    // depends on the abort flag: an abandoned wait only skips the item's work.
+    const int q = warp & 3;
+    const int half = (warp - 4) >> 2;
+    const int key = q * 32 + lane;
+    const int etid = threadIdx.x - 128;
+    constexpr int HH = GP / 2;
+    const float sl2 = p.scale * kLog2e;
     int it = 0;
-    // The forward-statistics path uses named barriers between the four
-    // epilogue warps, so its trip count never depends on the abort flag: an
-    // abandoned wait only skips the work of the item.
-    for (int item = blockIdx.x; item < nitems && (MODE == kModeFwdStats || !abort_flag); item += gridDim.x, ++it) {
+    for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++it) {
       const int set = it & 1;
       const uint32_t tph = (it >> 1) & 1;
       const int tl = item / ntiles, kt = item % ntiles;
       const int t = p.tok0 + tl;
       const int slot = kt * kKeys + key;
-      const int row = slot_row(p, p.meta[t], t, slot);
-      const bool valid = row >= 0;
-      const bool ok = !abort_flag && mbar_wait(&tfull_bar[set], tph, &abort_flag, gerr);
-      if (!ok && MODE != kModeFwdStats) break;
-      tc_fence_after();
-      const uint32_t tS = tbase + set * (2 * GP) + ((uint32_t)(ew * 32) << 16);
+      const bool valid = p.rowtab[(size_t)tl * p.Kpad + slot] >= 0;
+      float* st = stats_s[it & 1];
+      if (MODE != kModeFwdStats) {
+        // per-head statistics of token t: exponent offset, 1/sum (0 for an
+        // empty row or a padded head) and Dsum * scale
+        for (int h = etid; h < GP; h += kEpiThreads) {
+          float ml = 0.f, il = 0.f, dsc = 0.f;
+          if (h < p.G) {
+            const float l = __ldg(p.ssum + (size_t)t * p.G + h);
+            if (l > 0.f) {
+              ml = __ldg(p.smax + (size_t)t * p.G + h) * kLog2e;
+              il = 1.f / l;
+            }
+            if (bwd) dsc = __ldg(p.dsum + (size_t)t * p.G + h) * p.scale;
+          }
+          st[h] = ml;
+          st[GP + h] = il;
+          st[2 * GP + h] = dsc;
+        }
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+      const bool ok = __all_sync(0xffffffffu, !abort_flag && mbar_wait(&tfull_bar[set], tph, &abort_flag, gerr));
+      if (ok) tc_fence_after();
+      const uint32_t tS = tbase + set * (2 * GP) + ((uint32_t)(q * 32) << 16);
       const uint32_t tP = tS + GP;
-      const float* smax = p.smax + (size_t)t * p.G;
-      const float* ssum = p.ssum + (size_t)t * p.G;
-      const float* dsum = p.dsum + (size_t)t * p.G;
       if (MODE == kModeFwdStats) {
         // per head over the tile's valid keys: max of the raw score s and
         // sum of exp((s - max) * scale)
 #pragma unroll 1
-        for (int hc = 0; hc < GP / 32; ++hc) {
+        for (int c = 0; c < HH / 32; ++c) {
+          const int h0 = half * HH + c * 32;
           float s[32];
-          if (ok) tmem_ld32(tS + hc * 32, s);
+          if (ok) tmem_ld32(tS + h0, s);
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const float x = (valid && ok) ? s[j] : -INFINITY;
             float mx = x;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            float e = (x == -INFINITY) ? 0.f : exp2f((x - mx) * sl2);
+            float e = (x == -INFINITY) ? 0.f : ex2((x - mx) * sl2);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
             if (lane == 0) {
-              red_buf[ew][hc * 32 + j][0] = mx;
-              red_buf[ew][hc * 32 + j][1] = e;
+              red_buf[q][h0 + j][0] = mx;
+              red_buf[q][h0 + j][1] = e;
             }
           }
         }
         tc_fence_before();
         if (ok) mbar_arrive(&tempty_bar[set]);
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (key < p.G) {
+        asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+        if (etid < p.G) {
           float mx = -INFINITY;
-          for (int w = 0; w < 4; ++w) mx = fmaxf(mx, red_buf[w][key][0]);
+          for (int w = 0; w < 4; ++w) mx = fmaxf(mx, red_buf[w][etid][0]);
           float l = 0.f;
           if (mx != -INFINITY)
             for (int w = 0; w < 4; ++w)
-              if (red_buf[w][key][0] != -INFINITY) l += red_buf[w][key][1] * exp2f((red_buf[w][key][0] - mx) * sl2);
-          float* ts = tile_stats + (((size_t)tl * ntiles + kt) * p.G + key) * 2;
+              if (red_buf[w][etid][0] != -INFINITY) l += red_buf[w][etid][1] * ex2((red_buf[w][etid][0] - mx) * sl2);
+          float* ts = tile_stats + (((size_t)tl * ntiles + kt) * p.G + etid) * 2;
           ts[0] = mx;   // raw score (unscaled)
           ts[1] = l;
         }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+        asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
         continue;
       }
+      if (!ok) continue;
       T* prow = static_cast<T*>(out_p) + ((size_t)tl * p.Kpad + slot) * GP;
       T* dsrow = bwd ? static_cast<T*>(out_ds) + ((size_t)tl * p.Kpad + slot) * GP : nullptr;
 #pragma unroll 1
-      for (int hc = 0; hc < GP / 32; ++hc) {
+      for (int c = 0; c < HH / 32; ++c) {
+        const int h0 = half * HH + c * 32;
         float s[32], dp[32];
-        tmem_ld32(tS + hc * 32, s);
-        if (bwd) tmem_ld32(tP + hc * 32, dp);
+        tmem_ld32(tS + h0, s);
+        if (bwd) tmem_ld32(tP + h0, dp);
         uint32_t pk[16], dk[16];
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
           float pv[2], dv[2];
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const int h = hc * 32 + j + u;
-            float pp = 0.f, dd = 0.f;
-            if (valid && h < p.G) {
-              const float l = __ldg(ssum + h);
-              if (l > 0.f) {
-                const float mlog = __ldg(smax + h) * log2e;
-                pp = exp2f(s[j + u] * sl2 - mlog) * (1.0f / l);
-                if (bwd) dd = pp * (dp[j + u] - __ldg(dsum + h)) * p.scale;
-              }
-            }
+            const int h = h0 + j + u;
+            const float x = valid ? fmaf(s[j + u], sl2, -st[h]) : -INFINITY;
+            const float pp = ex2(x) * st[GP + h];
             pv[u] = pp;
-            dv[u] = dd;
+            dv[u] = bwd ? pp * fmaf(dp[j + u], p.scale, -st[2 * GP + h]) : 0.f;
           }
           pk[j / 2] = E::pack(pv[0], pv[1]);
           dk[j / 2] = E::pack(dv[0], dv[1]);
         }
-        uint4* pd = reinterpret_cast<uint4*>(prow + hc * 32);
+        uint4* pd = reinterpret_cast<uint4*>(prow + h0);
 #pragma unroll
         for (int u = 0; u < 4; ++u) pd[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
         if (bwd) {
-          uint4* dd = reinterpret_cast<uint4*>(dsrow + hc * 32);
+          uint4* dd = reinterpret_cast<uint4*>(dsrow + h0);
 #pragma unroll
           for (int u = 0; u < 4; ++u) dd[u] = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
         }
@@ -292,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(Prob p, void* out_p, v
 }
 
 template <typename T, int GP, int MODE>
-cudaError_t launch_one(const Prob& p, void* out_p, void* out_ds, float* tile_stats, int* gerr, int nsm,
+cudaError_t launch_one(const Maps& maps, const Prob& p, void* out_p, void* out_ds, float* tile_stats, int* gerr, int nsm,
                        cudaStream_t st) {
   auto kern = sdp_kernel<T, GP, MODE>;
   const int smem = SdpSmem<GP>::kBytes > kOneCtaSmem ? SdpSmem<GP>::kBytes : kOneCtaSmem;
@@ -301,26 +310,26 @@ cudaError_t launch_one(const Prob& p, void* out_p, void* out_ds, float* tile_sta
   const int nitems = p.ntok * (p.Kpad / kKeys);
   const int grid = nitems < nsm ? nitems : nsm;
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, kThreads, smem, st>>>(p, out_p, out_ds, tile_stats, gerr);
+  kern<<<grid, kThreads, smem, st>>>(maps, p, out_p, out_ds, tile_stats, gerr);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 template <typename T>
-cudaError_t launch_sdp(const Prob& p, int mode, void* out_p, void* out_ds, float* tile_stats, int* gerr, int nsm,
+cudaError_t launch_sdp(const Maps& maps, const Prob& p, int mode, void* out_p, void* out_ds, float* tile_stats, int* gerr, int nsm,
                        cudaStream_t st) {
   if (p.Gp == 64) {
-    if (mode == kModeBwd) return launch_one<T, 64, kModeBwd>(p, out_p, out_ds, tile_stats, gerr, nsm, st);
-    if (mode == kModeFwdStats) return launch_one<T, 64, kModeFwdStats>(p, out_p, out_ds, tile_stats, gerr, nsm, st);
-    return launch_one<T, 64, kModeFwdP>(p, out_p, out_ds, tile_stats, gerr, nsm, st);
+    if (mode == kModeBwd) return launch_one<T, 64, kModeBwd>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
+    if (mode == kModeFwdStats) return launch_one<T, 64, kModeFwdStats>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
+    return launch_one<T, 64, kModeFwdP>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
   }
-  if (mode == kModeBwd) return launch_one<T, 128, kModeBwd>(p, out_p, out_ds, tile_stats, gerr, nsm, st);
-  if (mode == kModeFwdStats) return launch_one<T, 128, kModeFwdStats>(p, out_p, out_ds, tile_stats, gerr, nsm, st);
-  return launch_one<T, 128, kModeFwdP>(p, out_p, out_ds, tile_stats, gerr, nsm, st);
+  if (mode == kModeBwd) return launch_one<T, 128, kModeBwd>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
+  if (mode == kModeFwdStats) return launch_one<T, 128, kModeFwdStats>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
+  return launch_one<T, 128, kModeFwdP>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
 }
 
-template cudaError_t launch_sdp<__nv_bfloat16>(const Prob&, int, void*, void*, float*, int*, int, cudaStream_t);
-template cudaError_t launch_sdp<__half>(const Prob&, int, void*, void*, float*, int*, int, cudaStream_t);
+template cudaError_t launch_sdp<__nv_bfloat16>(const Maps&, const Prob&, int, void*, void*, float*, int*, int, cudaStream_t);
+template cudaError_t launch_sdp<__half>(const Maps&, const Prob&, int, void*, void*, float*, int*, int, cudaStream_t);
 
 }  // namespace sfa
