@@ -19,8 +19,9 @@ OUT = os.path.join(HERE, "libsfa.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 SOURCES = ["api.cu", "sdp.cu", "dkv.cu", "dq.cu", "prep.cu", "det.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
-         "-diag-suppress", "177"]
+         "-diag-suppress", "177", "-I", INCLUDE]
 
 
 def nvcc() -> str:

@@ -10,7 +10,7 @@
 
 #include <cudaTypedefs.h>
 
-#include "../../include/sfa_grad.h"
+#include "sfa_grad.h"
 #include "common.cuh"
 #include "kernels.h"
 

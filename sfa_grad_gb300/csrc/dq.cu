@@ -133,17 +133,21 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
           for (int hp = 0; hp < kHP; ++hp)
             tma_2d(a + hp * (kSlots * 128), mA, hp * 64, tl * p.Kpad + c * kSlots, &full_bar[me]);
         }
-        for (int e = lane; e < kSlots * kCpr; e += 32) {
-          const int r = e / kCpr, cc = e - r * kCpr;
-          const int row = rows[r];
-          const int f = f0 + cc * 8;
-          const T* src;
-          uint32_t nb = row >= 0 ? 16u : 0u;
-          const size_t rr = (size_t)(row < 0 ? 0 : row);
-          if (MODE == 1 || f < 512) src = kmain + rr * 512 + f;
-          else if (p.has_rope) src = krope + rr * 64 + (f - 512);
-          else { src = kmain; nb = 0u; }
-          cp_async16(b + (cc >> 3) * (kSlots * 128) + swz_chunk(r, cc & 7), src, nb);
+        // lane < kCpr owns 16-byte piece `lane` of every gathered row
+        if (lane < kCpr) {
+          const int f = f0 + lane * 8;
+          const bool rope = MODE == 0 && f >= 512;
+          const T* base = rope ? (p.has_rope ? krope + (f - 512) : kmain) : kmain + f;
+          const int rlen = rope ? 64 : 512;
+          const bool zero = rope && !p.has_rope;
+          const uint32_t dst0 = b + (lane >> 3) * (kSlots * 128);
+          const uint32_t c = lane & 7;
+#pragma unroll 8
+          for (int r = 0; r < kSlots; ++r) {
+            const int row = rows[r];
+            cp_async16(dst0 + r * 128 + ((c ^ (r & 7)) << 4), base + (size_t)(row < 0 ? 0 : row) * rlen,
+                       (row < 0 || zero) ? 0u : 16u);
+          }
         }
         cp_async_commit();
         cp_async_wait<0>();

@@ -155,15 +155,27 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
           const CUtensorMap* mq = ck.kind == 0 ? &maps.q : ck.kind == 1 ? &maps.qr : &maps.dO;
           for (int pn = 0; pn < ck.npan; ++pn) tma_2d(b + pn * S::kPanelB, mq, ck.f0 + pn * 64, t * p.G, &full_bar[me]);
         }
-        // gathered rows: 8 * npan 16-byte pieces per row, contiguous in global memory
-        const T* base = ck.kind == 0 ? k : ck.kind == 1 ? kr : v;
-        const int rlen = ck.kind == 1 ? 64 : 512;
-        const int cpr = ck.npan * 8;
-        for (int e = lane; e < kKeys * cpr; e += 32) {
-          const int r = e / cpr, cc = e - r * cpr;
-          const int row = rows[r];
-          const T* src = base + (size_t)(row < 0 ? 0 : row) * rlen + ck.f0 + cc * 8;
-          cp_async16(a + (cc >> 3) * S::kPanelA + swz_chunk(r, cc & 7), src, row < 0 ? 0u : 16u);
+        // gathered rows, contiguous in global memory: with two panels a lane
+        // owns 16-byte piece (lane & 15) of rows (lane >> 4) + 2i; with one
+        // panel piece (lane & 7) of rows (lane >> 3) + 4i
+        if (ck.npan == 2) {
+          const T* base = (ck.kind == 0 ? k : v) + ck.f0 + (lane & 15) * 8;
+          const uint32_t dst0 = a + ((lane >> 3) & 1) * S::kPanelA;
+          const uint32_t c = lane & 7;
+#pragma unroll 8
+          for (int r = lane >> 4; r < kKeys; r += 2) {
+            const int row = rows[r];
+            cp_async16(dst0 + r * 128 + ((c ^ (r & 7)) << 4), base + (size_t)(row < 0 ? 0 : row) * 512,
+                       row < 0 ? 0u : 16u);
+          }
+        } else {
+          const T* base = kr + (lane & 7) * 8;
+          const uint32_t c = lane & 7;
+#pragma unroll 8
+          for (int r = lane >> 3; r < kKeys; r += 4) {
+            const int row = rows[r];
+            cp_async16(a + r * 128 + ((c ^ (r & 7)) << 4), base + (size_t)(row < 0 ? 0 : row) * 64, row < 0 ? 0u : 16u);
+          }
         }
         cp_async_commit();
         cp_async_wait<0>();
