@@ -186,9 +186,35 @@ sfa_status sfa_decode_keys(const sfa_params* p, const int32_t* indices, const in
 sfa_status sfa_read_device_error(void* workspace, void* stream, int32_t* code);
 
 /*
+ * Allocation-free backward, for callers that cannot allocate device memory:
+ * for example a plugin whose host framework's memory pool owns the whole
+ * device, code running while a stream is captured into a CUDA graph, or a
+ * path that must not risk the device-wide synchronisation cudaMalloc/cudaFree
+ * can cause.  (The pages have no counterpart: their second phase always takes
+ * a caller-allocated workspace.)
+ *
+ * Same arguments and results as sfa_grad without the workspace: the scratch
+ * is a static device array of SFA_NOALLOC_SCRATCH_BYTES inside the library,
+ * held by every GPU that loads the library until the process exits.  Problems
+ * whose sfa_grad_workspace_size exceeds it are rejected with SFA_ERR_SHAPE
+ * (detail in sfa_last_error_message).  The first call on a device looks up
+ * the array's device address; make that first call before any stream
+ * capture.  All calls share the array: calls whose GPU work overlaps (other
+ * streams or threads) race and must be serialised by the caller.  Calls no
+ * cudaMalloc/cudaFree or allocating routine.
+ */
+#define SFA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+sfa_status sfa_grad_noalloc(const sfa_params* p, const void* q, const void* k, const void* v, const int32_t* indices,
+                            const void* d_out, const void* out, const float* softmax_max, const float* softmax_sum,
+                            const int32_t* act_seq_q, const int32_t* act_seq_kv, const void* q_rope,
+                            const void* k_rope, void* dq, void* dk, void* dv, void* dq_rope, void* dk_rope,
+                            void* stream);
+
+/*
  * Human-readable detail of the most recent SFA_ERR_RUNTIME returned on the
- * calling thread (the failing CUDA call's error text and location); empty if
- * none.  The pointer stays valid until the thread's next library call.
+ * calling thread (the failing CUDA call's error text and location), or of a
+ * size rejection by sfa_grad_noalloc; empty if none.  The pointer stays valid
+ * until the thread's next library call.
  */
 const char* sfa_last_error_message(void);
 

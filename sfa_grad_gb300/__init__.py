@@ -28,7 +28,7 @@ DTYPES = {torch.bfloat16: 0, torch.float16: 1}
 
 EXPORTS = ("sfa_grad_workspace_size", "sfa_grad", "sfa_grad_profile", "sfa_grad_plan_info",
            "sfa_fwd_workspace_size", "sfa_fwd", "sfa_decode_keys", "sfa_read_device_error", "sfa_status_string",
-           "sfa_last_error_message")
+           "sfa_last_error_message", "sfa_grad_noalloc")
 
 
 class SfaParams(ctypes.Structure):
@@ -48,7 +48,7 @@ class SfaError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
         detail = ""
-        if code == SFA_ERR_RUNTIME:
+        if code in (SFA_ERR_RUNTIME, SFA_ERR_SHAPE):
             detail = " - " + lib().sfa_last_error_message().decode()
         super().__init__(f"{where}: {status_string(code)} ({code}){detail}")
 
@@ -71,6 +71,7 @@ def lib() -> ctypes.CDLL:
     L.sfa_grad.argtypes = [P] + [vp] * 18 + [sz, vp]
     L.sfa_grad_profile.argtypes = [P] + [vp] * 18 + [sz, vp, ctypes.POINTER(vp), ctypes.c_int32]
     L.sfa_grad_plan_info.argtypes = [P, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]
+    L.sfa_grad_noalloc.argtypes = [P] + [vp] * 17 + [vp]
     L.sfa_fwd.argtypes = [P] + [vp] * 12 + [sz, vp]
     L.sfa_decode_keys.argtypes = [P, vp, vp, vp, vp, vp, sz, vp]
     L.sfa_read_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
@@ -79,7 +80,7 @@ def lib() -> ctypes.CDLL:
     L.sfa_status_string.argtypes = [ctypes.c_int32]
     L.sfa_status_string.restype = ctypes.c_char_p
     for name in ("sfa_grad_workspace_size", "sfa_fwd_workspace_size", "sfa_grad", "sfa_grad_profile",
-                 "sfa_grad_plan_info", "sfa_fwd", "sfa_decode_keys", "sfa_read_device_error"):
+                 "sfa_grad_plan_info", "sfa_fwd", "sfa_decode_keys", "sfa_read_device_error", "sfa_grad_noalloc"):
         getattr(L, name).restype = ctypes.c_int32
     _lib = L
     return L
@@ -185,6 +186,30 @@ def grad(q, k, v, indices, d_out, out, softmax_max, softmax_sum, scale, *, q_rop
         _check(lib().sfa_grad_profile(*args, handles, len(events)), "sfa_grad_profile")
     else:
         _check(lib().sfa_grad(*args), "sfa_grad")
+    return dq, dk, dv, dqr, dkr
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def grad_noalloc(q, k, v, indices, d_out, out, softmax_max, softmax_sum, scale, *, q_rope=None, k_rope=None,
+                 sparse_block_size=1, layout="BSND", sparse_mode=0, deterministic=False, act_seq_q=None,
+                 act_seq_kv=None, outputs=None, stream=None):
+    """sfa_grad_noalloc: the backward with its workspace taken from the
+    library's static device scratch (for callers that cannot allocate device
+    memory); outputs are allocated here unless passed in."""
+    has_rope = q_rope is not None
+    batch = act_seq_q.numel() if act_seq_q is not None else None
+    p = make_params(q, k, indices, scale, layout=layout, sparse_block_size=sparse_block_size,
+                    sparse_mode=sparse_mode, deterministic=deterministic, has_rope=has_rope, batch=batch)
+    if outputs is None:
+        outputs = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v),
+                   torch.empty_like(q_rope) if has_rope else None, torch.empty_like(k_rope) if has_rope else None)
+    dq, dk, dv, dqr, dkr = outputs
+    rc = lib().sfa_grad_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(indices), _ptr(d_out), _ptr(out),
+                                _ptr(softmax_max), _ptr(softmax_sum), _ptr(act_seq_q), _ptr(act_seq_kv), _ptr(q_rope),
+                                _ptr(k_rope), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dqr), _ptr(dkr), _stream(stream))
+    _check(rc, "sfa_grad_noalloc")
     return dq, dk, dv, dqr, dkr
 
 

@@ -190,6 +190,12 @@ sfa_status fail(cudaError_t e, int line) {
   return SFA_ERR_RUNTIME;
 }
 
+}  // namespace
+
+void set_last_error(const char* msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
+
+namespace {
+
 #define SFA_CK(x)                                   \
   do {                                              \
     const cudaError_t sfa_e_ = (x);                 \

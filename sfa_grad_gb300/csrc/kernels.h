@@ -37,6 +37,9 @@ template <typename T>
 cudaError_t launch_cast(const float* acc, int T2, void* dk, void* dkr, void* dv, int has_rope, cudaStream_t st);
 cudaError_t launch_stats_combine(const Prob& p, const float* tile_stats, float* smax, float* ssum, cudaStream_t st);
 
+// Records a message for sfa_last_error_message on the calling thread (api.cu).
+void set_last_error(const char* msg);
+
 // Deterministic key-side reduction (det.cu).
 cudaError_t launch_sort_keys(const Prob& p, int* sorted_key, int* sorted_slot, cudaStream_t st);
 cudaError_t launch_det_reduce(const Prob& p, const int* sorted_key, const int* sorted_slot, const float* partials,
