@@ -147,9 +147,10 @@ sfa_status sfa_grad_profile(const sfa_params* p, const void* q, const void* k, c
  * Static plan of one sfa_grad call: *chunk_tokens = query tokens processed
  * per chunk of the staging buffers, *kernel_launches = number of kernels the
  * call launches (in order: [batch prefix (TND)], token metadata, Dsum, then
- * per chunk: row table, score/softmax-gradient, [key sort (deterministic)], key-side
- * contraction, [fixed-order reduction (deterministic)], query-side
- * contraction; finally the output cast).  Either output pointer may be null.
+ * per chunk: row table, score/softmax-gradient, and either the combined
+ * key-side + query-side contraction (deterministic = 0) or key sort, key-side
+ * contraction, fixed-order reduction, query-side contraction (deterministic
+ * = 1); finally the output cast).  Either output pointer may be null.
  */
 sfa_status sfa_grad_plan_info(const sfa_params* p, int64_t* chunk_tokens, int64_t* kernel_launches);
 

@@ -222,7 +222,7 @@ struct Marks {
 
 int64_t launch_count(const Plan& P) {
   const int64_t chunks = P.T1 > 0 ? (P.T1 + P.chunk - 1) / P.chunk : 0;
-  return (P.layout == SFA_LAYOUT_TND ? 1 : 0) + 2 + chunks * (P.det ? 6 : 4) + 1;
+  return (P.layout == SFA_LAYOUT_TND ? 1 : 0) + 2 + chunks * (P.det ? 6 : 3) + 1;
 }
 
 template <typename T>
@@ -275,12 +275,12 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
       SFA_CK(mk.mark(st));
       SFA_CK(launch_det_reduce(pr, skey, sslot, part, acc, st));
       SFA_CK(mk.mark(st));
+      SFA_CK(launch_dq<T>(maps, pr, 0, dq, P.has_rope ? dqr : nullptr, gerr, nsm, st));
+      SFA_CK(mk.mark(st));
     } else {
-      SFA_CK(launch_dkv<T>(maps, pr, acc, nullptr, gerr, nsm, st));
+      SFA_CK(launch_kvq<T>(maps, pr, acc, dq, P.has_rope ? dqr : nullptr, gerr, nsm, st));
       SFA_CK(mk.mark(st));
     }
-    SFA_CK(launch_dq<T>(maps, pr, 0, dq, P.has_rope ? dqr : nullptr, gerr, nsm, st));
-    SFA_CK(mk.mark(st));
   }
   SFA_CK(launch_cast<T>(acc, P.T2, dk, P.has_rope ? dkr : nullptr, dv, P.has_rope, st));
   SFA_CK(mk.mark(st));

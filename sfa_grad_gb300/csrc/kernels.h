@@ -20,6 +20,12 @@ template <typename T>
 cudaError_t launch_dkv(const Maps& maps, const Prob& p, float* acc, float* partials, int* gerr, int nsm,
                        cudaStream_t st);
 
+// Key-side and query-side contractions in one launch, two pipelines per CTA
+// (kvq.cu): non-deterministic key-side reductions into acc, dQ / dQRope out.
+template <typename T>
+cudaError_t launch_kvq(const Maps& maps, const Prob& p, float* acc, void* dq, void* dqr, int* gerr, int nsm,
+                       cudaStream_t st);
+
 // Query-side contraction (dq.cu): dQ = dS K (mode 0) or O = P V (mode 1).
 template <typename T>
 cudaError_t launch_dq(const Maps& maps, const Prob& p, int mode, void* out_main, void* out_rope, int* gerr, int nsm,

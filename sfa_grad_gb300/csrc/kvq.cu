@@ -1,0 +1,391 @@
+// Key-side and query-side contractions of a token chunk in one launch.  Each
+// CTA (one per SM) runs two independent tensor-core pipelines that share the
+// SM:
+//   key side:   dV_tile = P^T . dO and [dK|dKRope]_tile = dS^T . [q || qRope]
+//               for 128 keys x 128 features, drained into the fp32 key-row
+//               accumulator with vector reductions;
+//   query side: [dQ || dQRope](t) = dS(t) . [K || KRope]_sel, 192 features,
+//               accumulated in tensor memory over all the token's keys.
+// The key side is bound by the SM-to-L2 reduction path and leaves the tensor
+// pipe mostly idle; the query side is bound by gathers and the tensor pipe.
+// Running both in the same CTA overlaps the two.
+//
+// aclnnSparseFlashAttentionGrad doc, 阶段1 (dV = P^T dO) and 阶段3 (dQ, dK);
+// MindSpore flash_attention_bwd.py, update_dVj / update_dQi / update_dKj.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace sfa {
+
+namespace {
+
+constexpr int kThreads = 640;   // 20 warps, roles below
+// warp 0: key-side MMA issuer          warp 1: key-side TMA producer
+// warp 2: query-side MMA issuer        warp 3: idle
+// warps 4-11: key-side drain           warps 12-15: query-side epilogue
+// warps 16-17: query-side gather producers, warps 18-19: idle
+constexpr int kDrainThreads = 256;
+
+constexpr int kKeys = 128;        // key-side tile (MMA M)
+constexpr int kKvStages = 3;      // key-side A stages: 128 slots x 64 heads
+constexpr int kKvChunks = 9;      // dK 4 x 128 + dKRope 64, dV 4 x 128
+constexpr int kAccRow = 1088;
+constexpr int kQSlots = 64;       // query-side keys per stage (MMA K extent)
+constexpr int kQStages = 2;
+constexpr int kQCol = 192;        // query-side features per item (MMA N)
+constexpr int kQParts = 3;
+
+// dynamic shared memory layout (offsets from a 1024-aligned base)
+constexpr int kKvB = 0;                                   // 2 feature panels x 128 head rows
+constexpr int kKvA = kKvB + 2 * 128 * 128;                // 3 stages x 16 KB
+constexpr int kKvAStage = kKeys * 128;
+constexpr int kKvStg = kKvA + kKvStages * kKvAStage;      // 8 warps x 32 rows x 32 floats
+constexpr int kQ = kKvStg + 8 * 32 * 32 * 4;              // 2 stages x (A 16 KB + B 24 KB)
+constexpr int kQA = 2 * kQSlots * 128;
+constexpr int kQStage = kQA + (kQCol / 64) * kQSlots * 128;
+constexpr int kSmemBytes = kQ + kQStages * kQStage + 1024;
+
+// TMEM columns: key-side accumulators [0,128) and [128,256), query side [256,448)
+constexpr uint32_t kQCol0 = 256;
+
+__device__ __forceinline__ void kv_chunk(int ch, int& ncol, int& col0) {
+  if (ch < 4) { ncol = 128; col0 = ch * 128; }
+  else if (ch == 4) { ncol = 64; col0 = 512; }
+  else { ncol = 128; col0 = 576 + (ch - 5) * 128; }
+}
+
+__device__ __forceinline__ void red_add_v4(float* dst, float4 x) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(dst), "f"(x.x), "f"(x.y), "f"(x.z), "f"(x.w)
+               : "memory");
+}
+
+template <typename T, int GP>
+__global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant__ Maps maps, Prob p, float* acc,
+                                                          T* dq, T* dqr, int* gerr) {
+  using E = Elt<T>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t kv_full[kKvStages], kv_empty[kKvStages], kv_tfull[2], kv_tempty[2], kv_bfull, kv_bempty;
+  __shared__ uint64_t q_full[kQStages], q_empty[kQStages], q_tfull, q_tempty;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+  __shared__ __align__(16) int q_rows[kQStages][kQSlots];   // read and written as int2
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ntiles = p.Kpad / kKeys;
+  const int nkv = p.ntok * kKvChunks;
+  const int qchunks = p.Kpad / kQSlots;
+  const int nq = p.ntok * kQParts;
+
+  if (GP == 64) {
+    // query side: heads 64-127 do not exist, their A panel stays zero
+    for (int s = 0; s < kQStages; ++s) {
+      uint4* z = reinterpret_cast<uint4*>(smem + kQ + s * kQStage + kQSlots * 128);
+      for (int i = threadIdx.x; i < kQSlots * 128 / 16; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
+    }
+    fence_async_smem();
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kKvStages; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kv_tfull[i], 1);
+      mbar_init(&kv_tempty[i], kDrainThreads);
+    }
+    mbar_init(&kv_bfull, 1);
+    mbar_init(&kv_bempty, 1);
+    for (int i = 0; i < kQStages; ++i) {
+      mbar_init(&q_full[i], 32 + 1);   // the owning warp's lanes + the TMA transaction arrive
+      mbar_init(&q_empty[i], 1);
+    }
+    mbar_init(&q_tfull, 1);
+    mbar_init(&q_tempty, 128);
+    abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0) tmem_alloc(&tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base;
+
+  if (warp == 0) {
+    // ================================================================ key side: MMA issuer
+    if (lane == 0) {
+      int stage = 0, tcount = 0, icount = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      const uint32_t b = smem_u32(smem + kKvB);
+      for (int item = blockIdx.x; item < nkv && ok; item += gridDim.x, ++icount) {
+        const int ch = item % kKvChunks;
+        int ncol, col0;
+        kv_chunk(ch, ncol, col0);
+        const uint32_t idesc = idesc_f16(kKeys, ncol, E::is_f16, false, true);
+        ok = mbar_wait(&kv_bfull, icount & 1, &abort_flag, gerr);
+        if (!ok) break;
+        for (int kt = 0; kt < ntiles && ok; ++kt, ++tcount) {
+          const int set = tcount & 1;
+          ok = mbar_wait(&kv_tempty[set], ((tcount >> 1) & 1) ^ 1, &abort_flag, gerr);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t d = tbase + set * 128;
+          for (int hp = 0; hp < GP / 64 && ok; ++hp) {
+            ok = mbar_wait(&kv_full[stage], phase, &abort_flag, gerr);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t a = smem_u32(smem + kKvA + stage * kKvAStage);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              mma_ss(d, sdesc_kmajor(a, ks), sdesc_mnmajor(b, hp * 4 + ks, GP), idesc, (hp > 0 || ks > 0) ? 1u : 0u);
+            mma_commit(&kv_empty[stage]);
+            if (++stage == kKvStages) { stage = 0; phase ^= 1; }
+          }
+          if (ok) mma_commit(&kv_tfull[set]);
+        }
+        if (ok) mma_commit(&kv_bempty);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================================================================ key side: TMA producer
+    // Per item: the token's head rows of q / qRope / dO for the chunk's
+    // feature panels (B, kept for the whole item); per key tile and 64-head
+    // panel: the staged dS^T or P^T rows (A, 128 slots x 64 heads).
+    if (lane == 0) {
+      int stage = 0, icount = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      const uint32_t b = smem_u32(smem + kKvB);
+      for (int item = blockIdx.x; item < nkv && ok; item += gridDim.x, ++icount) {
+        const int tl = item / kKvChunks, ch = item % kKvChunks;
+        const int t = p.tok0 + tl;
+        int ncol, col0;
+        kv_chunk(ch, ncol, col0);
+        if (icount > 0) ok = mbar_wait(&kv_bempty, (icount - 1) & 1, &abort_flag, gerr);
+        if (!ok) break;
+        const int npan = ncol / 64;
+        mbar_expect_tx(&kv_bfull, npan * GP * 128);
+        for (int pb = 0; pb < npan; ++pb) {
+          const CUtensorMap* mp;
+          int x, y = t * p.G;
+          if (ch >= 5) { mp = &maps.dO; x = col0 - 576 + pb * 64; }
+          else if (ch < 4) { mp = &maps.q; x = col0 + pb * 64; }
+          else if (p.has_rope) { mp = &maps.qr; x = 0; }
+          else { mp = &maps.q; x = 0; y = -2 * GP; }   // no rope part: rows outside the map read as zeros
+          tma_2d(b + pb * (GP * 128), mp, x, y, &kv_bfull);
+        }
+        const CUtensorMap* mA = ch < 5 ? &maps.dS : &maps.P;
+        for (int kt = 0; kt < ntiles && ok; ++kt) {
+          const int y0 = tl * p.Kpad + kt * kKeys;
+          for (int hp = 0; hp < GP / 64 && ok; ++hp) {
+            ok = mbar_wait(&kv_empty[stage], phase ^ 1, &abort_flag, gerr);
+            if (!ok) break;
+            const uint32_t a = smem_u32(smem + kKvA + stage * kKvAStage);
+            mbar_expect_tx(&kv_full[stage], kKvAStage);
+            tma_2d(a, mA, hp * 64, y0, &kv_full[stage]);
+            tma_2d(a + 64 * 128, mA, hp * 64, y0 + 64, &kv_full[stage]);
+            if (++stage == kKvStages) { stage = 0; phase ^= 1; }
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4 && warp < 12) {
+    // ================================================================ key side: drain
+    // Eight warps: warp w reads TMEM lanes (key slots) 32*(w%4) .. +31 and one
+    // half of the chunk's columns.  Each 32-column slice is transposed
+    // through a per-warp shared buffer (16-byte chunks XOR-swizzled by row)
+    // so that one reduction instruction covers four key rows x 128
+    // contiguous bytes.
+    const int qd = warp & 3;
+    const int half = (warp - 4) >> 2;
+    const int key = qd * 32 + lane;
+    float* stg = reinterpret_cast<float*>(smem + kKvStg) + (warp - 4) * 32 * 32;
+    int tcount = 0;
+    for (int item = blockIdx.x; item < nkv && !abort_flag; item += gridDim.x) {
+      const int tl = item / kKvChunks, ch = item % kKvChunks;
+      int ncol, col0;
+      kv_chunk(ch, ncol, col0);
+      bool ok = true;
+      for (int kt = 0; kt < ntiles; ++kt, ++tcount) {
+        const int set = tcount & 1;
+        const int row = p.rowtab[(size_t)tl * p.Kpad + kt * kKeys + key];
+        ok = __all_sync(0xffffffffu, mbar_wait(&kv_tfull[set], (tcount >> 1) & 1, &abort_flag, gerr));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t td = tbase + set * 128 + ((uint32_t)(qd * 32) << 16);
+        for (int c = half * (ncol / 2); c < (half + 1) * (ncol / 2); c += 32) {
+          float v[32];
+          tmem_ld32(td + c, v);
+          float4* mine = reinterpret_cast<float4*>(stg + lane * 32);
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            mine[u ^ (lane & 7)] = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int rr = 0; rr < 8; ++rr) {
+            const int rl = rr * 4 + (lane >> 3), c4 = lane & 7;
+            const float4 x = reinterpret_cast<const float4*>(stg + rl * 32)[c4 ^ (rl & 7)];
+            const int grow = __shfl_sync(0xffffffffu, row, rl);
+            if (grow >= 0) red_add_v4(acc + (size_t)grow * kAccRow + col0 + c + c4 * 4, x);
+          }
+          __syncwarp();
+        }
+        tc_fence_before();
+        mbar_arrive(&kv_tempty[set]);
+      }
+      if (!ok) break;
+    }
+  } else if (warp == 2) {
+    // ================================================================ query side: MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(128, kQCol, E::is_f16, true, true);
+      const uint32_t d = tbase + kQCol0;
+      int it = 0, g = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < nq && ok; item += gridDim.x, ++it) {
+        ok = mbar_wait(&q_tempty, (it & 1) ^ 1, &abort_flag, gerr);
+        if (!ok) break;
+        tc_fence_after();
+        for (int c = 0; c < qchunks; ++c, ++g) {
+          const int slot = g % kQStages;
+          ok = mbar_wait(&q_full[slot], (g / kQStages) & 1, &abort_flag, gerr);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t a = smem_u32(smem + kQ + slot * kQStage);
+          const uint32_t b = a + kQA;
+#pragma unroll
+          for (int ks = 0; ks < kQSlots / 16; ++ks)
+            mma_ss(d, sdesc_mnmajor(a, ks, kQSlots), sdesc_mnmajor(b, ks, kQSlots), idesc,
+                   (c == 0 && ks == 0) ? 0u : 1u);
+          mma_commit(&q_empty[slot]);
+        }
+        if (ok) mma_commit(&q_tfull);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 16 || warp == 17) {
+    // ================================================================ query side: gather producers
+    // Warp 16 + s owns stage slot s and takes every second stage of 64 keys:
+    // the staged dS^T rows as one TMA box per 64-head panel and the keys'
+    // feature rows by cp.async; it waits only for its own copies, then fences
+    // them for the tensor core and arrives.
+    constexpr int kHP = GP / 64;
+    constexpr int kCpr = kQCol / 8;
+    const int me = warp - 16;
+    const T* kmain = static_cast<const T*>(p.k);
+    const T* krope = static_cast<const T*>(p.kr);
+    const uint32_t a = smem_u32(smem + kQ + me * kQStage);
+    const uint32_t b = a + kQA;
+    int* rows = q_rows[me];
+    int g = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < nq && ok; item += gridDim.x) {
+      const int tl = item / kQParts, part = item % kQParts;
+      const int f0 = part * kQCol;
+      for (int c = 0; c < qchunks; ++c, ++g) {
+        if (g % kQStages != me) continue;
+        const int2 r2 = *reinterpret_cast<const int2*>(p.rowtab + (size_t)tl * p.Kpad + c * kQSlots + 2 * lane);
+        if (lane == 0) ok = mbar_wait(&q_empty[me], ((g / kQStages) & 1) ^ 1, &abort_flag, gerr);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        *reinterpret_cast<int2*>(rows + 2 * lane) = r2;
+        __syncwarp();
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_expect_tx(&q_full[me], kHP * kQSlots * 128);
+          for (int hp = 0; hp < kHP; ++hp)
+            tma_2d(a + hp * (kQSlots * 128), &maps.dS, hp * 64, tl * p.Kpad + c * kQSlots, &q_full[me]);
+        }
+        if (lane < kCpr) {   // lane owns 16-byte piece `lane` of every gathered row
+          const int f = f0 + lane * 8;
+          const bool rope = f >= 512;
+          const T* base = rope ? (p.has_rope ? krope + (f - 512) : kmain) : kmain + f;
+          const int rlen = rope ? 64 : 512;
+          const bool zero = rope && !p.has_rope;
+          const uint32_t dst0 = b + (lane >> 3) * (kQSlots * 128);
+          const uint32_t cc = lane & 7;
+#pragma unroll 8
+          for (int r = 0; r < kQSlots; ++r) {
+            const int row = rows[r];
+            cp_async16(dst0 + r * 128 + ((cc ^ (r & 7)) << 4), base + (size_t)(row < 0 ? 0 : row) * rlen,
+                       (row < 0 || zero) ? 0u : 16u);
+          }
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        fence_async_smem();
+        mbar_arrive(&q_full[me]);
+        __syncwarp();
+      }
+    }
+  } else if (warp >= 12 && warp < 16) {
+    // ================================================================ query side: epilogue (thread = head)
+    const int ew = warp - 12;
+    const int h = ew * 32 + lane;
+    int it = 0;
+    for (int item = blockIdx.x; item < nq && !abort_flag; item += gridDim.x, ++it) {
+      const int tl = item / kQParts, part = item % kQParts;
+      const int t = p.tok0 + tl;
+      const bool ok = mbar_wait(&q_tfull, it & 1, &abort_flag, gerr);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const uint32_t td = tbase + kQCol0 + ((uint32_t)(ew * 32) << 16);
+      for (int c = 0; c < kQCol; c += 32) {
+        float v[32];
+        tmem_ld32(td + c, v);
+        const int f = part * kQCol + c;
+        T* dst = nullptr;
+        if (h < p.G) {
+          if (f < 512) dst = dq + ((size_t)t * p.G + h) * 512 + f;
+          else if (p.has_rope) dst = dqr + ((size_t)t * p.G + h) * 64 + (f - 512);
+        }
+        if (dst) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) pk[j] = E::pack(v[2 * j], v[2 * j + 1]);
+          uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) d4[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&q_tempty);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <typename T, int GP>
+cudaError_t launch_gp(const Maps& maps, const Prob& p, float* acc, void* dq, void* dqr, int* gerr, int nsm,
+                      cudaStream_t st) {
+  auto kern = kvq_kernel<T, GP>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int nitems = p.ntok * kKvChunks;
+  const int grid = nitems < nsm ? nitems : nsm;
+  if (grid <= 0) return cudaSuccess;
+  kern<<<grid, kThreads, kSmemBytes, st>>>(maps, p, acc, static_cast<T*>(dq), static_cast<T*>(dqr), gerr);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+template <typename T>
+cudaError_t launch_kvq(const Maps& maps, const Prob& p, float* acc, void* dq, void* dqr, int* gerr, int nsm,
+                       cudaStream_t st) {
+  if (p.Gp == 64) return launch_gp<T, 64>(maps, p, acc, dq, dqr, gerr, nsm, st);
+  return launch_gp<T, 128>(maps, p, acc, dq, dqr, gerr, nsm, st);
+}
+
+template cudaError_t launch_kvq<__nv_bfloat16>(const Maps&, const Prob&, float*, void*, void*, int*, int,
+                                               cudaStream_t);
+template cudaError_t launch_kvq<__half>(const Maps&, const Prob&, float*, void*, void*, int*, int, cudaStream_t);
+
+}  // namespace sfa

@@ -195,33 +195,41 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
     const int etid = threadIdx.x - 128;
     constexpr int HH = GP / 2;
     const float sl2 = p.scale * kLog2e;
+    // The next item's key validity and per-head statistics (softmaxMax,
+    // softmaxSum, Dsum of head etid) are loaded one item ahead, so their
+    // latency hides behind the current item's work.
+    auto fetch = [&](int item, int& rowv, float& a, float& b, float& c) {
+      rowv = -1;
+      a = b = c = 0.f;
+      if (item >= nitems) return;
+      const int tl = item / ntiles, kt = item % ntiles;
+      const int t = p.tok0 + tl;
+      rowv = p.rowtab[(size_t)tl * p.Kpad + kt * kKeys + key];
+      if (MODE != kModeFwdStats && etid < p.G) {
+        a = __ldg(p.smax + (size_t)t * p.G + etid);
+        b = __ldg(p.ssum + (size_t)t * p.G + etid);
+        if (bwd) c = __ldg(p.dsum + (size_t)t * p.G + etid);
+      }
+    };
+    int nrow;
+    float nmax, nsum, ndsum;
+    fetch(blockIdx.x, nrow, nmax, nsum, ndsum);
     int it = 0;
     for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++it) {
       const int set = it & 1;
       const uint32_t tph = (it >> 1) & 1;
       const int tl = item / ntiles, kt = item % ntiles;
-      const int t = p.tok0 + tl;
       const int slot = kt * kKeys + key;
-      const bool valid = p.rowtab[(size_t)tl * p.Kpad + slot] >= 0;
+      const bool valid = nrow >= 0;
       float* st = stats_s[it & 1];
-      if (MODE != kModeFwdStats) {
-        // per-head statistics of token t: exponent offset, 1/sum (0 for an
-        // empty row or a padded head) and Dsum * scale
-        for (int h = etid; h < GP; h += kEpiThreads) {
-          float ml = 0.f, il = 0.f, dsc = 0.f;
-          if (h < p.G) {
-            const float l = __ldg(p.ssum + (size_t)t * p.G + h);
-            if (l > 0.f) {
-              ml = __ldg(p.smax + (size_t)t * p.G + h) * kLog2e;
-              il = 1.f / l;
-            }
-            if (bwd) dsc = __ldg(p.dsum + (size_t)t * p.G + h) * p.scale;
-          }
-          st[h] = ml;
-          st[GP + h] = il;
-          st[2 * GP + h] = dsc;
-        }
+      if (MODE != kModeFwdStats && etid < GP) {
+        // exponent offset, 1/sum (0 for an empty row or a padded head), Dsum * scale
+        const bool live = nsum > 0.f;
+        st[etid] = live ? nmax * kLog2e : 0.f;
+        st[GP + etid] = live ? 1.f / nsum : 0.f;
+        st[2 * GP + etid] = ndsum * p.scale;
       }
+      fetch(item + gridDim.x, nrow, nmax, nsum, ndsum);
       asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
       const bool ok = __all_sync(0xffffffffu, !abort_flag && mbar_wait(&tfull_bar[set], tph, &abort_flag, gerr));
       if (ok) tc_fence_after();

@@ -69,6 +69,9 @@ WORKLOADS = {
                       dtype="fp16", std=0.5, seed=104, index_kind="block"),
     "long": Workload("long", "BSND", B=1, S1=8192, S2=65536, N1=128, K=8192, seed=105,
                      index_kind="skewed"),
+    # MLA shape with 512 query tokens: the case the per-kernel profiles capture
+    # (staged P/dS of 512 MB, larger than L2, a few GB on the device).
+    "mla_q512": Workload("mla_q512", "BSND", B=1, S1=512, S2=4096, N1=128, K=2048, seed=106),
 }
 
 
