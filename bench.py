@@ -189,7 +189,10 @@ def workload_desc(w, det):
 # token counts.  Reported only while the kernel source still hashes to the
 # value it had when the counters were taken.
 TRAFFIC = {
-    "dkv": {"sources": ["dkv.cu", "common.cuh"], "sha256": None, "bytes_per_token": None},
+    # profiles/kvq_mla_q512.md: 923.8 MB read + 80.1 MB written per 512-token launch
+    "kvq": {"sources": ["kvq.cu", "common.cuh"],
+             "sha256": "e6ec723cf8e6a49a0bb5b57fb9d28f40fc2659fa216a15e9ba95f1f90eb43c62",
+             "bytes_per_token": 1003.9e6 / 512},
 }
 
 
