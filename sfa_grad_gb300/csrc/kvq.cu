@@ -204,14 +204,20 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
     const int key = qd * 32 + lane;
     float* stg = reinterpret_cast<float*>(smem + kKvStg) + (warp - 4) * 32 * 32;
     int tcount = 0;
+    // the row id of the next tile is loaded one tile ahead
+    auto row_of = [&](int item, int kt) {
+      return item < nkv ? p.rowtab[(size_t)(item / kKvChunks) * p.Kpad + kt * kKeys + key] : -1;
+    };
+    int next_row = row_of(blockIdx.x, 0);
     for (int item = blockIdx.x; item < nkv && !abort_flag; item += gridDim.x) {
-      const int tl = item / kKvChunks, ch = item % kKvChunks;
+      const int ch = item % kKvChunks;
       int ncol, col0;
       kv_chunk(ch, ncol, col0);
       bool ok = true;
       for (int kt = 0; kt < ntiles; ++kt, ++tcount) {
         const int set = tcount & 1;
-        const int row = p.rowtab[(size_t)tl * p.Kpad + kt * kKeys + key];
+        const int row = next_row;
+        next_row = kt + 1 < ntiles ? row_of(item, kt + 1) : row_of(item + gridDim.x, 0);
         ok = __all_sync(0xffffffffu, mbar_wait(&kv_tfull[set], (tcount >> 1) & 1, &abort_flag, gerr));
         if (!ok) break;
         tc_fence_after();

@@ -10,11 +10,12 @@
 // or P from final statistics.
 //
 // Pipeline: the contraction runs in stages of 128 features (64 for the rope
-// part).  Gathered key/value rows arrive by cp.async, 256 contiguous bytes per
-// row per stage (scattered 128-byte pieces halve the achievable gather rate);
-// three producer warps each own one shared-memory stage slot and take every
-// third stage, so up to three stages are in flight while each warp waits only
-// for its own copies.  The token's head rows (the other operand) arrive by TMA.
+// part).  The gathered key/value rows (A) and the token's head rows (B) have
+// separate rings.  A: four slots, each owned by a producer warp that takes
+// every fourth stage, copies 256 contiguous bytes per gathered row by cp.async
+// (scattered 128-byte pieces halve the achievable gather rate) and waits only
+// for its own copies, so up to four gathers are in flight.  B: two slots
+// filled by TMA from one thread.
 //
 // aclnnSparseFlashAttentionGrad doc, 功能说明 (gather by topkIndices) and
 // 阶段1/阶段2 (dP, dS); MindSpore flash_attention_bwd.py, compute_Pij
@@ -27,17 +28,21 @@ namespace sfa {
 namespace {
 
 constexpr int kKeys = 128;           // keys per work item (MMA M)
-constexpr int kSlots = 3;            // shared-memory stage slots = producer warps
+constexpr int kSlots = 4;            // gathered-operand slots = gather producer warps
+constexpr int kBSlots = 2;           // head-row operand slots (TMA)
 constexpr int kEpiThreads = 256;     // warps 4-11
-constexpr int kThreads = 128 + kEpiThreads;  // warp 0 MMA, 1-3 producers, 4-11 epilogue
+// warp 0: MMA issuer; warps 1-3 and 12: gather producers (slots 0-2, 3);
+// warps 4-11: epilogue; warp 13: TMA producer of the head-row operand
+constexpr int kThreads = 14 * 32;
 
 template <int GP>
 struct SdpSmem {
   static constexpr int kPanelA = kKeys * 128;   // 64 features x 128 key rows
   static constexpr int kPanelB = GP * 128;      // 64 features x GP head rows
-  static constexpr int kA = 2 * kPanelA;
-  static constexpr int kSlot = kA + 2 * kPanelB;
-  static constexpr int kBytes = kSlots * kSlot + 1024;  // + alignment slack
+  static constexpr int kA = 2 * kPanelA;                 // one gathered slot
+  static constexpr int kB = 2 * kPanelB;                 // one head-row slot
+  static constexpr int kBOff = kSlots * kA;              // B ring after the A ring
+  static constexpr int kBytes = kBOff + kBSlots * kB + 1024;  // + alignment slack
 };
 
 // Stage c of an item: first source feature, 64-wide panel count, tensors.
@@ -59,7 +64,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
   using S = SdpSmem<GP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t full_bar[kSlots], empty_bar[kSlots], tfull_bar[2], tempty_bar[2];
+  __shared__ uint64_t full_bar[kSlots], empty_bar[kSlots], bfull_bar[kBSlots], bempty_bar[kBSlots], tfull_bar[2],
+      tempty_bar[2];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ float red_buf[4][GP][2];
@@ -75,8 +81,12 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kSlots; ++i) {
-      mbar_init(&full_bar[i], 32 + 1);   // the owning warp's lanes + the TMA transaction arrive
+      mbar_init(&full_bar[i], 32);       // the owning warp's lanes
       mbar_init(&empty_bar[i], 1);
+    }
+    for (int i = 0; i < kBSlots; ++i) {
+      mbar_init(&bfull_bar[i], 1);       // the TMA transaction arrive
+      mbar_init(&bempty_bar[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull_bar[i], 1);
@@ -105,44 +115,71 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
         const uint32_t tS = tbase + set * (2 * GP);
         const uint32_t tP = tS + GP;
         for (int c = 0; c < nchunks; ++c, ++g) {
-          const int slot = g % kSlots;
-          ok = mbar_wait(&full_bar[slot], (g / kSlots) & 1, &abort_flag, gerr);
+          const int slot = g % kSlots, bslot = g % kBSlots;
+          ok = mbar_wait(&full_bar[slot], (g / kSlots) & 1, &abort_flag, gerr) &&
+               mbar_wait(&bfull_bar[bslot], (g / kBSlots) & 1, &abort_flag, gerr);
           if (!ok) break;
           tc_fence_after();
           const Chunk ck = chunk_of(c, nS);
-          const uint32_t a = smem_u32(smem + slot * S::kSlot);
-          const uint32_t b = a + S::kA;
+          const uint32_t a = smem_u32(smem + slot * S::kA);
+          const uint32_t b = smem_u32(smem + S::kBOff + bslot * S::kB);
           const uint32_t d = c < nS ? tS : tP;
           const bool first = (c == 0 || c == nS);
           for (int ks = 0; ks < ck.npan * 4; ++ks)
             mma_ss(d, sdesc_kmajor(a + (ks >> 2) * S::kPanelA, ks & 3), sdesc_kmajor(b + (ks >> 2) * S::kPanelB, ks & 3),
                    idesc, (first && ks == 0) ? 0u : 1u);
           mma_commit(&empty_bar[slot]);
+          mma_commit(&bempty_bar[bslot]);
         }
         if (!ok) break;
         mma_commit(&tfull_bar[set]);
       }
     }
     __syncwarp();
-  } else if (warp <= kSlots) {
-    // ---------------------------------------------------------------- producers
-    const int me = warp - 1;                  // owned stage slot
+  } else if (warp == 13) {
+    // ---------------------------------------------------------------- head-row operand (TMA)
+    if (lane == 0) {
+      int g = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
+        const int t = p.tok0 + item / ntiles;
+        for (int c = 0; c < nchunks && ok; ++c, ++g) {
+          const int bslot = g % kBSlots;
+          ok = mbar_wait(&bempty_bar[bslot], ((g / kBSlots) & 1) ^ 1, &abort_flag, gerr);
+          if (!ok) break;
+          const Chunk ck = chunk_of(c, nS);
+          const uint32_t b = smem_u32(smem + S::kBOff + bslot * S::kB);
+          mbar_expect_tx(&bfull_bar[bslot], ck.npan * S::kPanelB);
+          const CUtensorMap* mq = ck.kind == 0 ? &maps.q : ck.kind == 1 ? &maps.qr : &maps.dO;
+          for (int pn = 0; pn < ck.npan; ++pn)
+            tma_2d(b + pn * S::kPanelB, mq, ck.f0 + pn * 64, t * p.G, &bfull_bar[bslot]);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp <= 3 || warp == 12) {
+    // ---------------------------------------------------------------- gather producers
+    const int me = warp == 12 ? 3 : warp - 1;   // owned stage slot
     const T* k = static_cast<const T*>(p.k);
     const T* kr = static_cast<const T*>(p.kr);
     const T* v = static_cast<const T*>(p.v);
-    const uint32_t a = smem_u32(smem + me * S::kSlot);
-    const uint32_t b = a + S::kA;
+    const uint32_t a = smem_u32(smem + me * S::kA);
     int* rows = rows_s[me];
+    // the 128 kv rows (-1: masked) of an item, loaded one item ahead
+    auto rows_of = [&](int item) {
+      if (item >= nitems) return make_int4(-1, -1, -1, -1);
+      return *reinterpret_cast<const int4*>(p.rowtab + (size_t)(item / ntiles) * p.Kpad + (item % ntiles) * kKeys +
+                                            4 * lane);
+    };
+    int4 next4 = rows_of(blockIdx.x);
     int g = 0, loaded_item = -1;
     bool ok = true;
     for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
-      const int tl = item / ntiles, kt = item % ntiles;
-      const int t = p.tok0 + tl;
       for (int c = 0; c < nchunks; ++c, ++g) {
         if (g % kSlots != me) continue;
-        if (loaded_item != item) {   // the item's 128 kv rows (-1: masked)
-          const int4 r4 = *reinterpret_cast<const int4*>(p.rowtab + (size_t)tl * p.Kpad + kt * kKeys + 4 * lane);
-          *reinterpret_cast<int4*>(rows + 4 * lane) = r4;
+        if (loaded_item != item) {
+          *reinterpret_cast<int4*>(rows + 4 * lane) = next4;
+          next4 = rows_of(item + gridDim.x);
           loaded_item = item;
         }
         if (lane == 0) ok = mbar_wait(&empty_bar[me], ((g / kSlots) & 1) ^ 1, &abort_flag, gerr);
@@ -150,11 +187,6 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
         __syncwarp();
         if (!ok) break;
         const Chunk ck = chunk_of(c, nS);
-        if (lane == 0) {
-          mbar_expect_tx(&full_bar[me], ck.npan * S::kPanelB);
-          const CUtensorMap* mq = ck.kind == 0 ? &maps.q : ck.kind == 1 ? &maps.qr : &maps.dO;
-          for (int pn = 0; pn < ck.npan; ++pn) tma_2d(b + pn * S::kPanelB, mq, ck.f0 + pn * 64, t * p.G, &full_bar[me]);
-        }
         // gathered rows, contiguous in global memory: with two panels a lane
         // owns 16-byte piece (lane & 15) of rows (lane >> 4) + 2i; with one
         // panel piece (lane & 7) of rows (lane >> 3) + 4i
@@ -183,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
         mbar_arrive(&full_bar[me]);
       }
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 12) {
     // ---------------------------------------------------------------- epilogue
     // Eight warps: warp w reads TMEM lanes (keys) 32*(w%4) .. +31 and the
     // head half (w-4)/4, i.e. heads [half*GP/2, (half+1)*GP/2).  Named
