@@ -71,6 +71,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
   __shared__ float red_buf[4][GP][2];
   __shared__ float stats_s[2][3 * GP];
   __shared__ __align__(16) int rows_s[kSlots][kKeys];   // read and written as int4
+  __shared__ uint4 epi_stage[8][32 * 4];                 // epilogue row transposition, 2 KB per warp
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool bwd = (MODE == kModeBwd);
@@ -243,6 +244,23 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
         if (bwd) c = __ldg(p.dsum + (size_t)t * p.G + etid);
       }
     };
+    // A lane holds 32 heads (64 bytes) of its own key row.  The warp's 32
+    // rows pass through a private shared buffer (16-byte pieces XOR-swizzled
+    // by row) so that each global store instruction writes eight rows x 64
+    // contiguous bytes instead of 32 scattered 16-byte pieces.
+    uint4* stg = epi_stage[warp - 4];
+    auto put_rows = [&](const uint32_t* pk, T* dst) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        stg[lane * 4 + (u ^ ((lane >> 1) & 3))] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = i * 8 + (lane >> 2), pc = lane & 3;
+        *reinterpret_cast<uint4*>(dst + (size_t)r * GP + pc * 8) = stg[r * 4 + (pc ^ ((r >> 1) & 3))];
+      }
+      __syncwarp();
+    };
     int nrow;
     float nmax, nsum, ndsum;
     fetch(blockIdx.x, nrow, nmax, nsum, ndsum);
@@ -251,7 +269,6 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
       const int set = it & 1;
       const uint32_t tph = (it >> 1) & 1;
       const int tl = item / ntiles, kt = item % ntiles;
-      const int slot = kt * kKeys + key;
       const bool valid = nrow >= 0;
       float* st = stats_s[it & 1];
       if (MODE != kModeFwdStats && etid < GP) {
@@ -308,8 +325,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
         continue;
       }
       if (!ok) continue;
-      T* prow = static_cast<T*>(out_p) + ((size_t)tl * p.Kpad + slot) * GP;
-      T* dsrow = bwd ? static_cast<T*>(out_ds) + ((size_t)tl * p.Kpad + slot) * GP : nullptr;
+      T* ptile = static_cast<T*>(out_p) + ((size_t)tl * p.Kpad + kt * kKeys + q * 32) * GP;
+      T* dstile = bwd ? static_cast<T*>(out_ds) + ((size_t)tl * p.Kpad + kt * kKeys + q * 32) * GP : nullptr;
 #pragma unroll 1
       for (int c = 0; c < HH / 32; ++c) {
         const int h0 = half * HH + c * 32;
@@ -331,14 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
           pk[j / 2] = E::pack(pv[0], pv[1]);
           dk[j / 2] = E::pack(dv[0], dv[1]);
         }
-        uint4* pd = reinterpret_cast<uint4*>(prow + h0);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) pd[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-        if (bwd) {
-          uint4* dd = reinterpret_cast<uint4*>(dsrow + h0);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) dd[u] = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
-        }
+        put_rows(pk, ptile + h0);
+        if (bwd) put_rows(dk, dstile + h0);
       }
       tc_fence_before();
       mbar_arrive(&tempty_bar[set]);
