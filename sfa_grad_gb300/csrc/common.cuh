@@ -62,6 +62,31 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   atomicExch(gerr, kErrTimeout);
   return false;
 }
+// The same bounded wait by non-suspending polls (test_wait), for the
+// single-thread MMA issuers: the tensor core keeps only a few MMAs queued, so
+// every cycle the issuer spends waiting can leave it idle, and a suspending
+// try_wait returns later than a poll.
+__device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, volatile int* abort, int* gerr) {
+  const uint32_t a = smem_u32(bar);
+  for (uint32_t it = 0; it < kSpinLimit; ++it) {
+    if (mbar_poll(a, parity)) return true;
+    if ((it & 255u) == 255u && *abort) return false;
+  }
+  *abort = 1;
+  atomicExch(gerr, kErrTimeout);
+  return false;
+}
 
 // ------------------------------------------------------------------ cp.async
 // 16-byte global -> shared copy; src_bytes = 0 fills the destination with zeros
@@ -177,6 +202,26 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, 
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Four consecutive K steps (64 elements) into one accumulator.  `a` and `b`
+// are the descriptors of step 0; each step advances the encoded start address
+// by SA / SB units of 16 B (2 for a K-major 128-byte-swizzled panel, 128 for
+// an MN-major one).  The MMA issue path is a single thread whose instruction
+// latency is not hidden, so callers build descriptors once per stage and this
+// only offsets them.
+template <uint32_t SA, uint32_t SB>
+__device__ __forceinline__ void mma_ss_k64(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc_first) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %3, 1;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %3, 1;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %10, %3, 1;\n}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc_first), "l"(a + SA), "l"(b + SB), "l"(a + 2 * SA), "l"(b + 2 * SB),
+      "l"(a + 3 * SA), "l"(b + 3 * SB)
+      : "memory");
+}
+// Descriptor offset, in encoded 16-byte units, of a byte offset inside shared memory.
+__device__ __forceinline__ uint64_t desc_off(uint32_t bytes) { return (uint64_t)(bytes >> 4); }
 // Arrives on `bar` once every MMA issued so far by this thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))

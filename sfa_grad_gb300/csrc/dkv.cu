@@ -90,18 +90,17 @@ __global__ void __launch_bounds__(kThreads, 1) dkv_kernel(const __grid_constant_
         chunk_geom(ch, ncol, col0);
         const uint32_t idesc = idesc_f16(kKeys, ncol, E::is_f16, false, true);
         const uint32_t b = smem_u32(sB);
-        if (!mbar_wait(&bfull_bar, icount & 1, &abort_flag, gerr)) break;
+        if (!mbar_wait_poll(&bfull_bar, icount & 1, &abort_flag, gerr)) break;
         for (int kt = 0; kt < ntiles; ++kt, ++tcount) {
           const int set = tcount & 1;
-          if (!mbar_wait(&tempty_bar[set], ((tcount >> 1) & 1) ^ 1, &abort_flag, gerr)) break;
-          if (!mbar_wait(&full_bar[stage], phase, &abort_flag, gerr)) break;
+          if (!mbar_wait_poll(&tempty_bar[set], ((tcount >> 1) & 1) ^ 1, &abort_flag, gerr)) break;
+          if (!mbar_wait_poll(&full_bar[stage], phase, &abort_flag, gerr)) break;
           tc_fence_after();
-          const uint32_t a = smem_u32(sA + stage * DkvSmem<GP>::kA);
+          const uint64_t da = sdesc_kmajor(smem_u32(sA + stage * DkvSmem<GP>::kA), 0);
+          const uint64_t db = sdesc_mnmajor(b, 0, GP);
           const uint32_t d = tbase + set * 256;
-#pragma unroll
-          for (int ks = 0; ks < GP / 16; ++ks)
-            mma_ss(d, sdesc_kmajor(a + (ks >> 2) * (kKeys * 128), ks & 3), sdesc_mnmajor(b, ks, GP), idesc,
-                   ks > 0 ? 1u : 0u);
+          mma_ss_k64<2, 128>(d, da, db, idesc, 0u);
+          if (GP == 128) mma_ss_k64<2, 128>(d, da + desc_off(kKeys * 128), db + 512, idesc, 1u);
           mma_commit(&empty_bar[stage]);
           mma_commit(&tfull_bar[set]);
           if (++stage == kStages) { stage = 0; phase ^= 1; }

@@ -74,24 +74,24 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
   if (warp == 0) {
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(128, NCOL, E::is_f16, true, true);
+      const uint64_t da0 = sdesc_mnmajor(smem_u32(smem), 0, kSlots);
+      const uint64_t db0 = sdesc_mnmajor(smem_u32(smem + S::kA), 0, kSlots);
       int it = 0, g = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++it) {
         const int set = it & 1;
-        ok = mbar_wait(&tempty_bar[set], ((it >> 1) & 1) ^ 1, &abort_flag, gerr);
+        ok = mbar_wait_poll(&tempty_bar[set], ((it >> 1) & 1) ^ 1, &abort_flag, gerr);
         if (!ok) break;
         tc_fence_after();
         const uint32_t d = tbase + set * 256;
         for (int c = 0; c < nchunks; ++c, ++g) {
           const int slot = g % kStages;
-          ok = mbar_wait(&full_bar[slot], (g / kStages) & 1, &abort_flag, gerr);
+          ok = mbar_wait_poll(&full_bar[slot], (g / kStages) & 1, &abort_flag, gerr);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t a = smem_u32(smem + slot * S::kStage);
-          const uint32_t b = a + S::kA;
-#pragma unroll
-          for (int ks = 0; ks < kSlots / 16; ++ks)
-            mma_ss(d, sdesc_mnmajor(a, ks, kSlots), sdesc_mnmajor(b, ks, kSlots), idesc, (c == 0 && ks == 0) ? 0u : 1u);
+          static_assert(kSlots == 64, "four K steps per stage");
+          mma_ss_k64<128, 128>(d, da0 + desc_off(slot * S::kStage), db0 + desc_off(slot * S::kStage), idesc,
+                               c == 0 ? 0u : 1u);
           mma_commit(&empty_bar[slot]);
         }
         if (!ok) break;

@@ -117,28 +117,26 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
       int stage = 0, tcount = 0, icount = 0;
       uint32_t phase = 0;
       bool ok = true;
-      const uint32_t b = smem_u32(smem + kKvB);
+      const uint64_t da0 = sdesc_kmajor(smem_u32(smem + kKvA), 0);
+      const uint64_t db0 = sdesc_mnmajor(smem_u32(smem + kKvB), 0, GP);
       for (int item = blockIdx.x; item < nkv && ok; item += gridDim.x, ++icount) {
         const int ch = item % kKvChunks;
         int ncol, col0;
         kv_chunk(ch, ncol, col0);
         const uint32_t idesc = idesc_f16(kKeys, ncol, E::is_f16, false, true);
-        ok = mbar_wait(&kv_bfull, icount & 1, &abort_flag, gerr);
+        ok = mbar_wait_poll(&kv_bfull, icount & 1, &abort_flag, gerr);
         if (!ok) break;
         for (int kt = 0; kt < ntiles && ok; ++kt, ++tcount) {
           const int set = tcount & 1;
-          ok = mbar_wait(&kv_tempty[set], ((tcount >> 1) & 1) ^ 1, &abort_flag, gerr);
+          ok = mbar_wait_poll(&kv_tempty[set], ((tcount >> 1) & 1) ^ 1, &abort_flag, gerr);
           if (!ok) break;
           tc_fence_after();
           const uint32_t d = tbase + set * 128;
           for (int hp = 0; hp < GP / 64 && ok; ++hp) {
-            ok = mbar_wait(&kv_full[stage], phase, &abort_flag, gerr);
+            ok = mbar_wait_poll(&kv_full[stage], phase, &abort_flag, gerr);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t a = smem_u32(smem + kKvA + stage * kKvAStage);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              mma_ss(d, sdesc_kmajor(a, ks), sdesc_mnmajor(b, hp * 4 + ks, GP), idesc, (hp > 0 || ks > 0) ? 1u : 0u);
+            mma_ss_k64<2, 128>(d, da0 + desc_off(stage * kKvAStage), db0 + (uint64_t)(hp * 512), idesc, hp > 0 ? 1u : 0u);
             mma_commit(&kv_empty[stage]);
             if (++stage == kKvStages) { stage = 0; phase ^= 1; }
           }
@@ -248,24 +246,23 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
     // ================================================================ query side: MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(128, kQCol, E::is_f16, true, true);
+      const uint64_t dqa0 = sdesc_mnmajor(smem_u32(smem + kQ), 0, kQSlots);
+      const uint64_t dqb0 = sdesc_mnmajor(smem_u32(smem + kQ + kQA), 0, kQSlots);
       const uint32_t d = tbase + kQCol0;
       int it = 0, g = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < nq && ok; item += gridDim.x, ++it) {
-        ok = mbar_wait(&q_tempty, (it & 1) ^ 1, &abort_flag, gerr);
+        ok = mbar_wait_poll(&q_tempty, (it & 1) ^ 1, &abort_flag, gerr);
         if (!ok) break;
         tc_fence_after();
         for (int c = 0; c < qchunks; ++c, ++g) {
           const int slot = g % kQStages;
-          ok = mbar_wait(&q_full[slot], (g / kQStages) & 1, &abort_flag, gerr);
+          ok = mbar_wait_poll(&q_full[slot], (g / kQStages) & 1, &abort_flag, gerr);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t a = smem_u32(smem + kQ + slot * kQStage);
-          const uint32_t b = a + kQA;
-#pragma unroll
-          for (int ks = 0; ks < kQSlots / 16; ++ks)
-            mma_ss(d, sdesc_mnmajor(a, ks, kQSlots), sdesc_mnmajor(b, ks, kQSlots), idesc,
-                   (c == 0 && ks == 0) ? 0u : 1u);
+          static_assert(kQSlots == 64, "four K steps per stage");
+          mma_ss_k64<128, 128>(d, dqa0 + desc_off(slot * kQStage), dqb0 + desc_off(slot * kQStage), idesc,
+                               c == 0 ? 0u : 1u);
           mma_commit(&q_empty[slot]);
         }
         if (ok) mma_commit(&q_tfull);

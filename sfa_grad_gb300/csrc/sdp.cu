@@ -15,7 +15,8 @@
 // every fourth stage, copies 256 contiguous bytes per gathered row by cp.async
 // (scattered 128-byte pieces halve the achievable gather rate) and waits only
 // for its own copies, so up to four gathers are in flight.  B: two slots
-// filled by TMA from one thread.
+// filled by TMA from one thread.  Both operands of a stage complete on one
+// barrier, so the MMA issuer waits once per stage.
 //
 // aclnnSparseFlashAttentionGrad doc, 功能说明 (gather by topkIndices) and
 // 阶段1/阶段2 (dP, dS); MindSpore flash_attention_bwd.py, compute_Pij
@@ -64,8 +65,9 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
   using S = SdpSmem<GP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t full_bar[kSlots], empty_bar[kSlots], bfull_bar[kBSlots], bempty_bar[kBSlots], tfull_bar[2],
-      tempty_bar[2];
+  // full_bar[s]: both operands of the stage in gathered slot s are in shared
+  // memory (the owning gather warp's 32 lanes + the head-row TMA transaction)
+  __shared__ uint64_t full_bar[kSlots], empty_bar[kSlots], bempty_bar[kBSlots], tfull_bar[2], tempty_bar[2];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ float red_buf[4][GP][2];
@@ -82,13 +84,10 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kSlots; ++i) {
-      mbar_init(&full_bar[i], 32);       // the owning warp's lanes
+      mbar_init(&full_bar[i], 32 + 1);   // the owning warp's lanes + the head-row transaction arrive
       mbar_init(&empty_bar[i], 1);
     }
-    for (int i = 0; i < kBSlots; ++i) {
-      mbar_init(&bfull_bar[i], 1);       // the TMA transaction arrive
-      mbar_init(&bempty_bar[i], 1);
-    }
+    for (int i = 0; i < kBSlots; ++i) mbar_init(&bempty_bar[i], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull_bar[i], 1);
       mbar_init(&tempty_bar[i], kEpiThreads);
@@ -106,29 +105,28 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(kKeys, GP, E::is_f16, false, false);
+      const uint64_t dbase = sdesc_kmajor(smem_u32(smem), 0);
       int it = 0, g = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++it) {
         const int set = it & 1;
-        ok = mbar_wait(&tempty_bar[set], ((it >> 1) & 1) ^ 1, &abort_flag, gerr);
+        ok = mbar_wait_poll(&tempty_bar[set], ((it >> 1) & 1) ^ 1, &abort_flag, gerr);
         if (!ok) break;
         tc_fence_after();
         const uint32_t tS = tbase + set * (2 * GP);
         const uint32_t tP = tS + GP;
         for (int c = 0; c < nchunks; ++c, ++g) {
           const int slot = g % kSlots, bslot = g % kBSlots;
-          ok = mbar_wait(&full_bar[slot], (g / kSlots) & 1, &abort_flag, gerr) &&
-               mbar_wait(&bfull_bar[bslot], (g / kBSlots) & 1, &abort_flag, gerr);
+          ok = mbar_wait_poll(&full_bar[slot], (g / kSlots) & 1, &abort_flag, gerr);
           if (!ok) break;
           tc_fence_after();
           const Chunk ck = chunk_of(c, nS);
-          const uint32_t a = smem_u32(smem + slot * S::kA);
-          const uint32_t b = smem_u32(smem + S::kBOff + bslot * S::kB);
+          const uint64_t da = dbase + desc_off(slot * S::kA);
+          const uint64_t db = dbase + desc_off(S::kBOff + bslot * S::kB);
           const uint32_t d = c < nS ? tS : tP;
           const bool first = (c == 0 || c == nS);
-          for (int ks = 0; ks < ck.npan * 4; ++ks)
-            mma_ss(d, sdesc_kmajor(a + (ks >> 2) * S::kPanelA, ks & 3), sdesc_kmajor(b + (ks >> 2) * S::kPanelB, ks & 3),
-                   idesc, (first && ks == 0) ? 0u : 1u);
+          mma_ss_k64<2, 2>(d, da, db, idesc, first ? 0u : 1u);
+          if (ck.npan == 2) mma_ss_k64<2, 2>(d, da + desc_off(S::kPanelA), db + desc_off(S::kPanelB), idesc, 1u);
           mma_commit(&empty_bar[slot]);
           mma_commit(&bempty_bar[bslot]);
         }
@@ -150,10 +148,10 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
           if (!ok) break;
           const Chunk ck = chunk_of(c, nS);
           const uint32_t b = smem_u32(smem + S::kBOff + bslot * S::kB);
-          mbar_expect_tx(&bfull_bar[bslot], ck.npan * S::kPanelB);
+          uint64_t* fb = &full_bar[g % kSlots];
+          mbar_expect_tx(fb, ck.npan * S::kPanelB);
           const CUtensorMap* mq = ck.kind == 0 ? &maps.q : ck.kind == 1 ? &maps.qr : &maps.dO;
-          for (int pn = 0; pn < ck.npan; ++pn)
-            tma_2d(b + pn * S::kPanelB, mq, ck.f0 + pn * 64, t * p.G, &bfull_bar[bslot]);
+          for (int pn = 0; pn < ck.npan; ++pn) tma_2d(b + pn * S::kPanelB, mq, ck.f0 + pn * 64, t * p.G, fb);
         }
       }
     }
