@@ -189,10 +189,10 @@ def workload_desc(w, det):
 # token counts.  Reported only while the kernel source still hashes to the
 # value it had when the counters were taken.
 TRAFFIC = {
-    # profiles/kvq_mla_q512.md: 923.8 MB read + 80.1 MB written per 512-token launch
+    # profiles/kvq_mla_q512.md: 908.4 MB read + 81.0 MB written per 512-token launch
     "kvq": {"sources": ["kvq.cu", "common.cuh"],
-             "sha256": "e6ec723cf8e6a49a0bb5b57fb9d28f40fc2659fa216a15e9ba95f1f90eb43c62",
-             "bytes_per_token": 1003.9e6 / 512},
+             "sha256": "97e94b65b61ce7a25d846796905bac83209d7c9423138249806a0ddea5cf67a5",
+             "bytes_per_token": 989.3e6 / 512},
 }
 
 
