@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&kv_tfull[i], 1);
-      mbar_init(&kv_tempty[i], kDrainThreads);
+      mbar_init(&kv_tempty[i], kDrainThreads / 2);   // one drain group per TMEM set
     }
     mbar_init(&kv_bfull, 1);
     mbar_init(&kv_bempty, 1);
@@ -192,21 +192,31 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
     __syncwarp();
   } else if (warp >= 4 && warp < 12) {
     // ================================================================ key side: drain
-    // Eight warps: warp w reads TMEM lanes (key slots) 32*(w%4) .. +31 and one
-    // half of the chunk's columns.  Each 32-column slice is transposed
-    // through a per-warp shared buffer (16-byte chunks XOR-swizzled by row)
-    // so that one reduction instruction covers four key rows x 128
-    // contiguous bytes.
+    // Two groups of four warps take alternate tiles (group g drains TMEM
+    // set g), so one group's reductions overlap the other group's TMEM loads
+    // and staging instead of all eight warps pausing together.  Warp w of a
+    // group reads TMEM lanes (key slots) 32*(w%4) .. +31 and all of the
+    // chunk's columns; each 32-column slice is transposed through a per-warp
+    // shared buffer (16-byte chunks XOR-swizzled by row) so that one
+    // reduction instruction covers four key rows x 128 contiguous bytes.
     const int qd = warp & 3;
-    const int half = (warp - 4) >> 2;
+    const int grp = (warp - 4) >> 2;
     const int key = qd * 32 + lane;
     float* stg = reinterpret_cast<float*>(smem + kKvStg) + (warp - 4) * 32 * 32;
     int tcount = 0;
-    // the row id of the next tile is loaded one tile ahead
+    // the row id of the group's next tile is loaded one tile ahead
     auto row_of = [&](int item, int kt) {
       return item < nkv ? p.rowtab[(size_t)(item / kKvChunks) * p.Kpad + kt * kKeys + key] : -1;
     };
-    int next_row = row_of(blockIdx.x, 0);
+    auto advance = [&](int& item, int& kt) {
+      if (++kt == ntiles) {
+        kt = 0;
+        item += gridDim.x;
+      }
+    };
+    int nitem = blockIdx.x, nkt = 0;
+    if (grp) advance(nitem, nkt);
+    int next_row = row_of(nitem, nkt);
     for (int item = blockIdx.x; item < nkv && !abort_flag; item += gridDim.x) {
       const int ch = item % kKvChunks;
       int ncol, col0;
@@ -214,13 +224,16 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
       bool ok = true;
       for (int kt = 0; kt < ntiles; ++kt, ++tcount) {
         const int set = tcount & 1;
+        if (set != grp) continue;
         const int row = next_row;
-        next_row = kt + 1 < ntiles ? row_of(item, kt + 1) : row_of(item + gridDim.x, 0);
+        advance(nitem, nkt);
+        advance(nitem, nkt);
+        next_row = row_of(nitem, nkt);
         ok = __all_sync(0xffffffffu, mbar_wait(&kv_tfull[set], (tcount >> 1) & 1, &abort_flag, gerr));
         if (!ok) break;
         tc_fence_after();
         const uint32_t td = tbase + set * 128 + ((uint32_t)(qd * 32) << 16);
-        for (int c = half * (ncol / 2); c < (half + 1) * (ncol / 2); c += 32) {
+        for (int c = 0; c < ncol; c += 32) {
           float v[32];
           tmem_ld32(td + c, v);
           float4* mine = reinterpret_cast<float4*>(stg + lane * 32);
