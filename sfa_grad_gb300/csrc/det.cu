@@ -3,7 +3,7 @@
 // [dK | dKRope | dV] per (token, slot) instead of using atomics; then
 //  1. every token's (kv row, slot) pairs are sorted by (row, slot) in shared
 //     memory (bitonic sort, a fixed network, so the result is unique), and
-//  2. a block owning 32 consecutive kv rows walks the chunk's tokens in
+//  2. a block owning 8 consecutive kv rows walks the chunk's tokens in
 //     ascending order, finds the rows it owns in each token's sorted list by
 //     binary search, and adds the matching partial rows in (token, slot)
 //     order into a shared-memory accumulator, which it finally adds to the
@@ -18,7 +18,7 @@ namespace sfa {
 
 namespace {
 
-constexpr int kRowsPerBlock = 32;
+constexpr int kRowsPerBlock = 8;      // 35 KB of shared accumulator: several blocks per SM
 constexpr int kAccRow = 1088;
 constexpr int kCols4 = kAccRow / 4;     // 272 float4 columns
 constexpr int kRedThreads = 288;
@@ -121,13 +121,13 @@ __global__ void __launch_bounds__(kRedThreads) det_reduce_kernel(Prob p, const i
       if (tid < kCols4) {
         const int n = m1 - m0;
         int e = 0;
-        for (; e + 4 <= n; e += 4) {
-          float4 v[4];
+        for (; e + 8 <= n; e += 8) {
+          float4 v[8];
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
+          for (int u = 0; u < 8; ++u)
             v[u] = __ldg(reinterpret_cast<const float4*>(partials + ((size_t)m_tok[e + u] * p.Kpad + m_slot[e + u]) * kAccRow) + tid);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
+          for (int u = 0; u < 8; ++u) {
             float4& a = acc_s[m_key[e + u] * kCols4 + tid];
             a.x += v[u].x; a.y += v[u].y; a.z += v[u].z; a.w += v[u].w;
           }
