@@ -3,7 +3,7 @@
 // [dK | dKRope | dV] per (token, slot) instead of using atomics; then
 //  1. every token's (kv row, slot) pairs are sorted by (row, slot) in shared
 //     memory (bitonic sort, a fixed network, so the result is unique), and
-//  2. a block owning 8 consecutive kv rows walks the chunk's tokens in
+//  2. a block owning 4 consecutive kv rows walks the chunk's tokens in
 //     ascending order, finds the rows it owns in each token's sorted list by
 //     binary search, and adds the matching partial rows in (token, slot)
 //     order into a shared-memory accumulator, which it finally adds to the
@@ -18,7 +18,7 @@ namespace sfa {
 
 namespace {
 
-constexpr int kRowsPerBlock = 8;      // 35 KB of shared accumulator: several blocks per SM
+constexpr int kRowsPerBlock = 4;      // 17 KB of shared accumulator: several blocks per SM
 constexpr int kAccRow = 1088;
 constexpr int kCols4 = kAccRow / 4;     // 272 float4 columns
 constexpr int kRedThreads = 288;
