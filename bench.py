@@ -179,9 +179,10 @@ def run_reference(args):
     return 0
 
 
-def workload_desc(w, det):
+def workload_desc(w, det, shared_kv=False):
     return (f"{w.name}: {w.layout} B={w.B} S1={w.S1} S2={w.S2} N1={w.N1} N2=1 D=512 Dr=64 K={w.K} "
-            f"sparseBlockSize={w.block_size} sparseMode={w.mode} {w.dtype} deterministic={int(det)}")
+            f"sparseBlockSize={w.block_size} sparseMode={w.mode} {w.dtype} deterministic={int(det)}"
+            + (" value=key" if shared_kv else ""))
 
 
 # DRAM bytes (read + write) per query token of one launch, from an ncu capture
@@ -239,7 +240,11 @@ def run_sfa(args):
     w = WORKLOADS[args.workload]
     det = args.deterministic
     inp = make_inputs(w)
-    d = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
+    if args.shared_kv:
+        inp["v"] = inp["k"]
+    d = {k: (v.to(dev) if v is not None else None) for k, v in inp.items() if not (args.shared_kv and k == "v")}
+    if args.shared_kv:
+        d["v"] = d["k"]
     kw = dict(q_rope=d["q_rope"], k_rope=d["k_rope"], sparse_block_size=w.block_size, layout=w.layout,
               sparse_mode=w.mode, act_seq_q=d.get("act_seq_q"), act_seq_kv=d.get("act_seq_kv"))
     out, smax, ssum = sfa.fwd(d["q"], d["k"], d["v"], d["indices"], w.scale_value, **kw)
@@ -301,8 +306,10 @@ def run_sfa(args):
     res_host = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
     in_list = [host["q"], host["k"], host["v"], host["indices"], host["d_out"], h_out, h_m, h_l, host["q_rope"],
                host["k_rope"]]
-    dev_in = [x.to(dev) for x in in_list]
-    h2d = sum(x.numel() * x.element_size() for x in in_list)
+    if args.shared_kv:
+        in_list[2] = None          # the value buffer is the key buffer
+    dev_in = [x.to(dev) if x is not None else None for x in in_list]
+    h2d = sum(x.numel() * x.element_size() for x in in_list if x is not None)
     d2h = sum(x.numel() * x.element_size() for x in res_host)
     e2e_steps = max(3, min(args.steps, 10))
     e2e_ms = []
@@ -311,8 +318,11 @@ def run_sfa(args):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for dst, src in zip(dev_in, in_list):
-            dst.copy_(src, non_blocking=True)
+            if src is not None:
+                dst.copy_(src, non_blocking=True)
         q_, k_, v_, idx_, do_, o_, m_, l_, qr_, kr_ = dev_in
+        if args.shared_kv:
+            v_ = k_
         sfa.grad(q_, k_, v_, idx_, do_, o_, m_, l_, w.scale_value, q_rope=qr_, k_rope=kr_,
                  sparse_block_size=w.block_size, layout=w.layout, sparse_mode=w.mode, deterministic=det,
                  outputs=outs, workspace=ws)
@@ -371,7 +381,7 @@ def run_sfa(args):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": workload_desc(w, det), "l2": "flushed between steps (256 MB write, outside the events)",
+        "config": {"workload": workload_desc(w, det, args.shared_kv), "l2": "flushed between steps (256 MB write, outside the events)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "valid_query_head_key": pairs * G},
         "frac_of_dense_bf16_peak": value / world / peaks["bf16_tflops"],
@@ -400,6 +410,8 @@ def main():
     ap.add_argument("--impl", choices=["sfa", "reference"], default="sfa")
     ap.add_argument("--workload", default="mla", choices=list(WORKLOADS))
     ap.add_argument("--deterministic", action="store_true")
+    ap.add_argument("--shared-kv", action="store_true",
+                    help="pass the key tensor as the value tensor too (value identical to key)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per launch of the dominant kernel from an ncu capture")

@@ -31,19 +31,27 @@ namespace {
 constexpr int kKeys = 128;           // keys per work item (MMA M)
 constexpr int kSlots = 4;            // gathered-operand slots = gather producer warps
 constexpr int kBSlots = 2;           // head-row operand slots (TMA)
+constexpr int kMaxSlots = 4;         // barrier arrays sized for either ring layout
 constexpr int kEpiThreads = 256;     // warps 4-11
 // warp 0: MMA issuer; warps 1-3 and 12: gather producers (slots 0-2, 3);
 // warps 4-11: epilogue; warp 13: TMA producer of the head-row operand
 constexpr int kThreads = 14 * 32;
 
-template <int GP>
+// SH: key and value are the same tensor.  A gathered stage of key rows then
+// serves both the score and the dP contraction, so half as many rows are
+// gathered; the rings become two gathered slots (two producer warps each,
+// one half of the rows per warp) and four head-row slots (q and dO of a
+// stage are both resident).
+template <int GP, bool SH>
 struct SdpSmem {
+  static constexpr int kNA = SH ? 2 : kSlots;            // gathered slots
+  static constexpr int kNB = SH ? 4 : kBSlots;           // head-row slots
   static constexpr int kPanelA = kKeys * 128;   // 64 features x 128 key rows
   static constexpr int kPanelB = GP * 128;      // 64 features x GP head rows
   static constexpr int kA = 2 * kPanelA;                 // one gathered slot
   static constexpr int kB = 2 * kPanelB;                 // one head-row slot
-  static constexpr int kBOff = kSlots * kA;              // B ring after the A ring
-  static constexpr int kBytes = kBOff + kBSlots * kB + 1024;  // + alignment slack
+  static constexpr int kBOff = kNA * kA;                 // B ring after the A ring
+  static constexpr int kBytes = kBOff + kNB * kB + 1024;  // + alignment slack
 };
 
 // Stage c of an item: first source feature, 64-wide panel count, tensors.
@@ -58,21 +66,22 @@ __device__ __forceinline__ Chunk chunk_of(int c, int nS) {
   return Chunk{(c - nS) * 128, 2, 2};
 }
 
-template <typename T, int GP, int MODE>
+template <typename T, int GP, int MODE, bool SH>
 __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant__ Maps maps, Prob p, void* out_p, void* out_ds,
                                                           float* tile_stats, int* gerr) {
   using E = Elt<T>;
-  using S = SdpSmem<GP>;
+  using S = SdpSmem<GP, SH>;
+  static_assert(!SH || MODE == kModeBwd, "the shared key/value layout serves the backward only");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  // full_bar[s]: both operands of the stage in gathered slot s are in shared
-  // memory (the owning gather warp's 32 lanes + the head-row TMA transaction)
-  __shared__ uint64_t full_bar[kSlots], empty_bar[kSlots], bempty_bar[kBSlots], tfull_bar[2], tempty_bar[2];
+  // full_bar[s]: all operands of the stage in gathered slot s are in shared
+  // memory (the gather warps' lanes + the head-row TMA transaction arrivals)
+  __shared__ uint64_t full_bar[kMaxSlots], empty_bar[kMaxSlots], bempty_bar[kMaxSlots], tfull_bar[2], tempty_bar[2];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ float red_buf[4][GP][2];
   __shared__ float stats_s[2][3 * GP];
-  __shared__ __align__(16) int rows_s[kSlots][kKeys];   // read and written as int4
+  __shared__ __align__(16) int rows_s[4][kKeys];        // one per gather warp; read and written as int4
   __shared__ uint4 epi_stage[8][32 * 4];                 // epilogue row transposition, 2 KB per warp
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -83,11 +92,12 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
   const int nitems = p.ntok * ntiles;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kSlots; ++i) {
-      mbar_init(&full_bar[i], 32 + 1);   // the owning warp's lanes + the head-row transaction arrive
+    for (int i = 0; i < S::kNA; ++i) {
+      // SH: two gather warps + two head-row arrivals; else the owning warp + one
+      mbar_init(&full_bar[i], SH ? 64 + 2 : 32 + 1);
       mbar_init(&empty_bar[i], 1);
     }
-    for (int i = 0; i < kBSlots; ++i) mbar_init(&bempty_bar[i], 1);
+    for (int i = 0; i < S::kNB; ++i) mbar_init(&bempty_bar[i], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull_bar[i], 1);
       mbar_init(&tempty_bar[i], kEpiThreads);
@@ -106,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(kKeys, GP, E::is_f16, false, false);
       const uint64_t dbase = sdesc_kmajor(smem_u32(smem), 0);
-      int it = 0, g = 0;
+      int it = 0, g = 0, gb = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++it) {
         const int set = it & 1;
@@ -115,20 +125,48 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
         tc_fence_after();
         const uint32_t tS = tbase + set * (2 * GP);
         const uint32_t tP = tS + GP;
-        for (int c = 0; c < nchunks; ++c, ++g) {
-          const int slot = g % kSlots, bslot = g % kBSlots;
-          ok = mbar_wait_poll(&full_bar[slot], (g / kSlots) & 1, &abort_flag, gerr);
-          if (!ok) break;
-          tc_fence_after();
-          const Chunk ck = chunk_of(c, nS);
-          const uint64_t da = dbase + desc_off(slot * S::kA);
-          const uint64_t db = dbase + desc_off(S::kBOff + bslot * S::kB);
-          const uint32_t d = c < nS ? tS : tP;
-          const bool first = (c == 0 || c == nS);
-          mma_ss_k64<2, 2>(d, da, db, idesc, first ? 0u : 1u);
-          if (ck.npan == 2) mma_ss_k64<2, 2>(d, da + desc_off(S::kPanelA), db + desc_off(S::kPanelB), idesc, 1u);
-          mma_commit(&empty_bar[slot]);
-          mma_commit(&bempty_bar[bslot]);
+        if constexpr (SH) {
+          // stage c: gathered key rows of chunk c; head rows q_c (and dO_c
+          // for the 512-wide part, where the same rows act as value rows)
+          for (int c = 0; c < nS; ++c, ++g) {
+            const int slot = g % S::kNA;
+            ok = mbar_wait_poll(&full_bar[slot], (g / S::kNA) & 1, &abort_flag, gerr);
+            if (!ok) break;
+            tc_fence_after();
+            const Chunk ck = chunk_of(c, nS);
+            const uint64_t da = dbase + desc_off(slot * S::kA);
+            const int bs0 = gb % S::kNB;
+            const uint64_t db0 = dbase + desc_off(S::kBOff + bs0 * S::kB);
+            mma_ss_k64<2, 2>(tS, da, db0, idesc, c == 0 ? 0u : 1u);
+            if (ck.npan == 2) mma_ss_k64<2, 2>(tS, da + desc_off(S::kPanelA), db0 + desc_off(S::kPanelB), idesc, 1u);
+            mma_commit(&bempty_bar[bs0]);
+            ++gb;
+            if (ck.kind == 0) {
+              const int bs1 = gb % S::kNB;
+              const uint64_t db1 = dbase + desc_off(S::kBOff + bs1 * S::kB);
+              mma_ss_k64<2, 2>(tP, da, db1, idesc, c == 0 ? 0u : 1u);
+              mma_ss_k64<2, 2>(tP, da + desc_off(S::kPanelA), db1 + desc_off(S::kPanelB), idesc, 1u);
+              mma_commit(&bempty_bar[bs1]);
+              ++gb;
+            }
+            mma_commit(&empty_bar[slot]);
+          }
+        } else {
+          for (int c = 0; c < nchunks; ++c, ++g) {
+            const int slot = g % S::kNA, bslot = g % S::kNB;
+            ok = mbar_wait_poll(&full_bar[slot], (g / S::kNA) & 1, &abort_flag, gerr);
+            if (!ok) break;
+            tc_fence_after();
+            const Chunk ck = chunk_of(c, nS);
+            const uint64_t da = dbase + desc_off(slot * S::kA);
+            const uint64_t db = dbase + desc_off(S::kBOff + bslot * S::kB);
+            const uint32_t d = c < nS ? tS : tP;
+            const bool first = (c == 0 || c == nS);
+            mma_ss_k64<2, 2>(d, da, db, idesc, first ? 0u : 1u);
+            if (ck.npan == 2) mma_ss_k64<2, 2>(d, da + desc_off(S::kPanelA), db + desc_off(S::kPanelB), idesc, 1u);
+            mma_commit(&empty_bar[slot]);
+            mma_commit(&bempty_bar[bslot]);
+          }
         }
         if (!ok) break;
         mma_commit(&tfull_bar[set]);
@@ -138,31 +176,61 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
   } else if (warp == 13) {
     // ---------------------------------------------------------------- head-row operand (TMA)
     if (lane == 0) {
-      int g = 0;
+      int g = 0, gb = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
         const int t = p.tok0 + item / ntiles;
-        for (int c = 0; c < nchunks && ok; ++c, ++g) {
-          const int bslot = g % kBSlots;
-          ok = mbar_wait(&bempty_bar[bslot], ((g / kBSlots) & 1) ^ 1, &abort_flag, gerr);
-          if (!ok) break;
-          const Chunk ck = chunk_of(c, nS);
-          const uint32_t b = smem_u32(smem + S::kBOff + bslot * S::kB);
-          uint64_t* fb = &full_bar[g % kSlots];
-          mbar_expect_tx(fb, ck.npan * S::kPanelB);
-          const CUtensorMap* mq = ck.kind == 0 ? &maps.q : ck.kind == 1 ? &maps.qr : &maps.dO;
-          for (int pn = 0; pn < ck.npan; ++pn) tma_2d(b + pn * S::kPanelB, mq, ck.f0 + pn * 64, t * p.G, fb);
+        if constexpr (SH) {
+          for (int c = 0; c < nS && ok; ++c, ++g) {
+            const Chunk ck = chunk_of(c, nS);
+            uint64_t* fb = &full_bar[g % S::kNA];
+            const int nb = ck.kind == 0 ? 2 : 1;
+            // The stage barrier's previous phase (stage g - 2) must be over
+            // before this stage's transactions are posted on it; the head-row
+            // slot waits alone do not imply that once a one-load rope stage
+            // shifts the head-row sequence.
+            ok = mbar_wait(&empty_bar[g % S::kNA], ((g / S::kNA) & 1) ^ 1, &abort_flag, gerr);
+            if (!ok) break;
+            for (int j = 0; j < nb && ok; ++j, ++gb) {
+              const int bslot = gb % S::kNB;
+              ok = mbar_wait(&bempty_bar[bslot], ((gb / S::kNB) & 1) ^ 1, &abort_flag, gerr);
+              if (!ok) break;
+              const uint32_t b = smem_u32(smem + S::kBOff + bslot * S::kB);
+              mbar_expect_tx(fb, ck.npan * S::kPanelB);
+              const CUtensorMap* mq = j == 1 ? &maps.dO : ck.kind == 0 ? &maps.q : &maps.qr;
+              for (int pn = 0; pn < ck.npan; ++pn) tma_2d(b + pn * S::kPanelB, mq, ck.f0 + pn * 64, t * p.G, fb);
+            }
+            if (ok && nb == 1) mbar_arrive(fb);   // the stage barrier counts two head-row arrivals
+          }
+        } else {
+          for (int c = 0; c < nchunks && ok; ++c, ++g) {
+            const int bslot = g % S::kNB;
+            ok = mbar_wait(&bempty_bar[bslot], ((g / S::kNB) & 1) ^ 1, &abort_flag, gerr);
+            if (!ok) break;
+            const Chunk ck = chunk_of(c, nS);
+            const uint32_t b = smem_u32(smem + S::kBOff + bslot * S::kB);
+            uint64_t* fb = &full_bar[g % S::kNA];
+            mbar_expect_tx(fb, ck.npan * S::kPanelB);
+            const CUtensorMap* mq = ck.kind == 0 ? &maps.q : ck.kind == 1 ? &maps.qr : &maps.dO;
+            for (int pn = 0; pn < ck.npan; ++pn) tma_2d(b + pn * S::kPanelB, mq, ck.f0 + pn * 64, t * p.G, fb);
+          }
         }
       }
     }
     __syncwarp();
   } else if (warp <= 3 || warp == 12) {
     // ---------------------------------------------------------------- gather producers
-    const int me = warp == 12 ? 3 : warp - 1;   // owned stage slot
+    // Without SH warp me owns slot me and all 128 rows of its stages; with SH
+    // warps 2s and 2s+1 share slot s, one half of the rows each.
+    const int me = warp == 12 ? 3 : warp - 1;
+    const int slot = SH ? (me >> 1) : me;
+    const int r0 = SH ? (me & 1) * (kKeys / 2) : 0;
+    const int r1 = SH ? r0 + kKeys / 2 : kKeys;
+    const int nst = SH ? nS : nchunks;           // stages that gather rows
     const T* k = static_cast<const T*>(p.k);
     const T* kr = static_cast<const T*>(p.kr);
     const T* v = static_cast<const T*>(p.v);
-    const uint32_t a = smem_u32(smem + me * S::kA);
+    const uint32_t a = smem_u32(smem + slot * S::kA);
     int* rows = rows_s[me];
     // the 128 kv rows (-1: masked) of an item, loaded one item ahead
     auto rows_of = [&](int item) {
@@ -174,14 +242,14 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
     int g = 0, loaded_item = -1;
     bool ok = true;
     for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
-      for (int c = 0; c < nchunks; ++c, ++g) {
-        if (g % kSlots != me) continue;
+      for (int c = 0; c < nst; ++c, ++g) {
+        if (g % S::kNA != slot) continue;
         if (loaded_item != item) {
           *reinterpret_cast<int4*>(rows + 4 * lane) = next4;
           next4 = rows_of(item + gridDim.x);
           loaded_item = item;
         }
-        if (lane == 0) ok = mbar_wait(&empty_bar[me], ((g / kSlots) & 1) ^ 1, &abort_flag, gerr);
+        if (lane == 0) ok = mbar_wait(&empty_bar[slot], ((g / S::kNA) & 1) ^ 1, &abort_flag, gerr);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         __syncwarp();
         if (!ok) break;
@@ -194,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
           const uint32_t dst0 = a + ((lane >> 3) & 1) * S::kPanelA;
           const uint32_t c = lane & 7;
 #pragma unroll 8
-          for (int r = lane >> 4; r < kKeys; r += 2) {
+          for (int r = r0 + (lane >> 4); r < r1; r += 2) {
             const int row = rows[r];
             cp_async16(dst0 + r * 128 + ((c ^ (r & 7)) << 4), base + (size_t)(row < 0 ? 0 : row) * 512,
                        row < 0 ? 0u : 16u);
@@ -203,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
           const T* base = kr + (lane & 7) * 8;
           const uint32_t c = lane & 7;
 #pragma unroll 8
-          for (int r = lane >> 3; r < kKeys; r += 4) {
+          for (int r = r0 + (lane >> 3); r < r1; r += 4) {
             const int row = rows[r];
             cp_async16(a + r * 128 + ((c ^ (r & 7)) << 4), base + (size_t)(row < 0 ? 0 : row) * 64, row < 0 ? 0u : 16u);
           }
@@ -211,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
         cp_async_commit();
         cp_async_wait<0>();
         fence_async_smem();
-        mbar_arrive(&full_bar[me]);
+        mbar_arrive(&full_bar[slot]);
       }
     }
   } else if (warp >= 4 && warp < 12) {
@@ -361,11 +429,12 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
   }
 }
 
-template <typename T, int GP, int MODE>
+template <typename T, int GP, int MODE, bool SH = false>
 cudaError_t launch_one(const Maps& maps, const Prob& p, void* out_p, void* out_ds, float* tile_stats, int* gerr, int nsm,
                        cudaStream_t st) {
-  auto kern = sdp_kernel<T, GP, MODE>;
-  const int smem = SdpSmem<GP>::kBytes > kOneCtaSmem ? SdpSmem<GP>::kBytes : kOneCtaSmem;
+  auto kern = sdp_kernel<T, GP, MODE, SH>;
+  using S = SdpSmem<GP, SH>;
+  const int smem = S::kBytes > kOneCtaSmem ? S::kBytes : kOneCtaSmem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int nitems = p.ntok * (p.Kpad / kKeys);
@@ -380,11 +449,15 @@ cudaError_t launch_one(const Maps& maps, const Prob& p, void* out_p, void* out_d
 template <typename T>
 cudaError_t launch_sdp(const Maps& maps, const Prob& p, int mode, void* out_p, void* out_ds, float* tile_stats, int* gerr, int nsm,
                        cudaStream_t st) {
+  // key and value given as the same tensor: gather the rows once per stage
+  const bool shared_kv = p.k == p.v;
   if (p.Gp == 64) {
+    if (mode == kModeBwd && shared_kv) return launch_one<T, 64, kModeBwd, true>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
     if (mode == kModeBwd) return launch_one<T, 64, kModeBwd>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
     if (mode == kModeFwdStats) return launch_one<T, 64, kModeFwdStats>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
     return launch_one<T, 64, kModeFwdP>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
   }
+  if (mode == kModeBwd && shared_kv) return launch_one<T, 128, kModeBwd, true>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
   if (mode == kModeBwd) return launch_one<T, 128, kModeBwd>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
   if (mode == kModeFwdStats) return launch_one<T, 128, kModeFwdStats>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
   return launch_one<T, 128, kModeFwdP>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);

@@ -51,6 +51,38 @@ def test_grad_small(name, det):
         compare(f"{name}/{n}", x, ref[n], w.dtype)
 
 
+# Key and value given as one tensor (the documentation's own constraint,
+# 约束说明: value identical to key): the library gathers each key row once.
+SHARED_KV = {
+    "g128_shared": small_workload(N1=128, S1=4, S2=1024, K=640, seed=19),
+    "g64_shared_norope": small_workload(N1=64, S1=4, S2=700, K=300, Dr=0, seed=20),
+    "g16_shared_block_fp16": small_workload(N1=16, S1=6, S2=1024, K=40, block_size=8, index_kind="block",
+                                            dtype="fp16", std=0.5, seed=21),
+    "g64_shared_tnd": small_workload(name="tnd_shared", layout="TND", B=3, N1=64, K=200, mode=3, index_kind="causal",
+                                     kv_extra=150, T1=8, act_q=(3, 0, 5), seed=22),
+}
+
+
+@pytest.mark.parametrize("name", list(SHARED_KV))
+@pytest.mark.parametrize("det", [False, True])
+def test_grad_shared_kv(name, det):
+    w = SHARED_KV[name]
+    inp = make_inputs(w)
+    inp["v"] = inp["k"]
+    out, smax, ssum = oracle_saved(w, inp)
+    dev = {k: to_cuda(v) for k, v in inp.items() if k != "v"}
+    dev["v"] = dev["k"]
+    g = sfa.grad(dev["q"], dev["k"], dev["v"], dev["indices"], dev["d_out"], out.cuda(), smax.cuda(), ssum.cuda(),
+                 w.scale_value, deterministic=det, **gpu_call_kwargs(w, dev))
+    torch.cuda.synchronize()
+    ref = oracle.sfa_bwd(d_out=inp["d_out"], out=out, softmax_max=smax, softmax_sum=ssum, **oracle_kwargs(w, inp))
+    for n, x in zip(OUT_NAMES, g):
+        if ref[n] is None:
+            assert x is None
+            continue
+        compare(f"{name}/{n}", x, ref[n], w.dtype)
+
+
 @pytest.mark.parametrize("name", ["tiny", "g16_ragged", "g64_tnd", "g16_block_fp16", "g32_padding_dups"])
 def test_decode_bit_exact(name):
     w = SMALL[name]
@@ -179,6 +211,37 @@ def test_full_size_sampled(name):
     compare(f"{name}/dk_rope", dkr.reshape(T2, -1)[keys], ref["dk_rope"].reshape(T2, -1)[keys], w.dtype)
     for x in g:
         assert torch.isfinite(x.float()).all()
+
+
+def test_full_size_shared_kv_sampled():
+    """MLA shape with value = key: the shared-row path against the oracle on
+    sampled tokens and key rows, and against the path that gathers value rows
+    separately (the same tensor passed as two buffers) within tolerance."""
+    w = WORKLOADS["mla"]
+    inp = make_inputs(w)
+    inp["v"] = inp["k"]
+    dev = {k: to_cuda(v) for k, v in inp.items() if k != "v"}
+    dev["v"] = dev["k"]
+    kw = gpu_call_kwargs(w, dev)
+    out, smax, ssum = sfa.fwd(dev["q"], dev["k"], dev["v"], dev["indices"], w.scale_value, **kw)
+    g = sfa.grad(dev["q"], dev["k"], dev["v"], dev["indices"], dev["d_out"], out, smax, ssum, w.scale_value, **kw)
+    g_sep = sfa.grad(dev["q"], dev["k"], dev["k"].clone(), dev["indices"], dev["d_out"], out, smax, ssum,
+                     w.scale_value, **kw)
+    torch.cuda.synchronize()
+    T1, T2 = w.S1, w.S2
+    rng = np.random.default_rng(1)
+    toks = np.sort(rng.choice(T1, size=4, replace=False))
+    keys = np.sort(rng.choice(T2, size=6, replace=False))
+    ref = oracle.sfa_bwd(d_out=inp["d_out"], out=out.cpu(), softmax_max=smax.cpu(), softmax_sum=ssum.cpu(),
+                         token_rows=toks, key_rows=keys, **oracle_kwargs(w, inp))
+    dq, dk, dv, dqr, dkr = g
+    compare("shared/dq", dq.reshape(T1, -1)[toks], ref["dq"].reshape(T1, -1)[toks], w.dtype)
+    compare("shared/dq_rope", dqr.reshape(T1, -1)[toks], ref["dq_rope"].reshape(T1, -1)[toks], w.dtype)
+    compare("shared/dk", dk.reshape(T2, -1)[keys], ref["dk"].reshape(T2, -1)[keys], w.dtype)
+    compare("shared/dv", dv.reshape(T2, -1)[keys], ref["dv"].reshape(T2, -1)[keys], w.dtype)
+    compare("shared/dk_rope", dkr.reshape(T2, -1)[keys], ref["dk_rope"].reshape(T2, -1)[keys], w.dtype)
+    for n, a, b in zip(OUT_NAMES, g, g_sep):
+        compare(f"shared_vs_separate/{n}", a, b.float().cpu().double().numpy(), w.dtype)
 
 
 @pytest.mark.parametrize("name", ["mla"])
