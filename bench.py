@@ -122,26 +122,41 @@ def dist_info():
 
 
 def cpu_oracle_sample(w, inp, n_tokens: int):
-    """Runs the fp64 oracle backward on the first n_tokens query tokens of the
-    workload (full K/V); returns (seconds, flops, sample description)."""
+    """Runs the fp64 oracle backward on a few query tokens of the workload with
+    their full K/V segment; returns (seconds, flops, sample description).
+    BSND: the first n tokens of batch 0.  TND: the last n tokens of the first
+    non-empty batch, which keeps each token's causal limit kvlen - qlen + i."""
     import oracle
     sub = {}
-    B, S1 = w.B, w.S1
-    n = min(n_tokens, S1)
-    sl = slice(0, n)
-    sub["q"] = inp["q"][:1, sl]
-    sub["q_rope"] = inp["q_rope"][:1, sl]
-    sub["d_out"] = inp["d_out"][:1, sl]
-    sub["indices"] = inp["indices"][:1, sl]
-    kw = dict(k=inp["k"][:1], v=inp["v"][:1], k_rope=inp["k_rope"][:1], scale=w.scale_value,
-              sparse_block_size=w.block_size, layout="BSND", sparse_mode=w.mode)
+    if w.layout == "TND":
+        aq = inp["act_seq_q"].tolist()
+        akv = inp["act_seq_kv"].tolist()
+        b = next(i for i, x in enumerate(aq) if x > 0)
+        q0, kv0, qlen, kvlen = sum(aq[:b]), sum(akv[:b]), aq[b], akv[b]
+        n = min(n_tokens, qlen)
+        sl = slice(q0 + qlen - n, q0 + qlen)
+        kvs = slice(kv0, kv0 + kvlen)
+        for name in ("q", "q_rope", "d_out", "indices"):
+            sub[name] = inp[name][sl]
+        kw = dict(k=inp["k"][kvs], v=inp["v"][kvs], k_rope=inp["k_rope"][kvs], scale=w.scale_value,
+                  sparse_block_size=w.block_size, layout="TND", sparse_mode=w.mode,
+                  act_seq_q=torch.tensor([n], dtype=torch.int32), act_seq_kv=torch.tensor([kvlen], dtype=torch.int32))
+        what = f"last {n} query tokens of batch {b} of {w.name} (its full K/V segment), fp64 numpy"
+    else:
+        n = min(n_tokens, w.S1)
+        sl = slice(0, n)
+        for name in ("q", "q_rope", "d_out", "indices"):
+            sub[name] = inp[name][:1, sl]
+        kw = dict(k=inp["k"][:1], v=inp["v"][:1], k_rope=inp["k_rope"][:1], scale=w.scale_value,
+                  sparse_block_size=w.block_size, layout="BSND", sparse_mode=w.mode)
+        what = f"first {n} query tokens of {w.name} (full K/V), fp64 numpy"
     out, smax, ssum = oracle.sfa_fwd(q=sub["q"], indices=sub["indices"], q_rope=sub["q_rope"], **kw)
     t0 = time.perf_counter()
     oracle.sfa_bwd(q=sub["q"], indices=sub["indices"], q_rope=sub["q_rope"], d_out=sub["d_out"], out=out,
                    softmax_max=smax, softmax_sum=ssum, **kw)
     dt = time.perf_counter() - t0
     pairs = int((sub["indices"] >= 0).sum().item()) * w.block_size
-    return dt, pairs * w.N1 * FLOPS_PER_QHK, f"first {n} query tokens of {w.name} (full K/V), fp64 numpy"
+    return dt, pairs * w.N1 * FLOPS_PER_QHK, what
 
 
 def cpu_cores():
@@ -305,7 +320,7 @@ def run_sfa(args):
     h_out, h_m, h_l = out.cpu().pin_memory(), smax.cpu().pin_memory(), ssum.cpu().pin_memory()
     res_host = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
     in_list = [host["q"], host["k"], host["v"], host["indices"], host["d_out"], h_out, h_m, h_l, host["q_rope"],
-               host["k_rope"]]
+               host["k_rope"], host.get("act_seq_q"), host.get("act_seq_kv")]
     if args.shared_kv:
         in_list[2] = None          # the value buffer is the key buffer
     dev_in = [x.to(dev) if x is not None else None for x in in_list]
@@ -320,12 +335,12 @@ def run_sfa(args):
         for dst, src in zip(dev_in, in_list):
             if src is not None:
                 dst.copy_(src, non_blocking=True)
-        q_, k_, v_, idx_, do_, o_, m_, l_, qr_, kr_ = dev_in
+        q_, k_, v_, idx_, do_, o_, m_, l_, qr_, kr_, aq_, akv_ = dev_in
         if args.shared_kv:
             v_ = k_
         sfa.grad(q_, k_, v_, idx_, do_, o_, m_, l_, w.scale_value, q_rope=qr_, k_rope=kr_,
                  sparse_block_size=w.block_size, layout=w.layout, sparse_mode=w.mode, deterministic=det,
-                 outputs=outs, workspace=ws)
+                 act_seq_q=aq_, act_seq_kv=akv_, outputs=outs, workspace=ws)
         for dst, src in zip(res_host, outs):
             dst.copy_(src, non_blocking=True)
         e1.record(stream)
