@@ -361,24 +361,37 @@ def run_sfa(args):
         return 0
 
     peaks, peak_src = load_peaks()
-    # dominant kernel and its roofline
-    dom = max(range(launches), key=lambda j: per_launch[j])
-    dname = names[dom] if dom < len(names) else f"launch{dom}"
-    G, Kp = w.N1, w.keff
+    # Dominant kernel (largest summed time per step; a workload in several
+    # token chunks launches each kernel once per chunk) and its roofline:
+    # algorithmic work of all its launches over their summed time, which is the
+    # per-launch work over the mean launch duration.
+    by_name, n_by_name = {}, {}
+    for j in range(launches):
+        nm = names[j] if j < len(names) else f"launch{j}"
+        by_name[nm] = by_name.get(nm, 0.0) + per_launch[j]
+        n_by_name[nm] = n_by_name.get(nm, 0) + 1
+    dname = max(by_name, key=by_name.get)
+    k_ms, k_n = by_name[dname], n_by_name[dname]
+    G = w.N1
     if dname in ("sdp", "dq"):
         fl = pairs * G * 2 * ((576 + 512) if dname == "sdp" else 576)
-        achieved = fl / (per_launch[dom] * 1e-3) / 1e12
+        achieved = fl / (k_ms * 1e-3) / 1e12
         peak = peaks["bf16_tflops"]
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak}
     else:
         # key-side contraction: algorithmic bytes = the fp32 reductions of the
         # key rows, 1088 floats = 4352 B per valid (query, key) pair
         by = pairs * 1088 * 4
-        achieved = by / (per_launch[dom] * 1e-3) / 1e9
+        achieved = by / (k_ms * 1e-3) / 1e9
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak}
-    roof["traffic"] = args.traffic if args.traffic is not None else kernel_traffic(dname, p.T1)
+    if args.traffic is not None:
+        roof["traffic"] = args.traffic                        # given per launch
+    else:
+        tr = kernel_traffic(dname, p.T1)                      # all tokens of the step
+        roof["traffic"] = None if tr is None else tr / k_n    # per launch
     roof["kernel"] = dname
+    roof["launches_per_step"] = k_n
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
 
     cpu = None
