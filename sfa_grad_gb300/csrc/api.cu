@@ -220,6 +220,18 @@ struct Marks {
   }
 };
 
+// Key tiles per key-side work item.  The fp32 accumulator rows one batch's
+// tokens reduce into span its KV extent (S2, or the mean TND segment).  When
+// that stays well inside the 129 MB L2, token-major order is best (one group
+// of all tiles).  Otherwise groups of four tiles run tile-group major, so
+// that with sorted index lists the concurrent reductions share a narrow band
+// of key rows.
+int kvq_tile_group(const Plan& P) {
+  const int64_t rows = P.layout == SFA_LAYOUT_BSND ? (int64_t)P.S2 : (int64_t)P.T2 / (P.B > 0 ? P.B : 1);
+  const int64_t bytes = rows * 1088 * 4;
+  return bytes <= (int64_t)64 << 20 ? P.Kpad / 128 : 4;
+}
+
 int64_t launch_count(const Plan& P) {
   const int64_t chunks = P.T1 > 0 ? (P.T1 + P.chunk - 1) / P.chunk : 0;
   return (P.layout == SFA_LAYOUT_TND ? 1 : 0) + 2 + chunks * (P.det ? 6 : 3) + 1;
@@ -278,7 +290,7 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
       SFA_CK(launch_dq<T>(maps, pr, 0, dq, P.has_rope ? dqr : nullptr, gerr, nsm, st));
       SFA_CK(mk.mark(st));
     } else {
-      SFA_CK(launch_kvq<T>(maps, pr, acc, dq, P.has_rope ? dqr : nullptr, gerr, nsm, st));
+      SFA_CK(launch_kvq<T>(maps, pr, acc, dq, P.has_rope ? dqr : nullptr, kvq_tile_group(P), gerr, nsm, st));
       SFA_CK(mk.mark(st));
     }
   }

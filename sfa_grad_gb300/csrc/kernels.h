@@ -22,9 +22,11 @@ cudaError_t launch_dkv(const Maps& maps, const Prob& p, float* acc, float* parti
 
 // Key-side and query-side contractions in one launch, two pipelines per CTA
 // (kvq.cu): non-deterministic key-side reductions into acc, dQ / dQRope out.
+// tile_group: key tiles per key-side work item (items run tile-group major;
+// a group of all tiles gives token-major order).
 template <typename T>
-cudaError_t launch_kvq(const Maps& maps, const Prob& p, float* acc, void* dq, void* dqr, int* gerr, int nsm,
-                       cudaStream_t st);
+cudaError_t launch_kvq(const Maps& maps, const Prob& p, float* acc, void* dq, void* dqr, int tile_group, int* gerr,
+                       int nsm, cudaStream_t st);
 
 // Query-side contraction (dq.cu): dQ = dS K (mode 0) or O = P V (mode 1).
 template <typename T>

@@ -54,6 +54,27 @@ __device__ __forceinline__ void kv_chunk(int ch, int& ncol, int& col0) {
   else { ncol = 128; col0 = 576 + (ch - 5) * 128; }
 }
 
+// Key-side work item: (tile group, token, feature chunk), tile-group major,
+// `tg` tiles per group.  With sorted index lists a token's consecutive
+// 128-slot tiles cover ascending key ranges, so while every SM works on the
+// same group of tiles the reductions land in a narrow band of key rows that
+// stays in L2 even when the whole accumulator does not fit.  When it does
+// fit, one group spans all tiles (token-major order, the head rows of a
+// chunk loaded once per token).
+struct KvItem {
+  int tl, ch, kt0, kt1;
+};
+__device__ __forceinline__ KvItem kv_item(int item, int ntok, int ntiles, int tg) {
+  const int per = ntok * kKvChunks;
+  const int grp = item / per, r = item - grp * per;
+  KvItem it;
+  it.tl = r / kKvChunks;
+  it.ch = r - it.tl * kKvChunks;
+  it.kt0 = grp * tg;
+  it.kt1 = it.kt0 + tg < ntiles ? it.kt0 + tg : ntiles;
+  return it;
+}
+
 __device__ __forceinline__ void red_add_v4(float* dst, float4 x) {
   asm volatile("red.global.add.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(dst), "f"(x.x), "f"(x.y), "f"(x.z), "f"(x.w)
                : "memory");
@@ -61,7 +82,7 @@ __device__ __forceinline__ void red_add_v4(float* dst, float4 x) {
 
 template <typename T, int GP>
 __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant__ Maps maps, Prob p, float* acc,
-                                                          T* dq, T* dqr, int* gerr) {
+                                                          T* dq, T* dqr, int tg, int* gerr) {
   using E = Elt<T>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -73,7 +94,7 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntiles = p.Kpad / kKeys;
-  const int nkv = p.ntok * kKvChunks;
+  const int nkv = (ntiles + tg - 1) / tg * p.ntok * kKvChunks;
   const int qchunks = p.Kpad / kQSlots;
   const int nq = p.ntok * kQParts;
 
@@ -120,13 +141,13 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
       const uint64_t da0 = sdesc_kmajor(smem_u32(smem + kKvA), 0);
       const uint64_t db0 = sdesc_mnmajor(smem_u32(smem + kKvB), 0, GP);
       for (int item = blockIdx.x; item < nkv && ok; item += gridDim.x, ++icount) {
-        const int ch = item % kKvChunks;
+        const KvItem ki = kv_item(item, p.ntok, ntiles, tg);
         int ncol, col0;
-        kv_chunk(ch, ncol, col0);
+        kv_chunk(ki.ch, ncol, col0);
         const uint32_t idesc = idesc_f16(kKeys, ncol, E::is_f16, false, true);
         ok = mbar_wait_poll(&kv_bfull, icount & 1, &abort_flag, gerr);
         if (!ok) break;
-        for (int kt = 0; kt < ntiles && ok; ++kt, ++tcount) {
+        for (int kt = ki.kt0; kt < ki.kt1 && ok; ++kt, ++tcount) {
           const int set = tcount & 1;
           ok = mbar_wait_poll(&kv_tempty[set], ((tcount >> 1) & 1) ^ 1, &abort_flag, gerr);
           if (!ok) break;
@@ -157,7 +178,8 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
       bool ok = true;
       const uint32_t b = smem_u32(smem + kKvB);
       for (int item = blockIdx.x; item < nkv && ok; item += gridDim.x, ++icount) {
-        const int tl = item / kKvChunks, ch = item % kKvChunks;
+        const KvItem ki = kv_item(item, p.ntok, ntiles, tg);
+        const int tl = ki.tl, ch = ki.ch;
         const int t = p.tok0 + tl;
         int ncol, col0;
         kv_chunk(ch, ncol, col0);
@@ -175,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
           tma_2d(b + pb * (GP * 128), mp, x, y, &kv_bfull);
         }
         const CUtensorMap* mA = ch < 5 ? &maps.dS : &maps.P;
-        for (int kt = 0; kt < ntiles && ok; ++kt) {
+        for (int kt = ki.kt0; kt < ki.kt1 && ok; ++kt) {
           const int y0 = tl * p.Kpad + kt * kKeys;
           for (int hp = 0; hp < GP / 64 && ok; ++hp) {
             ok = mbar_wait(&kv_empty[stage], phase ^ 1, &abort_flag, gerr);
@@ -206,23 +228,24 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
     int tcount = 0;
     // the row id of the group's next tile is loaded one tile ahead
     auto row_of = [&](int item, int kt) {
-      return item < nkv ? p.rowtab[(size_t)(item / kKvChunks) * p.Kpad + kt * kKeys + key] : -1;
+      return item < nkv ? p.rowtab[(size_t)kv_item(item, p.ntok, ntiles, tg).tl * p.Kpad + kt * kKeys + key] : -1;
     };
     auto advance = [&](int& item, int& kt) {
-      if (++kt == ntiles) {
-        kt = 0;
+      if (++kt == kv_item(item, p.ntok, ntiles, tg).kt1) {
         item += gridDim.x;
+        kt = kv_item(item, p.ntok, ntiles, tg).kt0;
       }
     };
-    int nitem = blockIdx.x, nkt = 0;
+    int nitem = blockIdx.x, nkt = kv_item(blockIdx.x, p.ntok, ntiles, tg).kt0;
     if (grp) advance(nitem, nkt);
     int next_row = row_of(nitem, nkt);
     for (int item = blockIdx.x; item < nkv && !abort_flag; item += gridDim.x) {
-      const int ch = item % kKvChunks;
+      const KvItem ki = kv_item(item, p.ntok, ntiles, tg);
+      const int ch = ki.ch;
       int ncol, col0;
       kv_chunk(ch, ncol, col0);
       bool ok = true;
-      for (int kt = 0; kt < ntiles; ++kt, ++tcount) {
+      for (int kt = ki.kt0; kt < ki.kt1; ++kt, ++tcount) {
         const int set = tcount & 1;
         if (set != grp) continue;
         const int row = next_row;
@@ -379,29 +402,30 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
 }
 
 template <typename T, int GP>
-cudaError_t launch_gp(const Maps& maps, const Prob& p, float* acc, void* dq, void* dqr, int* gerr, int nsm,
-                      cudaStream_t st) {
+cudaError_t launch_gp(const Maps& maps, const Prob& p, float* acc, void* dq, void* dqr, int tile_group, int* gerr,
+                      int nsm, cudaStream_t st) {
   auto kern = kvq_kernel<T, GP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const int nitems = p.ntok * kKvChunks;
   const int grid = nitems < nsm ? nitems : nsm;
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, kThreads, kSmemBytes, st>>>(maps, p, acc, static_cast<T*>(dq), static_cast<T*>(dqr), gerr);
+  const int tg = tile_group < 1 ? 1 : tile_group;
+  kern<<<grid, kThreads, kSmemBytes, st>>>(maps, p, acc, static_cast<T*>(dq), static_cast<T*>(dqr), tg, gerr);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 template <typename T>
-cudaError_t launch_kvq(const Maps& maps, const Prob& p, float* acc, void* dq, void* dqr, int* gerr, int nsm,
-                       cudaStream_t st) {
-  if (p.Gp == 64) return launch_gp<T, 64>(maps, p, acc, dq, dqr, gerr, nsm, st);
-  return launch_gp<T, 128>(maps, p, acc, dq, dqr, gerr, nsm, st);
+cudaError_t launch_kvq(const Maps& maps, const Prob& p, float* acc, void* dq, void* dqr, int tile_group, int* gerr,
+                       int nsm, cudaStream_t st) {
+  if (p.Gp == 64) return launch_gp<T, 64>(maps, p, acc, dq, dqr, tile_group, gerr, nsm, st);
+  return launch_gp<T, 128>(maps, p, acc, dq, dqr, tile_group, gerr, nsm, st);
 }
 
-template cudaError_t launch_kvq<__nv_bfloat16>(const Maps&, const Prob&, float*, void*, void*, int*, int,
+template cudaError_t launch_kvq<__nv_bfloat16>(const Maps&, const Prob&, float*, void*, void*, int, int*, int,
                                                cudaStream_t);
-template cudaError_t launch_kvq<__half>(const Maps&, const Prob&, float*, void*, void*, int*, int, cudaStream_t);
+template cudaError_t launch_kvq<__half>(const Maps&, const Prob&, float*, void*, void*, int, int*, int, cudaStream_t);
 
 }  // namespace sfa

@@ -25,6 +25,8 @@ SMALL = {
     "g64_norope": small_workload(N1=64, S1=4, S2=700, K=256, Dr=0, seed=16),
     "g128_fp16": small_workload(N1=128, S1=3, S2=600, K=384, dtype="fp16", seed=17),
     "g4_bs64": small_workload(N1=4, S1=4, S2=4096, K=5, block_size=64, index_kind="block", seed=18),
+    # KV extent past 64 MB of fp32 key rows: key-side items run tile-group major
+    "g64_wide_kv": small_workload(N1=64, S1=4, S2=16384, K=640, seed=23),
 }
 
 
