@@ -166,9 +166,12 @@ bool make_maps(Maps* M, const Plan& P, const void* q, const void* qr, const void
   bool ok = encode2d(&M->q, f, q, 512, TG, P.Gp);
   ok = ok && encode2d(&M->qr, f, qr ? qr : q, qr ? 64 : 512, TG, P.Gp);
   ok = ok && encode2d(&M->dO, f, dO ? dO : q, 512, TG, P.Gp);
-  ok = ok && encode2d(&M->k, f, k, 512, T2, 1);
-  ok = ok && encode2d(&M->kr, f, kr ? kr : k, kr ? 64 : 512, T2, 1);
-  ok = ok && encode2d(&M->v, f, v, 512, T2, 1);
+  // key / value rows: one box = one selected block of bs rows (block-sparse
+  // indices, bs >= 8); unused with single-key indices
+  const uint32_t kb = P.bs >= 8 ? (uint32_t)P.bs : 1u;
+  ok = ok && encode2d(&M->k, f, k, 512, T2, kb);
+  ok = ok && encode2d(&M->kr, f, kr ? kr : k, kr ? 64 : 512, T2, kb);
+  ok = ok && encode2d(&M->v, f, v, 512, T2, kb);
   ok = ok && encode2d(&M->P, f, Pst, P.Gp, R, 64);
   ok = ok && encode2d(&M->dS, f, dSst ? dSst : Pst, P.Gp, R, 64);
   return ok;

@@ -66,7 +66,8 @@ __device__ __forceinline__ Chunk chunk_of(int c, int nS) {
   return Chunk{(c - nS) * 128, 2, 2};
 }
 
-template <typename T, int GP, int MODE, bool SH>
+// BLK: block-sparse indices (sparseBlockSize >= 8), key/value rows by TMA boxes.
+template <typename T, int GP, int MODE, bool SH, bool BLK>
 __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant__ Maps maps, Prob p, void* out_p, void* out_ds,
                                                           float* tile_stats, int* gerr) {
   using E = Elt<T>;
@@ -232,20 +233,43 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
     const T* v = static_cast<const T*>(p.v);
     const uint32_t a = smem_u32(smem + slot * S::kA);
     int* rows = rows_s[me];
-    // the 128 kv rows (-1: masked) of an item, loaded one item ahead
+    // Block-sparse indices (sparseBlockSize >= 8): a selected block is bs
+    // contiguous kv rows, fetched as one TMA box per 64-feature panel.  Lane
+    // i < nidx owns the i-th index of the warp's rows and keeps the first kv
+    // row of its block; a padding, negative or out-of-range index reads rows
+    // below row 0, which arrive as zeros.  Keys of a block past the segment
+    // end or the causal limit hold finite data and are masked by the epilogue
+    // from the row table.
+    constexpr bool blk = BLK;
+    const int nidx = blk ? (r1 - r0) / p.bs : 0;
+    // an item's 128 kv rows (-1: masked), or with block indices the lane's
+    // first block row in .x, loaded one item ahead
     auto rows_of = [&](int item) {
-      if (item >= nitems) return make_int4(-1, -1, -1, -1);
+      if (item >= nitems) return make_int4(-p.bs, -1, -1, -1);
+      if constexpr (blk) {
+        const int tl = item / ntiles, kt = item % ntiles, t = p.tok0 + tl;
+        const int i = (kt * kKeys + r0) / p.bs + lane;
+        int y = -p.bs;
+        if (lane < nidx && i < p.Kidx) {
+          const int r = __ldg(p.idx + (size_t)t * p.Kidx + i);
+          const long long yy = (long long)p.meta[t].kv_start + r;
+          if (r >= 0 && yy < p.T2) y = (int)yy;
+        }
+        return make_int4(y, -1, -1, -1);
+      }
       return *reinterpret_cast<const int4*>(p.rowtab + (size_t)(item / ntiles) * p.Kpad + (item % ntiles) * kKeys +
                                             4 * lane);
     };
     int4 next4 = rows_of(blockIdx.x);
+    int cur_y = -p.bs;
     int g = 0, loaded_item = -1;
     bool ok = true;
     for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
       for (int c = 0; c < nst; ++c, ++g) {
         if (g % S::kNA != slot) continue;
         if (loaded_item != item) {
-          *reinterpret_cast<int4*>(rows + 4 * lane) = next4;
+          if (blk) cur_y = next4.x;
+          else *reinterpret_cast<int4*>(rows + 4 * lane) = next4;
           next4 = rows_of(item + gridDim.x);
           loaded_item = item;
         }
@@ -254,6 +278,17 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
         __syncwarp();
         if (!ok) break;
         const Chunk ck = chunk_of(c, nS);
+        if constexpr (blk) {
+          if (lane == 0) mbar_expect_tx(&full_bar[slot], (uint32_t)(nidx * p.bs * 128 * ck.npan));
+          __syncwarp();
+          if (lane < nidx) {
+            const CUtensorMap* mk = ck.kind == 0 ? &maps.k : ck.kind == 1 ? &maps.kr : &maps.v;
+            const uint32_t dst = a + (uint32_t)(r0 + lane * p.bs) * 128;
+            for (int pn = 0; pn < ck.npan; ++pn) tma_2d(dst + pn * S::kPanelA, mk, ck.f0 + pn * 64, cur_y, &full_bar[slot]);
+          }
+          if (lane != 0) mbar_arrive(&full_bar[slot]);
+          continue;
+        }
         // gathered rows, contiguous in global memory: with two panels a lane
         // owns 16-byte piece (lane & 15) of rows (lane >> 4) + 2i; with one
         // panel piece (lane & 7) of rows (lane >> 3) + 4i
@@ -409,7 +444,9 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
             const float x = valid ? fmaf(s[j + u], sl2, -st[h]) : -INFINITY;
             const float pp = ex2(x) * st[GP + h];
             pv[u] = pp;
-            dv[u] = bwd ? pp * fmaf(dp[j + u], p.scale, -st[2 * GP + h]) : 0.f;
+            // pp == 0 for a masked key: its dS is 0 even if the (unused) value
+            // row it was computed from is not finite
+            dv[u] = (bwd && pp != 0.f) ? pp * fmaf(dp[j + u], p.scale, -st[2 * GP + h]) : 0.f;
           }
           pk[j / 2] = E::pack(pv[0], pv[1]);
           dk[j / 2] = E::pack(dv[0], dv[1]);
@@ -432,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
 template <typename T, int GP, int MODE, bool SH = false>
 cudaError_t launch_one(const Maps& maps, const Prob& p, void* out_p, void* out_ds, float* tile_stats, int* gerr, int nsm,
                        cudaStream_t st) {
-  auto kern = sdp_kernel<T, GP, MODE, SH>;
+  auto kern = p.bs >= 8 ? sdp_kernel<T, GP, MODE, SH, true> : sdp_kernel<T, GP, MODE, SH, false>;
   using S = SdpSmem<GP, SH>;
   const int smem = S::kBytes > kOneCtaSmem ? S::kBytes : kOneCtaSmem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
