@@ -231,17 +231,8 @@ def kernel_traffic(name, tokens):
 
 
 def kernel_names(p, det):
-    names = []
-    if p.layout == 1:
-        names.append("batch_prefix")
-    names += ["meta", "dsum"]
     import sfa_grad_gb300 as sfa
-    chunk, _ = sfa.plan_info(p)
-    nch = (p.T1 + chunk - 1) // chunk
-    for _ in range(nch):
-        names += (["rowtab", "sdp", "sort_keys", "dkv", "det_reduce", "dq"] if det else ["rowtab", "sdp", "kvq"])
-    names.append("cast")
-    return names
+    return sfa.plan_names(p)
 
 
 def run_sfa(args):
@@ -373,8 +364,13 @@ def run_sfa(args):
     dname = max(by_name, key=by_name.get)
     k_ms, k_n = by_name[dname], n_by_name[dname]
     G = w.N1
-    if dname in ("sdp", "dq"):
-        fl = pairs * G * 2 * ((576 + 512) if dname == "sdp" else 576)
+    # contraction work per (query, head, key): sdp S and dP, kvb dK and dV,
+    # dq (and kvq when kvb took the key side) dQ
+    tensor_work = {"sdp": 576 + 512, "kvb": 576 + 512, "dq": 576}
+    if "kvb" in names:
+        tensor_work["kvq"] = 576
+    if dname in tensor_work:
+        fl = pairs * G * 2 * tensor_work[dname]
         achieved = fl / (k_ms * 1e-3) / 1e12
         peak = peaks["bf16_tflops"]
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak}
@@ -430,6 +426,50 @@ def run_sfa(args):
     return 0
 
 
+def run_forward(args):
+    """Times the companion forward sfa_fwd (out, softmaxMax, softmaxSum) on the
+    workload, same timing rules as the backward; one JSON line.  Work counted
+    as 2 * (576 + 512) flops per valid (query, head, key): S and P.V."""
+    import sfa_grad_gb300 as sfa
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w)
+    d = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
+    kw = dict(q_rope=d["q_rope"], k_rope=d["k_rope"], sparse_block_size=w.block_size, layout=w.layout,
+              sparse_mode=w.mode, act_seq_q=d.get("act_seq_q"), act_seq_kv=d.get("act_seq_kv"))
+    p = sfa.make_params(d["q"], d["k"], d["indices"], w.scale_value, layout=w.layout,
+                        sparse_block_size=w.block_size, sparse_mode=w.mode, has_rope=True,
+                        batch=w.B if w.layout == "TND" else None)
+    ws = torch.empty(max(sfa.fwd_workspace_size(p), 256), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    flops = valid_pairs(w, inp) * w.N1 * 2 * (576 + 512)
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        sfa.fwd(d["q"], d["k"], d["v"], d["indices"], w.scale_value, workspace=ws, **kw)
+    torch.cuda.synchronize()
+    times = []
+    for i in range(args.steps):
+        flush.fill_(i & 0xff)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        sfa.fwd(d["q"], d["k"], d["v"], d["indices"], w.scale_value, workspace=ws, **kw)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = statistics.mean(times)
+    peaks, peak_src = load_peaks()
+    value = flops / (ms * 1e-3) / 1e12
+    print(json.dumps({"metric": "sparse-attn fwd TFLOP/s (1×GB300)", "value": value, "unit": "TFLOP/s",
+                      "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                      "higher_is_better": True, "dtype": w.dtype, "data": "synthetic",
+                      "frac_of_dense_bf16_peak": value / peaks["bf16_tflops"], "peak_source": peak_src,
+                      "config": {"workload": workload_desc(w, False),
+                                 "l2": "flushed between steps (256 MB write, outside the events)"}}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -441,6 +481,7 @@ def main():
     ap.add_argument("--shared-kv", action="store_true",
                     help="pass the key tensor as the value tensor too (value identical to key)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--forward", action="store_true", help="time the companion forward sfa_fwd instead")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per launch of the dominant kernel from an ncu capture")
     args = ap.parse_args()
@@ -448,6 +489,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.forward:
+        return run_forward(args)
     return run_sfa(args)
 
 

@@ -146,13 +146,25 @@ sfa_status sfa_grad_profile(const sfa_params* p, const void* q, const void* k, c
 /*
  * Static plan of one sfa_grad call: *chunk_tokens = query tokens processed
  * per chunk of the staging buffers, *kernel_launches = number of kernels the
- * call launches (in order: [batch prefix (TND)], token metadata, Dsum, then
- * per chunk: row table, score/softmax-gradient, and either the combined
- * key-side + query-side contraction (deterministic = 0) or key sort, key-side
- * contraction, fixed-order reduction, query-side contraction (deterministic
- * = 1); finally the output cast).  Either output pointer may be null.
+ * call launches, in the order sfa_grad_plan_names lists them.  Either output
+ * pointer may be null.
  */
 sfa_status sfa_grad_plan_info(const sfa_params* p, int64_t* chunk_tokens, int64_t* kernel_launches);
+
+/*
+ * Names of the kernels one sfa_grad call launches, in launch order (the
+ * intervals the events of sfa_grad_profile delimit): "batch_prefix" (TND),
+ * "meta", "dsum", then per token chunk "rowtab", "sdp" and either "kvq"
+ * (combined key-side and query-side contractions), or "blk_count",
+ * "blk_scan", "blk_scatter", "kvb", "kvq" (block-sparse indices whose blocks
+ * many tokens select: pairs grouped by block start, key side accumulated per
+ * block, then the query side alone), or with deterministic = 1 "sort_keys",
+ * "dkv", "det_reduce", "dq"; finally "cast".  Writes at most `capacity`
+ * pointers to static strings into names[] (names may be null when capacity
+ * is 0) and the total count into *count (may be null).  Host only; validates
+ * *p like sfa_grad_workspace_size.
+ */
+sfa_status sfa_grad_plan_names(const sfa_params* p, const char** names, int32_t capacity, int32_t* count);
 
 /*
  * Companion forward that produces the backward's saved inputs (the page lists

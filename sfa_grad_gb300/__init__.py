@@ -26,7 +26,7 @@ SFA_ERR_SHAPE = 561002
 LAYOUTS = {"BSND": 0, "TND": 1}
 DTYPES = {torch.bfloat16: 0, torch.float16: 1}
 
-EXPORTS = ("sfa_grad_workspace_size", "sfa_grad", "sfa_grad_profile", "sfa_grad_plan_info",
+EXPORTS = ("sfa_grad_workspace_size", "sfa_grad", "sfa_grad_profile", "sfa_grad_plan_info", "sfa_grad_plan_names",
            "sfa_fwd_workspace_size", "sfa_fwd", "sfa_decode_keys", "sfa_read_device_error", "sfa_status_string",
            "sfa_last_error_message", "sfa_grad_noalloc")
 
@@ -71,6 +71,7 @@ def lib() -> ctypes.CDLL:
     L.sfa_grad.argtypes = [P] + [vp] * 18 + [sz, vp]
     L.sfa_grad_profile.argtypes = [P] + [vp] * 18 + [sz, vp, ctypes.POINTER(vp), ctypes.c_int32]
     L.sfa_grad_plan_info.argtypes = [P, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]
+    L.sfa_grad_plan_names.argtypes = [P, ctypes.POINTER(ctypes.c_char_p), ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]
     L.sfa_grad_noalloc.argtypes = [P] + [vp] * 17 + [vp]
     L.sfa_fwd.argtypes = [P] + [vp] * 12 + [sz, vp]
     L.sfa_decode_keys.argtypes = [P, vp, vp, vp, vp, vp, sz, vp]
@@ -80,7 +81,8 @@ def lib() -> ctypes.CDLL:
     L.sfa_status_string.argtypes = [ctypes.c_int32]
     L.sfa_status_string.restype = ctypes.c_char_p
     for name in ("sfa_grad_workspace_size", "sfa_fwd_workspace_size", "sfa_grad", "sfa_grad_profile",
-                 "sfa_grad_plan_info", "sfa_fwd", "sfa_decode_keys", "sfa_read_device_error", "sfa_grad_noalloc"):
+                 "sfa_grad_plan_info", "sfa_grad_plan_names", "sfa_fwd", "sfa_decode_keys", "sfa_read_device_error",
+                 "sfa_grad_noalloc"):
         getattr(L, name).restype = ctypes.c_int32
     _lib = L
     return L
@@ -147,6 +149,15 @@ def plan_info(p: SfaParams):
     c, n = ctypes.c_int64(0), ctypes.c_int64(0)
     _check(lib().sfa_grad_plan_info(ctypes.byref(p), ctypes.byref(c), ctypes.byref(n)), "sfa_grad_plan_info")
     return c.value, n.value
+
+
+def plan_names(p: SfaParams) -> list:
+    """Names of the kernels one sfa_grad call launches, in launch order."""
+    n = ctypes.c_int32(0)
+    _check(lib().sfa_grad_plan_names(ctypes.byref(p), None, 0, ctypes.byref(n)), "sfa_grad_plan_names")
+    buf = (ctypes.c_char_p * max(n.value, 1))()
+    _check(lib().sfa_grad_plan_names(ctypes.byref(p), buf, n.value, ctypes.byref(n)), "sfa_grad_plan_names")
+    return [buf[i].decode() for i in range(n.value)]
 
 
 def _stream(stream) -> int:

@@ -27,9 +27,11 @@ size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Plan {
   int layout, B, S1, S2, T1, T2, G, Gp, Kidx, bs, Keff, Kpad, mode, has_rope, det, is_f16;
+  int kvb;   // key-major dK / dV for block-sparse indices (kvb.cu)
   float scale;
   int chunk;
   size_t off_err, off_batch, off_meta, off_dsum, off_acc, off_P, off_dS, off_rows, off_part, off_skey, off_sslot, off_tstats;
+  size_t off_bcnt, off_bcur, off_bgrp, off_bbeg, off_bng, off_bent;
   size_t total;
 };
 
@@ -79,6 +81,12 @@ sfa_status validate(const sfa_params* p, bool fwd, Plan* out) {
   P.det = fwd ? 0 : p->deterministic;
   P.is_f16 = p->dtype == SFA_DTYPE_FP16;
   P.scale = (float)p->scale;
+  // Block-sparse indices selected by many tokens: group the (token, index)
+  // pairs by block start and accumulate each block's dK / dV in tensor memory
+  // (one accumulator write per block instead of one reduction per pair).
+  // Used when blocks hold >= 16 keys, at most 64 heads, and the average kv
+  // row is selected by >= 8 query tokens.
+  P.kvb = !fwd && !P.det && P.bs >= 16 && P.Gp == 64 && T2 > 0 && T1 * keff >= 8 * T2;
   // token chunking keeps the per-chunk staging bounded
   const size_t pds_per_tok = (size_t)P.Kpad * P.Gp * 2 * (fwd ? 1 : 2);
   size_t chunk = kPdsCap / pds_per_tok;
@@ -103,6 +111,13 @@ sfa_status validate(const sfa_params* p, bool fwd, Plan* out) {
   P.off_skey = o; o += P.det ? up(chunk * P.Kpad * 4) : 0;
   P.off_sslot = o; o += P.det ? up(chunk * P.Kpad * 4) : 0;
   P.off_tstats = o; o += fwd ? up(chunk * (P.Kpad / 128) * P.G * 2 * 4) : 0;
+  const size_t nb = P.kvb ? (size_t)P.T2 + P.bs : 0;    // block-start bins (start + bs)
+  P.off_bcnt = o; o += P.kvb ? up(nb * 4) : 0;
+  P.off_bcur = o; o += P.kvb ? up(nb * 4) : 0;
+  P.off_bgrp = o; o += P.kvb ? up(nb * 4) : 0;
+  P.off_bbeg = o; o += P.kvb ? up((nb + 1) * 4) : 0;
+  P.off_bng = o; o += P.kvb ? up(4) : 0;
+  P.off_bent = o; o += P.kvb ? up(chunk * P.Kidx * 4) : 0;
   P.total = o;
   return SFA_OK;
 }
@@ -155,6 +170,21 @@ bool encode2d(CUtensorMap* m, bool f16, const void* base, uint64_t cols, uint64_
   return fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
             strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Maps of the key-major block kernel: head rows with boxes of GK = G rounded
+// up to 16 rows (one token's heads), staged P^T / dS^T as in Maps.
+bool make_blk_maps(BlkMaps* M, const Plan& P, const void* q, const void* qr, const void* dO, const void* Pst,
+                   const void* dSst) {
+  const bool f = P.is_f16;
+  const uint64_t TG = (uint64_t)P.T1 * P.G, R = (uint64_t)P.chunk * P.Kpad;
+  const uint32_t gk = (uint32_t)((P.G + 15) / 16 * 16);
+  bool ok = encode2d(&M->q, f, q, 512, TG, gk);
+  ok = ok && encode2d(&M->qr, f, qr ? qr : q, qr ? 64 : 512, TG, gk);
+  ok = ok && encode2d(&M->dO, f, dO, 512, TG, gk);
+  ok = ok && encode2d(&M->P, f, Pst, P.Gp, R, 64);
+  ok = ok && encode2d(&M->dS, f, dSst, P.Gp, R, 64);
+  return ok;
 }
 
 // Maps of one call.  Tensors a call does not use (dO and dS in the forward,
@@ -235,10 +265,35 @@ int kvq_tile_group(const Plan& P) {
   return bytes <= (int64_t)64 << 20 ? P.Kpad / 128 : 4;
 }
 
-int64_t launch_count(const Plan& P) {
-  const int64_t chunks = P.T1 > 0 ? (P.T1 + P.chunk - 1) / P.chunk : 0;
-  return (P.layout == SFA_LAYOUT_TND ? 1 : 0) + 2 + chunks * (P.det ? 6 : 3) + 1;
+// Kernel launches of one sfa_grad call, in order (sfa_grad_plan_names).
+const char* const kChunkDet[] = {"rowtab", "sdp", "sort_keys", "dkv", "det_reduce", "dq"};
+const char* const kChunkKvq[] = {"rowtab", "sdp", "kvq"};
+const char* const kChunkKvb[] = {"rowtab", "sdp", "blk_count", "blk_scan", "blk_scatter", "kvb", "kvq"};
+
+int64_t plan_names(const Plan& P, const char** out, int64_t cap) {
+  int64_t n = 0;
+  auto put = [&](const char* s) {
+    if (n < cap && out) out[n] = s;
+    ++n;
+  };
+  if (P.T1 == 0) return 0;
+  if (P.layout == SFA_LAYOUT_TND) put("batch_prefix");
+  put("meta");
+  put("dsum");
+  const int64_t chunks = (P.T1 + P.chunk - 1) / P.chunk;
+  for (int64_t c = 0; c < chunks; ++c) {
+    if (P.det)
+      for (const char* s : kChunkDet) put(s);
+    else if (P.kvb)
+      for (const char* s : kChunkKvb) put(s);
+    else
+      for (const char* s : kChunkKvq) put(s);
+  }
+  put("cast");
+  return n;
 }
+
+int64_t launch_count(const Plan& P) { return plan_names(P, nullptr, 0); }
 
 template <typename T>
 sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const void* k, const void* v,
@@ -254,7 +309,9 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
   pr.dsum = reinterpret_cast<const float*>(ws + P.off_dsum);
   const int nsm = sm_count();
   Maps maps;
-  if (!make_maps(&maps, P, q, pr.qr, dO, k, pr.kr, v, ws + P.off_P, ws + P.off_dS)) {
+  BlkMaps bmaps;
+  if (!make_maps(&maps, P, q, pr.qr, dO, k, pr.kr, v, ws + P.off_P, ws + P.off_dS) ||
+      (P.kvb && !make_blk_maps(&bmaps, P, q, pr.qr, dO, ws + P.off_P, ws + P.off_dS))) {
     snprintf(g_last_error, sizeof(g_last_error), "tensor map encoding failed");
     return SFA_ERR_RUNTIME;
   }
@@ -291,6 +348,23 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
       SFA_CK(launch_det_reduce(pr, skey, sslot, part, acc, st));
       SFA_CK(mk.mark(st));
       SFA_CK(launch_dq<T>(maps, pr, 0, dq, P.has_rope ? dqr : nullptr, gerr, nsm, st));
+      SFA_CK(mk.mark(st));
+    } else if (P.kvb) {
+      int* bcnt = reinterpret_cast<int*>(ws + P.off_bcnt);
+      int* bcur = reinterpret_cast<int*>(ws + P.off_bcur);
+      int* bgrp = reinterpret_cast<int*>(ws + P.off_bgrp);
+      int* bbeg = reinterpret_cast<int*>(ws + P.off_bbeg);
+      int* bng = reinterpret_cast<int*>(ws + P.off_bng);
+      int* bent = reinterpret_cast<int*>(ws + P.off_bent);
+      SFA_CK(launch_blk_count(pr, bcnt, st));
+      SFA_CK(mk.mark(st));
+      SFA_CK(launch_blk_scan(bcnt, P.T2 + P.bs, bcur, bgrp, bbeg, bng, st));
+      SFA_CK(mk.mark(st));
+      SFA_CK(launch_blk_scatter(pr, bcur, bent, st));
+      SFA_CK(mk.mark(st));
+      SFA_CK(launch_kvb<T>(bmaps, pr, P.bs, bgrp, bbeg, bng, bent, acc, gerr, nsm, st));
+      SFA_CK(mk.mark(st));
+      SFA_CK(launch_kvq<T>(maps, pr, acc, dq, P.has_rope ? dqr : nullptr, 0, gerr, nsm, st));   // query side only
       SFA_CK(mk.mark(st));
     } else {
       SFA_CK(launch_kvq<T>(maps, pr, acc, dq, P.has_rope ? dqr : nullptr, kvq_tile_group(P), gerr, nsm, st));
@@ -378,6 +452,16 @@ sfa_status sfa_grad_plan_info(const sfa_params* p, int64_t* chunk_tokens, int64_
   if (s != SFA_OK) return s;
   if (chunk_tokens) *chunk_tokens = P.chunk;
   if (kernel_launches) *kernel_launches = P.T1 == 0 ? 0 : sfa::launch_count(P);
+  return SFA_OK;
+}
+
+sfa_status sfa_grad_plan_names(const sfa_params* p, const char** names, int32_t capacity, int32_t* count) {
+  if (!p) return SFA_ERR_NULLPTR;
+  Plan P;
+  sfa_status s = sfa::validate(p, false, &P);
+  if (s != SFA_OK) return s;
+  const int64_t n = sfa::plan_names(P, names, capacity > 0 ? capacity : 0);
+  if (count) *count = (int32_t)n;
   return SFA_OK;
 }
 

@@ -110,9 +110,18 @@ struct Maps {
   CUtensorMap q;    // (T1*G, 512), box 64 x GP
   CUtensorMap qr;   // (T1*G, 64),  box 64 x GP
   CUtensorMap dO;   // (T1*G, 512), box 64 x GP
-  CUtensorMap k;    // (T2, 512),   box 64 x 1 (row gathers)
-  CUtensorMap kr;   // (T2, 64),    box 64 x 1
-  CUtensorMap v;    // (T2, 512),   box 64 x 1
+  CUtensorMap k;    // (T2, 512),   box 64 x bs (block-sparse indices, bs >= 8), else unused
+  CUtensorMap kr;   // (T2, 64),    box 64 x bs
+  CUtensorMap v;    // (T2, 512),   box 64 x bs
+  CUtensorMap P;    // (chunk*Kpad, GP) staged P^T,  box 64 x 64
+  CUtensorMap dS;   // (chunk*Kpad, GP) staged dS^T, box 64 x 64
+};
+
+// Tensor maps of the key-major block kernel (kvb.cu).
+struct BlkMaps {
+  CUtensorMap q;    // (T1*G, 512), box 64 x GK (one token's heads, GK = G rounded up to 16)
+  CUtensorMap qr;   // (T1*G, 64),  box 64 x GK
+  CUtensorMap dO;   // (T1*G, 512), box 64 x GK
   CUtensorMap P;    // (chunk*Kpad, GP) staged P^T,  box 64 x 64
   CUtensorMap dS;   // (chunk*Kpad, GP) staged dS^T, box 64 x 64
 };

@@ -23,7 +23,18 @@ cudaError_t launch_dkv(const Maps& maps, const Prob& p, float* acc, float* parti
 // Key-side and query-side contractions in one launch, two pipelines per CTA
 // (kvq.cu): non-deterministic key-side reductions into acc, dQ / dQRope out.
 // tile_group: key tiles per key-side work item (items run tile-group major;
-// a group of all tiles gives token-major order).
+// a group of all tiles gives token-major order); 0 runs the query side only.
+// Key-major dK / dV for block-sparse indices (kvb.cu): group the chunk's
+// (token, index) pairs by block start (count, scan, scatter), then accumulate
+// every group's block in tensor memory and add it to acc once.
+cudaError_t launch_blk_count(const Prob& p, int* cnt, cudaStream_t st);
+cudaError_t launch_blk_scan(const int* cnt, int nbins, int* cursor, int* groups, int* gbeg, int* ngroups,
+                            cudaStream_t st);
+cudaError_t launch_blk_scatter(const Prob& p, int* cursor, int* entries, cudaStream_t st);
+template <typename T>
+cudaError_t launch_kvb(const BlkMaps& maps, const Prob& p, int bs, const int* groups, const int* gbeg,
+                       const int* ngroups, const int* entries, float* acc, int* gerr, int nsm, cudaStream_t st);
+
 template <typename T>
 cudaError_t launch_kvq(const Maps& maps, const Prob& p, float* acc, void* dq, void* dqr, int tile_group, int* gerr,
                        int nsm, cudaStream_t st);

@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntiles = p.Kpad / kKeys;
-  const int nkv = (ntiles + tg - 1) / tg * p.ntok * kKvChunks;
+  const int nkv = tg > 0 ? (ntiles + tg - 1) / tg * p.ntok * kKvChunks : 0;   // tg = 0: query side only
   const int qchunks = p.Kpad / kQSlots;
   const int nq = p.ntok * kQParts;
 
@@ -332,12 +332,37 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
         *reinterpret_cast<int2*>(rows + 2 * lane) = r2;
         __syncwarp();
         if (!ok) break;
+        const bool blk = p.bs >= 8;
         if (lane == 0) {
-          mbar_expect_tx(&q_full[me], kHP * kQSlots * 128);
+          mbar_expect_tx(&q_full[me], kHP * kQSlots * 128 + (blk ? (kQCol / 64) * kQSlots * 128 : 0));
           for (int hp = 0; hp < kHP; ++hp)
             tma_2d(a + hp * (kQSlots * 128), &maps.dS, hp * 64, tl * p.Kpad + c * kQSlots, &q_full[me]);
         }
-        if (lane < kCpr) {   // lane owns 16-byte piece `lane` of every gathered row
+        if (blk) {
+          // block-sparse indices: each selected block of bs kv rows is one TMA
+          // box per 64-feature panel (lane i < 64/bs owns the stage's i-th
+          // index); an index with no key at or above 0, past the last row or
+          // past the index list reads zeros from below row 0
+          __syncwarp();
+          const int nidx = kQSlots / p.bs;
+          if (lane < nidx) {
+            const int i = (c * kQSlots) / p.bs + lane;
+            const int t = p.tok0 + tl;
+            int y = -p.bs;
+            if (i < p.Kidx) {
+              const int r = __ldg(p.idx + (size_t)t * p.Kidx + i);
+              const long long yy = (long long)p.meta[t].kv_start + r;
+              if ((long long)r + p.bs > 0 && yy < p.T2) y = (int)yy;
+            }
+            for (int pn = 0; pn < kQCol / 64; ++pn) {
+              const int f = f0 + pn * 64;
+              const uint32_t dst = b + pn * (kQSlots * 128) + lane * p.bs * 128;
+              if (f < 512) tma_2d(dst, &maps.k, f, y, &q_full[me]);
+              else tma_2d(dst, p.has_rope ? &maps.kr : &maps.k, p.has_rope ? f - 512 : 0, p.has_rope ? y : -p.bs,
+                          &q_full[me]);
+            }
+          }
+        } else if (lane < kCpr) {   // lane owns 16-byte piece `lane` of every gathered row
           const int f = f0 + lane * 8;
           const bool rope = f >= 512;
           const T* base = rope ? (p.has_rope ? krope + (f - 512) : kmain) : kmain + f;
@@ -410,7 +435,7 @@ cudaError_t launch_gp(const Maps& maps, const Prob& p, float* acc, void* dq, voi
   const int nitems = p.ntok * kKvChunks;
   const int grid = nitems < nsm ? nitems : nsm;
   if (grid <= 0) return cudaSuccess;
-  const int tg = tile_group < 1 ? 1 : tile_group;
+  const int tg = tile_group < 0 ? 0 : tile_group;
   kern<<<grid, kThreads, kSmemBytes, st>>>(maps, p, acc, static_cast<T*>(dq), static_cast<T*>(dqr), tg, gerr);
   return cudaGetLastError();
 }

@@ -236,10 +236,10 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
     // Block-sparse indices (sparseBlockSize >= 8): a selected block is bs
     // contiguous kv rows, fetched as one TMA box per 64-feature panel.  Lane
     // i < nidx owns the i-th index of the warp's rows and keeps the first kv
-    // row of its block; a padding, negative or out-of-range index reads rows
-    // below row 0, which arrive as zeros.  Keys of a block past the segment
-    // end or the causal limit hold finite data and are masked by the epilogue
-    // from the row table.
+    // row of its block; an index with no key at or above 0, or past the last
+    // row, reads rows below row 0, which arrive as zeros.  Keys of a block
+    // outside its segment or past the causal limit hold finite data and are
+    // masked by the epilogue from the row table.
     constexpr bool blk = BLK;
     const int nidx = blk ? (r1 - r0) / p.bs : 0;
     // an item's 128 kv rows (-1: masked), or with block indices the lane's
@@ -251,9 +251,11 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
         const int i = (kt * kKeys + r0) / p.bs + lane;
         int y = -p.bs;
         if (lane < nidx && i < p.Kidx) {
+          // keys r .. r+bs-1; a start below 0 still covers keys 0 .. r+bs-1
+          // (rows below the segment, or below row 0, are masked or zeros)
           const int r = __ldg(p.idx + (size_t)t * p.Kidx + i);
           const long long yy = (long long)p.meta[t].kv_start + r;
-          if (r >= 0 && yy < p.T2) y = (int)yy;
+          if ((long long)r + p.bs > 0 && yy < p.T2) y = (int)yy;
         }
         return make_int4(y, -1, -1, -1);
       }

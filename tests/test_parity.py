@@ -27,6 +27,15 @@ SMALL = {
     "g4_bs64": small_workload(N1=4, S1=4, S2=4096, K=5, block_size=64, index_kind="block", seed=18),
     # KV extent past 64 MB of fp32 key rows: key-side items run tile-group major
     "g64_wide_kv": small_workload(N1=64, S1=4, S2=16384, K=640, seed=23),
+    # Blocks of >= 16 keys that many tokens select: the non-deterministic path
+    # groups the (token, index) pairs by block start (key-major dK / dV)
+    "g16_kvb_bs16": small_workload(N1=16, S1=64, S2=512, K=16, block_size=16, index_kind="block", seed=24),
+    "g16_kvb_bs32_unaligned": small_workload(N1=16, S1=48, S2=640, K=8, block_size=32, seed=25),
+    "g32_kvb_bs64_norope_fp16": small_workload(N1=32, S1=32, S2=512, K=4, block_size=64, index_kind="block", Dr=0,
+                                               dtype="fp16", std=0.5, seed=26),
+    "g12_kvb_tnd_causal": small_workload(name="tnd_kvb", layout="TND", B=2, N1=12, K=6, block_size=16, mode=3,
+                                         index_kind="causal", kv_extra=64, T1=40, act_q=(24, 16), seed=27),
+    "g16_kvb_padding_dups": small_workload(N1=16, S1=32, S2=256, K=8, block_size=16, index_kind="random_any", seed=28),
 }
 
 
