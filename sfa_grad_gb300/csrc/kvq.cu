@@ -80,7 +80,11 @@ __device__ __forceinline__ void red_add_v4(float* dst, float4 x) {
                : "memory");
 }
 
-template <typename T, int GP>
+// BLK: block-sparse indices (sparseBlockSize >= 8): the query side loads key
+// rows as one TMA box per selected block.  A compile-time switch: the unused
+// branch in the row-gather loop alone costs the single-key path a quarter of
+// its query-side throughput.
+template <typename T, int GP, bool BLK>
 __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant__ Maps maps, Prob p, float* acc,
                                                           T* dq, T* dqr, int tg, int* gerr) {
   using E = Elt<T>;
@@ -332,13 +336,13 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
         *reinterpret_cast<int2*>(rows + 2 * lane) = r2;
         __syncwarp();
         if (!ok) break;
-        const bool blk = p.bs >= 8;
+        constexpr bool blk = BLK;
         if (lane == 0) {
           mbar_expect_tx(&q_full[me], kHP * kQSlots * 128 + (blk ? (kQCol / 64) * kQSlots * 128 : 0));
           for (int hp = 0; hp < kHP; ++hp)
             tma_2d(a + hp * (kQSlots * 128), &maps.dS, hp * 64, tl * p.Kpad + c * kQSlots, &q_full[me]);
         }
-        if (blk) {
+        if constexpr (blk) {
           // block-sparse indices: each selected block of bs kv rows is one TMA
           // box per 64-feature panel (lane i < 64/bs owns the stage's i-th
           // index); an index with no key at or above 0, past the last row or
@@ -429,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
 template <typename T, int GP>
 cudaError_t launch_gp(const Maps& maps, const Prob& p, float* acc, void* dq, void* dqr, int tile_group, int* gerr,
                       int nsm, cudaStream_t st) {
-  auto kern = kvq_kernel<T, GP>;
+  auto kern = p.bs >= 8 ? kvq_kernel<T, GP, true> : kvq_kernel<T, GP, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const int nitems = p.ntok * kKvChunks;

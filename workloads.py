@@ -72,6 +72,10 @@ WORKLOADS = {
     # MLA shape with 512 query tokens: the case the per-kernel profiles capture
     # (staged P/dS of 512 MB, larger than L2, a few GB on the device).
     "mla_q512": Workload("mla_q512", "BSND", B=1, S1=512, S2=4096, N1=128, K=2048, seed=106),
+    # Block-sparse shape with 2048 query tokens: the key-major block kernel's
+    # profiling case (2 GB of staged P/dS, 142 MB accumulator).
+    "block_q2048": Workload("block_q2048", "BSND", B=1, S1=2048, S2=32768, N1=16, K=64, block_size=64,
+                            dtype="fp16", std=0.5, seed=107, index_kind="block"),
 }
 
 
