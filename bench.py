@@ -121,6 +121,22 @@ def dist_info():
     return world, rank, local
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest x over the ranks of the default process group (x itself
+    when running alone).  Every rank must call it."""
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flops_per_rank: float, ms: float) -> float:
+    """Whole-job TFLOP/s: every rank runs flops_per_rank of work (independent
+    replicas, weak scaling) and the job takes the slowest rank's ms."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 def cpu_oracle_sample(w, inp, n_tokens: int):
     """Runs the fp64 oracle backward on a few query tokens of the workload with
     their full K/V segment; returns (seconds, flops, sample description).
@@ -295,13 +311,9 @@ def run_sfa(args):
     step_ms = [ev[i][0].elapsed_time(ev[i][-1]) for i in range(args.steps)]
     per_launch = [statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
                   for j in range(launches)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     ms = total_ms / args.steps
-    value = world * flops / (ms * 1e-3) / 1e12
+    value = job_tflops(world, flops, ms)
     err = sfa.read_device_error(ws)
     if err != 0:
         raise RuntimeError(f"device error word {err}")
@@ -338,12 +350,8 @@ def run_sfa(args):
         torch.cuda.synchronize()
         if i >= 2:
             e2e_ms.append(e0.elapsed_time(e1))
-    e2e_mean = statistics.mean(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e_mean], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_mean = float(t.item())
-    e2e_value = world * flops / (e2e_mean * 1e-3) / 1e12
+    e2e_mean = max_over_ranks(statistics.mean(e2e_ms), world, dev)
+    e2e_value = job_tflops(world, flops, e2e_mean)
 
     if rank != 0:
         if world > 1:
