@@ -172,6 +172,21 @@ bool encode2d(CUtensorMap* m, bool f16, const void* base, uint64_t cols, uint64_
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// (T1*G rows x 512) viewed as (64 features, rows, 8 panels): a box of `rows`
+// head rows covers all eight 64-feature panels, panel after panel.
+bool encode_panels3d(CUtensorMap* m, bool f16, const void* base, uint64_t rows, uint32_t box_rows) {
+  EncodeTiled fn = encoder();
+  if (!fn) return false;
+  if (rows == 0) rows = 1;
+  cuuint64_t dims[3] = {64, rows, 8};
+  cuuint64_t strides[2] = {512 * 2, 64 * 2};
+  cuuint32_t box[3] = {64, box_rows, 8};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+            strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Maps of the key-major block kernel: head rows with boxes of GK = G rounded
 // up to 16 rows (one token's heads), staged P^T / dS^T as in Maps.
 bool make_blk_maps(BlkMaps* M, const Plan& P, const void* q, const void* qr, const void* dO, const void* Pst,
@@ -179,9 +194,9 @@ bool make_blk_maps(BlkMaps* M, const Plan& P, const void* q, const void* qr, con
   const bool f = P.is_f16;
   const uint64_t TG = (uint64_t)P.T1 * P.G, R = (uint64_t)P.chunk * P.Kpad;
   const uint32_t gk = (uint32_t)((P.G + 15) / 16 * 16);
-  bool ok = encode2d(&M->q, f, q, 512, TG, gk);
+  bool ok = encode_panels3d(&M->q, f, q, TG, gk);
   ok = ok && encode2d(&M->qr, f, qr ? qr : q, qr ? 64 : 512, TG, gk);
-  ok = ok && encode2d(&M->dO, f, dO, 512, TG, gk);
+  ok = ok && encode_panels3d(&M->dO, f, dO, TG, gk);
   ok = ok && encode2d(&M->P, f, Pst, P.Gp, R, 64);
   ok = ok && encode2d(&M->dS, f, dSst, P.Gp, R, 64);
   return ok;

@@ -119,9 +119,12 @@ struct Maps {
 
 // Tensor maps of the key-major block kernel (kvb.cu).
 struct BlkMaps {
-  CUtensorMap q;    // (T1*G, 512), box 64 x GK (one token's heads, GK = G rounded up to 16)
-  CUtensorMap qr;   // (T1*G, 64),  box 64 x GK
-  CUtensorMap dO;   // (T1*G, 512), box 64 x GK
+  // q and dO as (64 features, T1*G rows, 8 panels): one box = all eight
+  // 64-feature panels of one token's GK head rows (GK = G rounded up to 16),
+  // landing as eight consecutive [GK x 64] panels
+  CUtensorMap q;
+  CUtensorMap qr;   // (T1*G, 64), box 64 x GK
+  CUtensorMap dO;
   CUtensorMap P;    // (chunk*Kpad, GP) staged P^T,  box 64 x 64
   CUtensorMap dS;   // (chunk*Kpad, GP) staged dS^T, box 64 x 64
 };
@@ -131,6 +134,14 @@ struct BlkMaps {
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
+}
+// One box at (x, y, z) of a 3-D map into shared memory at `dst`.
+__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+          dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
 }
 // One box at (x = column, y = row) into shared memory at `dst`.
 __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {

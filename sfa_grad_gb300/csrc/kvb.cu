@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1) kvb_kernel(const __grid_constant_
     }
     __syncwarp();
   } else if (warp <= nprod) {
-    // One thread per producer warp issues ~10 small boxes per pair; nprod
+    // One thread per producer warp issues two or three boxes per pair; nprod
     // producers take every nprod-th pair.  nstages is a multiple of nprod, so
     // each stage slot has one producer and is refilled in order.
     if (lane == 0) {
@@ -205,15 +205,10 @@ __global__ void __launch_bounds__(kThreads, 1) kvb_kernel(const __grid_constant_
           uint64_t* fb = &full_bar[s];
           const uint32_t base = smem_u32(smem + s * sbytes);
           mbar_expect_tx(fb, abytes + 64 * 128);
-          for (int c = 0; c < nc; ++c) {
-            if (kind == 0 && c == 4) {
-              tma_2d(base + 8 * panel, &maps.qr, 0, hrow, fb);
-            } else {
-              const CUtensorMap* m = kind == 0 ? &maps.q : &maps.dO;
-              tma_2d(base + 2 * c * panel, m, c * 128, hrow, fb);
-              tma_2d(base + (2 * c + 1) * panel, m, c * 128 + 64, hrow, fb);
-            }
-          }
+          // all eight 64-feature panels of the token's head rows in one box,
+          // plus the rope panel
+          tma_3d(base, kind == 0 ? &maps.q : &maps.dO, 0, hrow, 0, fb);
+          if (nc == 5) tma_2d(base + 8 * panel, &maps.qr, 0, hrow, fb);
           tma_2d(base + 9 * panel, kind == 0 ? &maps.dS : &maps.P, 0, tl * p.Kpad + ii * bs, fb);
         }
       }
