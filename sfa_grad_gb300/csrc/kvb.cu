@@ -112,8 +112,12 @@ __global__ void blk_scatter_kernel(Prob p, int* cursor, int* entries) {
 // x 64 heads of the staged dS^T or P^T (K-major).
 __host__ __device__ constexpr int stage_bytes(int gk) { return 9 * gk * 128 + 64 * 128; }
 
-template <typename T>
-__global__ void __launch_bounds__(kThreads, 1) kvb_kernel(const __grid_constant__ BlkMaps maps, Prob p, int bs, int gk,
+// GK (the token's heads rounded up to 16) is a template parameter: the MMA
+// issue path is one thread whose instruction latency is not hidden, and with
+// compile-time K steps and panel offsets a pair's 4-5 MMAs issue back to back
+// (runtime trip counts cost about four times the MMA time).
+template <typename T, int GK>
+__global__ void __launch_bounds__(kThreads, 1) kvb_kernel(const __grid_constant__ BlkMaps maps, Prob p, int bs,
                                                           int nstages, int nprod, const int* groups, const int* gbeg,
                                                           const int* ngroups_p, const int* entries, float* acc,
                                                           int* gerr) {
@@ -126,9 +130,10 @@ __global__ void __launch_bounds__(kThreads, 1) kvb_kernel(const __grid_constant_
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ngroups = *ngroups_p;
   const int nitems = 2 * ngroups;          // (group, dK | dV)
-  const int sbytes = stage_bytes(gk);
-  const int panel = gk * 128;              // one 64-feature panel of gk head rows
-  const int nks = gk / 16;                 // K steps per pair
+  constexpr int gk = GK;
+  constexpr int sbytes = stage_bytes(GK);
+  constexpr int panel = GK * 128;          // one 64-feature panel of GK head rows
+  constexpr int nks = GK / 16;             // K steps per pair
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < nstages; ++i) {
@@ -154,28 +159,40 @@ __global__ void __launch_bounds__(kThreads, 1) kvb_kernel(const __grid_constant_
       const uint32_t idesc = idesc_f16(128, bs, E::is_f16, true, false);
       const uint64_t d0 = sdesc_mnmajor(smem_u32(smem), 0, gk);
       const uint64_t b0 = sdesc_kmajor(smem_u32(smem + 9 * panel), 0);
-      int g = 0, it = 0;
+      const uint32_t dcol[5] = {tbase, tbase + bs, tbase + 2 * bs, tbase + 3 * bs, tbase + 4 * bs};
+      int s = 0, it = 0;
+      uint32_t ph = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++it) {
         const int grp = item >> 1, kind = item & 1;
-        const int nc = nchunks_of(kind);
+        const bool five = nchunks_of(kind) == 5;
         const int e0 = gbeg[grp], e1 = gbeg[grp + 1];
         ok = mbar_wait_poll(&tempty_bar, (it & 1) ^ 1, &abort_flag, gerr);
         if (!ok) break;
         tc_fence_after();
-        for (int e = e0; e < e1 && ok; ++e, ++g) {
-          const int s = g % nstages;
-          ok = mbar_wait_poll(&full_bar[s], (g / nstages) & 1, &abort_flag, gerr);
+        for (int e = e0; e < e1 && ok; ++e) {
+          ok = mbar_wait_poll(&full_bar[s], ph, &abort_flag, gerr);
           if (!ok) break;
           tc_fence_after();
           const uint64_t sa = d0 + desc_off(s * sbytes), sb = b0 + desc_off(s * sbytes);
-          for (int c = 0; c < nc; ++c) {
-            const uint32_t d = tbase + c * bs;
-            const uint64_t a = sa + desc_off(2 * c * panel);
+          const uint32_t acc0 = e > e0 ? 1u : 0u;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
             for (int ks = 0; ks < nks; ++ks)
-              mma_ss(d, a + (uint64_t)(ks * 128), sb + (uint64_t)(ks * 2), idesc, (e > e0 || ks > 0) ? 1u : 0u);
+              mma_ss(dcol[c], sa + desc_off(2 * c * panel) + (uint64_t)(ks * 128), sb + (uint64_t)(ks * 2), idesc,
+                     ks > 0 ? 1u : acc0);
+          if (five) {
+#pragma unroll
+            for (int ks = 0; ks < nks; ++ks)
+              mma_ss(dcol[4], sa + desc_off(8 * panel) + (uint64_t)(ks * 128), sb + (uint64_t)(ks * 2), idesc,
+                     ks > 0 ? 1u : acc0);
           }
           mma_commit(&empty_bar[s]);
+          if (++s == nstages) {
+            s = 0;
+            ph ^= 1;
+          }
         }
         if (ok) mma_commit(&tfull_bar);
       }
@@ -300,10 +317,10 @@ cudaError_t launch_kvb(const BlkMaps& maps, const Prob& p, int bs, const int* gr
   const int nprod = nst % 3 == 0 ? 3 : nst % 2 == 0 ? 2 : 1;
   const int smem_b = nst * stage_bytes(gk) + 1024;
   const int smem = smem_b > kOneCtaSmem ? smem_b : kOneCtaSmem;
-  auto kern = kvb_kernel<T>;
+  auto kern = gk == 16 ? kvb_kernel<T, 16> : gk == 32 ? kvb_kernel<T, 32> : gk == 48 ? kvb_kernel<T, 48> : kvb_kernel<T, 64>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<nsm, kThreads, smem, st>>>(maps, p, bs, gk, nst, nprod, groups, gbeg, ngroups, entries, acc, gerr);
+  kern<<<nsm, kThreads, smem, st>>>(maps, p, bs, nst, nprod, groups, gbeg, ngroups, entries, acc, gerr);
   return cudaGetLastError();
 }
 
