@@ -109,3 +109,29 @@ def test_tnd_workspace_independent_of_lengths(sfa):
 def test_status_strings(sfa):
     for c in (0, 161001, 161002, 361001, 561002):
         assert sfa.status_string(c).startswith("SFA_")
+
+
+def test_plan_names(sfa):
+    """The launch sequence a call plans, as sfa_grad_plan_names lists it: one
+    chunk of the combined kernel for an MLA shape; the grouped key-major block
+    path for block indices that many tokens select; the fixed-order path when
+    deterministic; a batch prefix first for TND."""
+    mla = sfa.plan_names(_p(sfa, S1=4096, S2=4096, N1=128, K=2048))
+    assert mla == ["meta", "dsum", "rowtab", "sdp", "kvq", "cast"]
+    assert sfa.plan_info(_p(sfa, S1=4096, S2=4096, N1=128, K=2048))[1] == len(mla)
+    blk = sfa.plan_names(_p(sfa, dtype=1, B=2, S1=8192, S2=32768, N1=16, K=64, sparse_block_size=64))
+    chunk = ["rowtab", "sdp", "blk_count", "blk_scan", "blk_scatter", "kvb", "kvq"]
+    assert blk[:2] == ["meta", "dsum"] and blk[-1] == "cast"
+    ctok, nl = sfa.plan_info(_p(sfa, dtype=1, B=2, S1=8192, S2=32768, N1=16, K=64, sparse_block_size=64))
+    nchunks = (2 * 8192 + ctok - 1) // ctok
+    assert len(blk) == nl == 3 + len(chunk) * nchunks
+    assert blk[2:2 + len(chunk)] == chunk
+    # few selections per key row, or bs < 16, or more than 64 heads: per-pair path
+    assert "kvb" not in sfa.plan_names(_p(sfa, S1=4, S2=4096, N1=16, K=5, sparse_block_size=64))
+    assert "kvb" not in sfa.plan_names(_p(sfa, S1=2048, S2=4096, N1=16, K=64, sparse_block_size=8))
+    assert "kvb" not in sfa.plan_names(_p(sfa, S1=2048, S2=4096, N1=128, K=64, sparse_block_size=64))
+    det = sfa.plan_names(_p(sfa, deterministic=1))
+    assert det == ["meta", "dsum", "rowtab", "sdp", "sort_keys", "dkv", "det_reduce", "dq", "cast"]
+    tnd = sfa.plan_names(_p(sfa, layout=1, B=4, T1=16384, T2=32768, N1=64, K=2048, sparse_mode=3))
+    assert tnd[0] == "batch_prefix" and "kvq" in tnd
+    assert sfa.plan_names(_p(sfa, S1=0)) == []
