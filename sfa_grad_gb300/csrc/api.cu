@@ -21,7 +21,6 @@ constexpr size_t kAlign = 256;
 constexpr size_t kPdsCap = size_t(8) << 30;    // P + dS staging per token chunk
 constexpr size_t kPartCap = size_t(8) << 30;   // deterministic partial rows per chunk
 constexpr int kAccRow = 1088;
-constexpr int kDetMaxKeff = 16384;             // per-token sort runs in shared memory
 
 size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -30,7 +29,7 @@ struct Plan {
   int kvb;   // key-major dK / dV for block-sparse indices (kvb.cu)
   float scale;
   int chunk;
-  size_t off_err, off_batch, off_meta, off_dsum, off_acc, off_P, off_dS, off_rows, off_part, off_skey, off_sslot, off_tstats;
+  size_t off_err, off_batch, off_meta, off_dsum, off_acc, off_P, off_dS, off_rows, off_part, off_dscr, off_tstats;
   size_t off_bcnt, off_bcur, off_bgrp, off_bbeg, off_bng, off_bent;
   size_t total;
 };
@@ -61,7 +60,6 @@ sfa_status validate(const sfa_params* p, bool fwd, Plan* out) {
   const int64_t keff = p->K * bs;
   if (keff > (1 << 24) || T1 > INT32_MAX / 2 || T2 > INT32_MAX / 2 || T1 * p->N1 > INT32_MAX / 2)
     return SFA_ERR_SHAPE;
-  if (!fwd && p->deterministic && keff > kDetMaxKeff) return SFA_ERR_SHAPE;
   Plan& P = *out;
   std::memset(&P, 0, sizeof(P));
   P.layout = (int)p->layout;
@@ -108,16 +106,18 @@ sfa_status validate(const sfa_params* p, bool fwd, Plan* out) {
   P.off_dS = o; o += fwd ? 0 : up(chunk * P.Kpad * P.Gp * 2);
   P.off_rows = o; o += up(chunk * P.Kpad * 4);
   P.off_part = o; o += P.det ? up(chunk * P.Kpad * kAccRow * 4) : 0;
-  P.off_skey = o; o += P.det ? up(chunk * P.Kpad * 4) : 0;
-  P.off_sslot = o; o += P.det ? up(chunk * P.Kpad * 4) : 0;
+  P.off_dscr = o; o += P.det ? up(2 * chunk * P.Kpad * 4) : 0;   // padded copies of long segments
   P.off_tstats = o; o += fwd ? up(chunk * (P.Kpad / 128) * P.G * 2 * 4) : 0;
-  const size_t nb = P.kvb ? (size_t)P.T2 + P.bs : 0;    // block-start bins (start + bs)
-  P.off_bcnt = o; o += P.kvb ? up(nb * 4) : 0;
-  P.off_bcur = o; o += P.kvb ? up(nb * 4) : 0;
-  P.off_bgrp = o; o += P.kvb ? up(nb * 4) : 0;
-  P.off_bbeg = o; o += P.kvb ? up((nb + 1) * 4) : 0;
-  P.off_bng = o; o += P.kvb ? up(4) : 0;
-  P.off_bent = o; o += P.kvb ? up(chunk * P.Kidx * 4) : 0;
+  // counting-sort bins: block starts + bs (key-major blocks) or kv rows
+  // (deterministic reduction), and the sorted entries
+  const bool bins = P.kvb || P.det;
+  const size_t nb = bins ? (size_t)P.T2 + P.bs : 0;
+  P.off_bcnt = o; o += bins ? up(nb * 4) : 0;
+  P.off_bcur = o; o += bins ? up(nb * 4) : 0;
+  P.off_bgrp = o; o += bins ? up(nb * 4) : 0;
+  P.off_bbeg = o; o += bins ? up((nb + 1) * 4) : 0;
+  P.off_bng = o; o += bins ? up(4) : 0;
+  P.off_bent = o; o += bins ? up(chunk * (P.det ? P.Kpad : P.Kidx) * 4) : 0;
   P.total = o;
   return SFA_OK;
 }
@@ -281,7 +281,8 @@ int kvq_tile_group(const Plan& P) {
 }
 
 // Kernel launches of one sfa_grad call, in order (sfa_grad_plan_names).
-const char* const kChunkDet[] = {"rowtab", "sdp", "sort_keys", "dkv", "det_reduce", "dq"};
+const char* const kChunkDet[] = {"rowtab", "sdp", "det_count", "det_scan", "det_scatter", "det_sort",
+                                 "dkv", "det_reduce", "dq"};
 const char* const kChunkKvq[] = {"rowtab", "sdp", "kvq"};
 const char* const kChunkKvb[] = {"rowtab", "sdp", "blk_count", "blk_scan", "blk_scatter", "kvb", "kvq"};
 
@@ -353,14 +354,25 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
     SFA_CK(launch_sdp<T>(maps, pr, kModeBwd, Pst, dSst, nullptr, gerr, nsm, st));
     SFA_CK(mk.mark(st));
     if (P.det) {
-      int* skey = reinterpret_cast<int*>(ws + P.off_skey);
-      int* sslot = reinterpret_cast<int*>(ws + P.off_sslot);
+      int* bcnt = reinterpret_cast<int*>(ws + P.off_bcnt);
+      int* bcur = reinterpret_cast<int*>(ws + P.off_bcur);
+      int* bgrp = reinterpret_cast<int*>(ws + P.off_bgrp);
+      int* bbeg = reinterpret_cast<int*>(ws + P.off_bbeg);
+      int* bng = reinterpret_cast<int*>(ws + P.off_bng);
+      int* bent = reinterpret_cast<int*>(ws + P.off_bent);
+      int* dscr = reinterpret_cast<int*>(ws + P.off_dscr);
       float* part = reinterpret_cast<float*>(ws + P.off_part);
-      SFA_CK(launch_sort_keys(pr, skey, sslot, st));
+      SFA_CK(launch_det_count(pr, bcnt, st));
+      SFA_CK(mk.mark(st));
+      SFA_CK(launch_blk_scan(bcnt, P.T2, bcur, bgrp, bbeg, bng, st));
+      SFA_CK(mk.mark(st));
+      SFA_CK(launch_det_scatter(pr, bcur, bent, st));
+      SFA_CK(mk.mark(st));
+      SFA_CK(launch_det_sort(pr, bbeg, bng, bent, dscr, st));
       SFA_CK(mk.mark(st));
       SFA_CK(launch_dkv<T>(maps, pr, acc, part, gerr, nsm, st));
       SFA_CK(mk.mark(st));
-      SFA_CK(launch_det_reduce(pr, skey, sslot, part, acc, st));
+      SFA_CK(launch_det_reduce(pr, bgrp, bbeg, bng, bent, part, acc, st));
       SFA_CK(mk.mark(st));
       SFA_CK(launch_dq<T>(maps, pr, 0, dq, P.has_rope ? dqr : nullptr, gerr, nsm, st));
       SFA_CK(mk.mark(st));

@@ -59,9 +59,14 @@ cudaError_t launch_stats_combine(const Prob& p, const float* tile_stats, float* 
 // Records a message for sfa_last_error_message on the calling thread (api.cu).
 void set_last_error(const char* msg);
 
-// Deterministic key-side reduction (det.cu).
-cudaError_t launch_sort_keys(const Prob& p, int* sorted_key, int* sorted_slot, cudaStream_t st);
-cudaError_t launch_det_reduce(const Prob& p, const int* sorted_key, const int* sorted_slot, const float* partials,
-                              float* acc, cudaStream_t st);
+// Deterministic key-side reduction (det.cu): counting sort of the chunk's
+// (kv row, token, slot) entries by row (count, then launch_blk_scan over the
+// T2 rows, scatter, per-row sort), then one fixed-order sum per row.
+cudaError_t launch_det_count(const Prob& p, int* cnt, cudaStream_t st);
+cudaError_t launch_det_scatter(const Prob& p, int* cursor, int* ent, cudaStream_t st);
+cudaError_t launch_det_sort(const Prob& p, const int* gbeg, const int* ngroups, int* ent, int* scratch,
+                            cudaStream_t st);
+cudaError_t launch_det_reduce(const Prob& p, const int* groups, const int* gbeg, const int* ngroups, const int* ent,
+                              const float* partials, float* acc, cudaStream_t st);
 
 }  // namespace sfa

@@ -56,46 +56,80 @@ __global__ void blk_count_kernel(Prob p, int* cnt) {
   }
 }
 
-// One block: exclusive scan of the per-bin counts (nbins = T2 + bs) into
+// One block: exclusive scan of the per-bin counts (nbins entries) into
 // cursor[] (the next free entry of each bin), and the compacted list of
 // non-empty bins with their first entry: groups[k], gbeg[k];
-// gbeg[ngroups] = total pairs.
+// gbeg[ngroups] = total entries.  The block walks the bins 4096 at a time
+// (four consecutive bins per thread, coalesced), scanning each tile with warp
+// shuffles and carrying the running totals.
 __global__ void __launch_bounds__(1024) blk_scan_kernel(const int* cnt, int nbins, int* cursor, int* groups, int* gbeg,
                                                         int* ngroups) {
-  __shared__ int s_sum[1024], s_nz[1024];
-  const int tid = threadIdx.x;
-  const int per = (nbins + 1023) / 1024;
-  const int b0 = tid * per, b1 = min(b0 + per, nbins);
-  int sum = 0, nz = 0;
-  for (int g = b0; g < b1; ++g) {
-    const int c = cnt[g];
-    sum += c;
-    nz += c > 0;
-  }
-  s_sum[tid] = sum;
-  s_nz[tid] = nz;
+  __shared__ int ex_sum[32], ex_nz[32];
+  __shared__ int carry[2];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) carry[0] = carry[1] = 0;
   __syncthreads();
-  for (int o = 1; o < 1024; o <<= 1) {
-    const int a = tid >= o ? s_sum[tid - o] : 0, b = tid >= o ? s_nz[tid - o] : 0;
-    __syncthreads();
-    s_sum[tid] += a;
-    s_nz[tid] += b;
-    __syncthreads();
-  }
-  int off = s_sum[tid] - sum, k = s_nz[tid] - nz;
-  for (int g = b0; g < b1; ++g) {
-    const int c = cnt[g];
-    cursor[g] = off;
-    if (c > 0) {
-      groups[k] = g;
-      gbeg[k] = off;
-      ++k;
+  for (int base = 0; base < nbins; base += 4096) {
+    const int b0 = base + tid * 4;
+    int c[4], sum = 0, nz = 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      c[u] = b0 + u < nbins ? cnt[b0 + u] : 0;
+      sum += c[u];
+      nz += c[u] > 0;
     }
-    off += c;
+    int is = sum, in = nz;   // inclusive scans within the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, is, o), b = __shfl_up_sync(0xffffffffu, in, o);
+      if (lane >= o) {
+        is += a;
+        in += b;
+      }
+    }
+    if (lane == 31) {
+      ex_sum[warp] = is;
+      ex_nz[warp] = in;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const int v = ex_sum[lane], w = ex_nz[lane];
+      int a = v, b = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, a, o), y = __shfl_up_sync(0xffffffffu, b, o);
+        if (lane >= o) {
+          a += x;
+          b += y;
+        }
+      }
+      ex_sum[lane] = a - v;
+      ex_nz[lane] = b - w;
+    }
+    __syncthreads();
+    int off = carry[0] + ex_sum[warp] + is - sum, k = carry[1] + ex_nz[warp] + in - nz;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (b0 + u < nbins) {
+        cursor[b0 + u] = off;
+        if (c[u] > 0) {
+          groups[k] = b0 + u;
+          gbeg[k] = off;
+          ++k;
+        }
+        off += c[u];
+      }
+    }
+    __syncthreads();
+    if (tid == 1023) {   // the tile's last bins: running totals through the tile
+      carry[0] = off;
+      carry[1] = k;
+    }
+    __syncthreads();
   }
-  if (tid == 1023) {
-    *ngroups = s_nz[1023];
-    gbeg[s_nz[1023]] = s_sum[1023];
+  if (tid == 0) {
+    *ngroups = carry[1];
+    gbeg[carry[1]] = carry[0];
   }
 }
 
