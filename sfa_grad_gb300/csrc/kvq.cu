@@ -8,7 +8,10 @@
 //               accumulated in tensor memory over all the token's keys.
 // The key side is bound by the SM-to-L2 reduction path and leaves the tensor
 // pipe mostly idle; the query side is bound by gathers and the tensor pipe.
-// Running both in the same CTA overlaps the two.
+// Running both in the same CTA overlaps the two.  Key-side items run
+// token-major, or tile-group major when the accumulator rows a batch touches
+// exceed L2; with tile_group = 0 only the query side runs (the key side of
+// block indices is then done per block, kvb.cu).
 //
 // aclnnSparseFlashAttentionGrad doc, 阶段1 (dV = P^T dO) and 阶段3 (dQ, dK);
 // MindSpore flash_attention_bwd.py, update_dVj / update_dQi / update_dKj.

@@ -16,7 +16,9 @@
 // (scattered 128-byte pieces halve the achievable gather rate) and waits only
 // for its own copies, so up to four gathers are in flight.  B: two slots
 // filled by TMA from one thread.  Both operands of a stage complete on one
-// barrier, so the MMA issuer waits once per stage.
+// barrier, so the MMA issuer waits once per stage.  Compile-time variants:
+// value = key (one gathered stage feeds both contractions) and block indices
+// (each selected block of rows arrives as one TMA box per panel).
 //
 // aclnnSparseFlashAttentionGrad doc, 功能说明 (gather by topkIndices) and
 // 阶段1/阶段2 (dP, dS); MindSpore flash_attention_bwd.py, compute_Pij
