@@ -223,7 +223,7 @@ def workload_desc(w, det, shared_kv=False):
 TRAFFIC = {
     # profiles/kvq_mla_q512.md: 937.6 MB read + 82.4 MB written per 512-token launch
     "kvq": {"sources": ["kvq.cu", "common.cuh"],
-             "sha256": "104c83ed095aff9c8a89be0902995a24882198467fc53d6745b32af1e11a081e",
+             "sha256": "48809eef5e350fa29986a15471ce38b7d511b19364341c5b72fc0dec128ee1cb",
              "bytes_per_token": 1020.0e6 / 512},
 }
 
