@@ -27,7 +27,9 @@ struct DqSmem {
   static constexpr int kBytes = kStages * kStage + 1024;
 };
 
-template <typename T, int GP, int MODE>
+// BLK: block-sparse indices (sparseBlockSize >= 8): the key / value rows of a
+// stage arrive as one TMA box per selected block and feature panel.
+template <typename T, int GP, int MODE, bool BLK>
 __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__ Maps maps, Prob p, T* out_main, T* out_rope,
                                                          int* gerr) {
   using E = Elt<T>;
@@ -129,12 +131,35 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
         __syncwarp();
         if (!ok) break;
         if (lane == 0) {
-          mbar_expect_tx(&full_bar[me], kHP * kSlots * 128);
+          mbar_expect_tx(&full_bar[me], kHP * kSlots * 128 + (BLK ? (NCOL / 64) * kSlots * 128 : 0));
           for (int hp = 0; hp < kHP; ++hp)
             tma_2d(a + hp * (kSlots * 128), mA, hp * 64, tl * p.Kpad + c * kSlots, &full_bar[me]);
         }
-        // lane < kCpr owns 16-byte piece `lane` of every gathered row
-        if (lane < kCpr) {
+        if constexpr (BLK) {
+          // lane i < 64/bs owns the stage's i-th index: one box of bs rows per
+          // feature panel (an index with no key at or above 0, past the last
+          // row or past the index list reads zeros from below row 0)
+          __syncwarp();
+          const int nidx = kSlots / p.bs;
+          if (lane < nidx) {
+            const int i = (c * kSlots) / p.bs + lane;
+            const int t = p.tok0 + tl;
+            int y = -p.bs;
+            if (i < p.Kidx) {
+              const int r = __ldg(p.idx + (size_t)t * p.Kidx + i);
+              const long long yy = (long long)p.meta[t].kv_start + r;
+              if ((long long)r + p.bs > 0 && yy < p.T2) y = (int)yy;
+            }
+            for (int pn = 0; pn < NCOL / 64; ++pn) {
+              const int f = f0 + pn * 64;
+              const uint32_t dst = b + pn * (kSlots * 128) + lane * p.bs * 128;
+              if (MODE == 1) tma_2d(dst, &maps.v, f, y, &full_bar[me]);
+              else if (f < 512) tma_2d(dst, &maps.k, f, y, &full_bar[me]);
+              else tma_2d(dst, p.has_rope ? &maps.kr : &maps.k, p.has_rope ? f - 512 : 0, p.has_rope ? y : -p.bs,
+                          &full_bar[me]);
+            }
+          }
+        } else if (lane < kCpr) {   // lane < kCpr owns 16-byte piece `lane` of every gathered row
           const int f = f0 + lane * 8;
           const bool rope = MODE == 0 && f >= 512;
           const T* base = rope ? (p.has_rope ? krope + (f - 512) : kmain) : kmain + f;
@@ -203,7 +228,7 @@ template <typename T, int GP, int MODE>
 cudaError_t launch_one(const Maps& maps, const Prob& p, void* o1, void* o2, int* gerr, int nsm, cudaStream_t st) {
   constexpr int NCOL = MODE == 0 ? 192 : 256;
   constexpr int NPART = MODE == 0 ? 3 : 2;
-  auto kern = dq_kernel<T, GP, MODE>;
+  auto kern = p.bs >= 8 ? dq_kernel<T, GP, MODE, true> : dq_kernel<T, GP, MODE, false>;
   const int smem = DqSmem<NCOL>::kBytes > kOneCtaSmem ? DqSmem<NCOL>::kBytes : kOneCtaSmem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
