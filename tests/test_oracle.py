@@ -326,6 +326,21 @@ def test_scalar_brute_force_with_duplicates(mode, bs):
         np.testing.assert_allclose(g[n], r[n], rtol=1e-12, atol=1e-13, err_msg=n)
 
 
+@pytest.mark.parametrize("mode", [0, 3])
+def test_scalar_brute_force_blocks_across_edges(mode):
+    """Block starts below 0 and blocks running past the sequence end: only the
+    keys inside [0, kvlen) (and under the causal limit) count."""
+    rng = np.random.default_rng(41 + mode)
+    case, dO = _rand_case(rng, B=1, S1=3, S2=10, G=2, D=3, Dr=2, K=3, bs=4, distinct=False)
+    case["indices"][0, :, 0, :] = np.array([[-1, 3, 8], [-3, 0, 7], [-4, 6, 9]])   # -4: no key >= 0
+    out, smax, ssum = sfa_fwd(scale=0.5, sparse_block_size=4, sparse_mode=mode, **case)
+    g = sfa_bwd(d_out=dO, out=out, softmax_max=smax, softmax_sum=ssum, scale=0.5,
+                sparse_block_size=4, sparse_mode=mode, **case)
+    r = _brute(case, dO, out, smax, ssum, 0.5, 4, mode)
+    for n in r:
+        np.testing.assert_allclose(g[n], r[n], rtol=1e-12, atol=1e-13, err_msg=n)
+
+
 def test_sampled_rows_match_full():
     rng = np.random.default_rng(41)
     case, dO = _rand_case(rng, B=2, S1=5, S2=12, K=6)

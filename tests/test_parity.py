@@ -39,6 +39,8 @@ SMALL = {
     # edge cases: a single index per token; a KV sequence shorter than one key tile, every key selected
     "g8_single_index": small_workload(N1=8, S1=6, S2=300, K=1, seed=29),
     "g32_short_kv_all": small_workload(N1=32, S1=5, S2=64, K=64, index_kind="all", seed=30),
+    # blocks of 8 starting below 0 or running past the end, through the per-pair key side
+    "g16_bs8_edges": small_workload(N1=16, S1=6, S2=200, K=10, block_size=8, index_kind="random_any", seed=31),
 }
 
 
