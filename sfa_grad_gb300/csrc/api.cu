@@ -219,6 +219,10 @@ bool make_maps(Maps* M, const Plan& P, const void* q, const void* qr, const void
   ok = ok && encode2d(&M->v, f, v, 512, T2, kb);
   ok = ok && encode2d(&M->P, f, Pst, P.Gp, R, 64);
   ok = ok && encode2d(&M->dS, f, dSst ? dSst : Pst, P.Gp, R, 64);
+  const uint32_t gk = (uint32_t)((P.G + 15) / 16 * 16);
+  ok = ok && encode2d(&M->qg, f, q, 512, TG, gk);
+  ok = ok && encode2d(&M->qrg, f, qr ? qr : q, qr ? 64 : 512, TG, gk);
+  ok = ok && encode2d(&M->dOg, f, dO ? dO : q, 512, TG, gk);
   return ok;
 }
 

@@ -115,6 +115,10 @@ struct Maps {
   CUtensorMap v;    // (T2, 512),   box 64 x bs
   CUtensorMap P;    // (chunk*Kpad, GP) staged P^T,  box 64 x 64
   CUtensorMap dS;   // (chunk*Kpad, GP) staged dS^T, box 64 x 64
+  // q, qRope, dO with boxes of GK = G rounded up to 16 rows: the score
+  // kernel loads only a token's own head rows (the padded rows up to GP stay
+  // zero in its shared memory)
+  CUtensorMap qg, qrg, dOg;
 };
 
 // Tensor maps of the key-major block kernel (kvb.cu).

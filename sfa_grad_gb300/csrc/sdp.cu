@@ -93,6 +93,14 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
   const int nchunks = bwd ? nS + 4 : nS;      // + 4 stages of dP
   const int ntiles = p.Kpad / kKeys;
   const int nitems = p.ntok * ntiles;
+  // head rows per token as loaded (G rounded up to 16); the slot rows from gk
+  // to GP are zeroed once here and never written, so padded heads score 0
+  const int gk = (p.G + 15) / 16 * 16;
+  if (gk < GP) {
+    uint4* z = reinterpret_cast<uint4*>(smem + S::kBOff);
+    for (int i = threadIdx.x; i < S::kNB * S::kB / 16; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
+    fence_async_smem();
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S::kNA; ++i) {
@@ -199,8 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
               ok = mbar_wait(&bempty_bar[bslot], ((gb / S::kNB) & 1) ^ 1, &abort_flag, gerr);
               if (!ok) break;
               const uint32_t b = smem_u32(smem + S::kBOff + bslot * S::kB);
-              mbar_expect_tx(fb, ck.npan * S::kPanelB);
-              const CUtensorMap* mq = j == 1 ? &maps.dO : ck.kind == 0 ? &maps.q : &maps.qr;
+              mbar_expect_tx(fb, ck.npan * gk * 128);
+              const CUtensorMap* mq = j == 1 ? &maps.dOg : ck.kind == 0 ? &maps.qg : &maps.qrg;
               for (int pn = 0; pn < ck.npan; ++pn) tma_2d(b + pn * S::kPanelB, mq, ck.f0 + pn * 64, t * p.G, fb);
             }
             if (ok && nb == 1) mbar_arrive(fb);   // the stage barrier counts two head-row arrivals
@@ -213,8 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
             const Chunk ck = chunk_of(c, nS);
             const uint32_t b = smem_u32(smem + S::kBOff + bslot * S::kB);
             uint64_t* fb = &full_bar[g % S::kNA];
-            mbar_expect_tx(fb, ck.npan * S::kPanelB);
-            const CUtensorMap* mq = ck.kind == 0 ? &maps.q : ck.kind == 1 ? &maps.qr : &maps.dO;
+            mbar_expect_tx(fb, ck.npan * gk * 128);
+            const CUtensorMap* mq = ck.kind == 0 ? &maps.qg : ck.kind == 1 ? &maps.qrg : &maps.dOg;
             for (int pn = 0; pn < ck.npan; ++pn) tma_2d(b + pn * S::kPanelB, mq, ck.f0 + pn * 64, t * p.G, fb);
           }
         }
