@@ -22,9 +22,10 @@
  * Conventions
  *  - Two phases, as on the documentation page (函数原型): ask for the workspace
  *    size, allocate it, then call.  The caller owns every buffer; the library
- *    allocates nothing, keeps no state between calls and is thread-safe.
+ *    allocates no memory, keeps no state between calls and is thread-safe
+ *    (sfa_grad_host creates two streams and a few events per call).
  *  - All tensor pointers are DEVICE pointers to contiguous row-major data
- *    (16-byte aligned).  Shapes use the page's names (参数说明 table):
+ *    (16-byte aligned), except those of sfa_grad_host (host buffers).  Shapes use the page's names (参数说明 table):
  *      BSND: q, dOut, out (B,S1,N1,D); k, v (B,S2,1,D); indices (B,S1,1,K);
  *            softmaxMax/Sum (B,1,S1,N1); qRope (B,S1,N1,Dr); kRope (B,S2,1,Dr)
  *      TND:  q, dOut, out (T1,N1,D); k, v (T2,1,D); indices (T1,1,K);
@@ -223,6 +224,42 @@ sfa_status sfa_grad_noalloc(const sfa_params* p, const void* q, const void* k, c
                             const int32_t* act_seq_q, const int32_t* act_seq_kv, const void* q_rope,
                             const void* k_rope, void* dq, void* dk, void* dv, void* dq_rope, void* dk_rope,
                             void* stream);
+
+/*
+ * sfa_grad from host buffers, with the copies overlapped with the kernels.
+ * Same arguments, shapes and results as sfa_grad, except that every tensor
+ * argument (the inputs, act_seq_q / act_seq_kv and the five outputs) is a
+ * HOST pointer.  Page-locked (pinned) memory makes the copies asynchronous so
+ * that they overlap the kernels; pageable memory works, but its copies are
+ * synchronous.  `workspace` is a DEVICE buffer of at least
+ * sfa_grad_host_workspace_size bytes (256-byte aligned, caller-owned): the
+ * backward's workspace followed by device copies of the inputs and outputs.
+ *
+ * The call splits the query tokens into chunks of at most an eighth of them
+ * (at least 64 tokens).  On two streams it creates, it copies k, v, kRope and
+ * the lengths, then each chunk's query-side rows (q, qRope, dOut, out,
+ * softmaxMax, softmaxSum, indices) to the device.  Chunk c's kernels start
+ * when its rows have landed, and its dQ / dQRope rows are copied back while
+ * chunk c + 1 computes; dK / dV / dKRope follow the final cast.  All of it is
+ * ordered after earlier work on `stream`, and `stream` waits for the last
+ * copy: the host outputs are complete, and the host inputs free, once
+ * `stream` has been synchronised.  The two streams and the events are
+ * released at the end of the call (the runtime frees them once their work is
+ * done); not for use while `stream` is being captured into a graph.  With
+ * deterministic = 1 the outputs are bitwise reproducible from call to call;
+ * their last bits can differ from sfa_grad's, whose token chunks may be
+ * larger (the fixed order of the key-side sums is chunk, token, slot).
+ * Errors: those of sfa_grad (the workspace size is checked against
+ * sfa_grad_host_workspace_size).  When an error is returned after copies
+ * were queued, the call first waits for them, so none still reads or writes
+ * the caller's host buffers.
+ */
+sfa_status sfa_grad_host_workspace_size(const sfa_params* p, size_t* bytes);
+sfa_status sfa_grad_host(const sfa_params* p, const void* q, const void* k, const void* v, const int32_t* indices,
+                         const void* d_out, const void* out, const float* softmax_max, const float* softmax_sum,
+                         const int32_t* act_seq_q, const int32_t* act_seq_kv, const void* q_rope, const void* k_rope,
+                         void* dq, void* dk, void* dv, void* dq_rope, void* dk_rope, void* workspace,
+                         size_t workspace_bytes, void* stream);
 
 /*
  * Human-readable detail of the most recent SFA_ERR_RUNTIME returned on the

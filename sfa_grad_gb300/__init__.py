@@ -28,7 +28,7 @@ DTYPES = {torch.bfloat16: 0, torch.float16: 1}
 
 EXPORTS = ("sfa_grad_workspace_size", "sfa_grad", "sfa_grad_profile", "sfa_grad_plan_info", "sfa_grad_plan_names",
            "sfa_fwd_workspace_size", "sfa_fwd", "sfa_decode_keys", "sfa_read_device_error", "sfa_status_string",
-           "sfa_last_error_message", "sfa_grad_noalloc")
+           "sfa_last_error_message", "sfa_grad_noalloc", "sfa_grad_host_workspace_size", "sfa_grad_host")
 
 
 class SfaParams(ctypes.Structure):
@@ -73,6 +73,8 @@ def lib() -> ctypes.CDLL:
     L.sfa_grad_plan_info.argtypes = [P, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]
     L.sfa_grad_plan_names.argtypes = [P, ctypes.POINTER(ctypes.c_char_p), ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]
     L.sfa_grad_noalloc.argtypes = [P] + [vp] * 17 + [vp]
+    L.sfa_grad_host_workspace_size.argtypes = [P, ctypes.POINTER(sz)]
+    L.sfa_grad_host.argtypes = [P] + [vp] * 18 + [sz, vp]
     L.sfa_fwd.argtypes = [P] + [vp] * 12 + [sz, vp]
     L.sfa_decode_keys.argtypes = [P, vp, vp, vp, vp, vp, sz, vp]
     L.sfa_read_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
@@ -82,7 +84,7 @@ def lib() -> ctypes.CDLL:
     L.sfa_status_string.restype = ctypes.c_char_p
     for name in ("sfa_grad_workspace_size", "sfa_fwd_workspace_size", "sfa_grad", "sfa_grad_profile",
                  "sfa_grad_plan_info", "sfa_grad_plan_names", "sfa_fwd", "sfa_decode_keys", "sfa_read_device_error",
-                 "sfa_grad_noalloc"):
+                 "sfa_grad_noalloc", "sfa_grad_host_workspace_size", "sfa_grad_host"):
         getattr(L, name).restype = ctypes.c_int32
     _lib = L
     return L
@@ -221,6 +223,53 @@ def grad_noalloc(q, k, v, indices, d_out, out, softmax_max, softmax_sum, scale, 
                                 _ptr(softmax_max), _ptr(softmax_sum), _ptr(act_seq_q), _ptr(act_seq_kv), _ptr(q_rope),
                                 _ptr(k_rope), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dqr), _ptr(dkr), _stream(stream))
     _check(rc, "sfa_grad_noalloc")
+    return dq, dk, dv, dqr, dkr
+
+
+def grad_host_workspace_size(p: SfaParams) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().sfa_grad_host_workspace_size(ctypes.byref(p), ctypes.byref(n)), "sfa_grad_host_workspace_size")
+    return n.value
+
+
+def _hptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise ValueError("sfa_grad_host takes host (CPU) tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def grad_host(q, k, v, indices, d_out, out, softmax_max, softmax_sum, scale, *, q_rope=None, k_rope=None,
+              sparse_block_size=1, layout="BSND", sparse_mode=0, deterministic=False, act_seq_q=None,
+              act_seq_kv=None, outputs=None, workspace=None, device=None, stream=None):
+    """sfa_grad_host on host (CPU, preferably pinned) tensors: the library
+    copies them to the device chunk by chunk, overlapping the copies with the
+    kernels, and copies the results back into `outputs` (pinned CPU tensors
+    allocated here unless passed in).  The results are complete once the
+    stream has been synchronised.  `workspace` is a device tensor of at least
+    grad_host_workspace_size bytes (allocated on `device`, default the
+    current CUDA device, unless passed in).  Returns (dq, dk, dv, dq_rope,
+    dk_rope)."""
+    has_rope = q_rope is not None
+    batch = act_seq_q.numel() if act_seq_q is not None else None
+    p = make_params(q, k, indices, scale, layout=layout, sparse_block_size=sparse_block_size,
+                    sparse_mode=sparse_mode, deterministic=deterministic, has_rope=has_rope, batch=batch)
+    if outputs is None:
+        def pinned(t):
+            return torch.empty(t.shape, dtype=t.dtype).pin_memory()
+        outputs = (pinned(q), pinned(k), pinned(v), pinned(q_rope) if has_rope else None,
+                   pinned(k_rope) if has_rope else None)
+    dq, dk, dv, dqr, dkr = outputs
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    ws = _workspace(grad_host_workspace_size(p), dev, workspace)
+    rc = lib().sfa_grad_host(ctypes.byref(p), _hptr(q), _hptr(k), _hptr(v), _hptr(indices), _hptr(d_out), _hptr(out),
+                             _hptr(softmax_max), _hptr(softmax_sum), _hptr(act_seq_q), _hptr(act_seq_kv),
+                             _hptr(q_rope), _hptr(k_rope), _hptr(dq), _hptr(dk), _hptr(dv), _hptr(dqr), _hptr(dkr),
+                             _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    _check(rc, "sfa_grad_host")
     return dq, dk, dv, dqr, dkr
 
 

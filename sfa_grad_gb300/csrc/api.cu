@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <vector>
 
 #include <cudaTypedefs.h>
 
@@ -34,7 +35,11 @@ struct Plan {
   size_t total;
 };
 
-sfa_status validate(const sfa_params* p, bool fwd, Plan* out) {
+// host_pipe: plan of sfa_grad_host, whose token chunks are also the units
+// of its copy pipeline: at most an eighth of the tokens (at least 64) per
+// chunk, so that the first chunk's inputs arrive early and the copies of the
+// others overlap the kernels.
+sfa_status validate(const sfa_params* p, bool fwd, Plan* out, bool host_pipe = false) {
   if (!p) return SFA_ERR_NULLPTR;
   if (p->dtype != SFA_DTYPE_BF16 && p->dtype != SFA_DTYPE_FP16) return SFA_ERR_PARAM_INVALID;
   if (p->layout != SFA_LAYOUT_BSND && p->layout != SFA_LAYOUT_TND) return SFA_ERR_PARAM_INVALID;
@@ -92,6 +97,10 @@ sfa_status validate(const sfa_params* p, bool fwd, Plan* out) {
     const size_t part_per_tok = (size_t)P.Kpad * kAccRow * 4;
     const size_t c2 = kPartCap / part_per_tok;
     if (c2 < chunk) chunk = c2;
+  }
+  if (host_pipe) {
+    const size_t cap = ((size_t)P.T1 + 7) / 8 > 64 ? ((size_t)P.T1 + 7) / 8 : 64;
+    if (chunk > cap) chunk = cap;
   }
   if (chunk < 1) chunk = 1;
   if (chunk > (size_t)P.T1) chunk = P.T1 > 0 ? P.T1 : 1;
@@ -315,11 +324,23 @@ int64_t plan_names(const Plan& P, const char** out, int64_t cap) {
 
 int64_t launch_count(const Plan& P) { return plan_names(P, nullptr, 0); }
 
+// Copy pipeline of sfa_grad_host around the chunk loop: the compute stream
+// waits for in_ready[c] (chunk c's query-side inputs are on the device)
+// before the chunk's first kernel, and once the chunk's dQ rows are final the
+// d2h stream copies them to the host while the next chunk computes.
+struct Pipe {
+  cudaStream_t d2h;
+  const cudaEvent_t* in_ready;
+  const cudaEvent_t* out_ready;
+  void* h_dq;
+  void* h_dqr;
+};
+
 template <typename T>
 sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const void* k, const void* v,
                     const int32_t* idx, const void* dO, const void* out, const float* smax, const float* ssum,
                     const int32_t* aq, const int32_t* akv, const void* qr, const void* kr, void* dq, void* dk, void* dv,
-                    void* dqr, void* dkr, uint8_t* ws, cudaStream_t st, Marks mk) {
+                    void* dqr, void* dkr, uint8_t* ws, cudaStream_t st, Marks mk, const Pipe* pipe = nullptr) {
   int* gerr = reinterpret_cast<int*>(ws + P.off_err);
   Prob pr = make_prob(P, ws);
   pr.q = q; pr.k = k; pr.v = v; pr.dO = dO; pr.out = out; pr.idx = idx;
@@ -345,12 +366,19 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
   SFA_CK(launch_meta(pr, P.layout, P.B, P.S1, P.S2, P.mode, aq, akv, reinterpret_cast<int*>(ws + P.off_batch),
                      reinterpret_cast<TokMeta*>(ws + P.off_meta), gerr, st));
   SFA_CK(mk.mark(st));
-  SFA_CK(launch_dsum<T>(pr, reinterpret_cast<float*>(ws + P.off_dsum), st));
-  SFA_CK(mk.mark(st));
+  float* dsum = reinterpret_cast<float*>(ws + P.off_dsum);
+  if (!pipe) {
+    SFA_CK(launch_dsum<T>(pr, 0, P.T1, dsum, st));
+    SFA_CK(mk.mark(st));
+  }
   float* acc = reinterpret_cast<float*>(ws + P.off_acc);
-  for (int t0 = 0; t0 < P.T1; t0 += P.chunk) {
+  for (int t0 = 0, c = 0; t0 < P.T1; t0 += P.chunk, ++c) {
     pr.tok0 = t0;
     pr.ntok = (P.T1 - t0) < P.chunk ? (P.T1 - t0) : P.chunk;
+    if (pipe) {
+      SFA_CK(cudaStreamWaitEvent(st, pipe->in_ready[c], 0));
+      SFA_CK(launch_dsum<T>(pr, t0, pr.ntok, dsum, st));
+    }
     void* Pst = ws + P.off_P;
     void* dSst = ws + P.off_dS;
     SFA_CK(launch_rowtab(pr, st));
@@ -401,12 +429,80 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
       SFA_CK(launch_kvq<T>(maps, pr, acc, dq, P.has_rope ? dqr : nullptr, kvq_tile_group(P), gerr, nsm, st));
       SFA_CK(mk.mark(st));
     }
+    if (pipe) {
+      const size_t row = (size_t)P.G * 512 * sizeof(T), rrow = (size_t)P.G * 64 * sizeof(T);
+      SFA_CK(cudaEventRecord(pipe->out_ready[c], st));
+      SFA_CK(cudaStreamWaitEvent(pipe->d2h, pipe->out_ready[c], 0));
+      SFA_CK(cudaMemcpyAsync(static_cast<uint8_t*>(pipe->h_dq) + t0 * row, static_cast<const uint8_t*>(dq) + t0 * row,
+                             pr.ntok * row, cudaMemcpyDeviceToHost, pipe->d2h));
+      if (P.has_rope)
+        SFA_CK(cudaMemcpyAsync(static_cast<uint8_t*>(pipe->h_dqr) + t0 * rrow,
+                               static_cast<const uint8_t*>(dqr) + t0 * rrow, pr.ntok * rrow, cudaMemcpyDeviceToHost,
+                               pipe->d2h));
+    }
   }
   SFA_CK(launch_cast<T>(acc, P.T2, dk, P.has_rope ? dkr : nullptr, dv, P.has_rope, st));
   SFA_CK(mk.mark(st));
   (void)prm;
   return SFA_OK;
 }
+
+// Device copies of sfa_grad_host's host buffers, placed after the
+// backward's own workspace (byte offsets into the workspace).
+struct HostLayout {
+  size_t q, k, v, idx, dO, out, smax, ssum, aq, akv, qr, kr, dq, dk, dv, dqr, dkr, total;
+};
+
+HostLayout host_layout(const Plan& P) {
+  HostLayout L;
+  size_t o = P.total;
+  auto take = [&](size_t bytes) {
+    const size_t r = o;
+    o += up(bytes);
+    return r;
+  };
+  const size_t t1 = (size_t)P.T1, t2 = (size_t)P.T2, g = (size_t)P.G, e = 2;
+  const size_t rope = P.has_rope ? 64 : 0;
+  L.q = take(t1 * g * 512 * e);
+  L.dO = take(t1 * g * 512 * e);
+  L.out = take(t1 * g * 512 * e);
+  L.qr = take(t1 * g * rope * e);
+  L.idx = take(t1 * (size_t)P.Kidx * 4);
+  L.smax = take(t1 * g * 4);
+  L.ssum = take(t1 * g * 4);
+  L.k = take(t2 * 512 * e);
+  L.v = take(t2 * 512 * e);
+  L.kr = take(t2 * rope * e);
+  L.aq = take((size_t)P.B * 4);
+  L.akv = take((size_t)P.B * 4);
+  L.dq = take(t1 * g * 512 * e);
+  L.dqr = take(t1 * g * rope * e);
+  L.dk = take(t2 * 512 * e);
+  L.dv = take(t2 * 512 * e);
+  L.dkr = take(t2 * rope * e);
+  L.total = o;
+  return L;
+}
+
+// Streams and events of one sfa_grad_host call.  Destroying them with work
+// still queued is allowed (the runtime releases them when the work is done);
+// on an early error return the internal streams are drained first, so no
+// copy from or to the caller's host buffers is still running when the call
+// returns.
+struct HostRes {
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  std::vector<cudaEvent_t> ev;
+  bool joined = false;
+  ~HostRes() {
+    if (!joined) {
+      if (h2d) cudaStreamSynchronize(h2d);
+      if (d2h) cudaStreamSynchronize(d2h);
+    }
+    for (cudaEvent_t e : ev) cudaEventDestroy(e);
+    if (h2d) cudaStreamDestroy(h2d);
+    if (d2h) cudaStreamDestroy(d2h);
+  }
+};
 
 template <typename T>
 sfa_status run_fwd(const Plan& P, const void* q, const void* k, const void* v, const int32_t* idx, const int32_t* aq,
@@ -531,6 +627,126 @@ sfa_status sfa_grad_profile(const sfa_params* p, const void* q, const void* k, c
                                  q_rope, k_rope, dq, dk, dv, dq_rope, dk_rope, ws, st, mk);
   return sfa::run_grad<__nv_bfloat16>(P, p, q, k, v, indices, d_out, out, softmax_max, softmax_sum, act_seq_q,
                                       act_seq_kv, q_rope, k_rope, dq, dk, dv, dq_rope, dk_rope, ws, st, mk);
+}
+
+sfa_status sfa_grad_host_workspace_size(const sfa_params* p, size_t* bytes) {
+  if (!p || !bytes) return SFA_ERR_NULLPTR;
+  Plan P;
+  sfa_status s = sfa::validate(p, false, &P, true);
+  if (s != SFA_OK) return s;
+  *bytes = sfa::host_layout(P).total;
+  return SFA_OK;
+}
+
+sfa_status sfa_grad_host(const sfa_params* p, const void* q, const void* k, const void* v, const int32_t* indices,
+                         const void* d_out, const void* out, const float* softmax_max, const float* softmax_sum,
+                         const int32_t* act_seq_q, const int32_t* act_seq_kv, const void* q_rope, const void* k_rope,
+                         void* dq, void* dk, void* dv, void* dq_rope, void* dk_rope, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  if (!p) return SFA_ERR_NULLPTR;
+  Plan P;
+  sfa_status s = sfa::validate(p, false, &P, true);
+  if (s != SFA_OK) return s;
+  const sfa::HostLayout L = sfa::host_layout(P);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool rope = P.has_rope;
+  if (!dk || !dv || (rope && !dk_rope) || !workspace) return SFA_ERR_NULLPTR;
+  if (workspace_bytes < L.total) return SFA_ERR_PARAM_INVALID;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t e = 2, t1 = (size_t)P.T1, t2 = (size_t)P.T2, g = (size_t)P.G;
+  const cudaMemcpyKind H2D = cudaMemcpyHostToDevice, D2H = cudaMemcpyDeviceToHost;
+  if (P.T1 == 0) {  // empty query: nothing selects any key
+    if (P.T2 > 0) {
+      SFA_CK(cudaMemsetAsync(ws + L.dk, 0, L.total - L.dk, st));   // dk, dv, dkr
+      SFA_CK(cudaMemcpyAsync(dk, ws + L.dk, t2 * 512 * e, D2H, st));
+      SFA_CK(cudaMemcpyAsync(dv, ws + L.dv, t2 * 512 * e, D2H, st));
+      if (rope) SFA_CK(cudaMemcpyAsync(dk_rope, ws + L.dkr, t2 * 64 * e, D2H, st));
+    }
+    return SFA_OK;
+  }
+  if (!q || !k || !v || !indices || !d_out || !out || !softmax_max || !softmax_sum || !dq) return SFA_ERR_NULLPTR;
+  if (rope && (!q_rope || !k_rope || !dq_rope)) return SFA_ERR_NULLPTR;
+  if (P.layout == SFA_LAYOUT_TND && (!act_seq_q || !act_seq_kv)) return SFA_ERR_NULLPTR;
+  const bool shared_kv = v == k;
+  const int nch = (P.T1 + P.chunk - 1) / P.chunk;
+
+  sfa::HostRes R;
+  SFA_CK(cudaStreamCreateWithFlags(&R.h2d, cudaStreamNonBlocking));
+  SFA_CK(cudaStreamCreateWithFlags(&R.d2h, cudaStreamNonBlocking));
+  R.ev.reserve(4 + 2 * (size_t)nch);
+  for (int i = 0; i < 4 + 2 * nch; ++i) {
+    cudaEvent_t ev;
+    SFA_CK(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+    R.ev.push_back(ev);
+  }
+  const cudaEvent_t ev_start = R.ev[0], ev_kv = R.ev[1], ev_cast = R.ev[2], ev_done = R.ev[3];
+  const cudaEvent_t* in_ready = R.ev.data() + 4;
+  const cudaEvent_t* out_ready = R.ev.data() + 4 + nch;
+
+  // the copies start once earlier work on the caller's stream (which may
+  // still read this workspace) is done
+  SFA_CK(cudaEventRecord(ev_start, st));
+  SFA_CK(cudaStreamWaitEvent(R.h2d, ev_start, 0));
+  SFA_CK(cudaMemcpyAsync(ws + L.k, k, t2 * 512 * e, H2D, R.h2d));
+  if (!shared_kv) SFA_CK(cudaMemcpyAsync(ws + L.v, v, t2 * 512 * e, H2D, R.h2d));
+  if (rope) SFA_CK(cudaMemcpyAsync(ws + L.kr, k_rope, t2 * 64 * e, H2D, R.h2d));
+  if (P.layout == SFA_LAYOUT_TND) {
+    SFA_CK(cudaMemcpyAsync(ws + L.aq, act_seq_q, (size_t)P.B * 4, H2D, R.h2d));
+    SFA_CK(cudaMemcpyAsync(ws + L.akv, act_seq_kv, (size_t)P.B * 4, H2D, R.h2d));
+  }
+  SFA_CK(cudaEventRecord(ev_kv, R.h2d));
+  // per chunk, every query-side input row of its tokens
+  for (int c = 0; c < nch; ++c) {
+    const size_t t0 = (size_t)c * P.chunk, n = (t1 - t0) < (size_t)P.chunk ? (t1 - t0) : (size_t)P.chunk;
+    const size_t row = g * 512 * e, rrow = g * 64 * e, irow = (size_t)P.Kidx * 4, srow = g * 4;
+    SFA_CK(cudaMemcpyAsync(ws + L.q + t0 * row, static_cast<const uint8_t*>(q) + t0 * row, n * row, H2D, R.h2d));
+    if (rope)
+      SFA_CK(cudaMemcpyAsync(ws + L.qr + t0 * rrow, static_cast<const uint8_t*>(q_rope) + t0 * rrow, n * rrow, H2D,
+                             R.h2d));
+    SFA_CK(cudaMemcpyAsync(ws + L.idx + t0 * irow, reinterpret_cast<const uint8_t*>(indices) + t0 * irow, n * irow,
+                           H2D, R.h2d));
+    SFA_CK(cudaMemcpyAsync(ws + L.smax + t0 * srow, reinterpret_cast<const uint8_t*>(softmax_max) + t0 * srow,
+                           n * srow, H2D, R.h2d));
+    SFA_CK(cudaMemcpyAsync(ws + L.ssum + t0 * srow, reinterpret_cast<const uint8_t*>(softmax_sum) + t0 * srow,
+                           n * srow, H2D, R.h2d));
+    SFA_CK(cudaMemcpyAsync(ws + L.dO + t0 * row, static_cast<const uint8_t*>(d_out) + t0 * row, n * row, H2D, R.h2d));
+    SFA_CK(cudaMemcpyAsync(ws + L.out + t0 * row, static_cast<const uint8_t*>(out) + t0 * row, n * row, H2D, R.h2d));
+    SFA_CK(cudaEventRecord(in_ready[c], R.h2d));
+  }
+
+  SFA_CK(cudaStreamWaitEvent(st, ev_kv, 0));
+  sfa::Pipe pipe;
+  pipe.d2h = R.d2h;
+  pipe.in_ready = in_ready;
+  pipe.out_ready = out_ready;
+  pipe.h_dq = dq;
+  pipe.h_dqr = dq_rope;
+  uint8_t* d_v = shared_kv ? ws + L.k : ws + L.v;
+  const int32_t* d_aq = P.layout == SFA_LAYOUT_TND ? reinterpret_cast<const int32_t*>(ws + L.aq) : nullptr;
+  const int32_t* d_akv = P.layout == SFA_LAYOUT_TND ? reinterpret_cast<const int32_t*>(ws + L.akv) : nullptr;
+  if (P.is_f16)
+    s = sfa::run_grad<__half>(P, p, ws + L.q, ws + L.k, d_v, reinterpret_cast<const int32_t*>(ws + L.idx), ws + L.dO,
+                              ws + L.out, reinterpret_cast<const float*>(ws + L.smax),
+                              reinterpret_cast<const float*>(ws + L.ssum), d_aq, d_akv, ws + L.qr, ws + L.kr,
+                              ws + L.dq, ws + L.dk, ws + L.dv, ws + L.dqr, ws + L.dkr, ws, st, sfa::Marks{}, &pipe);
+  else
+    s = sfa::run_grad<__nv_bfloat16>(P, p, ws + L.q, ws + L.k, d_v, reinterpret_cast<const int32_t*>(ws + L.idx),
+                                     ws + L.dO, ws + L.out, reinterpret_cast<const float*>(ws + L.smax),
+                                     reinterpret_cast<const float*>(ws + L.ssum), d_aq, d_akv, ws + L.qr, ws + L.kr,
+                                     ws + L.dq, ws + L.dk, ws + L.dv, ws + L.dqr, ws + L.dkr, ws, st, sfa::Marks{},
+                                     &pipe);
+  if (s != SFA_OK) return s;
+  // key-side outputs after the final cast, then the caller's stream waits
+  // for every copy to the host
+  SFA_CK(cudaEventRecord(ev_cast, st));
+  SFA_CK(cudaStreamWaitEvent(R.d2h, ev_cast, 0));
+  SFA_CK(cudaMemcpyAsync(dk, ws + L.dk, t2 * 512 * e, D2H, R.d2h));
+  SFA_CK(cudaMemcpyAsync(dv, ws + L.dv, t2 * 512 * e, D2H, R.d2h));
+  if (rope) SFA_CK(cudaMemcpyAsync(dk_rope, ws + L.dkr, t2 * 64 * e, D2H, R.d2h));
+  SFA_CK(cudaEventRecord(ev_done, R.d2h));
+  SFA_CK(cudaStreamWaitEvent(st, ev_done, 0));
+  R.joined = true;
+  return SFA_OK;
 }
 
 sfa_status sfa_fwd(const sfa_params* p, const void* q, const void* k, const void* v, const int32_t* indices,

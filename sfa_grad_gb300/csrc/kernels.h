@@ -50,8 +50,9 @@ cudaError_t launch_batch_prefix(const Prob& p, int B, const int* act_q, const in
                                 cudaStream_t st);
 cudaError_t launch_meta(const Prob& p, int layout, int B, int S1, int S2, int mode, const int* act_q, const int* act_kv,
                         int* batch_ofs, TokMeta* meta, int* gerr, cudaStream_t st);
+// Dsum of tokens tok0 .. tok0 + ntok - 1 (all heads).
 template <typename T>
-cudaError_t launch_dsum(const Prob& p, float* dsum, cudaStream_t st);
+cudaError_t launch_dsum(const Prob& p, int tok0, int ntok, float* dsum, cudaStream_t st);
 template <typename T>
 cudaError_t launch_cast(const float* acc, int T2, void* dk, void* dkr, void* dv, int has_rope, cudaStream_t st);
 cudaError_t launch_stats_combine(const Prob& p, const float* tile_stats, float* smax, float* ssum, cudaStream_t st);

@@ -180,10 +180,12 @@ cudaError_t launch_rowtab(const Prob& p, cudaStream_t st) {
 }
 
 template <typename T>
-cudaError_t launch_dsum(const Prob& p, float* dsum, cudaStream_t st) {
-  const int rows = p.T1 * p.G;
+cudaError_t launch_dsum(const Prob& p, int tok0, int ntok, float* dsum, cudaStream_t st) {
+  const int rows = ntok * p.G;
   if (rows == 0) return cudaSuccess;
-  dsum_kernel<T><<<(rows + 7) / 8, 256, 0, st>>>(static_cast<const T*>(p.dO), static_cast<const T*>(p.out), rows, dsum);
+  const size_t r0 = (size_t)tok0 * p.G;
+  dsum_kernel<T><<<(rows + 7) / 8, 256, 0, st>>>(static_cast<const T*>(p.dO) + r0 * 512,
+                                                 static_cast<const T*>(p.out) + r0 * 512, rows, dsum + r0);
   return cudaGetLastError();
 }
 
@@ -206,8 +208,8 @@ cudaError_t launch_stats_combine(const Prob& p, const float* tile_stats, float* 
   return cudaGetLastError();
 }
 
-template cudaError_t launch_dsum<__nv_bfloat16>(const Prob&, float*, cudaStream_t);
-template cudaError_t launch_dsum<__half>(const Prob&, float*, cudaStream_t);
+template cudaError_t launch_dsum<__nv_bfloat16>(const Prob&, int, int, float*, cudaStream_t);
+template cudaError_t launch_dsum<__half>(const Prob&, int, int, float*, cudaStream_t);
 template cudaError_t launch_cast<__nv_bfloat16>(const float*, int, void*, void*, void*, int, cudaStream_t);
 template cudaError_t launch_cast<__half>(const float*, int, void*, void*, void*, int, cudaStream_t);
 

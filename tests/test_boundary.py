@@ -137,3 +137,25 @@ def test_plan_names(sfa):
     tnd = sfa.plan_names(_p(sfa, layout=1, B=4, T1=16384, T2=32768, N1=64, K=2048, sparse_mode=3))
     assert tnd[0] == "batch_prefix" and "kvq" in tnd
     assert sfa.plan_names(_p(sfa, S1=0)) == []
+
+
+def test_host_entry_validation(sfa):
+    """sfa_grad_host: its workspace holds the backward's (with pipeline-sized
+    token chunks) plus device copies of every input and output; missing
+    pointers and a short workspace are rejected before any CUDA call."""
+    p = _p(sfa, S1=4096, S2=4096, N1=128, K=2048)
+    n = ctypes.c_size_t(0)
+    assert sfa.lib().sfa_grad_host_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 0
+    t1, t2, g = 4096, 4096, 128
+    io = (3 * t1 * g * 512 + t1 * g * 64) * 2 + t1 * 2048 * 4 + 2 * t1 * g * 4 + (2 * t2 * 512 + t2 * 64) * 2 \
+        + (t1 * g * 576 + t2 * 1088) * 2
+    assert n.value >= io
+    # pipeline chunks: an eighth of the tokens, so the staging is smaller than sfa_grad's
+    assert n.value - io < _ws(sfa, p)[1]
+    assert sfa.lib().sfa_grad_host_workspace_size(None, ctypes.byref(n)) == sfa.SFA_ERR_NULLPTR
+    assert sfa.lib().sfa_grad_host(ctypes.byref(p), *([None] * 18), 0, None) == sfa.SFA_ERR_NULLPTR
+    fake = ctypes.c_void_p(16)
+    rc = sfa.lib().sfa_grad_host(ctypes.byref(p), *([fake] * 18), 8, None)
+    assert rc == sfa.SFA_ERR_PARAM_INVALID
+    bad = _p(sfa, N2=2)
+    assert sfa.lib().sfa_grad_host(ctypes.byref(bad), *([fake] * 18), 1 << 40, None) == sfa.SFA_ERR_SHAPE
