@@ -14,15 +14,15 @@ from workloads import make_inputs, small_workload
 
 pytestmark = pytest.mark.gpu
 
-# Query token counts above 64 * 8 give eight chunks; the others give chunks of
-# 64 tokens with a ragged last one.
+# Chunk schedules: 200 tokens run as 64, 64, 64, 8; 600 as 128, 150, 150,
+# 128, 44 (growing, then halving, ragged last chunk); 16 tokens as one chunk.
 CASES = {
     "g16_chunks_ragged": small_workload(N1=16, S1=200, S2=512, K=128, seed=41),
     "g8_tnd_causal": small_workload(name="tnd_host", layout="TND", B=3, N1=8, K=96, mode=3, index_kind="causal",
                                     kv_extra=100, T1=150, act_q=(70, 0, 80), seed=42),
     "g16_kvb_fp16": small_workload(N1=16, S1=150, S2=512, K=8, block_size=16, index_kind="block", dtype="fp16",
                                    std=0.5, seed=43),
-    "g4_eight_chunks_norope": small_workload(N1=4, S1=600, S2=256, K=64, Dr=0, seed=44),
+    "g4_ramp_norope": small_workload(N1=4, S1=600, S2=256, K=64, Dr=0, seed=44),
     "tiny_one_chunk": small_workload(N1=4, S1=16, S2=2048, K=1024, seed=45),
 }
 
