@@ -161,7 +161,8 @@ sfa_status sfa_grad_plan_info(const sfa_params* p, int64_t* chunk_tokens, int64_
  * many tokens select: pairs grouped by block start, key side accumulated per
  * block, then the query side alone), or with deterministic = 1 "det_count",
  * "det_scan", "det_scatter", "det_sort" (entries sorted by kv row, then token
- * and slot), "dkv", "det_reduce", "dq"; finally "cast".  Writes at most `capacity`
+ * and slot), "kvq" (the key side stored as per-pair partial rows, with the
+ * query side), "det_reduce"; finally "cast".  Writes at most `capacity`
  * pointers to static strings into names[] (names may be null when capacity
  * is 0) and the total count into *count (may be null).  Host only; validates
  * *p like sfa_grad_workspace_size.

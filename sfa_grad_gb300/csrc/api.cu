@@ -294,7 +294,7 @@ int kvq_tile_group(const Plan& P) {
 
 // Kernel launches of one sfa_grad call, in order (sfa_grad_plan_names).
 const char* const kChunkDet[] = {"rowtab", "sdp", "det_count", "det_scan", "det_scatter", "det_sort",
-                                 "dkv", "det_reduce", "dq"};
+                                 "kvq", "det_reduce"};
 const char* const kChunkKvq[] = {"rowtab", "sdp", "kvq"};
 const char* const kChunkKvb[] = {"rowtab", "sdp", "blk_count", "blk_scan", "blk_scatter", "kvb", "kvq"};
 
@@ -406,11 +406,11 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
       SFA_CK(mk.mark(st));
       SFA_CK(launch_det_sort(pr, bbeg, bng, bent, dscr, st));
       SFA_CK(mk.mark(st));
-      SFA_CK(launch_dkv<T>(maps, pr, acc, part, gerr, nsm, st));
+      // key side as partial rows (token-major items) with the query side
+      // in the same launch, then the fixed-order sums
+      SFA_CK(launch_kvq<T>(maps, pr, part, dq, P.has_rope ? dqr : nullptr, P.Kpad / 128, true, gerr, nsm, st));
       SFA_CK(mk.mark(st));
       SFA_CK(launch_det_reduce(pr, bgrp, bbeg, bng, bent, part, acc, st));
-      SFA_CK(mk.mark(st));
-      SFA_CK(launch_dq<T>(maps, pr, 0, dq, P.has_rope ? dqr : nullptr, gerr, nsm, st));
       SFA_CK(mk.mark(st));
     } else if (P.kvb) {
       int* bcnt = reinterpret_cast<int*>(ws + P.off_bcnt);
@@ -427,10 +427,10 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
       SFA_CK(mk.mark(st));
       SFA_CK(launch_kvb<T>(bmaps, pr, P.bs, bgrp, bbeg, bng, bent, acc, gerr, nsm, st));
       SFA_CK(mk.mark(st));
-      SFA_CK(launch_kvq<T>(maps, pr, acc, dq, P.has_rope ? dqr : nullptr, 0, gerr, nsm, st));   // query side only
+      SFA_CK(launch_kvq<T>(maps, pr, acc, dq, P.has_rope ? dqr : nullptr, 0, false, gerr, nsm, st));   // query side only
       SFA_CK(mk.mark(st));
     } else {
-      SFA_CK(launch_kvq<T>(maps, pr, acc, dq, P.has_rope ? dqr : nullptr, kvq_tile_group(P), gerr, nsm, st));
+      SFA_CK(launch_kvq<T>(maps, pr, acc, dq, P.has_rope ? dqr : nullptr, kvq_tile_group(P), false, gerr, nsm, st));
       SFA_CK(mk.mark(st));
     }
     if (pipe) {
@@ -562,7 +562,7 @@ sfa_status run_fwd(const Plan& P, const void* q, const void* k, const void* v, c
     SFA_CK(launch_sdp<T>(maps, pr, kModeFwdStats, nullptr, nullptr, ts, gerr, nsm, st));
     SFA_CK(launch_stats_combine(pr, ts, smax, ssum, st));
     SFA_CK(launch_sdp<T>(maps, pr, kModeFwdP, ws + P.off_P, nullptr, nullptr, gerr, nsm, st));
-    SFA_CK(launch_dq<T>(maps, pr, 1, out, nullptr, gerr, nsm, st));
+    SFA_CK(launch_pv<T>(maps, pr, out, gerr, nsm, st));
   }
   return SFA_OK;
 }

@@ -2,6 +2,8 @@
 //   mode 0:  [dQ || dQRope](t) = dS(t) . [K || KRope]_sel   (3 chunks of 192 features;
 //            the softmax scale is already folded into the stored dS)
 //   mode 1:  O(t) = P(t) . V_sel                              (2 chunks of 256 features)
+// Only mode 1 is launched (the companion forward's output); the backward
+// forms dQ in kvq.cu, next to the key side.
 // Heads on M (padded to 128), features on N, keys (64 per pipeline stage) on K;
 // the accumulator stays in tensor memory for the whole key loop and is written
 // once, so dQ needs no atomics.
@@ -242,16 +244,12 @@ cudaError_t launch_one(const Maps& maps, const Prob& p, void* o1, void* o2, int*
 }  // namespace
 
 template <typename T>
-cudaError_t launch_dq(const Maps& maps, const Prob& p, int mode, void* out_main, void* out_rope, int* gerr, int nsm,
-                      cudaStream_t st) {
-  if (p.Gp == 64)
-    return mode == 0 ? launch_one<T, 64, 0>(maps, p, out_main, out_rope, gerr, nsm, st)
-                     : launch_one<T, 64, 1>(maps, p, out_main, out_rope, gerr, nsm, st);
-  return mode == 0 ? launch_one<T, 128, 0>(maps, p, out_main, out_rope, gerr, nsm, st)
-                   : launch_one<T, 128, 1>(maps, p, out_main, out_rope, gerr, nsm, st);
+cudaError_t launch_pv(const Maps& maps, const Prob& p, void* out, int* gerr, int nsm, cudaStream_t st) {
+  if (p.Gp == 64) return launch_one<T, 64, 1>(maps, p, out, nullptr, gerr, nsm, st);
+  return launch_one<T, 128, 1>(maps, p, out, nullptr, gerr, nsm, st);
 }
 
-template cudaError_t launch_dq<__nv_bfloat16>(const Maps&, const Prob&, int, void*, void*, int*, int, cudaStream_t);
-template cudaError_t launch_dq<__half>(const Maps&, const Prob&, int, void*, void*, int*, int, cudaStream_t);
+template cudaError_t launch_pv<__nv_bfloat16>(const Maps&, const Prob&, void*, int*, int, cudaStream_t);
+template cudaError_t launch_pv<__half>(const Maps&, const Prob&, void*, int*, int, cudaStream_t);
 
 }  // namespace sfa

@@ -13,17 +13,6 @@ template <typename T>
 cudaError_t launch_sdp(const Maps& maps, const Prob& p, int mode, void* out_p, void* out_ds, float* tile_stats, int* gerr, int nsm,
                        cudaStream_t st);
 
-// Key-side gradients (dkv.cu): dV = P^T dO, [dK || dKRope] = dS^T [q || qRope],
-// reduced into the fp32 accumulator acc (T2 x 1088) with atomics, or written
-// as per-(token, slot) partial rows when `partials` is non-null.
-template <typename T>
-cudaError_t launch_dkv(const Maps& maps, const Prob& p, float* acc, float* partials, int* gerr, int nsm,
-                       cudaStream_t st);
-
-// Key-side and query-side contractions in one launch, two pipelines per CTA
-// (kvq.cu): non-deterministic key-side reductions into acc, dQ / dQRope out.
-// tile_group: key tiles per key-side work item (items run tile-group major;
-// a group of all tiles gives token-major order); 0 runs the query side only.
 // Key-major dK / dV for block-sparse indices (kvb.cu): group the chunk's
 // (token, index) pairs by block start (count, scan, scatter), then accumulate
 // every group's block in tensor memory and add it to acc once.
@@ -35,14 +24,19 @@ template <typename T>
 cudaError_t launch_kvb(const BlkMaps& maps, const Prob& p, int bs, const int* groups, const int* gbeg,
                        const int* ngroups, const int* entries, float* acc, int* gerr, int nsm, cudaStream_t st);
 
+// Key-side and query-side contractions in one launch, two pipelines per CTA
+// (kvq.cu): key-side reductions into acc, dQ / dQRope out.  tile_group: key
+// tiles per key-side work item (items run tile-group major; a group of all
+// tiles gives token-major order); 0 runs the query side only.  part:
+// deterministic mode; acc is then the chunk's partial-row buffer and every
+// valid (token, slot) row is stored there instead of reduced.
 template <typename T>
-cudaError_t launch_kvq(const Maps& maps, const Prob& p, float* acc, void* dq, void* dqr, int tile_group, int* gerr,
-                       int nsm, cudaStream_t st);
+cudaError_t launch_kvq(const Maps& maps, const Prob& p, float* acc, void* dq, void* dqr, int tile_group, bool part,
+                       int* gerr, int nsm, cudaStream_t st);
 
-// Query-side contraction (dq.cu): dQ = dS K (mode 0) or O = P V (mode 1).
+// Companion forward's output O = P V over each token's selected keys (dq.cu).
 template <typename T>
-cudaError_t launch_dq(const Maps& maps, const Prob& p, int mode, void* out_main, void* out_rope, int* gerr, int nsm,
-                      cudaStream_t st);
+cudaError_t launch_pv(const Maps& maps, const Prob& p, void* out, int* gerr, int nsm, cudaStream_t st);
 
 // Small kernels (prep.cu).
 cudaError_t launch_rowtab(const Prob& p, cudaStream_t st);

@@ -3,7 +3,8 @@
 // SM:
 //   key side:   dV_tile = P^T . dO and [dK|dKRope]_tile = dS^T . [q || qRope]
 //               for 128 keys x 128 features, drained into the fp32 key-row
-//               accumulator with vector reductions;
+//               accumulator with vector reductions (deterministic mode:
+//               stored as per-pair partial rows for the fixed-order sums);
 //   query side: [dQ || dQRope](t) = dS(t) . [K || KRope]_sel, 192 features,
 //               accumulated in tensor memory over all the token's keys.
 // The key side is bound by the SM-to-L2 reduction path and leaves the tensor
@@ -87,7 +88,11 @@ __device__ __forceinline__ void red_add_v4(float* dst, float4 x) {
 // rows as one TMA box per selected block.  A compile-time switch: the unused
 // branch in the row-gather loop alone costs the single-key path a quarter of
 // its query-side throughput.
-template <typename T, int GP, bool BLK>
+// PART (deterministic = 1): instead of reducing into the accumulator, the
+// drain stores every valid (token, slot) pair's 1088-float row at
+// acc + (token_local * Kpad + slot) * 1088 (the partial rows the fixed-order
+// reduction of det.cu sums); masked slots are not written.
+template <typename T, int GP, bool BLK, bool PART>
 __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant__ Maps maps, Prob p, float* acc,
                                                           T* dq, T* dqr, int tg, int* gerr) {
   using E = Elt<T>;
@@ -276,7 +281,15 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
             const int rl = rr * 4 + (lane >> 3), c4 = lane & 7;
             const float4 x = reinterpret_cast<const float4*>(stg + rl * 32)[c4 ^ (rl & 7)];
             const int grow = __shfl_sync(0xffffffffu, row, rl);
-            if (grow >= 0) red_add_v4(acc + (size_t)grow * kAccRow + col0 + c + c4 * 4, x);
+            if constexpr (PART) {
+              // streaming store: the rows are read back once, after this kernel
+              if (grow >= 0)
+                __stcs(reinterpret_cast<float4*>(acc + ((size_t)ki.tl * p.Kpad + kt * kKeys + qd * 32 + rl) * kAccRow +
+                                                 col0 + c + c4 * 4),
+                       x);
+            } else if (grow >= 0) {
+              red_add_v4(acc + (size_t)grow * kAccRow + col0 + c + c4 * 4, x);
+            }
           }
           __syncwarp();
         }
@@ -434,9 +447,10 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
 }
 
 template <typename T, int GP>
-cudaError_t launch_gp(const Maps& maps, const Prob& p, float* acc, void* dq, void* dqr, int tile_group, int* gerr,
-                      int nsm, cudaStream_t st) {
-  auto kern = p.bs >= 8 ? kvq_kernel<T, GP, true> : kvq_kernel<T, GP, false>;
+cudaError_t launch_gp(const Maps& maps, const Prob& p, float* acc, void* dq, void* dqr, int tile_group, bool part,
+                      int* gerr, int nsm, cudaStream_t st) {
+  auto kern = p.bs >= 8 ? (part ? kvq_kernel<T, GP, true, true> : kvq_kernel<T, GP, true, false>)
+                        : (part ? kvq_kernel<T, GP, false, true> : kvq_kernel<T, GP, false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const int nitems = p.ntok * kKvChunks;
@@ -450,14 +464,15 @@ cudaError_t launch_gp(const Maps& maps, const Prob& p, float* acc, void* dq, voi
 }  // namespace
 
 template <typename T>
-cudaError_t launch_kvq(const Maps& maps, const Prob& p, float* acc, void* dq, void* dqr, int tile_group, int* gerr,
-                       int nsm, cudaStream_t st) {
-  if (p.Gp == 64) return launch_gp<T, 64>(maps, p, acc, dq, dqr, tile_group, gerr, nsm, st);
-  return launch_gp<T, 128>(maps, p, acc, dq, dqr, tile_group, gerr, nsm, st);
+cudaError_t launch_kvq(const Maps& maps, const Prob& p, float* acc, void* dq, void* dqr, int tile_group, bool part,
+                       int* gerr, int nsm, cudaStream_t st) {
+  if (p.Gp == 64) return launch_gp<T, 64>(maps, p, acc, dq, dqr, tile_group, part, gerr, nsm, st);
+  return launch_gp<T, 128>(maps, p, acc, dq, dqr, tile_group, part, gerr, nsm, st);
 }
 
-template cudaError_t launch_kvq<__nv_bfloat16>(const Maps&, const Prob&, float*, void*, void*, int, int*, int,
+template cudaError_t launch_kvq<__nv_bfloat16>(const Maps&, const Prob&, float*, void*, void*, int, bool, int*, int,
                                                cudaStream_t);
-template cudaError_t launch_kvq<__half>(const Maps&, const Prob&, float*, void*, void*, int, int*, int, cudaStream_t);
+template cudaError_t launch_kvq<__half>(const Maps&, const Prob&, float*, void*, void*, int, bool, int*, int,
+                                        cudaStream_t);
 
 }  // namespace sfa

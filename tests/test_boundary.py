@@ -132,8 +132,8 @@ def test_plan_names(sfa):
     assert "kvb" not in sfa.plan_names(_p(sfa, S1=2048, S2=4096, N1=16, K=64, sparse_block_size=8))
     assert "kvb" not in sfa.plan_names(_p(sfa, S1=2048, S2=4096, N1=128, K=64, sparse_block_size=64))
     det = sfa.plan_names(_p(sfa, deterministic=1))
-    assert det == ["meta", "dsum", "rowtab", "sdp", "det_count", "det_scan", "det_scatter", "det_sort", "dkv",
-                   "det_reduce", "dq", "cast"]
+    assert det == ["meta", "dsum", "rowtab", "sdp", "det_count", "det_scan", "det_scatter", "det_sort", "kvq",
+                   "det_reduce", "cast"]
     tnd = sfa.plan_names(_p(sfa, layout=1, B=4, T1=16384, T2=32768, N1=64, K=2048, sparse_mode=3))
     assert tnd[0] == "batch_prefix" and "kvq" in tnd
     assert sfa.plan_names(_p(sfa, S1=0)) == []
