@@ -352,17 +352,20 @@ def run_sfa(args):
     hkw = dict(q_rope=host["q_rope"], k_rope=host["k_rope"], sparse_block_size=w.block_size, layout=w.layout,
                sparse_mode=w.mode, act_seq_q=host.get("act_seq_q"), act_seq_kv=host.get("act_seq_kv"))
     e2e_steps = max(3, min(args.steps, 10))
-    e2e_ms = []
+    e2e_ms, call_ms = [], []
     for i in range(e2e_steps + 2):
         flush.fill_(2)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        c0 = time.perf_counter()
         sfa.grad_host(host["q"], host["k"], host["v"], host["indices"], host["d_out"], h_out, h_m, h_l,
                       w.scale_value, deterministic=det, outputs=res_host, workspace=ws_h, **hkw)
+        c1 = time.perf_counter()
         e1.record(stream)
         torch.cuda.synchronize()
         if i >= 2:
             e2e_ms.append(e0.elapsed_time(e1))
+            call_ms.append((c1 - c0) * 1e3)
     err = sfa.read_device_error(ws_h)
     if err != 0:
         raise RuntimeError(f"device error word {err} (host-buffer path)")
@@ -439,6 +442,7 @@ def run_sfa(args):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_mean, "h2d_gbs": round(h2d_gbs, 1), "d2h_gbs": round(d2h_gbs, 1),
+                "host_call_ms": round(statistics.mean(call_ms), 3),
                 "call": "sfa_grad_host: pinned host inputs and outputs, copies overlapped with the kernels per token chunk"},
         "gpu_launches": launches * args.steps,
         "clocks": clk,

@@ -237,12 +237,14 @@ sfa_status sfa_grad_noalloc(const sfa_params* p, const void* q, const void* k, c
  * backward's workspace followed by device copies of the inputs and outputs.
  *
  * The call splits the query tokens into chunks: the first of 128 tokens,
- * each next one up to 1.25 times larger (at most a quarter of the tokens),
- * and halving again towards the end, down to 128.  On two streams it creates, it copies k, v,
- * kRope and the lengths, then each chunk's query-side rows (q, qRope, dOut,
- * out, softmaxMax, softmaxSum, indices) to the device.  Chunk c's kernels start
- * when its rows have landed, and its dQ / dQRope rows are copied back while
- * chunk c + 1 computes; dK / dV / dKRope follow the final cast.  All of it is
+ * each next one larger by a factor estimated from the shape (how much longer
+ * a token's kernels run than its inputs take to copy, 1.25 to 8, e.g. 1.25
+ * for MLA), and halving again towards the end.  On two streams it creates,
+ * it copies k, v, kRope and the lengths, then each chunk's query-side rows
+ * (q, qRope, dOut, out, softmaxMax, softmaxSum, indices) to the device, one
+ * chunk ahead of the kernels.  Chunk c's kernels start when its rows have
+ * landed, and its dQ / dQRope rows are copied back while chunk c + 1
+ * computes; dK / dV / dKRope follow the final cast.  All of it is
  * ordered after earlier work on `stream`, and `stream` waits for the last
  * copy: the host outputs are complete, and the host inputs free, once
  * `stream` has been synchronised.  The two streams and the events are

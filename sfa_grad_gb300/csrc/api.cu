@@ -35,10 +35,7 @@ struct Plan {
   size_t total;
 };
 
-// host_pipe: plan of sfa_grad_host, whose token chunks are also the units
-// of its copy pipeline (host_bounds): its staging holds chunks of up to a
-// quarter of the tokens (at least 64).
-sfa_status validate(const sfa_params* p, bool fwd, Plan* out, bool host_pipe = false) {
+sfa_status validate(const sfa_params* p, bool fwd, Plan* out) {
   if (!p) return SFA_ERR_NULLPTR;
   if (p->dtype != SFA_DTYPE_BF16 && p->dtype != SFA_DTYPE_FP16) return SFA_ERR_PARAM_INVALID;
   if (p->layout != SFA_LAYOUT_BSND && p->layout != SFA_LAYOUT_TND) return SFA_ERR_PARAM_INVALID;
@@ -96,10 +93,6 @@ sfa_status validate(const sfa_params* p, bool fwd, Plan* out, bool host_pipe = f
     const size_t part_per_tok = (size_t)P.Kpad * kAccRow * 4;
     const size_t c2 = kPartCap / part_per_tok;
     if (c2 < chunk) chunk = c2;
-  }
-  if (host_pipe) {
-    const size_t cap = ((size_t)P.T1 + 3) / 4 > 64 ? ((size_t)P.T1 + 3) / 4 : 64;
-    if (chunk > cap) chunk = cap;
   }
   if (chunk < 1) chunk = 1;
   if (chunk > (size_t)P.T1) chunk = P.T1 > 0 ? P.T1 : 1;
@@ -323,13 +316,47 @@ int64_t plan_names(const Plan& P, const char** out, int64_t cap) {
 
 int64_t launch_count(const Plan& P) { return plan_names(P, nullptr, 0); }
 
-// Copy pipeline of sfa_grad_host around the chunk loop: the compute stream
-// waits for in_ready[c] (chunk c's query-side inputs are on the device)
-// before the chunk's first kernel, and once the chunk's dQ rows are final the
-// d2h stream copies them to the host while the next chunk computes.
+// Host-to-device copies of one chunk's query-side rows (q, qRope, indices,
+// softmaxMax, softmaxSum, dOut, out) on the h2d stream, then in_ready[c].
+struct HostCopies {
+  cudaStream_t h2d;
+  const int* bounds;
+  const cudaEvent_t* in_ready;
+  uint8_t* dq_;   // device copies: q, qRope, indices, max, sum, dO, out
+  uint8_t* dqr_;
+  uint8_t* didx;
+  uint8_t* dmax;
+  uint8_t* dsum_;
+  uint8_t* ddo;
+  uint8_t* dout;
+  const uint8_t *hq, *hqr, *hidx, *hmax, *hsum, *hdo, *hout;
+  size_t row, rrow, irow, srow;   // bytes per token
+  cudaError_t put(int c) const {
+    const size_t t0 = c > 0 ? (size_t)bounds[c - 1] : 0, n = (size_t)bounds[c] - t0;
+    const cudaMemcpyKind k = cudaMemcpyHostToDevice;
+    cudaError_t e = cudaMemcpyAsync(dq_ + t0 * row, hq + t0 * row, n * row, k, h2d);
+    if (e == cudaSuccess && rrow) e = cudaMemcpyAsync(dqr_ + t0 * rrow, hqr + t0 * rrow, n * rrow, k, h2d);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(didx + t0 * irow, hidx + t0 * irow, n * irow, k, h2d);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dmax + t0 * srow, hmax + t0 * srow, n * srow, k, h2d);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dsum_ + t0 * srow, hsum + t0 * srow, n * srow, k, h2d);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(ddo + t0 * row, hdo + t0 * row, n * row, k, h2d);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dout + t0 * row, hout + t0 * row, n * row, k, h2d);
+    if (e == cudaSuccess) e = cudaEventRecord(in_ready[c], h2d);
+    return e;
+  }
+};
+
+// Copy pipeline of sfa_grad_host around the chunk loop.  Before chunk c's
+// kernels are queued, chunk c + 1's copies are (so the host queues the first
+// kernels after two chunks' copies, not after all of them, and the h2d
+// stream still runs one chunk ahead); the compute stream waits for
+// in_ready[c] before the chunk's first kernel, and once the chunk's dQ rows
+// are final the d2h stream copies them to the host while the next chunk
+// computes.
 struct Pipe {
   const int* bounds;   // end token of each chunk
   int nch;
+  const HostCopies* copies;
   cudaStream_t d2h;
   const cudaEvent_t* in_ready;
   const cudaEvent_t* out_ready;
@@ -380,6 +407,7 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
     pr.tok0 = t0;
     pr.ntok = t_end - t0;
     if (pipe) {
+      if (c + 1 < pipe->nch) SFA_CK(pipe->copies->put(c + 1));
       SFA_CK(cudaStreamWaitEvent(st, pipe->in_ready[c], 0));
       SFA_CK(launch_dsum<T>(pr, t0, pr.ntok, dsum, st));
     }
@@ -489,28 +517,47 @@ HostLayout host_layout(const Plan& P) {
 }
 
 // Token chunks of sfa_grad_host (end token of each).  The first chunk is
-// small (128 tokens) so that the kernels start after a short copy, and each
-// next one is at most 1.25 times larger: the inputs of a token take less
-// time to copy than its kernels take to run (MLA shapes: about 2.0 us at the
-// measured 210 GB/s against 2.7 us per token at 128 heads), so chunk c + 1
-// lands while chunk c computes.  Chunks stop growing at the staging size
-// (cap) and shrink by halves at the end, down to 128 tokens, so that the last
-// dQ readback is short.  On MLA this schedule beat even splits into 4, 8 or
-// 16 chunks, a steeper ramp (x1.5) and a flatter one (x1.15).
-std::vector<int> host_bounds(int T1, int cap) {
+// small (128 tokens) so that the kernels start after a short copy.  Each
+// next chunk is at most `ratio` times larger, where ratio estimates how much
+// longer a token's kernels run than its inputs take to copy, so that chunk
+// c + 1 lands while chunk c computes.  Chunks stop growing at the staging
+// size (cap) and shrink by halves at the end, down to `tmin` tokens, so that
+// the last dQ readback is short.
+std::vector<int> host_bounds(int T1, int cap, double ratio, int tmin) {
   std::vector<int> b;
   double up = 128.0;
   for (int t = 0; t < T1;) {
     const int rem = T1 - t;
     int n = up < (double)cap ? (int)up : cap;
-    const int half = (rem + 1) / 2 > 128 ? (rem + 1) / 2 : 128;
+    const int half = (rem + 1) / 2 > tmin ? (rem + 1) / 2 : tmin;
     if (n > half) n = half;
     if (n > rem) n = rem;
     t += n;
     b.push_back(t);
-    up *= 1.25;
+    up *= ratio;
   }
   return b;
+}
+
+// Schedule parameters from the problem shape.  Kernel time per query token
+// ~ Kpad x Gp x 9 ps (measured on GB300: MLA 10.3, long context 10.5,
+// block-sparse 8.0 ps per slot and padded head); copy time per token = its
+// input bytes at 200 GB/s (pinned host memory measured at 211 GB/s).  The
+// ratio is 0.9 of that estimate, kept within [1.25, 8] (causal TND runs
+// slower per slot than the estimate, which only makes its ramp cautious).
+// The tail stops halving at the chunk whose dQ readback takes ~0.1 ms at
+// 190 GB/s, and at 128 tokens at least.  On MLA the ramp (x1.25) beat even
+// splits into 4, 8 or 16 chunks and ramps of x1.5 and x1.15; on the
+// block-sparse workload the shape-derived ramp (x8, tail 1000 tokens) took
+// 36.8 against 39.0 ms for x1.25.
+void host_schedule(const Plan& P, double* ratio, int* tmin) {
+  const double g = P.G, kernel_s = (double)P.Kpad * P.Gp * 9e-12;
+  const double copy_s = (g * (3 * 512 + (P.has_rope ? 64 : 0)) * 2 + (double)P.Kidx * 4 + 2 * g * 4) / 200e9;
+  double r = 0.9 * kernel_s / copy_s;
+  *ratio = r < 1.25 ? 1.25 : r > 8.0 ? 8.0 : r;
+  const double dq_bytes = g * (512 + (P.has_rope ? 64 : 0)) * 2;
+  const double tt = 1e-4 * 190e9 / dq_bytes;
+  *tmin = tt < 128.0 ? 128 : tt > 1e6 ? 1000000 : (int)tt;
 }
 
 // Streams and events of one sfa_grad_host call.  Destroying them with work
@@ -661,7 +708,7 @@ sfa_status sfa_grad_profile(const sfa_params* p, const void* q, const void* k, c
 sfa_status sfa_grad_host_workspace_size(const sfa_params* p, size_t* bytes) {
   if (!p || !bytes) return SFA_ERR_NULLPTR;
   Plan P;
-  sfa_status s = sfa::validate(p, false, &P, true);
+  sfa_status s = sfa::validate(p, false, &P);
   if (s != SFA_OK) return s;
   *bytes = sfa::host_layout(P).total;
   return SFA_OK;
@@ -674,7 +721,7 @@ sfa_status sfa_grad_host(const sfa_params* p, const void* q, const void* k, cons
                          size_t workspace_bytes, void* stream) {
   if (!p) return SFA_ERR_NULLPTR;
   Plan P;
-  sfa_status s = sfa::validate(p, false, &P, true);
+  sfa_status s = sfa::validate(p, false, &P);
   if (s != SFA_OK) return s;
   const sfa::HostLayout L = sfa::host_layout(P);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -682,7 +729,7 @@ sfa_status sfa_grad_host(const sfa_params* p, const void* q, const void* k, cons
   if (!dk || !dv || (rope && !dk_rope) || !workspace) return SFA_ERR_NULLPTR;
   if (workspace_bytes < L.total) return SFA_ERR_PARAM_INVALID;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const size_t e = 2, t1 = (size_t)P.T1, t2 = (size_t)P.T2, g = (size_t)P.G;
+  const size_t e = 2, t2 = (size_t)P.T2, g = (size_t)P.G;
   const cudaMemcpyKind H2D = cudaMemcpyHostToDevice, D2H = cudaMemcpyDeviceToHost;
   if (P.T1 == 0) {  // empty query: nothing selects any key
     if (P.T2 > 0) {
@@ -697,7 +744,10 @@ sfa_status sfa_grad_host(const sfa_params* p, const void* q, const void* k, cons
   if (rope && (!q_rope || !k_rope || !dq_rope)) return SFA_ERR_NULLPTR;
   if (P.layout == SFA_LAYOUT_TND && (!act_seq_q || !act_seq_kv)) return SFA_ERR_NULLPTR;
   const bool shared_kv = v == k;
-  const std::vector<int> bounds = sfa::host_bounds(P.T1, P.chunk);
+  double ratio;
+  int tmin;
+  sfa::host_schedule(P, &ratio, &tmin);
+  const std::vector<int> bounds = sfa::host_bounds(P.T1, P.chunk, ratio, tmin);
   const int nch = (int)bounds.size();
 
   sfa::HostRes R;
@@ -725,29 +775,37 @@ sfa_status sfa_grad_host(const sfa_params* p, const void* q, const void* k, cons
     SFA_CK(cudaMemcpyAsync(ws + L.akv, act_seq_kv, (size_t)P.B * 4, H2D, R.h2d));
   }
   SFA_CK(cudaEventRecord(ev_kv, R.h2d));
-  // per chunk, every query-side input row of its tokens
-  for (int c = 0; c < nch; ++c) {
-    const size_t t0 = c > 0 ? (size_t)bounds[c - 1] : 0, n = (size_t)bounds[c] - t0;
-    const size_t row = g * 512 * e, rrow = g * 64 * e, irow = (size_t)P.Kidx * 4, srow = g * 4;
-    SFA_CK(cudaMemcpyAsync(ws + L.q + t0 * row, static_cast<const uint8_t*>(q) + t0 * row, n * row, H2D, R.h2d));
-    if (rope)
-      SFA_CK(cudaMemcpyAsync(ws + L.qr + t0 * rrow, static_cast<const uint8_t*>(q_rope) + t0 * rrow, n * rrow, H2D,
-                             R.h2d));
-    SFA_CK(cudaMemcpyAsync(ws + L.idx + t0 * irow, reinterpret_cast<const uint8_t*>(indices) + t0 * irow, n * irow,
-                           H2D, R.h2d));
-    SFA_CK(cudaMemcpyAsync(ws + L.smax + t0 * srow, reinterpret_cast<const uint8_t*>(softmax_max) + t0 * srow,
-                           n * srow, H2D, R.h2d));
-    SFA_CK(cudaMemcpyAsync(ws + L.ssum + t0 * srow, reinterpret_cast<const uint8_t*>(softmax_sum) + t0 * srow,
-                           n * srow, H2D, R.h2d));
-    SFA_CK(cudaMemcpyAsync(ws + L.dO + t0 * row, static_cast<const uint8_t*>(d_out) + t0 * row, n * row, H2D, R.h2d));
-    SFA_CK(cudaMemcpyAsync(ws + L.out + t0 * row, static_cast<const uint8_t*>(out) + t0 * row, n * row, H2D, R.h2d));
-    SFA_CK(cudaEventRecord(in_ready[c], R.h2d));
-  }
+  // the first chunk's query-side rows; run_grad queues each next chunk's
+  // before the current chunk's kernels
+  sfa::HostCopies hc;
+  hc.h2d = R.h2d;
+  hc.bounds = bounds.data();
+  hc.in_ready = in_ready;
+  hc.dq_ = ws + L.q;
+  hc.dqr_ = ws + L.qr;
+  hc.didx = ws + L.idx;
+  hc.dmax = ws + L.smax;
+  hc.dsum_ = ws + L.ssum;
+  hc.ddo = ws + L.dO;
+  hc.dout = ws + L.out;
+  hc.hq = static_cast<const uint8_t*>(q);
+  hc.hqr = static_cast<const uint8_t*>(q_rope);
+  hc.hidx = reinterpret_cast<const uint8_t*>(indices);
+  hc.hmax = reinterpret_cast<const uint8_t*>(softmax_max);
+  hc.hsum = reinterpret_cast<const uint8_t*>(softmax_sum);
+  hc.hdo = static_cast<const uint8_t*>(d_out);
+  hc.hout = static_cast<const uint8_t*>(out);
+  hc.row = g * 512 * e;
+  hc.rrow = rope ? g * 64 * e : 0;
+  hc.irow = (size_t)P.Kidx * 4;
+  hc.srow = g * 4;
+  SFA_CK(hc.put(0));
 
   SFA_CK(cudaStreamWaitEvent(st, ev_kv, 0));
   sfa::Pipe pipe;
   pipe.bounds = bounds.data();
   pipe.nch = nch;
+  pipe.copies = &hc;
   pipe.d2h = R.d2h;
   pipe.in_ready = in_ready;
   pipe.out_ready = out_ready;

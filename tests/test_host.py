@@ -14,8 +14,9 @@ from workloads import make_inputs, small_workload
 
 pytestmark = pytest.mark.gpu
 
-# Chunk schedules: 200 tokens run as 64, 64, 64, 8; 600 as 128, 150, 150,
-# 128, 44 (growing, then halving, ragged last chunk); 16 tokens as one chunk.
+# Chunk schedules (first chunk 128 tokens, growing, ragged last chunk): 200
+# tokens run as 128, 72; 600 as 128, 160, 200, 112; 150 as 128, 22; 16 tokens
+# as one chunk.
 CASES = {
     "g16_chunks_ragged": small_workload(N1=16, S1=200, S2=512, K=128, seed=41),
     "g8_tnd_causal": small_workload(name="tnd_host", layout="TND", B=3, N1=8, K=96, mode=3, index_kind="causal",
@@ -96,3 +97,36 @@ def test_grad_host_empty_query():
     torch.cuda.synchronize()
     for x in outs[1:3] + outs[4:]:
         assert torch.all(x == 0)
+
+
+def test_full_size_host_sampled():
+    """The MLA workload through sfa_grad_host, as bench.py times it end to end
+    (pinned host buffers, ramped chunks): dQ on sampled tokens and dK / dV /
+    dKRope on sampled key rows against the oracle, and every output against
+    the device-buffer call within tolerance."""
+    import numpy as np
+    from parity_util import gpu_call_kwargs, to_cuda
+    from workloads import WORKLOADS
+    w = WORKLOADS["mla"]
+    inp = make_inputs(w)
+    dev = {k: to_cuda(v) for k, v in inp.items()}
+    kw = gpu_call_kwargs(w, dev)
+    out, smax, ssum = sfa.fwd(dev["q"], dev["k"], dev["v"], dev["indices"], w.scale_value, **kw)
+    g_dev = sfa.grad(dev["q"], dev["k"], dev["v"], dev["indices"], dev["d_out"], out, smax, ssum, w.scale_value, **kw)
+    torch.cuda.synchronize()
+    o_c, m_c, l_c = out.cpu(), smax.cpu(), ssum.cpu()
+    g = _host(inp, o_c, m_c, l_c, w, False)
+    T1, T2 = w.S1, w.S2
+    rng = np.random.default_rng(2)
+    toks = np.sort(rng.choice(T1, size=4, replace=False))
+    keys = np.sort(rng.choice(T2, size=6, replace=False))
+    ref = oracle.sfa_bwd(d_out=inp["d_out"], out=o_c, softmax_max=m_c, softmax_sum=l_c, token_rows=toks,
+                         key_rows=keys, **oracle_kwargs(w, inp))
+    dq, dk, dv, dqr, dkr = g
+    compare("host_full/dq", dq.reshape(T1, -1)[toks], ref["dq"].reshape(T1, -1)[toks], w.dtype)
+    compare("host_full/dq_rope", dqr.reshape(T1, -1)[toks], ref["dq_rope"].reshape(T1, -1)[toks], w.dtype)
+    compare("host_full/dk", dk.reshape(T2, -1)[keys], ref["dk"].reshape(T2, -1)[keys], w.dtype)
+    compare("host_full/dv", dv.reshape(T2, -1)[keys], ref["dv"].reshape(T2, -1)[keys], w.dtype)
+    compare("host_full/dk_rope", dkr.reshape(T2, -1)[keys], ref["dk_rope"].reshape(T2, -1)[keys], w.dtype)
+    for n, a, b in zip(OUT_NAMES, g, g_dev):
+        compare(f"host_vs_device/{n}", a, b.float().cpu().double().numpy(), w.dtype)
