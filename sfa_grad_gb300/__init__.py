@@ -134,6 +134,54 @@ def make_params(q: torch.Tensor, k: torch.Tensor, indices: torch.Tensor, scale: 
     return p
 
 
+def check_tensors(p: SfaParams, q, k, v, indices, *, d_out=None, out=None, softmax_max=None, softmax_sum=None,
+                  q_rope=None, k_rope=None, act_seq_q=None, act_seq_kv=None, outputs=None, backward=True):
+    """Checks every tensor's element count and dtype against the problem `p`
+    describes (from the shapes of q, k and indices), so that no buffer the
+    library reads or writes is shorter than it assumes, and that all tensors
+    share q's device.  Raises ValueError; called by grad, grad_host,
+    grad_noalloc and fwd before the library is."""
+    dt = q.dtype
+    T1, T2, G, K = int(p.T1), int(p.T2), int(p.N1), int(p.K)
+    rope = p.Dr == 64
+
+    def need(name, t, numel, dtype):
+        if t is None:
+            raise ValueError(f"{name} is required")
+        if t.dtype != dtype:
+            raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
+        if t.numel() != numel:
+            raise ValueError(f"{name}: {t.numel()} elements, expected {numel}")
+        if t.device != q.device:
+            raise ValueError(f"{name} is on {t.device}, q on {q.device}")
+
+    need("q", q, T1 * G * 512, dt)
+    need("k", k, T2 * 512, dt)
+    need("v", v, T2 * 512, dt)
+    need("indices", indices, T1 * K, torch.int32)
+    if rope:
+        need("q_rope", q_rope, T1 * G * 64, dt)
+        need("k_rope", k_rope, T2 * 64, dt)
+    elif k_rope is not None:
+        raise ValueError("k_rope given without q_rope")
+    if p.layout == 1:
+        need("act_seq_q", act_seq_q, int(p.B), torch.int32)
+        need("act_seq_kv", act_seq_kv, int(p.B), torch.int32)
+    if backward:
+        need("d_out", d_out, T1 * G * 512, dt)
+        need("out", out, T1 * G * 512, dt)
+        need("softmax_max", softmax_max, T1 * G, torch.float32)
+        need("softmax_sum", softmax_sum, T1 * G, torch.float32)
+    if outputs is not None:
+        dq, dk, dv, dqr, dkr = outputs
+        need("dq", dq, T1 * G * 512, dt)
+        need("dk", dk, T2 * 512, dt)
+        need("dv", dv, T2 * 512, dt)
+        if rope:
+            need("dq_rope", dqr, T1 * G * 64, dt)
+            need("dk_rope", dkr, T2 * 64, dt)
+
+
 def grad_workspace_size(p: SfaParams) -> int:
     n = ctypes.c_size_t(0)
     _check(lib().sfa_grad_workspace_size(ctypes.byref(p), ctypes.byref(n)), "sfa_grad_workspace_size")
@@ -186,9 +234,13 @@ def grad(q, k, v, indices, d_out, out, softmax_max, softmax_sum, scale, *, q_rop
     batch = act_seq_q.numel() if act_seq_q is not None else None
     p = make_params(q, k, indices, scale, layout=layout, sparse_block_size=sparse_block_size,
                     sparse_mode=sparse_mode, deterministic=deterministic, has_rope=has_rope, batch=batch)
+    check_tensors(p, q, k, v, indices, d_out=d_out, out=out, softmax_max=softmax_max, softmax_sum=softmax_sum,
+                  q_rope=q_rope, k_rope=k_rope, act_seq_q=act_seq_q, act_seq_kv=act_seq_kv)
     if outputs is None:
         outputs = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v),
                    torch.empty_like(q_rope) if has_rope else None, torch.empty_like(k_rope) if has_rope else None)
+    check_tensors(p, q, k, v, indices, outputs=outputs, backward=False, q_rope=q_rope, k_rope=k_rope,
+                  act_seq_q=act_seq_q, act_seq_kv=act_seq_kv)
     dq, dk, dv, dqr, dkr = outputs
     ws = _workspace(grad_workspace_size(p), q.device, workspace)
     args = (ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(indices), _ptr(d_out), _ptr(out), _ptr(softmax_max),
@@ -215,9 +267,13 @@ def grad_noalloc(q, k, v, indices, d_out, out, softmax_max, softmax_sum, scale, 
     batch = act_seq_q.numel() if act_seq_q is not None else None
     p = make_params(q, k, indices, scale, layout=layout, sparse_block_size=sparse_block_size,
                     sparse_mode=sparse_mode, deterministic=deterministic, has_rope=has_rope, batch=batch)
+    check_tensors(p, q, k, v, indices, d_out=d_out, out=out, softmax_max=softmax_max, softmax_sum=softmax_sum,
+                  q_rope=q_rope, k_rope=k_rope, act_seq_q=act_seq_q, act_seq_kv=act_seq_kv)
     if outputs is None:
         outputs = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v),
                    torch.empty_like(q_rope) if has_rope else None, torch.empty_like(k_rope) if has_rope else None)
+    check_tensors(p, q, k, v, indices, outputs=outputs, backward=False, q_rope=q_rope, k_rope=k_rope,
+                  act_seq_q=act_seq_q, act_seq_kv=act_seq_kv)
     dq, dk, dv, dqr, dkr = outputs
     rc = lib().sfa_grad_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(indices), _ptr(d_out), _ptr(out),
                                 _ptr(softmax_max), _ptr(softmax_sum), _ptr(act_seq_q), _ptr(act_seq_kv), _ptr(q_rope),
@@ -257,11 +313,15 @@ def grad_host(q, k, v, indices, d_out, out, softmax_max, softmax_sum, scale, *, 
     batch = act_seq_q.numel() if act_seq_q is not None else None
     p = make_params(q, k, indices, scale, layout=layout, sparse_block_size=sparse_block_size,
                     sparse_mode=sparse_mode, deterministic=deterministic, has_rope=has_rope, batch=batch)
+    check_tensors(p, q, k, v, indices, d_out=d_out, out=out, softmax_max=softmax_max, softmax_sum=softmax_sum,
+                  q_rope=q_rope, k_rope=k_rope, act_seq_q=act_seq_q, act_seq_kv=act_seq_kv)
     if outputs is None:
         def pinned(t):
             return torch.empty(t.shape, dtype=t.dtype).pin_memory()
         outputs = (pinned(q), pinned(k), pinned(v), pinned(q_rope) if has_rope else None,
                    pinned(k_rope) if has_rope else None)
+    check_tensors(p, q, k, v, indices, outputs=outputs, backward=False, q_rope=q_rope, k_rope=k_rope,
+                  act_seq_q=act_seq_q, act_seq_kv=act_seq_kv)
     dq, dk, dv, dqr, dkr = outputs
     dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
     ws = _workspace(grad_host_workspace_size(p), dev, workspace)
@@ -280,6 +340,8 @@ def fwd(q, k, v, indices, scale, *, q_rope=None, k_rope=None, sparse_block_size=
     batch = act_seq_q.numel() if act_seq_q is not None else None
     p = make_params(q, k, indices, scale, layout=layout, sparse_block_size=sparse_block_size,
                     sparse_mode=sparse_mode, has_rope=has_rope, batch=batch)
+    check_tensors(p, q, k, v, indices, q_rope=q_rope, k_rope=k_rope, act_seq_q=act_seq_q, act_seq_kv=act_seq_kv,
+                  backward=False)
     out = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
     if p.layout == 0:
         st_shape = (p.B, 1, p.S1, p.N1)
