@@ -34,7 +34,7 @@ def _rank(rank, world, port, times, out):
 @pytest.mark.timeout(120)
 def test_two_rank_max_and_aggregate():
     world, times = 2, [7.5, 9.0]
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()   # no fork of this (threaded) test process
     mp.spawn(_rank, args=(world, _free_port(), times, out), nprocs=world, join=True)
     for r in range(world):
         ms, value = out[r]
