@@ -1,0 +1,23 @@
+"""bench.py's recorded DRAM traffic (roofline.traffic) belongs to the source it
+was captured on: the figure is reported while kvq.cu and common.cuh hash to
+the recorded value, scaled by tokens, and is null as soon as they differ.
+No GPU."""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_kvq_traffic_matches_committed_source():
+    ent = bench.TRAFFIC["kvq"]
+    assert bench._source_hash(ent["sources"]) == ent["sha256"], "kvq changed since its ncu capture: recapture"
+    assert bench.kernel_traffic("kvq", 4096) == ent["bytes_per_token"] * 4096
+
+
+def test_traffic_null_when_source_differs(monkeypatch):
+    ent = dict(bench.TRAFFIC["kvq"], sha256="0" * 64)
+    monkeypatch.setitem(bench.TRAFFIC, "kvq", ent)
+    assert bench.kernel_traffic("kvq", 4096) is None
+    assert bench.kernel_traffic("sdp", 4096) is None
