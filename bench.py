@@ -221,7 +221,7 @@ def workload_desc(w, det, shared_kv=False):
 # token counts.  Reported only while the kernel source still hashes to the
 # value it had when the counters were taken.
 TRAFFIC = {
-    # profiles/kvq_mla_q512.md: 933.4 MB read + 82.0 MB written per 512-token launch
+    # ncu capture of the 512-token MLA profiling workload: 933.4 MB read + 82.0 MB written per launch
     "kvq": {"sources": ["kvq.cu", "common.cuh"],
              "sha256": "ea91b60ed15292525e113e2578845f5e569c1fadd1120ebc9bd571ebdd668dc3",
              "bytes_per_token": 1015.4e6 / 512},
@@ -244,6 +244,51 @@ def kernel_traffic(name, tokens):
     if _source_hash(ent["sources"]) != ent["sha256"]:
         return None
     return ent["bytes_per_token"] * tokens
+
+
+# Contraction work per valid (query, head, key) of each tensor-core kernel,
+# in flops: sdp recomputes S (576-deep) and dP (512-deep); kvq forms dV (512
+# features), [dK | dKRope] (576) and [dQ | dQRope] (576), only the last when
+# kvb has taken the key side; kvb forms dV and [dK | dKRope] per block.
+TENSOR_FLOPS = {"sdp": 2 * (576 + 512), "kvq": 2 * (512 + 576 + 576), "kvb": 2 * (512 + 576)}
+# Bytes a streaming kernel must move per valid (query, key) pair: det_reduce
+# reads each pair's 1088-float partial row once.
+STREAM_BYTES = {"det_reduce": 1088 * 4}
+# L2-resident fp32 vector reductions (red.global.add.v4.f32, four key rows x
+# 128 B per warp instruction) measured on this GPU by a microbenchmark: the
+# ceiling of the key-side scatter, which never reaches DRAM.
+L2_RED_CEILING_GBS = 6350.0
+
+
+def roofline(dname, names, qhk, pairs, k_ms, peaks, det):
+    """Roofline of the dominant kernel over all its launches of one step
+    (work of the launches over their summed time = per-launch work over the
+    mean launch time).  Tensor-core kernels: algorithmic flops against the
+    measured dense bf16 peak (burst: the step is milliseconds long and timed
+    alone).  Streaming kernels: algorithmic bytes against the HBM copy peak."""
+    t = k_ms * 1e-3
+    if dname in TENSOR_FLOPS:
+        per = TENSOR_FLOPS[dname]
+        if dname == "kvq" and "kvb" in names:
+            per = 2 * 576
+        achieved = qhk * per / t / 1e12
+        peak = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "flops_per_query_head_key": per}
+        if dname == "kvq" and "kvb" not in names and not det:
+            # the key side's scatter: 1088 fp32 reductions (4352 B) per pair
+            gbs = pairs * 4352 / t / 1e9
+            roof["l2_red"] = {"achieved_gbs": gbs, "ceiling_gbs": L2_RED_CEILING_GBS,
+                              "frac": gbs / L2_RED_CEILING_GBS,
+                              "ceiling_source": "red.global.add.v4.f32 microbenchmark on GB300 (152 SMs)"}
+        return roof
+    per_b = STREAM_BYTES.get(dname)
+    if per_b is None:
+        return {"bound": "hbm", "achieved": None, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": None,
+                "note": f"no algorithmic byte count for {dname}"}
+    achieved = pairs * per_b / t / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "bytes_per_pair": per_b}
 
 
 def kernel_names(p, det):
@@ -390,29 +435,17 @@ def run_sfa(args):
         n_by_name[nm] = n_by_name.get(nm, 0) + 1
     dname = max(by_name, key=by_name.get)
     k_ms, k_n = by_name[dname], n_by_name[dname]
-    G = w.N1
-    # contraction work per (query, head, key): sdp S and dP, kvb dK and dV,
-    # dq (and kvq when kvb took the key side) dQ
-    tensor_work = {"sdp": 576 + 512, "kvb": 576 + 512, "dq": 576}
-    if "kvb" in names:
-        tensor_work["kvq"] = 576
-    if dname in tensor_work:
-        fl = pairs * G * 2 * tensor_work[dname]
-        achieved = fl / (k_ms * 1e-3) / 1e12
-        peak = peaks["bf16_tflops"]
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak}
-    else:
-        # key-side contraction: algorithmic bytes = the fp32 reductions of the
-        # key rows, 1088 floats = 4352 B per valid (query, key) pair
-        by = pairs * 1088 * 4
-        achieved = by / (k_ms * 1e-3) / 1e9
-        peak = peaks["hbm_gbs"]
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak}
+    roof = roofline(dname, names, pairs * w.N1, pairs, k_ms, peaks, det)
     if args.traffic is not None:
         roof["traffic"] = args.traffic                        # given per launch
     else:
         tr = kernel_traffic(dname, p.T1)                      # all tokens of the step
         roof["traffic"] = None if tr is None else tr / k_n    # per launch
+    if roof["traffic"] is not None:
+        # the kernel's measured DRAM traffic over its mean launch time, against
+        # the HBM copy peak (a secondary bound: the contractions read mostly L2)
+        gbs = roof["traffic"] / (k_ms / k_n * 1e-3) / 1e9
+        roof["dram"] = {"achieved_gbs": gbs, "peak_gbs": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"]}
     roof["kernel"] = dname
     roof["launches_per_step"] = k_n
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
@@ -434,7 +467,7 @@ def run_sfa(args):
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": workload_desc(w, det, args.shared_kv), "l2": "flushed between steps (256 MB write, outside the events)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "valid_query_head_key": pairs * G},
+                   "valid_query_head_key": pairs * w.N1},
         "frac_of_dense_bf16_peak": value / world / peaks["bf16_tflops"],
         "peak_source": peak_src,
         "per_kernel_ms": {f"{j}:{names[j] if j < len(names) else j}": round(per_launch[j], 4) for j in range(launches)},

@@ -215,9 +215,12 @@ sfa_status sfa_read_device_error(void* workspace, void* stream, int32_t* code);
  * whose sfa_grad_workspace_size exceeds it are rejected with SFA_ERR_SHAPE
  * (detail in sfa_last_error_message).  The first call on a device looks up
  * the array's device address; make that first call before any stream
- * capture.  All calls share the array: calls whose GPU work overlaps (other
- * streams or threads) race and must be serialised by the caller.  Calls no
- * cudaMalloc/cudaFree or allocating routine.
+ * capture.  The looked-up address belongs to the device's context, so the
+ * library must not be used across cudaDeviceReset.  All calls share the
+ * array: calls whose GPU work overlaps (other streams or threads) race and
+ * must be serialised by the caller.  Calls no cudaMalloc/cudaFree or
+ * allocating routine.  Device-side problems (SFA_DEVERR_*) are recorded in the
+ * scratch; read them with sfa_noalloc_read_device_error.
  */
 #define SFA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 sfa_status sfa_grad_noalloc(const sfa_params* p, const void* q, const void* k, const void* v, const int32_t* indices,
@@ -225,6 +228,17 @@ sfa_status sfa_grad_noalloc(const sfa_params* p, const void* q, const void* k, c
                             const int32_t* act_seq_q, const int32_t* act_seq_kv, const void* q_rope,
                             const void* k_rope, void* dq, void* dk, void* dv, void* dq_rope, void* dk_rope,
                             void* stream);
+
+/*
+ * The device error word of sfa_grad_noalloc's static scratch on the current
+ * device: synchronises `stream`, copies the word (SFA_DEVERR_*) to *code and
+ * clears it, like sfa_read_device_error does for a caller's workspace.  Call
+ * it on the stream of the noalloc calls it should cover.  Returns
+ * SFA_ERR_NULLPTR for a null code and SFA_ERR_RUNTIME (with
+ * sfa_last_error_message) when the device or the scratch address cannot be
+ * determined or the copy fails.  (No counterpart on the pages.)
+ */
+sfa_status sfa_noalloc_read_device_error(void* stream, int32_t* code);
 
 /*
  * sfa_grad from host buffers, with the copies overlapped with the kernels.

@@ -28,7 +28,8 @@ DTYPES = {torch.bfloat16: 0, torch.float16: 1}
 
 EXPORTS = ("sfa_grad_workspace_size", "sfa_grad", "sfa_grad_profile", "sfa_grad_plan_info", "sfa_grad_plan_names",
            "sfa_fwd_workspace_size", "sfa_fwd", "sfa_decode_keys", "sfa_read_device_error", "sfa_status_string",
-           "sfa_last_error_message", "sfa_grad_noalloc", "sfa_grad_host_workspace_size", "sfa_grad_host")
+           "sfa_last_error_message", "sfa_grad_noalloc", "sfa_noalloc_read_device_error",
+           "sfa_grad_host_workspace_size", "sfa_grad_host")
 
 
 class SfaParams(ctypes.Structure):
@@ -78,13 +79,15 @@ def lib() -> ctypes.CDLL:
     L.sfa_fwd.argtypes = [P] + [vp] * 12 + [sz, vp]
     L.sfa_decode_keys.argtypes = [P, vp, vp, vp, vp, vp, sz, vp]
     L.sfa_read_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
+    L.sfa_noalloc_read_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
     L.sfa_last_error_message.argtypes = []
     L.sfa_last_error_message.restype = ctypes.c_char_p
     L.sfa_status_string.argtypes = [ctypes.c_int32]
     L.sfa_status_string.restype = ctypes.c_char_p
     for name in ("sfa_grad_workspace_size", "sfa_fwd_workspace_size", "sfa_grad", "sfa_grad_profile",
                  "sfa_grad_plan_info", "sfa_grad_plan_names", "sfa_fwd", "sfa_decode_keys", "sfa_read_device_error",
-                 "sfa_grad_noalloc", "sfa_grad_host_workspace_size", "sfa_grad_host"):
+                 "sfa_grad_noalloc", "sfa_noalloc_read_device_error", "sfa_grad_host_workspace_size",
+                 "sfa_grad_host"):
         getattr(L, name).restype = ctypes.c_int32
     _lib = L
     return L
@@ -215,10 +218,19 @@ def _stream(stream) -> int:
     return s.cuda_stream
 
 
+def _on(device):
+    """Makes `device` current for the library call: the C ABI launches on the
+    current device (and sfa_grad_noalloc uses that device's static scratch),
+    so a call on tensors of another device must switch to it first."""
+    return torch.cuda.device(device)
+
+
 def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]) -> torch.Tensor:
     if workspace is not None:
         if workspace.numel() * workspace.element_size() < nbytes:
             raise ValueError("workspace too small")
+        if workspace.device != torch.device(device):
+            raise ValueError(f"workspace is on {workspace.device}, the call runs on {device}")
         return workspace
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
 
@@ -242,15 +254,16 @@ def grad(q, k, v, indices, d_out, out, softmax_max, softmax_sum, scale, *, q_rop
     check_tensors(p, q, k, v, indices, outputs=outputs, backward=False, q_rope=q_rope, k_rope=k_rope,
                   act_seq_q=act_seq_q, act_seq_kv=act_seq_kv)
     dq, dk, dv, dqr, dkr = outputs
-    ws = _workspace(grad_workspace_size(p), q.device, workspace)
-    args = (ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(indices), _ptr(d_out), _ptr(out), _ptr(softmax_max),
-            _ptr(softmax_sum), _ptr(act_seq_q), _ptr(act_seq_kv), _ptr(q_rope), _ptr(k_rope), _ptr(dq), _ptr(dk),
-            _ptr(dv), _ptr(dqr), _ptr(dkr), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
-    if events:
-        handles = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
-        _check(lib().sfa_grad_profile(*args, handles, len(events)), "sfa_grad_profile")
-    else:
-        _check(lib().sfa_grad(*args), "sfa_grad")
+    with _on(q.device):
+        ws = _workspace(grad_workspace_size(p), q.device, workspace)
+        args = (ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(indices), _ptr(d_out), _ptr(out), _ptr(softmax_max),
+                _ptr(softmax_sum), _ptr(act_seq_q), _ptr(act_seq_kv), _ptr(q_rope), _ptr(k_rope), _ptr(dq), _ptr(dk),
+                _ptr(dv), _ptr(dqr), _ptr(dkr), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+        if events:
+            handles = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+            _check(lib().sfa_grad_profile(*args, handles, len(events)), "sfa_grad_profile")
+        else:
+            _check(lib().sfa_grad(*args), "sfa_grad")
     return dq, dk, dv, dqr, dkr
 
 
@@ -275,11 +288,25 @@ def grad_noalloc(q, k, v, indices, d_out, out, softmax_max, softmax_sum, scale, 
     check_tensors(p, q, k, v, indices, outputs=outputs, backward=False, q_rope=q_rope, k_rope=k_rope,
                   act_seq_q=act_seq_q, act_seq_kv=act_seq_kv)
     dq, dk, dv, dqr, dkr = outputs
-    rc = lib().sfa_grad_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(indices), _ptr(d_out), _ptr(out),
-                                _ptr(softmax_max), _ptr(softmax_sum), _ptr(act_seq_q), _ptr(act_seq_kv), _ptr(q_rope),
-                                _ptr(k_rope), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dqr), _ptr(dkr), _stream(stream))
+    with _on(q.device):
+        rc = lib().sfa_grad_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(indices), _ptr(d_out), _ptr(out),
+                                    _ptr(softmax_max), _ptr(softmax_sum), _ptr(act_seq_q), _ptr(act_seq_kv),
+                                    _ptr(q_rope), _ptr(k_rope), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dqr), _ptr(dkr),
+                                    _stream(stream))
     _check(rc, "sfa_grad_noalloc")
     return dq, dk, dv, dqr, dkr
+
+
+def noalloc_read_device_error(device=None, stream=None) -> int:
+    """sfa_noalloc_read_device_error: reads and clears the device error word
+    (SFA_DEVERR_*) of sfa_grad_noalloc's static scratch on `device` (default:
+    the current device), after synchronising `stream`."""
+    code = ctypes.c_int32(0)
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    with _on(dev):
+        _check(lib().sfa_noalloc_read_device_error(_stream(stream), ctypes.byref(code)),
+               "sfa_noalloc_read_device_error")
+    return code.value
 
 
 def grad_host_workspace_size(p: SfaParams) -> int:
@@ -324,11 +351,12 @@ def grad_host(q, k, v, indices, d_out, out, softmax_max, softmax_sum, scale, *, 
                   act_seq_q=act_seq_q, act_seq_kv=act_seq_kv)
     dq, dk, dv, dqr, dkr = outputs
     dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
-    ws = _workspace(grad_host_workspace_size(p), dev, workspace)
-    rc = lib().sfa_grad_host(ctypes.byref(p), _hptr(q), _hptr(k), _hptr(v), _hptr(indices), _hptr(d_out), _hptr(out),
-                             _hptr(softmax_max), _hptr(softmax_sum), _hptr(act_seq_q), _hptr(act_seq_kv),
-                             _hptr(q_rope), _hptr(k_rope), _hptr(dq), _hptr(dk), _hptr(dv), _hptr(dqr), _hptr(dkr),
-                             _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    with _on(dev):
+        ws = _workspace(grad_host_workspace_size(p), dev, workspace)
+        rc = lib().sfa_grad_host(ctypes.byref(p), _hptr(q), _hptr(k), _hptr(v), _hptr(indices), _hptr(d_out),
+                                 _hptr(out), _hptr(softmax_max), _hptr(softmax_sum), _hptr(act_seq_q),
+                                 _hptr(act_seq_kv), _hptr(q_rope), _hptr(k_rope), _hptr(dq), _hptr(dk), _hptr(dv),
+                                 _hptr(dqr), _hptr(dkr), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
     _check(rc, "sfa_grad_host")
     return dq, dk, dv, dqr, dkr
 
@@ -349,10 +377,11 @@ def fwd(q, k, v, indices, scale, *, q_rope=None, k_rope=None, sparse_block_size=
         st_shape = (1, p.T1, p.N1)
     smax = torch.empty(st_shape, dtype=torch.float32, device=q.device)
     ssum = torch.empty(st_shape, dtype=torch.float32, device=q.device)
-    ws = _workspace(fwd_workspace_size(p), q.device, workspace)
-    rc = lib().sfa_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(indices), _ptr(act_seq_q),
-                       _ptr(act_seq_kv), _ptr(q_rope), _ptr(k_rope), _ptr(out), _ptr(smax), _ptr(ssum), _ptr(ws),
-                       ws.numel() * ws.element_size(), _stream(stream))
+    with _on(q.device):
+        ws = _workspace(fwd_workspace_size(p), q.device, workspace)
+        rc = lib().sfa_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(indices), _ptr(act_seq_q),
+                           _ptr(act_seq_kv), _ptr(q_rope), _ptr(k_rope), _ptr(out), _ptr(smax), _ptr(ssum), _ptr(ws),
+                           ws.numel() * ws.element_size(), _stream(stream))
     _check(rc, "sfa_fwd")
     return out, smax, ssum
 
@@ -364,14 +393,17 @@ def decode_keys(q, k, indices, *, sparse_block_size=1, layout="BSND", sparse_mod
     p = make_params(q, k, indices, 1.0, layout=layout, sparse_block_size=sparse_block_size,
                     sparse_mode=sparse_mode, has_rope=has_rope, batch=batch)
     rows = torch.empty((p.T1, p.K * p.sparse_block_size), dtype=torch.int32, device=q.device)
-    ws = _workspace(grad_workspace_size(p), q.device, workspace)
-    rc = lib().sfa_decode_keys(ctypes.byref(p), _ptr(indices), _ptr(act_seq_q), _ptr(act_seq_kv), _ptr(rows),
-                               _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    with _on(q.device):
+        ws = _workspace(grad_workspace_size(p), q.device, workspace)
+        rc = lib().sfa_decode_keys(ctypes.byref(p), _ptr(indices), _ptr(act_seq_q), _ptr(act_seq_kv), _ptr(rows),
+                                   _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
     _check(rc, "sfa_decode_keys")
     return rows, ws
 
 
 def read_device_error(workspace: torch.Tensor, stream=None) -> int:
     code = ctypes.c_int32(0)
-    _check(lib().sfa_read_device_error(_ptr(workspace), _stream(stream), ctypes.byref(code)), "sfa_read_device_error")
+    with _on(workspace.device):
+        _check(lib().sfa_read_device_error(_ptr(workspace), _stream(stream), ctypes.byref(code)),
+               "sfa_read_device_error")
     return code.value

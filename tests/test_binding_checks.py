@@ -98,3 +98,63 @@ def test_grad_host_refuses_before_any_device_work():
     with pytest.raises(ValueError, match="d_out: dtype"):
         sfa.grad_host(inp["q"], inp["k"], inp["v"], inp["indices"], inp["d_out"].to(torch.float16), out, smax, ssum,
                       w.scale_value, q_rope=inp["q_rope"], k_rope=inp["k_rope"])
+
+
+class _Recorder:
+    """Stands in for the library and for torch's device switch: records the
+    device each call made current and the library calls made inside it."""
+
+    def __init__(self):
+        self.log = []
+        self.current = None
+
+    def on(self, device):
+        rec = self
+
+        class Ctx:
+            def __enter__(self):
+                rec.log.append(("enter", str(device)))
+                rec.current = str(device)
+
+            def __exit__(self, *a):
+                rec.log.append(("exit", str(device)))
+                rec.current = None
+        return Ctx()
+
+    def __getattr__(self, name):
+        if not name.startswith("sfa_"):
+            raise AttributeError(name)
+
+        def call(*a):
+            self.log.append((name, self.current))
+            return 0
+        return call
+
+
+def test_library_calls_run_with_the_tensors_device_current(monkeypatch):
+    """The C ABI launches on the current device (and sfa_grad_noalloc uses
+    that device's static scratch), so the binding makes the tensors' device
+    current around every library call."""
+    w = CASES["tiny"]
+    inp = make_inputs(w)
+    out, smax, ssum = oracle_saved(w, inp)
+    rec = _Recorder()
+    monkeypatch.setattr(sfa, "lib", lambda: rec)
+    monkeypatch.setattr(sfa, "_on", rec.on)
+    monkeypatch.setattr(sfa, "_ptr", lambda t: None if t is None else 16)
+    monkeypatch.setattr(sfa, "_stream", lambda s: 0)
+    monkeypatch.setattr(sfa, "grad_workspace_size", lambda p: 256)
+    monkeypatch.setattr(sfa, "fwd_workspace_size", lambda p: 256)
+    dev = str(inp["q"].device)
+    args = (inp["q"], inp["k"], inp["v"], inp["indices"], inp["d_out"], out, smax, ssum, w.scale_value)
+    kw = dict(q_rope=inp["q_rope"], k_rope=inp["k_rope"])
+    sfa.grad_noalloc(*args, **kw)
+    sfa.grad(*args, workspace=torch.empty(256, dtype=torch.uint8), **kw)
+    sfa.fwd(inp["q"], inp["k"], inp["v"], inp["indices"], w.scale_value, workspace=torch.empty(256, dtype=torch.uint8),
+            **kw)
+    calls = [e for e in rec.log if e[0].startswith("sfa_")]
+    assert [c[0] for c in calls] == ["sfa_grad_noalloc", "sfa_grad", "sfa_fwd"]
+    assert all(c[1] == dev for c in calls), rec.log
+    # a caller's workspace on another device than the tensors is refused
+    with pytest.raises(ValueError, match="workspace is on"):
+        sfa._workspace(256, torch.device("cuda", 0), torch.empty(256, dtype=torch.uint8))

@@ -357,6 +357,28 @@ def test_sampled_rows_match_full():
     np.testing.assert_allclose(pv[keys], fv[keys], rtol=1e-13, atol=1e-15)
 
 
+def test_sampled_forward_rows_match_full():
+    """The forward restricted to some query tokens (token_rows, used by the
+    full-size GPU checks) gives exactly the full forward's rows for those
+    tokens, and NaN elsewhere so that a wrong row set cannot pass unnoticed."""
+    rng = np.random.default_rng(43)
+    for layout in ("BSND", "TND"):
+        if layout == "BSND":
+            case, _ = _rand_case(rng, B=2, S1=5, S2=12, K=6)
+        else:
+            case, _ = _rand_case(rng, layout="TND", aq=[4, 6], akv=[12, 9], K=6)
+        out, smax, ssum = sfa_fwd(scale=0.5, **case)
+        toks = [0, 4, 7, 9]
+        po, pm, pl = sfa_fwd(scale=0.5, token_rows=toks, **case)
+        T1 = 10
+        fo, ffo = out.reshape(T1, -1), po.reshape(T1, -1)
+        np.testing.assert_array_equal(ffo[toks], fo[toks])
+        np.testing.assert_array_equal(pm.reshape(T1, -1)[toks], smax.reshape(T1, -1)[toks])
+        np.testing.assert_array_equal(pl.reshape(T1, -1)[toks], ssum.reshape(T1, -1)[toks])
+        rest = [t for t in range(T1) if t not in toks]
+        assert np.all(np.isnan(ffo[rest])) and np.all(np.isnan(pl.reshape(T1, -1)[rest]))
+
+
 def test_documentation_example_closed_form():
     with open(os.path.join(HERE, "golden", "sfag_doc_example.json")) as f:
         ex = json.load(f)

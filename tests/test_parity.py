@@ -41,6 +41,9 @@ SMALL = {
     "g32_short_kv_all": small_workload(N1=32, S1=5, S2=64, K=64, index_kind="all", seed=30),
     # blocks of 8 starting below 0 or running past the end, through the per-pair key side
     "g16_bs8_edges": small_workload(N1=16, S1=6, S2=200, K=10, block_size=8, index_kind="random_any", seed=31),
+    # ~1280 occurrences of each of four keys in one token chunk: the deterministic
+    # sort takes its path for row segments longer than one warp sorts in shared memory
+    "g4_pile_dups": small_workload(N1=4, S1=80, S2=512, K=128, index_kind="pile", seed=32),
 }
 
 
@@ -194,24 +197,76 @@ def _full_case(name, det):
     g = sfa.grad(dev["q"], dev["k"], dev["v"], dev["indices"], dev["d_out"], out, smax, ssum, w.scale_value,
                  deterministic=det, **kw)
     torch.cuda.synchronize()
-    return w, inp, (out, smax, ssum), g
+    return w, inp, dev, (out, smax, ssum), g
 
 
-@pytest.mark.parametrize("name", FULL)
-def test_full_size_sampled(name):
-    w, inp, (out, smax, ssum), g = _full_case(name, det=False)
-    rng = np.random.default_rng(0)
+def _segments(w, inp):
+    """Per query token: start row of its KV segment (global) and the segment length."""
+    if w.layout == "TND":
+        aq = inp["act_seq_q"].tolist()
+        akv = inp["act_seq_kv"].tolist()
+        starts = np.concatenate([[0], np.cumsum(akv)])[:-1]
+        kv0 = np.repeat(starts, aq)
+        kvlen = np.repeat(akv, aq)
+    else:
+        t = np.arange(w.B * w.S1)
+        kv0 = (t // w.S1) * w.S2
+        kvlen = np.full(t.shape, w.S2)
+    return kv0.astype(np.int64), kvlen.astype(np.int64)
+
+
+def _sample(w, inp, chunk, seed):
+    """Query tokens and global key rows to check at full size: the first and
+    last token, both sides of every token-chunk boundary (up to three
+    boundaries), and random tokens; key rows that sampled tokens select at
+    slots on both sides of the 128-slot tile and 512-slot tile-group
+    boundaries (global rows: the token's segment start plus the index), plus
+    random rows."""
+    rng = np.random.default_rng(seed)
     T1 = inp["q"].reshape(-1, w.N1, 512).shape[0]
     T2 = inp["k"].reshape(-1, 512).shape[0]
-    toks = np.sort(rng.choice(T1, size=6, replace=False))
-    # key rows: a few the sampled tokens select, plus random ones
-    idx = inp["indices"].reshape(T1, -1).numpy()
-    picks = [int(idx[toks[0], 0]), int(idx[toks[1], -1])]
-    if w.layout == "BSND":
-        b0 = toks[0] // w.S1
-        picks = [b0 * w.S2 + p for p in picks]
-    keys = np.unique(np.concatenate([picks, rng.choice(T2, size=6, replace=False)]))
-    keys = keys[(keys >= 0) & (keys < T2)]
+    toks = {0, T1 - 1}
+    bounds = list(range(chunk, T1, chunk))
+    for b in bounds[:2] + bounds[-1:]:
+        toks |= {b - 1, b}
+    toks |= set(int(x) for x in rng.choice(T1, size=3, replace=False))
+    toks = np.array(sorted(toks))
+    kv0, kvlen = _segments(w, inp)
+    idx = inp["indices"].reshape(T1, -1).numpy().astype(np.int64)
+    keff = w.K * w.block_size
+    keys = set()
+    for t in toks[:4]:
+        for slot in (0, 127, 128, 511, 512, keff - 1):
+            if slot >= keff:
+                continue
+            j = idx[t, slot // w.block_size] + slot % w.block_size
+            if 0 <= j < kvlen[t]:
+                keys.add(int(kv0[t] + j))
+    keys |= set(int(x) for x in rng.choice(T2, size=4, replace=False))
+    return toks, np.array(sorted(keys))
+
+
+@pytest.mark.parametrize("det", [False, True])
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(name, det):
+    """The launch configuration bench.py times, on the full workloads, against
+    the oracle on sampled tokens and key rows; in deterministic mode also
+    bitwise equal across two calls."""
+    w, inp, dev, (out, smax, ssum), g = _full_case(name, det)
+    p = sfa.make_params(dev["q"], dev["k"], dev["indices"], w.scale_value, layout=w.layout,
+                        sparse_block_size=w.block_size, sparse_mode=w.mode, deterministic=det,
+                        batch=w.B if w.layout == "TND" else None)
+    chunk, _ = sfa.plan_info(p)
+    T1 = inp["q"].reshape(-1, w.N1, 512).shape[0]
+    T2 = inp["k"].reshape(-1, 512).shape[0]
+    toks, keys = _sample(w, inp, chunk, seed=int(det))
+    if det:
+        g2 = sfa.grad(dev["q"], dev["k"], dev["v"], dev["indices"], dev["d_out"], out, smax, ssum, w.scale_value,
+                      deterministic=True, **gpu_call_kwargs(w, dev))
+        torch.cuda.synchronize()
+        for n, a, b in zip(OUT_NAMES, g, g2):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16)), f"{name}/{n} differs between two calls"
+        del g2
     o_c, m_c, l_c = out.cpu(), smax.cpu(), ssum.cpu()
     # the companion forward on the sampled tokens
     ro, rm, rl = oracle.sfa_fwd(**oracle_kwargs(w, inp), token_rows=toks)
@@ -227,6 +282,8 @@ def test_full_size_sampled(name):
     compare(f"{name}/dk_rope", dkr.reshape(T2, -1)[keys], ref["dk_rope"].reshape(T2, -1)[keys], w.dtype)
     for x in g:
         assert torch.isfinite(x.float()).all()
+    del g, dev, out, smax, ssum
+    torch.cuda.empty_cache()
 
 
 def test_full_size_shared_kv_sampled():
@@ -260,19 +317,11 @@ def test_full_size_shared_kv_sampled():
         compare(f"shared_vs_separate/{n}", a, b.float().cpu().double().numpy(), w.dtype)
 
 
-@pytest.mark.parametrize("name", ["mla"])
-def test_full_size_deterministic(name):
-    w, inp, saved, g1 = _full_case(name, det=True)
-    dev = {k: to_cuda(v) for k, v in inp.items()}
-    out, smax, ssum = saved
-    g2 = sfa.grad(dev["q"], dev["k"], dev["v"], dev["indices"], dev["d_out"], out, smax, ssum, w.scale_value,
-                  deterministic=True, **gpu_call_kwargs(w, dev))
-    torch.cuda.synchronize()
-    for a, b in zip(g1, g2):
-        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
-    # and it agrees with the atomic path within tolerance
+def test_full_size_deterministic_vs_atomic():
+    """MLA: the deterministic result agrees with the atomic one within tolerance."""
+    w, inp, dev, (out, smax, ssum), g1 = _full_case("mla", True)
     g3 = sfa.grad(dev["q"], dev["k"], dev["v"], dev["indices"], dev["d_out"], out, smax, ssum, w.scale_value,
                   deterministic=False, **gpu_call_kwargs(w, dev))
     torch.cuda.synchronize()
     for n, a, b in zip(OUT_NAMES, g1, g3):
-        compare(f"{name}/det_vs_atomic/{n}", a, b.float().cpu().double().numpy(), w.dtype)
+        compare(f"mla/det_vs_atomic/{n}", a, b.float().cpu().double().numpy(), w.dtype)

@@ -8,7 +8,9 @@ neither of them.
 Draw order (one ``torch.Generator`` on the CPU, seeded per workload):
 lengths (TND only) -> q -> qRope -> k -> kRope -> v -> dO -> indices.
 Values are N(0, std^2) drawn in fp32 and rounded to the dtype (round to
-nearest even).  Index lists are distinct positions, sorted ascending.
+nearest even).  Index lists are distinct positions, sorted ascending, except
+for the kinds that draw duplicates or out-of-range entries on purpose
+("pile", "random_any").
 """
 from __future__ import annotations
 
@@ -37,7 +39,7 @@ class Workload:
     seed: int = 101
     D: int = 512
     Dr: int = 64
-    index_kind: str = "uniform"   # uniform | causal | block | skewed | all | random_any
+    index_kind: str = "uniform"   # uniform | causal | block | skewed | all | pile | random_any
     kv_extra: int = 0             # TND: kvlen = qlen + kv_extra
     T1: int = 0                   # TND total query tokens
     deterministic: bool = False
@@ -122,6 +124,13 @@ def _indices_for_token(g, w: Workload, kvlen: int, qlen: int, i: int):
         half = K // 2
         a = torch.randperm(recent, generator=g)[:half] + (kvlen - recent)
         b = torch.randperm(kvlen - recent, generator=g)[: K - half]
+        r = torch.cat([a, b])
+    elif kind == "pile":
+        # half the slots piled onto keys 0-3 (many occurrences of one key in a
+        # token chunk), half distinct uniform positions
+        half = K // 2
+        a = torch.randint(0, 4, (half,), generator=g)
+        b = torch.randperm(kvlen, generator=g)[: K - half]
         r = torch.cat([a, b])
     elif kind == "random_any":
         # arbitrary (possibly duplicated / out-of-range / negative) entries
