@@ -69,7 +69,7 @@ typedef enum { SFA_LAYOUT_BSND = 0, SFA_LAYOUT_TND = 1 } sfa_layout;
 
 /* Device error word values (sfa_read_device_error). */
 #define SFA_DEVERR_NONE 0
-#define SFA_DEVERR_TIMEOUT 1  /* a kernel abandoned a pipeline wait (no hang) */
+#define SFA_DEVERR_TIMEOUT 1  /* a kernel abandoned a pipeline wait after the wall-clock limit (no hang) */
 #define SFA_DEVERR_SEQLENS 2  /* TND lengths negative or not summing to T1/T2: every key was masked */
 
 /*
@@ -89,6 +89,13 @@ typedef enum { SFA_LAYOUT_BSND = 0, SFA_LAYOUT_TND = 1 } sfa_layout;
  *   sparse_block_size  1, 8, 16, 32 or 64 keys per index
  *   sparse_mode        0 (no mask) or 3 (rightDownCausal)
  *   deterministic      0 or 1
+ *   wait_limit_us      0: every pipeline wait inside the kernels gives up
+ *                      after 2 s; > 0: after this many microseconds.  A wait
+ *                      that gives up makes its kernel wind down (no hang) and
+ *                      records SFA_DEVERR_TIMEOUT; the outputs are then
+ *                      incomplete.  A test hook for that path: ordinary
+ *                      callers leave it 0.  Negative values are
+ *                      SFA_ERR_PARAM_INVALID.
  */
 typedef struct sfa_params {
   int32_t layout;
@@ -99,14 +106,14 @@ typedef struct sfa_params {
   int64_t sparse_block_size;
   int64_t sparse_mode;
   int32_t deterministic;
-  int32_t reserved;
+  int32_t wait_limit_us;
 } sfa_params;
 
 /*
  * Phase 1 (aclnnSparseFlashAttentionGradGetWorkspaceSize): validates *p and
  * writes the device workspace size in bytes to *bytes.
- * Errors: SFA_ERR_NULLPTR (p or bytes null), SFA_ERR_PARAM_INVALID (dtype or
- * layout out of range), SFA_ERR_SHAPE (N2 != 1, D != 512, Dr not in {0,64},
+ * Errors: SFA_ERR_NULLPTR (p or bytes null), SFA_ERR_PARAM_INVALID (dtype,
+ * layout or deterministic out of range, negative wait_limit_us), SFA_ERR_SHAPE (N2 != 1, D != 512, Dr not in {0,64},
  * N1 not in 1..128, sparse_mode not in {0,3}, block size not in
  * {1,8,16,32,64}, K < 1, negative sizes, non-finite scale, sizes overflowing
  * 32-bit row counts).
@@ -159,10 +166,14 @@ sfa_status sfa_grad_plan_info(const sfa_params* p, int64_t* chunk_tokens, int64_
  * (combined key-side and query-side contractions), or "blk_count",
  * "blk_scan", "blk_scatter", "kvb", "kvq" (block-sparse indices whose blocks
  * many tokens select: pairs grouped by block start, key side accumulated per
- * block, then the query side alone), or with deterministic = 1 "det_count",
- * "det_scan", "det_scatter", "det_sort" (entries sorted by kv row, then token
- * and slot), "kvq" (the key side stored as per-pair partial rows, with the
- * query side), "det_reduce"; finally "cast".  Writes at most `capacity`
+ * block, then the query side alone; with deterministic = 1 the grouping is
+ * followed by "blk_sort", each group's pairs in ascending (token, index)
+ * order, and "kvb" is launched sparse_block_size times, once per block-start
+ * residue modulo the block size), or with deterministic = 1 and single-key or
+ * rarely shared indices "det_count", "det_scan", "det_scatter", "det_sort"
+ * (entries sorted by kv row, then token and slot), "kvq" (the key side stored
+ * as per-pair partial rows, with the query side), "det_reduce"; finally
+ * "cast".  Writes at most `capacity`
  * pointers to static strings into names[] (names may be null when capacity
  * is 0) and the total count into *count (may be null).  Host only; validates
  * *p like sfa_grad_workspace_size.

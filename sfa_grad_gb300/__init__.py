@@ -41,7 +41,7 @@ class SfaParams(ctypes.Structure):
         ("Dr", ctypes.c_int64), ("K", ctypes.c_int64),
         ("scale", ctypes.c_double),
         ("sparse_block_size", ctypes.c_int64), ("sparse_mode", ctypes.c_int64),
-        ("deterministic", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("deterministic", ctypes.c_int32), ("wait_limit_us", ctypes.c_int32),
     ]
 
 
@@ -114,7 +114,7 @@ def _ptr(t: Optional[torch.Tensor]):
 
 def make_params(q: torch.Tensor, k: torch.Tensor, indices: torch.Tensor, scale: float, *, layout: str = "BSND",
                 sparse_block_size: int = 1, sparse_mode: int = 0, deterministic: bool = False,
-                has_rope: bool = True, batch: Optional[int] = None) -> SfaParams:
+                has_rope: bool = True, batch: Optional[int] = None, wait_limit_us: int = 0) -> SfaParams:
     p = SfaParams()
     p.layout = LAYOUTS[layout.upper()]
     if q.dtype not in DTYPES:
@@ -134,6 +134,7 @@ def make_params(q: torch.Tensor, k: torch.Tensor, indices: torch.Tensor, scale: 
     p.sparse_block_size = int(sparse_block_size)
     p.sparse_mode = int(sparse_mode)
     p.deterministic = 1 if deterministic else 0
+    p.wait_limit_us = int(wait_limit_us)
     return p
 
 
@@ -237,15 +238,18 @@ def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]) -> torch.
 
 def grad(q, k, v, indices, d_out, out, softmax_max, softmax_sum, scale, *, q_rope=None, k_rope=None,
          sparse_block_size=1, layout="BSND", sparse_mode=0, deterministic=False, act_seq_q=None, act_seq_kv=None,
-         outputs=None, workspace=None, stream=None, events=None):
+         outputs=None, workspace=None, stream=None, events=None, wait_limit_us=0):
     """sfa_grad on torch CUDA tensors; returns (dq, dk, dv, dq_rope, dk_rope).
 
     events: optional list of torch.cuda.Event; when given, sfa_grad_profile
-    records events[0] before the first launch and events[i] after launch i."""
+    records events[0] before the first launch and events[i] after launch i.
+    wait_limit_us: the kernels' wait limit (0: the library's default); a test
+    hook for the timeout path."""
     has_rope = q_rope is not None
     batch = act_seq_q.numel() if act_seq_q is not None else None
     p = make_params(q, k, indices, scale, layout=layout, sparse_block_size=sparse_block_size,
-                    sparse_mode=sparse_mode, deterministic=deterministic, has_rope=has_rope, batch=batch)
+                    sparse_mode=sparse_mode, deterministic=deterministic, has_rope=has_rope, batch=batch,
+                    wait_limit_us=wait_limit_us)
     check_tensors(p, q, k, v, indices, d_out=d_out, out=out, softmax_max=softmax_max, softmax_sum=softmax_sum,
                   q_rope=q_rope, k_rope=k_rope, act_seq_q=act_seq_q, act_seq_kv=act_seq_kv)
     if outputs is None:
@@ -362,12 +366,12 @@ def grad_host(q, k, v, indices, d_out, out, softmax_max, softmax_sum, scale, *, 
 
 
 def fwd(q, k, v, indices, scale, *, q_rope=None, k_rope=None, sparse_block_size=1, layout="BSND", sparse_mode=0,
-        act_seq_q=None, act_seq_kv=None, workspace=None, stream=None):
+        act_seq_q=None, act_seq_kv=None, workspace=None, stream=None, wait_limit_us=0):
     """sfa_fwd on torch CUDA tensors; returns (out, softmax_max, softmax_sum)."""
     has_rope = q_rope is not None
     batch = act_seq_q.numel() if act_seq_q is not None else None
     p = make_params(q, k, indices, scale, layout=layout, sparse_block_size=sparse_block_size,
-                    sparse_mode=sparse_mode, has_rope=has_rope, batch=batch)
+                    sparse_mode=sparse_mode, has_rope=has_rope, batch=batch, wait_limit_us=wait_limit_us)
     check_tensors(p, q, k, v, indices, q_rope=q_rope, k_rope=k_rope, act_seq_q=act_seq_q, act_seq_kv=act_seq_kv,
                   backward=False)
     out = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)

@@ -20,7 +20,7 @@ namespace {
 
 constexpr size_t kAlign = 256;
 constexpr size_t kPdsCap = size_t(8) << 30;    // P + dS staging per token chunk
-constexpr size_t kPartCap = size_t(8) << 30;   // deterministic partial rows per chunk
+constexpr size_t kPartCap = size_t(8) << 30;   // deterministic partial rows (bf16) per chunk
 constexpr int kAccRow = 1088;
 
 size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -29,6 +29,7 @@ struct Plan {
   int layout, B, S1, S2, T1, T2, G, Gp, Kidx, bs, Keff, Kpad, mode, has_rope, det, is_f16;
   int kvb;   // key-major dK / dV for block-sparse indices (kvb.cu)
   float scale;
+  unsigned long long wait_ns;   // limit of every pipeline wait in the kernels
   int chunk;
   size_t off_err, off_batch, off_meta, off_dsum, off_acc, off_P, off_dS, off_rows, off_part, off_dscr, off_tstats;
   size_t off_bcnt, off_bcur, off_bgrp, off_bbeg, off_bng, off_bent;
@@ -47,6 +48,7 @@ sfa_status validate(const sfa_params* p, bool fwd, Plan* out) {
   if (p->K < 1 || p->K > (1 << 20)) return SFA_ERR_SHAPE;
   if (!std::isfinite(p->scale)) return SFA_ERR_SHAPE;
   if (p->deterministic != 0 && p->deterministic != 1) return SFA_ERR_PARAM_INVALID;
+  if (p->wait_limit_us < 0) return SFA_ERR_PARAM_INVALID;
   if (p->B < 1) return SFA_ERR_SHAPE;
   int64_t T1, T2;
   if (p->layout == SFA_LAYOUT_BSND) {
@@ -80,17 +82,20 @@ sfa_status validate(const sfa_params* p, bool fwd, Plan* out) {
   P.det = fwd ? 0 : p->deterministic;
   P.is_f16 = p->dtype == SFA_DTYPE_FP16;
   P.scale = (float)p->scale;
+  P.wait_ns = p->wait_limit_us > 0 ? (unsigned long long)p->wait_limit_us * 1000ull : kWaitNsDefault;
   // Block-sparse indices selected by many tokens: group the (token, index)
   // pairs by block start and accumulate each block's dK / dV in tensor memory
   // (one accumulator write per block instead of one reduction per pair).
   // Used when blocks hold >= 16 keys, at most 64 heads, and the average kv
-  // row is selected by >= 8 query tokens.
-  P.kvb = !fwd && !P.det && P.bs >= 16 && P.Gp == 64 && T2 > 0 && T1 * keff >= 8 * T2;
+  // row is selected by >= 8 query tokens.  Deterministic mode sorts each
+  // group's pairs and adds the groups in bs launches (one per start residue
+  // modulo bs, whose blocks share no key row).
+  P.kvb = !fwd && P.bs >= 16 && P.Gp == 64 && T2 > 0 && T1 * keff >= 8 * T2;
   // token chunking keeps the per-chunk staging bounded
   const size_t pds_per_tok = (size_t)P.Kpad * P.Gp * 2 * (fwd ? 1 : 2);
   size_t chunk = kPdsCap / pds_per_tok;
-  if (P.det) {
-    const size_t part_per_tok = (size_t)P.Kpad * kAccRow * 4;
+  if (P.det && !P.kvb) {
+    const size_t part_per_tok = (size_t)P.Kpad * kAccRow * 2;
     const size_t c2 = kPartCap / part_per_tok;
     if (c2 < chunk) chunk = c2;
   }
@@ -106,8 +111,9 @@ sfa_status validate(const sfa_params* p, bool fwd, Plan* out) {
   P.off_P = o; o += up(chunk * P.Kpad * P.Gp * 2);
   P.off_dS = o; o += fwd ? 0 : up(chunk * P.Kpad * P.Gp * 2);
   P.off_rows = o; o += up(chunk * P.Kpad * 4);
-  P.off_part = o; o += P.det ? up(chunk * P.Kpad * kAccRow * 4) : 0;
-  P.off_dscr = o; o += P.det ? up(2 * chunk * P.Kpad * 4) : 0;   // padded copies of long segments
+  const size_t ents = chunk * (P.kvb ? P.Kidx : P.Kpad);   // sorted entries per chunk
+  P.off_part = o; o += P.det && !P.kvb ? up(chunk * P.Kpad * kAccRow * 2) : 0;
+  P.off_dscr = o; o += P.det ? up(2 * ents * 4) : 0;   // padded copies of long segments
   P.off_tstats = o; o += fwd ? up(chunk * (P.Kpad / 128) * P.G * 2 * 4) : 0;
   // counting-sort bins: block starts + bs (key-major blocks) or kv rows
   // (deterministic reduction), and the sorted entries
@@ -118,7 +124,7 @@ sfa_status validate(const sfa_params* p, bool fwd, Plan* out) {
   P.off_bgrp = o; o += bins ? up(nb * 4) : 0;
   P.off_bbeg = o; o += bins ? up((nb + 1) * 4) : 0;
   P.off_bng = o; o += bins ? up(4) : 0;
-  P.off_bent = o; o += bins ? up(chunk * (P.det ? P.Kpad : P.Kidx) * 4) : 0;
+  P.off_bent = o; o += bins ? up(ents * 4) : 0;
   P.total = o;
   return SFA_OK;
 }
@@ -136,6 +142,7 @@ Prob make_prob(const Plan& P, uint8_t* ws) {
   pr.Kpad = P.Kpad;
   pr.has_rope = P.has_rope;
   pr.scale = P.scale;
+  pr.wait_ns = P.wait_ns;
   pr.meta = reinterpret_cast<const TokMeta*>(ws + P.off_meta);
   pr.rowtab = reinterpret_cast<int*>(ws + P.off_rows);
   return pr;
@@ -290,6 +297,7 @@ const char* const kChunkDet[] = {"rowtab", "sdp", "det_count", "det_scan", "det_
                                  "kvq", "det_reduce"};
 const char* const kChunkKvq[] = {"rowtab", "sdp", "kvq"};
 const char* const kChunkKvb[] = {"rowtab", "sdp", "blk_count", "blk_scan", "blk_scatter", "kvb", "kvq"};
+const char* const kChunkKvbDetHead[] = {"rowtab", "sdp", "blk_count", "blk_scan", "blk_scatter", "blk_sort"};
 
 int64_t plan_names(const Plan& P, const char** out, int64_t cap) {
   int64_t n = 0;
@@ -303,12 +311,17 @@ int64_t plan_names(const Plan& P, const char** out, int64_t cap) {
   put("dsum");
   const int64_t chunks = (P.T1 + P.chunk - 1) / P.chunk;
   for (int64_t c = 0; c < chunks; ++c) {
-    if (P.det)
+    if (P.kvb && P.det) {
+      for (const char* s : kChunkKvbDetHead) put(s);
+      for (int r = 0; r < P.bs; ++r) put("kvb");   // one launch per start residue
+      put("kvq");
+    } else if (P.det) {
       for (const char* s : kChunkDet) put(s);
-    else if (P.kvb)
+    } else if (P.kvb) {
       for (const char* s : kChunkKvb) put(s);
-    else
+    } else {
       for (const char* s : kChunkKvq) put(s);
+    }
   }
   put("cast");
   return n;
@@ -417,7 +430,7 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
     SFA_CK(mk.mark(st));
     SFA_CK(launch_sdp<T>(maps, pr, kModeBwd, Pst, dSst, nullptr, gerr, nsm, st));
     SFA_CK(mk.mark(st));
-    if (P.det) {
+    if (P.det && !P.kvb) {
       int* bcnt = reinterpret_cast<int*>(ws + P.off_bcnt);
       int* bcur = reinterpret_cast<int*>(ws + P.off_bcur);
       int* bgrp = reinterpret_cast<int*>(ws + P.off_bgrp);
@@ -425,7 +438,7 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
       int* bng = reinterpret_cast<int*>(ws + P.off_bng);
       int* bent = reinterpret_cast<int*>(ws + P.off_bent);
       int* dscr = reinterpret_cast<int*>(ws + P.off_dscr);
-      float* part = reinterpret_cast<float*>(ws + P.off_part);
+      uint16_t* part = reinterpret_cast<uint16_t*>(ws + P.off_part);
       SFA_CK(launch_det_count(pr, bcnt, st));
       SFA_CK(mk.mark(st));
       SFA_CK(launch_blk_scan(bcnt, P.T2, bcur, bgrp, bbeg, bng, st));
@@ -436,7 +449,8 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
       SFA_CK(mk.mark(st));
       // key side as partial rows (token-major items) with the query side
       // in the same launch, then the fixed-order sums
-      SFA_CK(launch_kvq<T>(maps, pr, part, dq, P.has_rope ? dqr : nullptr, P.Kpad / 128, true, gerr, nsm, st));
+      SFA_CK(launch_kvq<T>(maps, pr, reinterpret_cast<float*>(part), dq, P.has_rope ? dqr : nullptr, P.Kpad / 128,
+                           true, gerr, nsm, st));
       SFA_CK(mk.mark(st));
       SFA_CK(launch_det_reduce(pr, bgrp, bbeg, bng, bent, part, acc, st));
       SFA_CK(mk.mark(st));
@@ -453,8 +467,21 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
       SFA_CK(mk.mark(st));
       SFA_CK(launch_blk_scatter(pr, bcur, bent, st));
       SFA_CK(mk.mark(st));
-      SFA_CK(launch_kvb<T>(bmaps, pr, P.bs, bgrp, bbeg, bng, bent, acc, gerr, nsm, st));
-      SFA_CK(mk.mark(st));
+      if (P.det) {
+        // each group's pairs in ascending (token, index) order, so that the
+        // tensor-memory accumulation of a block has one fixed order; then the
+        // groups in bs launches by start residue, so that no two tiles added
+        // in one launch share a key row
+        SFA_CK(launch_det_sort(pr, bbeg, bng, bent, reinterpret_cast<int*>(ws + P.off_dscr), st));
+        SFA_CK(mk.mark(st));
+        for (int r = 0; r < P.bs; ++r) {
+          SFA_CK(launch_kvb<T>(bmaps, pr, P.bs, bgrp, bbeg, bng, bent, acc, r, gerr, nsm, st));
+          SFA_CK(mk.mark(st));
+        }
+      } else {
+        SFA_CK(launch_kvb<T>(bmaps, pr, P.bs, bgrp, bbeg, bng, bent, acc, -1, gerr, nsm, st));
+        SFA_CK(mk.mark(st));
+      }
       SFA_CK(launch_kvq<T>(maps, pr, acc, dq, P.has_rope ? dqr : nullptr, 0, false, gerr, nsm, st));   // query side only
       SFA_CK(mk.mark(st));
     } else {

@@ -1,5 +1,5 @@
 // Shared device helpers for the sm_103a kernels of the sparse flash-attention
-// backward: mbarrier waits with a spin limit, tcgen05 (TMEM allocation, MMA,
+// backward: mbarrier waits with a wall-clock limit, tcgen05 (TMEM allocation, MMA,
 // commit, TMEM loads), cp.async with zero fill, and the 128-byte-swizzled
 // shared-memory operand layouts the tensor-core descriptors describe.
 #pragma once
@@ -12,9 +12,13 @@
 namespace sfa {
 
 // ------------------------------------------------------------------ limits
-// Every mbarrier wait gives up after this many polls; the kernel then records
-// an error code and returns instead of hanging.
-constexpr uint32_t kSpinLimit = 1u << 25;
+// Every pipeline wait gives up after a wall-clock limit (Prob::wait_ns,
+// measured on %globaltimer); the kernel then records an error code and winds
+// down instead of hanging.
+constexpr unsigned long long kWaitNsDefault = 2000000000ull;   // 2 s
+// Wind-down waits (for copies and MMAs already issued) ignore the abort flag
+// and use this limit whatever the pipeline limit is.
+constexpr unsigned long long kSettleNs = 2000000000ull;
 
 // Kernels that allocate all 512 TMEM columns request at least this much
 // dynamic shared memory so that no two of their CTAs share an SM.
@@ -28,6 +32,13 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Nanoseconds of the GPU's global timer.
+__device__ __forceinline__ unsigned long long gtime_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -37,6 +48,10 @@ __device__ __forceinline__ void mbar_fence_init() {
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// n arrivals at once (n >= 1, at most the phase's pending count).
+__device__ __forceinline__ void mbar_arrive_n(uint64_t* bar, uint32_t n) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(n) : "memory");
 }
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -49,23 +64,10 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-
-// Bounded wait on phase `parity`.  `abort` is a shared flag any warp may raise;
-// `gerr` is the global error word.  Returns false when the wait was abandoned.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* gerr) {
-  const uint32_t a = smem_u32(bar);
-  for (uint32_t it = 0; it < kSpinLimit; ++it) {
-    if (mbar_test(a, parity)) return true;
-    if ((it & 255u) == 255u && *abort) return false;
-  }
-  *abort = 1;
-  atomicExch(gerr, kErrTimeout);
-  return false;
-}
-// The same bounded wait by non-suspending polls (test_wait), for the
-// single-thread MMA issuers: the tensor core keeps only a few MMAs queued, so
-// every cycle the issuer spends waiting can leave it idle, and a suspending
-// try_wait returns later than a poll.
+// Non-suspending poll (test_wait), for the single-thread MMA issuers: the
+// tensor core keeps only a few MMAs queued, so every cycle the issuer spends
+// waiting can leave it idle, and a suspending try_wait returns later than a
+// poll.
 __device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -77,16 +79,77 @@ __device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-__device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, volatile int* abort, int* gerr) {
+
+// What a pipeline wait needs besides the barrier: the CTA's abort flag (any
+// warp may raise it), the global error word and the wall-clock limit.
+struct Waiter {
+  volatile int* abort;
+  int* gerr;
+  unsigned long long limit_ns;
+};
+
+// Bounded wait on phase `parity`.  Returns false when the wait was abandoned:
+// another warp raised the abort flag, or the limit ran out (then this thread
+// raises the flag and records a timeout).  The flag and the clock are read
+// every 256 polls.
+template <bool POLL>
+__device__ __forceinline__ bool mbar_wait_t(uint64_t* bar, uint32_t parity, const Waiter& w) {
   const uint32_t a = smem_u32(bar);
-  for (uint32_t it = 0; it < kSpinLimit; ++it) {
-    if (mbar_poll(a, parity)) return true;
-    if ((it & 255u) == 255u && *abort) return false;
+  if (POLL ? mbar_poll(a, parity) : mbar_test(a, parity)) return true;
+  const unsigned long long t0 = gtime_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (POLL ? mbar_poll(a, parity) : mbar_test(a, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (*w.abort) return false;
+      if (gtime_ns() - t0 > w.limit_ns) break;
+    }
   }
-  *abort = 1;
-  atomicExch(gerr, kErrTimeout);
+  *w.abort = 1;
+  atomicExch(w.gerr, kErrTimeout);
   return false;
 }
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Waiter& w) {
+  return mbar_wait_t<false>(bar, parity, w);
+}
+__device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, const Waiter& w) {
+  return mbar_wait_t<true>(bar, parity, w);
+}
+
+// Wind-down wait for the completion of phase `parity` of `bar`, whatever the
+// abort flag says: used before a CTA exits so that no TMA copy or MMA it
+// issued is still writing its shared or tensor memory.  Gives up after
+// kSettleNs (recording a timeout) so that it cannot hang either.
+__device__ __forceinline__ void mbar_settle(uint64_t* bar, uint32_t parity, int* gerr) {
+  const uint32_t a = smem_u32(bar);
+  const unsigned long long t0 = gtime_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test(a, parity)) return;
+    if ((it & 255u) == 0 && gtime_ns() - t0 > kSettleNs) {
+      atomicExch(gerr, kErrTimeout);
+      return;
+    }
+  }
+}
+
+// Records, for a ring of up to 32 stage slots armed by one thread, the parity
+// of the last phase armed on each slot; settle() then waits for each of them.
+// A slot is only re-armed after its previous phase completed, so the last
+// armed phase is the only one that can still have copies in flight.
+struct ArmLog {
+  uint32_t armed = 0, parity = 0;
+  __device__ __forceinline__ void arm(int slot, uint32_t ph) {
+    armed |= 1u << slot;
+    parity = (parity & ~(1u << slot)) | ((ph & 1u) << slot);
+  }
+  __device__ __forceinline__ void settle(uint64_t* bars, int* gerr) const {
+    for (int s = 0; s < 32; ++s)
+      if (armed & (1u << s)) mbar_settle(&bars[s], (parity >> s) & 1u, gerr);
+  }
+};
+
+// The last MMAs issued by this thread, settled: commits them to `bar` (a
+// barrier of count 1 used for nothing else) and waits for its phase 0.
+__device__ __forceinline__ void mma_settle(uint64_t* bar, int* gerr);
 
 // ------------------------------------------------------------------ cp.async
 // 16-byte global -> shared copy; src_bytes = 0 fills the destination with zeros
@@ -251,6 +314,10 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
 }
+__device__ __forceinline__ void mma_settle(uint64_t* bar, int* gerr) {
+  mma_commit(bar);
+  mbar_settle(bar, 0, gerr);
+}
 
 // 32 lanes x 32 consecutive fp32 columns: thread i of the warp gets lane
 // (warp quadrant base + i), columns [col, col+32).
@@ -328,6 +395,7 @@ struct Prob {
   int has_rope;
   float scale;
   int tok0, ntok;  // token chunk processed by this launch
+  unsigned long long wait_ns;   // limit of every pipeline wait
 };
 
 // Expanded key position of slot s of token t (64-bit: index + block offset

@@ -1,7 +1,8 @@
 // Deterministic key-side reduction (deterministic = 1; aclnnSparseFlashAttentionGrad
 // doc, 约束说明 确定性计算).  The key-side kernel writes one partial row
-// [dK | dKRope | dV] per (token, slot) of the chunk instead of using atomics;
-// then, per chunk:
+// [dK | dKRope | dV] per (token, slot) of the chunk instead of using atomics,
+// each element rounded once to bf16 (half the bytes of fp32 through HBM;
+// the sums stay fp32); then, per chunk:
 //  1. a stable counting sort of the chunk's (kv row, token, slot) entries:
 //     count per kv row, scan into offsets and the list of rows that receive
 //     anything, scatter the entry ids (token * Kpad + slot), then sort each
@@ -80,10 +81,17 @@ __global__ void __launch_bounds__(256) det_segsort_kernel(const int* gbeg, const
   }
 }
 
-// One block (272 threads = float4 columns) per receiving row k: adds the
-// row's partial rows in sorted (token, slot) order, eight loads in flight.
+// Four bf16 of a partial row (8 bytes) as fp32.
+__device__ __forceinline__ float4 bf16x4(uint2 r) {
+  return make_float4(__uint_as_float(r.x << 16), __uint_as_float(r.x & 0xffff0000u), __uint_as_float(r.y << 16),
+                     __uint_as_float(r.y & 0xffff0000u));
+}
+
+// One block (272 threads, four columns each) per receiving row k: adds the
+// row's bf16 partial rows in sorted (token, slot) order in fp32, eight loads
+// in flight.
 __global__ void __launch_bounds__(kCols4) det_reduce_kernel(const int* groups, const int* gbeg, const int* ngroups_p,
-                                                            const int* ent, const float* partials, float* acc) {
+                                                            const int* ent, const uint16_t* partials, float* acc) {
   const int ngroups = *ngroups_p;
   const int tid = threadIdx.x;
   for (int k = blockIdx.x; k < ngroups; k += gridDim.x) {
@@ -92,18 +100,20 @@ __global__ void __launch_bounds__(kCols4) det_reduce_kernel(const int* groups, c
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
     int i = b;
     for (; i + 8 <= e; i += 8) {
-      float4 v[8];
+      uint2 v[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u)
-        v[u] = __ldg(reinterpret_cast<const float4*>(partials + (size_t)__ldg(ent + i + u) * kAccRow) + tid);
+        v[u] = __ldg(reinterpret_cast<const uint2*>(partials + (size_t)__ldg(ent + i + u) * kAccRow) + tid);
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        s.x += v[u].x; s.y += v[u].y; s.z += v[u].z; s.w += v[u].w;
+        const float4 f = bf16x4(v[u]);
+        s.x += f.x; s.y += f.y; s.z += f.z; s.w += f.w;
       }
     }
     for (; i < e; ++i) {
-      const float4 v = __ldg(reinterpret_cast<const float4*>(partials + (size_t)__ldg(ent + i) * kAccRow) + tid);
-      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+      const float4 f =
+          bf16x4(__ldg(reinterpret_cast<const uint2*>(partials + (size_t)__ldg(ent + i) * kAccRow) + tid));
+      s.x += f.x; s.y += f.y; s.z += f.z; s.w += f.w;
     }
     float4* g = reinterpret_cast<float4*>(acc + (size_t)row * kAccRow) + tid;
     float4 x = *g;
@@ -139,7 +149,7 @@ cudaError_t launch_det_sort(const Prob& p, const int* gbeg, const int* ngroups, 
 }
 
 cudaError_t launch_det_reduce(const Prob& p, const int* groups, const int* gbeg, const int* ngroups, const int* ent,
-                              const float* partials, float* acc, cudaStream_t st) {
+                              const uint16_t* partials, float* acc, cudaStream_t st) {
   if (p.ntok <= 0 || p.T2 <= 0) return cudaSuccess;
   const int grid = p.T2 < 16384 ? p.T2 : 16384;
   det_reduce_kernel<<<grid, kCols4, 0, st>>>(groups, gbeg, ngroups, ent, partials, acc);

@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
   using S = DqSmem<NCOL>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t full_bar[kStages], empty_bar[kStages], tfull_bar[2], tempty_bar[2];
+  __shared__ uint64_t full_bar[kStages], empty_bar[kStages], tfull_bar[2], tempty_bar[2], done_bar;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ __align__(16) int rows_s[kStages][kSlots];   // read and written as int2
@@ -66,6 +66,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
       mbar_init(&tfull_bar[i], 1);
       mbar_init(&tempty_bar[i], 128);
     }
+    mbar_init(&done_bar, 1);
     abort_flag = 0;
     mbar_fence_init();
   }
@@ -74,6 +75,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = tmem_base;
+  const Waiter wt{&abort_flag, gerr, p.wait_ns};
 
   if (warp == 0) {
     if (lane == 0) {
@@ -84,13 +86,13 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
       bool ok = true;
       for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++it) {
         const int set = it & 1;
-        ok = mbar_wait_poll(&tempty_bar[set], ((it >> 1) & 1) ^ 1, &abort_flag, gerr);
+        ok = mbar_wait_poll(&tempty_bar[set], ((it >> 1) & 1) ^ 1, wt);
         if (!ok) break;
         tc_fence_after();
         const uint32_t d = tbase + set * 256;
         for (int c = 0; c < nchunks; ++c, ++g) {
           const int slot = g % kStages;
-          ok = mbar_wait_poll(&full_bar[slot], (g / kStages) & 1, &abort_flag, gerr);
+          ok = mbar_wait_poll(&full_bar[slot], (g / kStages) & 1, wt);
           if (!ok) break;
           tc_fence_after();
           static_assert(kSlots == 64, "four K steps per stage");
@@ -101,6 +103,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
         if (!ok) break;
         mma_commit(&tfull_bar[set]);
       }
+      mma_settle(&done_bar, gerr);   // no MMA still writing tensor memory at exit
     }
     __syncwarp();
   } else if (warp <= kStages) {
@@ -121,19 +124,21 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
     int* rows = rows_s[me];
     int g = 0;
     bool ok = true;
+    ArmLog alog;
     for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
       const int tl = item / NPART, part = item % NPART;
       const int f0 = part * NCOL;
       for (int c = 0; c < nchunks; ++c, ++g) {
         if (g % kStages != me) continue;
         const int2 r2 = *reinterpret_cast<const int2*>(p.rowtab + (size_t)tl * p.Kpad + c * kSlots + 2 * lane);
-        if (lane == 0) ok = mbar_wait(&empty_bar[me], ((g / kStages) & 1) ^ 1, &abort_flag, gerr);
+        if (lane == 0) ok = mbar_wait(&empty_bar[me], ((g / kStages) & 1) ^ 1, wt);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         *reinterpret_cast<int2*>(rows + 2 * lane) = r2;
         __syncwarp();
         if (!ok) break;
         if (lane == 0) {
           mbar_expect_tx(&full_bar[me], kHP * kSlots * 128 + (BLK ? (NCOL / 64) * kSlots * 128 : 0));
+          alog.arm(me, (uint32_t)(g / kStages));
           for (int hp = 0; hp < kHP; ++hp)
             tma_2d(a + hp * (kSlots * 128), mA, hp * 64, tl * p.Kpad + c * kSlots, &full_bar[me]);
         }
@@ -183,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
         __syncwarp();
       }
     }
+    alog.settle(full_bar, gerr);   // no copy still landing in shared memory at exit
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- epilogue (thread = head)
     const int ew = warp - 4;
@@ -192,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
       const int set = it & 1;
       const int tl = item / NPART, part = item % NPART;
       const int t = p.tok0 + tl;
-      const bool ok = mbar_wait(&tfull_bar[set], (it >> 1) & 1, &abort_flag, gerr);
+      const bool ok = mbar_wait(&tfull_bar[set], (it >> 1) & 1, wt);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const uint32_t td = tbase + set * 256 + ((uint32_t)(ew * 32) << 16);

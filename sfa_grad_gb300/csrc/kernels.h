@@ -15,21 +15,25 @@ cudaError_t launch_sdp(const Maps& maps, const Prob& p, int mode, void* out_p, v
 
 // Key-major dK / dV for block-sparse indices (kvb.cu): group the chunk's
 // (token, index) pairs by block start (count, scan, scatter), then accumulate
-// every group's block in tensor memory and add it to acc once.
+// every group's block in tensor memory and add it to acc once.  res >= 0
+// (deterministic mode; entries sorted within each group): only the groups
+// whose start is res modulo bs, whose blocks share no key row.
 cudaError_t launch_blk_count(const Prob& p, int* cnt, cudaStream_t st);
 cudaError_t launch_blk_scan(const int* cnt, int nbins, int* cursor, int* groups, int* gbeg, int* ngroups,
                             cudaStream_t st);
 cudaError_t launch_blk_scatter(const Prob& p, int* cursor, int* entries, cudaStream_t st);
 template <typename T>
 cudaError_t launch_kvb(const BlkMaps& maps, const Prob& p, int bs, const int* groups, const int* gbeg,
-                       const int* ngroups, const int* entries, float* acc, int* gerr, int nsm, cudaStream_t st);
+                       const int* ngroups, const int* entries, float* acc, int res, int* gerr, int nsm,
+                       cudaStream_t st);
 
 // Key-side and query-side contractions in one launch, two pipelines per CTA
 // (kvq.cu): key-side reductions into acc, dQ / dQRope out.  tile_group: key
 // tiles per key-side work item (items run tile-group major; a group of all
 // tiles gives token-major order); 0 runs the query side only.  part:
-// deterministic mode; acc is then the chunk's partial-row buffer and every
-// valid (token, slot) row is stored there instead of reduced.
+// deterministic mode; acc is then the chunk's partial-row buffer (bf16
+// elements) and every valid (token, slot) row is stored there instead of
+// reduced.
 template <typename T>
 cudaError_t launch_kvq(const Maps& maps, const Prob& p, float* acc, void* dq, void* dqr, int tile_group, bool part,
                        int* gerr, int nsm, cudaStream_t st);
@@ -62,6 +66,6 @@ cudaError_t launch_det_scatter(const Prob& p, int* cursor, int* ent, cudaStream_
 cudaError_t launch_det_sort(const Prob& p, const int* gbeg, const int* ngroups, int* ent, int* scratch,
                             cudaStream_t st);
 cudaError_t launch_det_reduce(const Prob& p, const int* groups, const int* gbeg, const int* ngroups, const int* ent,
-                              const float* partials, float* acc, cudaStream_t st);
+                              const uint16_t* partials, float* acc, cudaStream_t st);
 
 }  // namespace sfa

@@ -150,15 +150,20 @@ __host__ __device__ constexpr int stage_bytes(int gk) { return 9 * gk * 128 + 64
 // issue path is one thread whose instruction latency is not hidden, and with
 // compile-time K steps and panel offsets a pair's 4-5 MMAs issue back to back
 // (runtime trip counts cost about four times the MMA time).
+// res >= 0 (deterministic mode): only the groups whose start is congruent to
+// res modulo bs.  Two such blocks never share a key row, so every key row
+// receives at most one tile per launch, and the launches for res = 0 .. bs-1
+// run in stream order: each row's sum has one fixed order.  res < 0: every
+// group.
 template <typename T, int GK>
 __global__ void __launch_bounds__(kThreads, 1) kvb_kernel(const __grid_constant__ BlkMaps maps, Prob p, int bs,
                                                           int nstages, int nprod, const int* groups, const int* gbeg,
                                                           const int* ngroups_p, const int* entries, float* acc,
-                                                          int* gerr) {
+                                                          int res, int* gerr) {
   using E = Elt<T>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages], tfull_bar, tempty_bar;
+  __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages], tfull_bar, tempty_bar, done_bar;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -176,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1) kvb_kernel(const __grid_constant_
     }
     mbar_init(&tfull_bar, 1);
     mbar_init(&tempty_bar, 128);
+    mbar_init(&done_bar, 1);
     abort_flag = 0;
     mbar_fence_init();
   }
@@ -184,9 +190,12 @@ __global__ void __launch_bounds__(kThreads, 1) kvb_kernel(const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = tmem_base;
+  const Waiter wt{&abort_flag, gerr, p.wait_ns};
 
   // chunks of an item: dK = 4 panels pairs of q (+ 1 rope panel), dV = 4 of dO
   auto nchunks_of = [&](int kind) { return kind == 0 ? (p.has_rope ? 5 : 4) : 4; };
+  // whether this launch takes group grp (bins are start + bs >= 1)
+  auto taken = [&](int grp) { return res < 0 || __ldg(groups + grp) % bs == res; };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -197,15 +206,16 @@ __global__ void __launch_bounds__(kThreads, 1) kvb_kernel(const __grid_constant_
       int s = 0, it = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++it) {
+      for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
         const int grp = item >> 1, kind = item & 1;
+        if (!taken(grp)) continue;
         const bool five = nchunks_of(kind) == 5;
         const int e0 = gbeg[grp], e1 = gbeg[grp + 1];
-        ok = mbar_wait_poll(&tempty_bar, (it & 1) ^ 1, &abort_flag, gerr);
+        ok = mbar_wait_poll(&tempty_bar, (it & 1) ^ 1, wt);
         if (!ok) break;
         tc_fence_after();
         for (int e = e0; e < e1 && ok; ++e) {
-          ok = mbar_wait_poll(&full_bar[s], ph, &abort_flag, gerr);
+          ok = mbar_wait_poll(&full_bar[s], ph, wt);
           if (!ok) break;
           tc_fence_after();
           const uint64_t sa = d0 + desc_off(s * sbytes), sb = b0 + desc_off(s * sbytes);
@@ -229,7 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1) kvb_kernel(const __grid_constant_
           }
         }
         if (ok) mma_commit(&tfull_bar);
+        ++it;
       }
+      mma_settle(&done_bar, gerr);   // no MMA still writing tensor memory at exit
     }
     __syncwarp();
   } else if (warp <= nprod) {
@@ -240,15 +252,17 @@ __global__ void __launch_bounds__(kThreads, 1) kvb_kernel(const __grid_constant_
       const int me = warp - 1;
       int g = 0;
       bool ok = true;
+      ArmLog alog;
       for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
         const int grp = item >> 1, kind = item & 1;
+        if (!taken(grp)) continue;
         const int nc = nchunks_of(kind);
         const int e0 = gbeg[grp], e1 = gbeg[grp + 1];
         const uint32_t abytes = (kind == 0 && p.has_rope ? 9 : 8) * panel;
         for (int e = e0; e < e1 && ok; ++e, ++g) {
           if (g % nprod != me) continue;
           const int s = g % nstages;
-          ok = mbar_wait(&empty_bar[s], ((g / nstages) & 1) ^ 1, &abort_flag, gerr);
+          ok = mbar_wait(&empty_bar[s], ((g / nstages) & 1) ^ 1, wt);
           if (!ok) break;
           const int pr = __ldg(entries + e);
           const int tl = pr / p.Kidx, ii = pr - tl * p.Kidx;
@@ -256,6 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) kvb_kernel(const __grid_constant_
           uint64_t* fb = &full_bar[s];
           const uint32_t base = smem_u32(smem + s * sbytes);
           mbar_expect_tx(fb, abytes + 64 * 128);
+          alog.arm(s, (uint32_t)(g / nstages));
           // all eight 64-feature panels of the token's head rows in one box,
           // plus the rope panel
           tma_3d(base, kind == 0 ? &maps.q : &maps.dO, 0, hrow, 0, fb);
@@ -263,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) kvb_kernel(const __grid_constant_
           tma_2d(base + 9 * panel, kind == 0 ? &maps.dS : &maps.P, 0, tl * p.Kpad + ii * bs, fb);
         }
       }
+      alog.settle(full_bar, gerr);   // no copy still landing in shared memory at exit
     }
     __syncwarp();
   } else if (warp >= 4) {
@@ -272,11 +288,12 @@ __global__ void __launch_bounds__(kThreads, 1) kvb_kernel(const __grid_constant_
     const int qd = warp & 3;
     const int f = qd * 32 + lane;
     int it = 0;
-    for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++it) {
+    for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
       const int grp = item >> 1, kind = item & 1;
+      if (!taken(grp)) continue;
       const int nc = nchunks_of(kind);
       const int g0 = groups[grp] - bs;   // first key row (may be below 0)
-      const bool ok = __all_sync(0xffffffffu, !abort_flag && mbar_wait(&tfull_bar, it & 1, &abort_flag, gerr));
+      const bool ok = __all_sync(0xffffffffu, !abort_flag && mbar_wait(&tfull_bar, it & 1, wt));
       if (ok) {
         tc_fence_after();
         for (int c = 0; c < nc; ++c) {
@@ -298,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1) kvb_kernel(const __grid_constant_
       }
       tc_fence_before();
       mbar_arrive(&tempty_bar);
+      ++it;
     }
   }
   tc_fence_before();
@@ -344,7 +362,8 @@ int kvb_stages(int gk) {
 
 template <typename T>
 cudaError_t launch_kvb(const BlkMaps& maps, const Prob& p, int bs, const int* groups, const int* gbeg,
-                       const int* ngroups, const int* entries, float* acc, int* gerr, int nsm, cudaStream_t st) {
+                       const int* ngroups, const int* entries, float* acc, int res, int* gerr, int nsm,
+                       cudaStream_t st) {
   if (p.ntok <= 0 || p.T2 <= 0) return cudaSuccess;
   const int gk = (p.G + 15) / 16 * 16;
   const int nst = kvb_stages(gk);
@@ -354,13 +373,13 @@ cudaError_t launch_kvb(const BlkMaps& maps, const Prob& p, int bs, const int* gr
   auto kern = gk == 16 ? kvb_kernel<T, 16> : gk == 32 ? kvb_kernel<T, 32> : gk == 48 ? kvb_kernel<T, 48> : kvb_kernel<T, 64>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<nsm, kThreads, smem, st>>>(maps, p, bs, nst, nprod, groups, gbeg, ngroups, entries, acc, gerr);
+  kern<<<nsm, kThreads, smem, st>>>(maps, p, bs, nst, nprod, groups, gbeg, ngroups, entries, acc, res, gerr);
   return cudaGetLastError();
 }
 
 template cudaError_t launch_kvb<__nv_bfloat16>(const BlkMaps&, const Prob&, int, const int*, const int*, const int*,
-                                               const int*, float*, int*, int, cudaStream_t);
+                                               const int*, float*, int, int*, int, cudaStream_t);
 template cudaError_t launch_kvb<__half>(const BlkMaps&, const Prob&, int, const int*, const int*, const int*,
-                                        const int*, float*, int*, int, cudaStream_t);
+                                        const int*, float*, int, int*, int, cudaStream_t);
 
 }  // namespace sfa

@@ -89,9 +89,10 @@ __device__ __forceinline__ void red_add_v4(float* dst, float4 x) {
 // branch in the row-gather loop alone costs the single-key path a quarter of
 // its query-side throughput.
 // PART (deterministic = 1): instead of reducing into the accumulator, the
-// drain stores every valid (token, slot) pair's 1088-float row at
-// acc + (token_local * Kpad + slot) * 1088 (the partial rows the fixed-order
-// reduction of det.cu sums); masked slots are not written.
+// drain stores every valid (token, slot) pair's 1088-element row, rounded to
+// bf16, as element (token_local * Kpad + slot) * 1088 of the bf16 array at
+// acc (the partial rows the fixed-order reduction of det.cu sums in fp32);
+// masked slots are not written.
 template <typename T, int GP, bool BLK, bool PART>
 __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant__ Maps maps, Prob p, float* acc,
                                                           T* dq, T* dqr, int tg, int* gerr) {
@@ -99,7 +100,7 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t kv_full[kKvStages], kv_empty[kKvStages], kv_tfull[2], kv_tempty[2], kv_bfull, kv_bempty;
-  __shared__ uint64_t q_full[kQStages], q_empty[kQStages], q_tfull, q_tempty;
+  __shared__ uint64_t q_full[kQStages], q_empty[kQStages], q_tfull, q_tempty, kv_done, q_done;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ __align__(16) int q_rows[kQStages][kQSlots];   // read and written as int2
@@ -135,6 +136,8 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
     }
     mbar_init(&q_tfull, 1);
     mbar_init(&q_tempty, 128);
+    mbar_init(&kv_done, 1);
+    mbar_init(&q_done, 1);
     abort_flag = 0;
     mbar_fence_init();
   }
@@ -143,6 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = tmem_base;
+  const Waiter wt{&abort_flag, gerr, p.wait_ns};
 
   if (warp == 0) {
     // ================================================================ key side: MMA issuer
@@ -157,16 +161,16 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
         int ncol, col0;
         kv_chunk(ki.ch, ncol, col0);
         const uint32_t idesc = idesc_f16(kKeys, ncol, E::is_f16, false, true);
-        ok = mbar_wait_poll(&kv_bfull, icount & 1, &abort_flag, gerr);
+        ok = mbar_wait_poll(&kv_bfull, icount & 1, wt);
         if (!ok) break;
         for (int kt = ki.kt0; kt < ki.kt1 && ok; ++kt, ++tcount) {
           const int set = tcount & 1;
-          ok = mbar_wait_poll(&kv_tempty[set], ((tcount >> 1) & 1) ^ 1, &abort_flag, gerr);
+          ok = mbar_wait_poll(&kv_tempty[set], ((tcount >> 1) & 1) ^ 1, wt);
           if (!ok) break;
           tc_fence_after();
           const uint32_t d = tbase + set * 128;
           for (int hp = 0; hp < GP / 64 && ok; ++hp) {
-            ok = mbar_wait_poll(&kv_full[stage], phase, &abort_flag, gerr);
+            ok = mbar_wait_poll(&kv_full[stage], phase, wt);
             if (!ok) break;
             tc_fence_after();
             mma_ss_k64<2, 128>(d, da0 + desc_off(stage * kKvAStage), db0 + (uint64_t)(hp * 512), idesc, hp > 0 ? 1u : 0u);
@@ -177,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
         }
         if (ok) mma_commit(&kv_bempty);
       }
+      mma_settle(&kv_done, gerr);   // no MMA still writing tensor memory at exit
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -188,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
       int stage = 0, icount = 0;
       uint32_t phase = 0;
       bool ok = true;
+      ArmLog alog_a, alog_b;
       const uint32_t b = smem_u32(smem + kKvB);
       for (int item = blockIdx.x; item < nkv && ok; item += gridDim.x, ++icount) {
         const KvItem ki = kv_item(item, p.ntok, ntiles, tg);
@@ -195,10 +201,11 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
         const int t = p.tok0 + tl;
         int ncol, col0;
         kv_chunk(ch, ncol, col0);
-        if (icount > 0) ok = mbar_wait(&kv_bempty, (icount - 1) & 1, &abort_flag, gerr);
+        if (icount > 0) ok = mbar_wait(&kv_bempty, (icount - 1) & 1, wt);
         if (!ok) break;
         const int npan = ncol / 64;
         mbar_expect_tx(&kv_bfull, npan * GP * 128);
+        alog_b.arm(0, (uint32_t)icount);
         for (int pb = 0; pb < npan; ++pb) {
           const CUtensorMap* mp;
           int x, y = t * p.G;
@@ -212,16 +219,20 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
         for (int kt = ki.kt0; kt < ki.kt1 && ok; ++kt) {
           const int y0 = tl * p.Kpad + kt * kKeys;
           for (int hp = 0; hp < GP / 64 && ok; ++hp) {
-            ok = mbar_wait(&kv_empty[stage], phase ^ 1, &abort_flag, gerr);
+            ok = mbar_wait(&kv_empty[stage], phase ^ 1, wt);
             if (!ok) break;
             const uint32_t a = smem_u32(smem + kKvA + stage * kKvAStage);
             mbar_expect_tx(&kv_full[stage], kKvAStage);
+            alog_a.arm(stage, phase);
             tma_2d(a, mA, hp * 64, y0, &kv_full[stage]);
             tma_2d(a + 64 * 128, mA, hp * 64, y0 + 64, &kv_full[stage]);
             if (++stage == kKvStages) { stage = 0; phase ^= 1; }
           }
         }
       }
+      // no copy still landing in shared memory at exit
+      alog_a.settle(kv_full, gerr);
+      alog_b.settle(&kv_bfull, gerr);
     }
     __syncwarp();
   } else if (warp >= 4 && warp < 12) {
@@ -264,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
         advance(nitem, nkt);
         advance(nitem, nkt);
         next_row = row_of(nitem, nkt);
-        ok = __all_sync(0xffffffffu, mbar_wait(&kv_tfull[set], (tcount >> 1) & 1, &abort_flag, gerr));
+        ok = __all_sync(0xffffffffu, mbar_wait(&kv_tfull[set], (tcount >> 1) & 1, wt));
         if (!ok) break;
         tc_fence_after();
         const uint32_t td = tbase + set * 128 + ((uint32_t)(qd * 32) << 16);
@@ -282,11 +293,17 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
             const float4 x = reinterpret_cast<const float4*>(stg + rl * 32)[c4 ^ (rl & 7)];
             const int grow = __shfl_sync(0xffffffffu, row, rl);
             if constexpr (PART) {
-              // streaming store: the rows are read back once, after this kernel
-              if (grow >= 0)
-                __stcs(reinterpret_cast<float4*>(acc + ((size_t)ki.tl * p.Kpad + kt * kKeys + qd * 32 + rl) * kAccRow +
-                                                 col0 + c + c4 * 4),
-                       x);
+              // streaming store of the pair's row rounded to bf16 (read back
+              // once, after this kernel, and summed in fp32)
+              if (grow >= 0) {
+                uint2 h;
+                h.x = Elt<__nv_bfloat16>::pack(x.x, x.y);
+                h.y = Elt<__nv_bfloat16>::pack(x.z, x.w);
+                __stcs(reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(acc) +
+                                                ((size_t)ki.tl * p.Kpad + kt * kKeys + qd * 32 + rl) * kAccRow + col0 +
+                                                c + c4 * 4),
+                       h);
+              }
             } else if (grow >= 0) {
               red_add_v4(acc + (size_t)grow * kAccRow + col0 + c + c4 * 4, x);
             }
@@ -308,12 +325,12 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
       int it = 0, g = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < nq && ok; item += gridDim.x, ++it) {
-        ok = mbar_wait_poll(&q_tempty, (it & 1) ^ 1, &abort_flag, gerr);
+        ok = mbar_wait_poll(&q_tempty, (it & 1) ^ 1, wt);
         if (!ok) break;
         tc_fence_after();
         for (int c = 0; c < qchunks; ++c, ++g) {
           const int slot = g % kQStages;
-          ok = mbar_wait_poll(&q_full[slot], (g / kQStages) & 1, &abort_flag, gerr);
+          ok = mbar_wait_poll(&q_full[slot], (g / kQStages) & 1, wt);
           if (!ok) break;
           tc_fence_after();
           static_assert(kQSlots == 64, "four K steps per stage");
@@ -323,6 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
         }
         if (ok) mma_commit(&q_tfull);
       }
+      mma_settle(&q_done, gerr);   // no MMA still writing tensor memory at exit
     }
     __syncwarp();
   } else if (warp == 16 || warp == 17) {
@@ -341,13 +359,14 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
     int* rows = q_rows[me];
     int g = 0;
     bool ok = true;
+    ArmLog alog;
     for (int item = blockIdx.x; item < nq && ok; item += gridDim.x) {
       const int tl = item / kQParts, part = item % kQParts;
       const int f0 = part * kQCol;
       for (int c = 0; c < qchunks; ++c, ++g) {
         if (g % kQStages != me) continue;
         const int2 r2 = *reinterpret_cast<const int2*>(p.rowtab + (size_t)tl * p.Kpad + c * kQSlots + 2 * lane);
-        if (lane == 0) ok = mbar_wait(&q_empty[me], ((g / kQStages) & 1) ^ 1, &abort_flag, gerr);
+        if (lane == 0) ok = mbar_wait(&q_empty[me], ((g / kQStages) & 1) ^ 1, wt);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         *reinterpret_cast<int2*>(rows + 2 * lane) = r2;
         __syncwarp();
@@ -355,6 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
         constexpr bool blk = BLK;
         if (lane == 0) {
           mbar_expect_tx(&q_full[me], kHP * kQSlots * 128 + (blk ? (kQCol / 64) * kQSlots * 128 : 0));
+          alog.arm(me, (uint32_t)(g / kQStages));
           for (int hp = 0; hp < kHP; ++hp)
             tma_2d(a + hp * (kQSlots * 128), &maps.dS, hp * 64, tl * p.Kpad + c * kQSlots, &q_full[me]);
         }
@@ -404,6 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
         __syncwarp();
       }
     }
+    alog.settle(q_full, gerr);   // no copy still landing in shared memory at exit
   } else if (warp >= 12 && warp < 16) {
     // ================================================================ query side: epilogue (thread = head)
     const int ew = warp - 12;
@@ -412,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
     for (int item = blockIdx.x; item < nq && !abort_flag; item += gridDim.x, ++it) {
       const int tl = item / kQParts, part = item % kQParts;
       const int t = p.tok0 + tl;
-      const bool ok = mbar_wait(&q_tfull, it & 1, &abort_flag, gerr);
+      const bool ok = mbar_wait(&q_tfull, it & 1, wt);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const uint32_t td = tbase + kQCol0 + ((uint32_t)(ew * 32) << 16);

@@ -80,8 +80,13 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
   // full_bar[s]: all operands of the stage in gathered slot s are in shared
   // memory (the gather warps' lanes + the head-row TMA transaction arrivals)
   __shared__ uint64_t full_bar[kMaxSlots], empty_bar[kMaxSlots], bempty_bar[kMaxSlots], tfull_bar[2], tempty_bar[2];
+  __shared__ uint64_t done_bar;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
+  // arrivals each producer made on full_bar (head-row TMA thread per slot;
+  // gather warps), for the wind-down that completes every phase one of them
+  // started
+  __shared__ int arr_tma[kMaxSlots], arr_gat[4];
   __shared__ float red_buf[4][GP][2];
   __shared__ float stats_s[2][3 * GP];
   __shared__ __align__(16) int rows_s[4][kKeys];        // one per gather warp; read and written as int4
@@ -113,6 +118,9 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
       mbar_init(&tfull_bar[i], 1);
       mbar_init(&tempty_bar[i], kEpiThreads);
     }
+    mbar_init(&done_bar, 1);
+    for (int i = 0; i < kMaxSlots; ++i) arr_tma[i] = 0;
+    for (int i = 0; i < 4; ++i) arr_gat[i] = 0;
     abort_flag = 0;
     mbar_fence_init();
   }
@@ -121,6 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = tmem_base;
+  const Waiter wt{&abort_flag, gerr, p.wait_ns};
 
   if (warp == 0) {
     // ---------------------------------------------------------------- MMA issuer
@@ -131,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
       bool ok = true;
       for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++it) {
         const int set = it & 1;
-        ok = mbar_wait_poll(&tempty_bar[set], ((it >> 1) & 1) ^ 1, &abort_flag, gerr);
+        ok = mbar_wait_poll(&tempty_bar[set], ((it >> 1) & 1) ^ 1, wt);
         if (!ok) break;
         tc_fence_after();
         const uint32_t tS = tbase + set * (2 * GP);
@@ -141,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
           // for the 512-wide part, where the same rows act as value rows)
           for (int c = 0; c < nS; ++c, ++g) {
             const int slot = g % S::kNA;
-            ok = mbar_wait_poll(&full_bar[slot], (g / S::kNA) & 1, &abort_flag, gerr);
+            ok = mbar_wait_poll(&full_bar[slot], (g / S::kNA) & 1, wt);
             if (!ok) break;
             tc_fence_after();
             const Chunk ck = chunk_of(c, nS);
@@ -165,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
         } else {
           for (int c = 0; c < nchunks; ++c, ++g) {
             const int slot = g % S::kNA, bslot = g % S::kNB;
-            ok = mbar_wait_poll(&full_bar[slot], (g / S::kNA) & 1, &abort_flag, gerr);
+            ok = mbar_wait_poll(&full_bar[slot], (g / S::kNA) & 1, wt);
             if (!ok) break;
             tc_fence_after();
             const Chunk ck = chunk_of(c, nS);
@@ -182,6 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
         if (!ok) break;
         mma_commit(&tfull_bar[set]);
       }
+      mma_settle(&done_bar, gerr);   // no MMA still writing tensor memory at exit
     }
     __syncwarp();
   } else if (warp == 13) {
@@ -200,28 +210,33 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
             // before this stage's transactions are posted on it; the head-row
             // slot waits alone do not imply that once a one-load rope stage
             // shifts the head-row sequence.
-            ok = mbar_wait(&empty_bar[g % S::kNA], ((g / S::kNA) & 1) ^ 1, &abort_flag, gerr);
+            ok = mbar_wait(&empty_bar[g % S::kNA], ((g / S::kNA) & 1) ^ 1, wt);
             if (!ok) break;
             for (int j = 0; j < nb && ok; ++j, ++gb) {
               const int bslot = gb % S::kNB;
-              ok = mbar_wait(&bempty_bar[bslot], ((gb / S::kNB) & 1) ^ 1, &abort_flag, gerr);
+              ok = mbar_wait(&bempty_bar[bslot], ((gb / S::kNB) & 1) ^ 1, wt);
               if (!ok) break;
               const uint32_t b = smem_u32(smem + S::kBOff + bslot * S::kB);
               mbar_expect_tx(fb, ck.npan * gk * 128);
+              ++arr_tma[g % S::kNA];
               const CUtensorMap* mq = j == 1 ? &maps.dOg : ck.kind == 0 ? &maps.qg : &maps.qrg;
               for (int pn = 0; pn < ck.npan; ++pn) tma_2d(b + pn * S::kPanelB, mq, ck.f0 + pn * 64, t * p.G, fb);
             }
-            if (ok && nb == 1) mbar_arrive(fb);   // the stage barrier counts two head-row arrivals
+            if (ok && nb == 1) {   // the stage barrier counts two head-row arrivals
+              mbar_arrive(fb);
+              ++arr_tma[g % S::kNA];
+            }
           }
         } else {
           for (int c = 0; c < nchunks && ok; ++c, ++g) {
             const int bslot = g % S::kNB;
-            ok = mbar_wait(&bempty_bar[bslot], ((g / S::kNB) & 1) ^ 1, &abort_flag, gerr);
+            ok = mbar_wait(&bempty_bar[bslot], ((g / S::kNB) & 1) ^ 1, wt);
             if (!ok) break;
             const Chunk ck = chunk_of(c, nS);
             const uint32_t b = smem_u32(smem + S::kBOff + bslot * S::kB);
             uint64_t* fb = &full_bar[g % S::kNA];
             mbar_expect_tx(fb, ck.npan * gk * 128);
+            ++arr_tma[g % S::kNA];
             const CUtensorMap* mq = ck.kind == 0 ? &maps.qg : ck.kind == 1 ? &maps.qrg : &maps.dOg;
             for (int pn = 0; pn < ck.npan; ++pn) tma_2d(b + pn * S::kPanelB, mq, ck.f0 + pn * 64, t * p.G, fb);
           }
@@ -285,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
           next4 = rows_of(item + gridDim.x);
           loaded_item = item;
         }
-        if (lane == 0) ok = mbar_wait(&empty_bar[slot], ((g / S::kNA) & 1) ^ 1, &abort_flag, gerr);
+        if (lane == 0) ok = mbar_wait(&empty_bar[slot], ((g / S::kNA) & 1) ^ 1, wt);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         __syncwarp();
         if (!ok) break;
@@ -299,6 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
             for (int pn = 0; pn < ck.npan; ++pn) tma_2d(dst + pn * S::kPanelA, mk, ck.f0 + pn * 64, cur_y, &full_bar[slot]);
           }
           if (lane != 0) mbar_arrive(&full_bar[slot]);
+          if (lane == 0) arr_gat[me] += 32;
           continue;
         }
         // gathered rows, contiguous in global memory: with two panels a lane
@@ -327,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
         cp_async_wait<0>();
         fence_async_smem();
         mbar_arrive(&full_bar[slot]);
+        if (lane == 0) arr_gat[me] += 32;
       }
     }
   } else if (warp >= 4 && warp < 12) {
@@ -393,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
       }
       fetch(item + gridDim.x, nrow, nmax, nsum, ndsum);
       asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-      const bool ok = __all_sync(0xffffffffu, !abort_flag && mbar_wait(&tfull_bar[set], tph, &abort_flag, gerr));
+      const bool ok = __all_sync(0xffffffffu, !abort_flag && mbar_wait(&tfull_bar[set], tph, wt));
       if (ok) tc_fence_after();
       const uint32_t tS = tbase + set * (2 * GP) + ((uint32_t)(q * 32) << 16);
       const uint32_t tP = tS + GP;
@@ -468,6 +485,34 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
       }
       tc_fence_before();
       mbar_arrive(&tempty_bar[set]);
+    }
+  }
+  // Wind-down.  A stage barrier collects arrivals from two producers (the
+  // gather warps and the head-row TMA thread); after an abandoned wait one of
+  // them may have started a phase the other never joined, with copies of the
+  // first still in flight.  Thread 0 completes every started phase with the
+  // missing arrivals and waits for each, so that no copy lands after the CTA
+  // exits.  The producers' roles are one phase apart at most per slot.
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S::kNA; ++s) {
+      constexpr int kTShare = SH ? 2 : 1;                // head-row arrivals per phase
+      int n[3], sh[3], nr = 0;
+      n[nr] = arr_tma[s], sh[nr++] = kTShare;
+      for (int w = 0; w < 4; ++w)
+        if ((SH ? (w >> 1) : w) == s) n[nr] = arr_gat[w], sh[nr++] = 32;
+      int klo = 1 << 30, khi = 0;
+      for (int r = 0; r < nr; ++r) {
+        klo = min(klo, n[r] / sh[r]);
+        khi = max(khi, (n[r] + sh[r] - 1) / sh[r]);
+      }
+      if (klo >= 1) mbar_settle(&full_bar[s], (uint32_t)(klo - 1) & 1u, gerr);
+      for (int k = klo; k < khi; ++k) {
+        int missing = 0;
+        for (int r = 0; r < nr; ++r) missing += sh[r] - min(max(n[r] - k * sh[r], 0), sh[r]);
+        if (missing > 0) mbar_arrive_n(&full_bar[s], (uint32_t)missing);
+        mbar_settle(&full_bar[s], (uint32_t)k & 1u, gerr);
+      }
     }
   }
   tc_fence_before();

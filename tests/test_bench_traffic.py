@@ -10,10 +10,16 @@ sys.path.insert(0, ROOT)
 import bench  # noqa: E402
 
 
-def test_kvq_traffic_matches_committed_source():
-    ent = bench.TRAFFIC["kvq"]
-    assert bench._source_hash(ent["sources"]) == ent["sha256"], "kvq changed since its ncu capture: recapture"
-    assert bench.kernel_traffic("kvq", 4096) == ent["bytes_per_token"] * 4096
+def test_recorded_traffic_matches_committed_source():
+    """A recorded figure carries the hash of the source it was captured on and
+    must match the committed source; an entry without a hash (the kernel
+    changed and was not recaptured yet) reports no traffic."""
+    for name, ent in bench.TRAFFIC.items():
+        if ent["sha256"] is None:
+            assert bench.kernel_traffic(name, 4096) is None
+            continue
+        assert bench._source_hash(ent["sources"]) == ent["sha256"], f"{name} changed since its ncu capture: recapture"
+        assert bench.kernel_traffic(name, 4096) == ent["bytes_per_token"] * 4096
 
 
 def test_traffic_null_when_source_differs(monkeypatch):

@@ -68,7 +68,7 @@ def test_null_pointers(sfa):
     assert sfa.lib().sfa_grad(ctypes.byref(p), *args, 0, None) == sfa.SFA_ERR_NULLPTR
 
 
-@pytest.mark.parametrize("field,value", [("dtype", 2), ("layout", 5), ("deterministic", 3)])
+@pytest.mark.parametrize("field,value", [("dtype", 2), ("layout", 5), ("deterministic", 3), ("wait_limit_us", -1)])
 def test_param_invalid(sfa, field, value):
     rc, _ = _ws(sfa, _p(sfa, **{field: value}))
     assert rc == sfa.SFA_ERR_PARAM_INVALID
@@ -134,6 +134,14 @@ def test_plan_names(sfa):
     det = sfa.plan_names(_p(sfa, deterministic=1))
     assert det == ["meta", "dsum", "rowtab", "sdp", "det_count", "det_scan", "det_scatter", "det_sort", "kvq",
                    "det_reduce", "cast"]
+    # deterministic block indices: the key-major path with sorted groups, one
+    # kvb launch per block-start residue
+    bdet = sfa.plan_names(_p(sfa, dtype=1, B=2, S1=8192, S2=32768, N1=16, K=64, sparse_block_size=64,
+                             deterministic=1))
+    cdet = ["rowtab", "sdp", "blk_count", "blk_scan", "blk_scatter", "blk_sort"] + ["kvb"] * 64 + ["kvq"]
+    assert bdet[2:2 + len(cdet)] == cdet and "det_reduce" not in bdet
+    assert sfa.plan_info(_p(sfa, dtype=1, B=2, S1=8192, S2=32768, N1=16, K=64, sparse_block_size=64,
+                            deterministic=1))[0] == ctok
     tnd = sfa.plan_names(_p(sfa, layout=1, B=4, T1=16384, T2=32768, N1=64, K=2048, sparse_mode=3))
     assert tnd[0] == "batch_prefix" and "kvq" in tnd
     assert sfa.plan_names(_p(sfa, S1=0)) == []

@@ -43,7 +43,7 @@ SMALL = {
     "g16_bs8_edges": small_workload(N1=16, S1=6, S2=200, K=10, block_size=8, index_kind="random_any", seed=31),
     # ~1280 occurrences of each of four keys in one token chunk: the deterministic
     # sort takes its path for row segments longer than one warp sorts in shared memory
-    "g4_pile_dups": small_workload(N1=4, S1=80, S2=512, K=128, index_kind="pile", seed=32),
+    "g4_pile_dups": small_workload(N1=4, S1=80, S2=512, K=128, index_kind="pile", std=0.25, seed=32),
 }
 
 
