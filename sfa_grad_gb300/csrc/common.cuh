@@ -14,7 +14,8 @@ namespace sfa {
 // ------------------------------------------------------------------ limits
 // Every pipeline wait gives up after a wall-clock limit (Prob::wait_ns,
 // measured on %globaltimer); the kernel then records an error code and winds
-// down instead of hanging.
+// down instead of hanging.  The limit's resolution is one poll (a try_wait
+// suspends for at most 10 us) plus the timer's update period.
 constexpr unsigned long long kWaitNsDefault = 2000000000ull;   // 2 s
 // Wind-down waits (for copies and MMAs already issued) ignore the abort flag
 // and use this limit whatever the pipeline limit is.
@@ -53,14 +54,16 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 __device__ __forceinline__ void mbar_arrive_n(uint64_t* bar, uint32_t n) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(n) : "memory");
 }
+// try_wait may suspend the thread until the phase completes; the hint caps
+// one suspension at 10 us so that the callers' wall-clock limits hold.
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n.reg .pred p;\n"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       "selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(10000u)
       : "memory");
   return ok != 0;
 }
@@ -90,8 +93,9 @@ struct Waiter {
 
 // Bounded wait on phase `parity`.  Returns false when the wait was abandoned:
 // another warp raised the abort flag, or the limit ran out (then this thread
-// raises the flag and records a timeout).  The flag and the clock are read
-// every 256 polls.
+// raises the flag and records a timeout).  A try_wait may suspend the thread
+// for a while inside one poll, so those waits read the flag and the clock
+// after every poll; the non-suspending polls of the MMA issuers every 32.
 template <bool POLL>
 __device__ __forceinline__ bool mbar_wait_t(uint64_t* bar, uint32_t parity, const Waiter& w) {
   const uint32_t a = smem_u32(bar);
@@ -99,7 +103,7 @@ __device__ __forceinline__ bool mbar_wait_t(uint64_t* bar, uint32_t parity, cons
   const unsigned long long t0 = gtime_ns();
   for (uint32_t it = 1;; ++it) {
     if (POLL ? mbar_poll(a, parity) : mbar_test(a, parity)) return true;
-    if ((it & 255u) == 0) {
+    if (!POLL || (it & 31u) == 0) {
       if (*w.abort) return false;
       if (gtime_ns() - t0 > w.limit_ns) break;
     }
@@ -122,9 +126,9 @@ __device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, c
 __device__ __forceinline__ void mbar_settle(uint64_t* bar, uint32_t parity, int* gerr) {
   const uint32_t a = smem_u32(bar);
   const unsigned long long t0 = gtime_ns();
-  for (uint32_t it = 1;; ++it) {
+  for (;;) {
     if (mbar_test(a, parity)) return;
-    if ((it & 255u) == 0 && gtime_ns() - t0 > kSettleNs) {
+    if (gtime_ns() - t0 > kSettleNs) {
       atomicExch(gerr, kErrTimeout);
       return;
     }

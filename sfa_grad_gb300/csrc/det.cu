@@ -21,7 +21,9 @@ namespace {
 
 constexpr int kAccRow = 1088;
 constexpr int kCols4 = kAccRow / 4;     // 272 float4 columns
-constexpr int kSortCap = 1024;          // segment length one warp sorts in shared memory
+constexpr int kSortCap = 4096;          // segment length one warp sorts in shared memory
+constexpr int kSortWarps = 8;
+constexpr int kSortSmem = kSortWarps * kSortCap * 4;   // 128 KB of dynamic shared memory
 
 __global__ void det_count_kernel(Prob p, int* cnt) {
   const long long n = (long long)p.ntok * p.Kpad;
@@ -64,7 +66,7 @@ __device__ __forceinline__ void warp_bitonic(int* a, int np, int lane) {
 // overlaps another segment's copy.
 __global__ void __launch_bounds__(256) det_segsort_kernel(const int* gbeg, const int* ngroups_p, int* ent,
                                                           int* scratch) {
-  __shared__ int buf[8][kSortCap];
+  extern __shared__ int sort_buf[];   // kSortWarps x kSortCap
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ngroups = *ngroups_p;
   for (int k = blockIdx.x * 8 + warp; k < ngroups; k += gridDim.x * 8) {
@@ -72,7 +74,7 @@ __global__ void __launch_bounds__(256) det_segsort_kernel(const int* gbeg, const
     if (n <= 1) continue;
     int np = 1;
     while (np < n) np <<= 1;
-    int* a = np <= kSortCap ? buf[warp] : scratch + 2 * (size_t)b;
+    int* a = np <= kSortCap ? sort_buf + warp * kSortCap : scratch + 2 * (size_t)b;
     for (int i = lane; i < np; i += 32) a[i] = i < n ? ent[b + i] : INT_MAX;
     __syncwarp();
     warp_bitonic(a, np, lane);
@@ -143,8 +145,10 @@ cudaError_t launch_det_scatter(const Prob& p, int* cursor, int* ent, cudaStream_
 cudaError_t launch_det_sort(const Prob& p, const int* gbeg, const int* ngroups, int* ent, int* scratch,
                             cudaStream_t st) {
   if (p.ntok <= 0 || p.T2 <= 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(det_segsort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSortSmem);
+  if (e != cudaSuccess) return e;
   const int grid = (p.T2 + 7) / 8 < 4096 ? (p.T2 + 7) / 8 : 4096;
-  det_segsort_kernel<<<grid, 256, 0, st>>>(gbeg, ngroups, ent, scratch);
+  det_segsort_kernel<<<grid, 256, kSortSmem, st>>>(gbeg, ngroups, ent, scratch);
   return cudaGetLastError();
 }
 

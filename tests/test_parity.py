@@ -41,9 +41,17 @@ SMALL = {
     "g32_short_kv_all": small_workload(N1=32, S1=5, S2=64, K=64, index_kind="all", seed=30),
     # blocks of 8 starting below 0 or running past the end, through the per-pair key side
     "g16_bs8_edges": small_workload(N1=16, S1=6, S2=200, K=10, block_size=8, index_kind="random_any", seed=31),
-    # ~1280 occurrences of each of four keys in one token chunk: the deterministic
+    # head counts that are not powers of two (the page's N1 list includes 3, 6,
+    # 12, 24 and 48): padded to 16-row boxes and 64 or 128 MMA columns
+    "g3_odd_heads": small_workload(N1=3, S1=5, S2=600, K=300, seed=33),
+    "g6_causal": small_workload(N1=6, S1=7, S2=400, K=200, mode=3, seed=34),
+    "g24_fp16": small_workload(N1=24, S1=4, S2=700, K=256, dtype="fp16", seed=35),
+    "g48_bs16": small_workload(N1=48, S1=24, S2=512, K=12, block_size=16, index_kind="block", seed=36),
+    "g12_tnd": small_workload(name="tnd_g12", layout="TND", B=2, N1=12, K=150, mode=3, index_kind="causal",
+                              kv_extra=100, T1=9, act_q=(4, 5), seed=37),
+    # ~5100 occurrences of each of two keys in one token chunk: the deterministic
     # sort takes its path for row segments longer than one warp sorts in shared memory
-    "g4_pile_dups": small_workload(N1=4, S1=80, S2=512, K=128, index_kind="pile", std=0.25, seed=32),
+    "g4_pile_dups": small_workload(N1=4, S1=160, S2=512, K=128, index_kind="pile", std=0.15, seed=32),
 }
 
 

@@ -86,14 +86,15 @@ def test_noalloc_device_error_word():
 
 
 def test_noalloc_refuses_oversize_problem():
-    w = WORKLOADS["tiny"]          # deterministic: its workspace exceeds the static scratch
+    # deterministic, 64 tokens x 2048 keys: the partial rows alone exceed the static scratch
+    w = small_workload(N1=16, S1=64, S2=4096, K=2048, seed=38, deterministic=True)
     inp = make_inputs(w)
     dev = {k: to_cuda(v) for k, v in inp.items()}
     p = sfa.make_params(dev["q"], dev["k"], dev["indices"], w.scale_value, deterministic=True)
     assert sfa.grad_workspace_size(p) > sfa.NOALLOC_SCRATCH_BYTES
+    st = torch.zeros(1, 1, 64, 16, device="cuda")
     with pytest.raises(sfa.SfaError) as e:
-        sfa.grad_noalloc(dev["q"], dev["k"], dev["v"], dev["indices"], dev["d_out"], dev["d_out"],
-                         torch.zeros(1, 1, 16, 4, device="cuda"), torch.ones(1, 1, 16, 4, device="cuda"),
+        sfa.grad_noalloc(dev["q"], dev["k"], dev["v"], dev["indices"], dev["d_out"], dev["d_out"], st, st + 1,
                          w.scale_value, deterministic=True, **gpu_call_kwargs(w, dev))
     assert e.value.code == sfa.SFA_ERR_SHAPE
     assert "static scratch" in str(e.value)

@@ -126,10 +126,10 @@ def _indices_for_token(g, w: Workload, kvlen: int, qlen: int, i: int):
         b = torch.randperm(kvlen - recent, generator=g)[: K - half]
         r = torch.cat([a, b])
     elif kind == "pile":
-        # half the slots piled onto keys 0-3 (many occurrences of one key in a
-        # token chunk), half distinct uniform positions
+        # half the slots piled onto keys 0 and 1 (thousands of occurrences of
+        # one key in a token chunk), half distinct uniform positions
         half = K // 2
-        a = torch.randint(0, 4, (half,), generator=g)
+        a = torch.randint(0, 2, (half,), generator=g)
         b = torch.randperm(kvlen, generator=g)[: K - half]
         r = torch.cat([a, b])
     elif kind == "random_any":
