@@ -167,13 +167,14 @@ sfa_status sfa_grad_plan_info(const sfa_params* p, int64_t* chunk_tokens, int64_
  * "blk_scan", "blk_scatter", "kvb", "kvq" (block-sparse indices whose blocks
  * many tokens select: pairs grouped by block start, key side accumulated per
  * block, then the query side alone; with deterministic = 1 the grouping is
- * followed by "blk_sort", each group's pairs in ascending (token, index)
- * order, and "kvb" is launched sparse_block_size times, once per block-start
+ * followed by "blk_sort" and "blk_sort_long", each group's pairs in
+ * ascending (token, index) order (groups of up to 1024 pairs, then longer
+ * ones), and "kvb" is launched sparse_block_size times, once per block-start
  * residue modulo the block size), or with deterministic = 1 and single-key or
- * rarely shared indices "det_count", "det_scan", "det_scatter", "det_sort"
- * (entries sorted by kv row, then token and slot), "kvq" (the key side stored
- * as per-pair partial rows, with the query side), "det_reduce"; finally
- * "cast".  Writes at most `capacity`
+ * rarely shared indices "det_count", "det_scan", "det_scatter", "det_sort",
+ * "det_sort_long" (entries sorted by kv row, then token and slot), "kvq" (the
+ * key side stored as per-pair partial rows, with the query side),
+ * "det_reduce"; finally "cast".  Writes at most `capacity`
  * pointers to static strings into names[] (names may be null when capacity
  * is 0) and the total count into *count (may be null).  Host only; validates
  * *p like sfa_grad_workspace_size.

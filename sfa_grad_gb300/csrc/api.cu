@@ -27,6 +27,7 @@ size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Plan {
   int layout, B, S1, S2, T1, T2, G, Gp, Kidx, bs, Keff, Kpad, mode, has_rope, det, is_f16;
+  int Gs;    // heads per staged P / dS row (G rounded up to 16)
   int kvb;   // key-major dK / dV for block-sparse indices (kvb.cu)
   float scale;
   unsigned long long wait_ns;   // limit of every pipeline wait in the kernels
@@ -73,6 +74,7 @@ sfa_status validate(const sfa_params* p, bool fwd, Plan* out) {
   P.T2 = (int)T2;
   P.G = (int)p->N1;
   P.Gp = P.G <= 64 ? 64 : 128;
+  P.Gs = (P.G + 15) / 16 * 16;
   P.Kidx = (int)p->K;
   P.bs = (int)bs;
   P.Keff = (int)keff;
@@ -92,7 +94,7 @@ sfa_status validate(const sfa_params* p, bool fwd, Plan* out) {
   // modulo bs, whose blocks share no key row).
   P.kvb = !fwd && P.bs >= 16 && P.Gp == 64 && T2 > 0 && T1 * keff >= 8 * T2;
   // token chunking keeps the per-chunk staging bounded
-  const size_t pds_per_tok = (size_t)P.Kpad * P.Gp * 2 * (fwd ? 1 : 2);
+  const size_t pds_per_tok = (size_t)P.Kpad * P.Gs * 2 * (fwd ? 1 : 2);
   size_t chunk = kPdsCap / pds_per_tok;
   if (P.det && !P.kvb) {
     const size_t part_per_tok = (size_t)P.Kpad * kAccRow * 2;
@@ -108,8 +110,8 @@ sfa_status validate(const sfa_params* p, bool fwd, Plan* out) {
   P.off_meta = o; o += up((size_t)P.T1 * sizeof(TokMeta));
   P.off_dsum = o; o += fwd ? 0 : up((size_t)P.T1 * P.G * 4);
   P.off_acc = o; o += fwd ? 0 : up((size_t)P.T2 * kAccRow * 4);
-  P.off_P = o; o += up(chunk * P.Kpad * P.Gp * 2);
-  P.off_dS = o; o += fwd ? 0 : up(chunk * P.Kpad * P.Gp * 2);
+  P.off_P = o; o += up(chunk * P.Kpad * P.Gs * 2);
+  P.off_dS = o; o += fwd ? 0 : up(chunk * P.Kpad * P.Gs * 2);
   P.off_rows = o; o += up(chunk * P.Kpad * 4);
   const size_t ents = chunk * (P.kvb ? P.Kidx : P.Kpad);   // sorted entries per chunk
   P.off_part = o; o += P.det && !P.kvb ? up(chunk * P.Kpad * kAccRow * 2) : 0;
@@ -136,6 +138,7 @@ Prob make_prob(const Plan& P, uint8_t* ws) {
   pr.T2 = P.T2;
   pr.G = P.G;
   pr.Gp = P.Gp;
+  pr.Gs = P.Gs;
   pr.Kidx = P.Kidx;
   pr.bs = P.bs;
   pr.Keff = P.Keff;
@@ -205,8 +208,8 @@ bool make_blk_maps(BlkMaps* M, const Plan& P, const void* q, const void* qr, con
   bool ok = encode_panels3d(&M->q, f, q, TG, gk);
   ok = ok && encode2d(&M->qr, f, qr ? qr : q, qr ? 64 : 512, TG, gk);
   ok = ok && encode_panels3d(&M->dO, f, dO, TG, gk);
-  ok = ok && encode2d(&M->P, f, Pst, P.Gp, R, 64);
-  ok = ok && encode2d(&M->dS, f, dSst, P.Gp, R, 64);
+  ok = ok && encode2d(&M->P, f, Pst, P.Gs, R, 64);
+  ok = ok && encode2d(&M->dS, f, dSst, P.Gs, R, 64);
   return ok;
 }
 
@@ -225,8 +228,8 @@ bool make_maps(Maps* M, const Plan& P, const void* q, const void* qr, const void
   ok = ok && encode2d(&M->k, f, k, 512, T2, kb);
   ok = ok && encode2d(&M->kr, f, kr ? kr : k, kr ? 64 : 512, T2, kb);
   ok = ok && encode2d(&M->v, f, v, 512, T2, kb);
-  ok = ok && encode2d(&M->P, f, Pst, P.Gp, R, 64);
-  ok = ok && encode2d(&M->dS, f, dSst ? dSst : Pst, P.Gp, R, 64);
+  ok = ok && encode2d(&M->P, f, Pst, P.Gs, R, 64);
+  ok = ok && encode2d(&M->dS, f, dSst ? dSst : Pst, P.Gs, R, 64);
   const uint32_t gk = (uint32_t)((P.G + 15) / 16 * 16);
   ok = ok && encode2d(&M->qg, f, q, 512, TG, gk);
   ok = ok && encode2d(&M->qrg, f, qr ? qr : q, qr ? 64 : 512, TG, gk);
@@ -294,10 +297,11 @@ int kvq_tile_group(const Plan& P) {
 
 // Kernel launches of one sfa_grad call, in order (sfa_grad_plan_names).
 const char* const kChunkDet[] = {"rowtab", "sdp", "det_count", "det_scan", "det_scatter", "det_sort",
-                                 "kvq", "det_reduce"};
+                                 "det_sort_long", "kvq", "det_reduce"};
 const char* const kChunkKvq[] = {"rowtab", "sdp", "kvq"};
 const char* const kChunkKvb[] = {"rowtab", "sdp", "blk_count", "blk_scan", "blk_scatter", "kvb", "kvq"};
-const char* const kChunkKvbDetHead[] = {"rowtab", "sdp", "blk_count", "blk_scan", "blk_scatter", "blk_sort"};
+const char* const kChunkKvbDetHead[] = {"rowtab", "sdp", "blk_count", "blk_scan", "blk_scatter", "blk_sort",
+                                        "blk_sort_long"};
 
 int64_t plan_names(const Plan& P, const char** out, int64_t cap) {
   int64_t n = 0;
@@ -445,7 +449,9 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
       SFA_CK(mk.mark(st));
       SFA_CK(launch_det_scatter(pr, bcur, bent, st));
       SFA_CK(mk.mark(st));
-      SFA_CK(launch_det_sort(pr, bbeg, bng, bent, dscr, st));
+      SFA_CK(launch_det_sort(pr, bbeg, bng, bent, dscr, false, st));
+      SFA_CK(mk.mark(st));
+      SFA_CK(launch_det_sort(pr, bbeg, bng, bent, dscr, true, st));
       SFA_CK(mk.mark(st));
       // key side as partial rows (token-major items) with the query side
       // in the same launch, then the fixed-order sums
@@ -472,7 +478,9 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
         // tensor-memory accumulation of a block has one fixed order; then the
         // groups in bs launches by start residue, so that no two tiles added
         // in one launch share a key row
-        SFA_CK(launch_det_sort(pr, bbeg, bng, bent, reinterpret_cast<int*>(ws + P.off_dscr), st));
+        SFA_CK(launch_det_sort(pr, bbeg, bng, bent, reinterpret_cast<int*>(ws + P.off_dscr), false, st));
+        SFA_CK(mk.mark(st));
+        SFA_CK(launch_det_sort(pr, bbeg, bng, bent, reinterpret_cast<int*>(ws + P.off_dscr), true, st));
         SFA_CK(mk.mark(st));
         for (int r = 0; r < P.bs; ++r) {
           SFA_CK(launch_kvb<T>(bmaps, pr, P.bs, bgrp, bbeg, bng, bent, acc, r, gerr, nsm, st));

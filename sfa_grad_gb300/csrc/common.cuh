@@ -180,8 +180,10 @@ struct Maps {
   CUtensorMap k;    // (T2, 512),   box 64 x bs (block-sparse indices, bs >= 8), else unused
   CUtensorMap kr;   // (T2, 64),    box 64 x bs
   CUtensorMap v;    // (T2, 512),   box 64 x bs
-  CUtensorMap P;    // (chunk*Kpad, GP) staged P^T,  box 64 x 64
-  CUtensorMap dS;   // (chunk*Kpad, GP) staged dS^T, box 64 x 64
+  // staged P^T / dS^T, (chunk*Kpad rows, Gs heads), box 64 heads x 64 rows:
+  // heads past Gs are outside the map and arrive as zeros
+  CUtensorMap P;
+  CUtensorMap dS;
   // q, qRope, dO with boxes of GK = G rounded up to 16 rows: the score
   // kernel loads only a token's own head rows (the padded rows up to GP stay
   // zero in its shared memory)
@@ -196,8 +198,8 @@ struct BlkMaps {
   CUtensorMap q;
   CUtensorMap qr;   // (T1*G, 64), box 64 x GK
   CUtensorMap dO;
-  CUtensorMap P;    // (chunk*Kpad, GP) staged P^T,  box 64 x 64
-  CUtensorMap dS;   // (chunk*Kpad, GP) staged dS^T, box 64 x 64
+  CUtensorMap P;    // staged P^T,  (chunk*Kpad, Gs), box 64 x 64 (as in Maps)
+  CUtensorMap dS;   // staged dS^T, (chunk*Kpad, Gs), box 64 x 64
 };
 
 // Arrive once on `bar` and add `bytes` to the transaction count the phase
@@ -396,6 +398,7 @@ struct Prob {
   const float* dsum;    // (T1, G)
   int* rowtab;          // (ntok, Kpad): kv row of every slot of the chunk, -1 if masked
   int T1, T2, G, Gp, Kidx, bs, Keff, Kpad;
+  int Gs;   // heads per staged P^T / dS^T row: G rounded up to 16
   int has_rope;
   float scale;
   int tok0, ntok;  // token chunk processed by this launch

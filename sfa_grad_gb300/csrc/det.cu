@@ -21,9 +21,14 @@ namespace {
 
 constexpr int kAccRow = 1088;
 constexpr int kCols4 = kAccRow / 4;     // 272 float4 columns
-constexpr int kSortCap = 4096;          // segment length one warp sorts in shared memory
+// Segment sort: segments of up to kShortCap entries are sorted by a launch
+// with many warps per SM (static shared memory); longer ones by a second
+// launch with kLongCap entries of dynamic shared memory per warp, and the
+// rare segments longer than that in global scratch.
 constexpr int kSortWarps = 8;
-constexpr int kSortSmem = kSortWarps * kSortCap * 4;   // 128 KB of dynamic shared memory
+constexpr int kShortCap = 1024;
+constexpr int kLongCap = 4096;
+constexpr int kLongSmem = kSortWarps * kLongCap * 4;   // 128 KB
 
 __global__ void det_count_kernel(Prob p, int* cnt) {
   const long long n = (long long)p.ntok * p.Kpad;
@@ -60,21 +65,26 @@ __device__ __forceinline__ void warp_bitonic(int* a, int np, int lane) {
   }
 }
 
-// One warp per receiving row sorts the row's entry ids ascending: segments of
-// up to kSortCap entries in shared memory, longer ones (many occurrences of
-// one key in the chunk) in a padded copy at scratch + 2 * begin, which never
-// overlaps another segment's copy.
+// One warp per receiving row sorts the row's entry ids ascending.  LONG = 0:
+// the segments of 2 .. kShortCap entries, in static shared memory; LONG = 1:
+// the longer ones (many occurrences of one key in the chunk), in dynamic
+// shared memory up to kLongCap entries, beyond that in a padded copy at
+// scratch + 2 * begin, which never overlaps another segment's copy.
+template <bool LONG>
 __global__ void __launch_bounds__(256) det_segsort_kernel(const int* gbeg, const int* ngroups_p, int* ent,
                                                           int* scratch) {
-  extern __shared__ int sort_buf[];   // kSortWarps x kSortCap
+  extern __shared__ int long_buf[];                  // LONG: kSortWarps x kLongCap
+  __shared__ int short_buf[LONG ? 1 : kSortWarps][kShortCap];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ngroups = *ngroups_p;
-  for (int k = blockIdx.x * 8 + warp; k < ngroups; k += gridDim.x * 8) {
+  for (int k = blockIdx.x * kSortWarps + warp; k < ngroups; k += gridDim.x * kSortWarps) {
     const int b = gbeg[k], n = gbeg[k + 1] - b;
-    if (n <= 1) continue;
+    if (n <= 1 || (n > kShortCap) != LONG) continue;
     int np = 1;
     while (np < n) np <<= 1;
-    int* a = np <= kSortCap ? sort_buf + warp * kSortCap : scratch + 2 * (size_t)b;
+    int* a;
+    if constexpr (LONG) a = np <= kLongCap ? long_buf + warp * kLongCap : scratch + 2 * (size_t)b;
+    else a = short_buf[warp];
     for (int i = lane; i < np; i += 32) a[i] = i < n ? ent[b + i] : INT_MAX;
     __syncwarp();
     warp_bitonic(a, np, lane);
@@ -142,13 +152,17 @@ cudaError_t launch_det_scatter(const Prob& p, int* cursor, int* ent, cudaStream_
   return cudaGetLastError();
 }
 
-cudaError_t launch_det_sort(const Prob& p, const int* gbeg, const int* ngroups, int* ent, int* scratch,
+cudaError_t launch_det_sort(const Prob& p, const int* gbeg, const int* ngroups, int* ent, int* scratch, bool long_segs,
                             cudaStream_t st) {
   if (p.ntok <= 0 || p.T2 <= 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(det_segsort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSortSmem);
+  if (!long_segs) {
+    const int grid = (p.T2 + 7) / 8 < 4096 ? (p.T2 + 7) / 8 : 4096;
+    det_segsort_kernel<false><<<grid, 256, 0, st>>>(gbeg, ngroups, ent, scratch);
+    return cudaGetLastError();
+  }
+  cudaError_t e = cudaFuncSetAttribute(det_segsort_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLongSmem);
   if (e != cudaSuccess) return e;
-  const int grid = (p.T2 + 7) / 8 < 4096 ? (p.T2 + 7) / 8 : 4096;
-  det_segsort_kernel<<<grid, 256, kSortSmem, st>>>(gbeg, ngroups, ent, scratch);
+  det_segsort_kernel<true><<<152, 256, kLongSmem, st>>>(gbeg, ngroups, ent, scratch);
   return cudaGetLastError();
 }
 

@@ -63,7 +63,9 @@ void set_last_error(const char* msg);
 // T2 rows, scatter, per-row sort), then one fixed-order sum per row.
 cudaError_t launch_det_count(const Prob& p, int* cnt, cudaStream_t st);
 cudaError_t launch_det_scatter(const Prob& p, int* cursor, int* ent, cudaStream_t st);
-cudaError_t launch_det_sort(const Prob& p, const int* gbeg, const int* ngroups, int* ent, int* scratch,
+// Sorts each row's segment of entry ids ascending: long_segs = false sorts the
+// segments of up to 1024 entries, true the longer ones (two launches).
+cudaError_t launch_det_sort(const Prob& p, const int* gbeg, const int* ngroups, int* ent, int* scratch, bool long_segs,
                             cudaStream_t st);
 cudaError_t launch_det_reduce(const Prob& p, const int* groups, const int* gbeg, const int* ngroups, const int* ent,
                               const uint16_t* partials, float* acc, cudaStream_t st);

@@ -5,8 +5,8 @@
 // in tensor memory, then applies the saved softmax statistics:
 //     P  = exp(S - softmaxMax) / softmaxSum                (masked keys -> 0)
 //     dS = P * (dP - Dsum) * scale
-// and writes P^T and dS^T (input dtype, heads contiguous) for the later
-// contractions.  Forward modes reuse the score half: per-tile max/sum partials,
+// and writes P^T and dS^T (input dtype, heads contiguous, rows of G rounded
+// up to 16 heads) for the later contractions.  Forward modes reuse the score half: per-tile max/sum partials,
 // or P from final statistics.
 //
 // Pipeline: the contraction runs in stages of 128 features (64 for the rope
@@ -377,9 +377,11 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
     // A lane holds 32 heads (64 bytes) of its own key row.  The warp's 32
     // rows pass through a private shared buffer (16-byte pieces XOR-swizzled
     // by row) so that each global store instruction writes eight rows x 64
-    // contiguous bytes instead of 32 scattered 16-byte pieces.
+    // contiguous bytes instead of 32 scattered 16-byte pieces.  Staged rows
+    // hold Gs heads (G rounded up to 16); the pieces past Gs are not written.
+    const int Gs = p.Gs;
     uint4* stg = epi_stage[warp - 4];
-    auto put_rows = [&](const uint32_t* pk, T* dst) {
+    auto put_rows = [&](const uint32_t* pk, T* dst, int npc) {
 #pragma unroll
       for (int u = 0; u < 4; ++u)
         stg[lane * 4 + (u ^ ((lane >> 1) & 3))] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
@@ -387,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int r = i * 8 + (lane >> 2), pc = lane & 3;
-        *reinterpret_cast<uint4*>(dst + (size_t)r * GP + pc * 8) = stg[r * 4 + (pc ^ ((r >> 1) & 3))];
+        if (pc < npc) *reinterpret_cast<uint4*>(dst + (size_t)r * Gs + pc * 8) = stg[r * 4 + (pc ^ ((r >> 1) & 3))];
       }
       __syncwarp();
     };
@@ -455,11 +457,13 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
         continue;
       }
       if (!ok) continue;
-      T* ptile = static_cast<T*>(out_p) + ((size_t)tl * p.Kpad + kt * kKeys + q * 32) * GP;
-      T* dstile = bwd ? static_cast<T*>(out_ds) + ((size_t)tl * p.Kpad + kt * kKeys + q * 32) * GP : nullptr;
+      T* ptile = static_cast<T*>(out_p) + ((size_t)tl * p.Kpad + kt * kKeys + q * 32) * Gs;
+      T* dstile = bwd ? static_cast<T*>(out_ds) + ((size_t)tl * p.Kpad + kt * kKeys + q * 32) * Gs : nullptr;
 #pragma unroll 1
       for (int c = 0; c < HH / 32; ++c) {
         const int h0 = half * HH + c * 32;
+        if (h0 >= Gs) break;                       // padded heads only: nothing is staged
+        const int npc = Gs - h0 >= 32 ? 4 : (Gs - h0) / 8;
         float s[32], dp[32];
         tmem_ld32(tS + h0, s);
         if (bwd) tmem_ld32(tP + h0, dp);
@@ -480,8 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
           pk[j / 2] = E::pack(pv[0], pv[1]);
           dk[j / 2] = E::pack(dv[0], dv[1]);
         }
-        put_rows(pk, ptile + h0);
-        if (bwd) put_rows(dk, dstile + h0);
+        put_rows(pk, ptile + h0, npc);
+        if (bwd) put_rows(dk, dstile + h0, npc);
       }
       tc_fence_before();
       mbar_arrive(&tempty_bar[set]);

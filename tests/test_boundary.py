@@ -132,13 +132,13 @@ def test_plan_names(sfa):
     assert "kvb" not in sfa.plan_names(_p(sfa, S1=2048, S2=4096, N1=16, K=64, sparse_block_size=8))
     assert "kvb" not in sfa.plan_names(_p(sfa, S1=2048, S2=4096, N1=128, K=64, sparse_block_size=64))
     det = sfa.plan_names(_p(sfa, deterministic=1))
-    assert det == ["meta", "dsum", "rowtab", "sdp", "det_count", "det_scan", "det_scatter", "det_sort", "kvq",
-                   "det_reduce", "cast"]
+    assert det == ["meta", "dsum", "rowtab", "sdp", "det_count", "det_scan", "det_scatter", "det_sort",
+                   "det_sort_long", "kvq", "det_reduce", "cast"]
     # deterministic block indices: the key-major path with sorted groups, one
     # kvb launch per block-start residue
     bdet = sfa.plan_names(_p(sfa, dtype=1, B=2, S1=8192, S2=32768, N1=16, K=64, sparse_block_size=64,
                              deterministic=1))
-    cdet = ["rowtab", "sdp", "blk_count", "blk_scan", "blk_scatter", "blk_sort"] + ["kvb"] * 64 + ["kvq"]
+    cdet = ["rowtab", "sdp", "blk_count", "blk_scan", "blk_scatter", "blk_sort", "blk_sort_long"] + ["kvb"] * 64 + ["kvq"]
     assert bdet[2:2 + len(cdet)] == cdet and "det_reduce" not in bdet
     assert sfa.plan_info(_p(sfa, dtype=1, B=2, S1=8192, S2=32768, N1=16, K=64, sparse_block_size=64,
                             deterministic=1))[0] == ctok
