@@ -21,14 +21,13 @@ namespace {
 
 constexpr int kAccRow = 1088;
 constexpr int kCols4 = kAccRow / 4;     // 272 float4 columns
-// Segment sort: segments of up to kShortCap entries are sorted by a launch
-// with many warps per SM (static shared memory); longer ones by a second
-// launch with kLongCap entries of dynamic shared memory per warp, and the
-// rare segments longer than that in global scratch.
+// Segment sort: segments of up to kShortCap entries are sorted one per warp
+// by a launch with many warps per SM; longer ones one per block by a second
+// launch, in shared memory up to kLongCap entries and in global scratch
+// beyond that.
 constexpr int kSortWarps = 8;
 constexpr int kShortCap = 1024;
 constexpr int kLongCap = 4096;
-constexpr int kLongSmem = kSortWarps * kLongCap * 4;   // 128 KB
 
 __global__ void det_count_kernel(Prob p, int* cnt) {
   const long long n = (long long)p.ntok * p.Kpad;
@@ -65,31 +64,60 @@ __device__ __forceinline__ void warp_bitonic(int* a, int np, int lane) {
   }
 }
 
-// One warp per receiving row sorts the row's entry ids ascending.  LONG = 0:
-// the segments of 2 .. kShortCap entries, in static shared memory; LONG = 1:
-// the longer ones (many occurrences of one key in the chunk), in dynamic
-// shared memory up to kLongCap entries, beyond that in a padded copy at
-// scratch + 2 * begin, which never overlaps another segment's copy.
-template <bool LONG>
-__global__ void __launch_bounds__(256) det_segsort_kernel(const int* gbeg, const int* ngroups_p, int* ent,
-                                                          int* scratch) {
-  extern __shared__ int long_buf[];                  // LONG: kSortWarps x kLongCap
-  __shared__ int short_buf[LONG ? 1 : kSortWarps][kShortCap];
+// One warp per receiving row sorts the row's entry ids ascending, for the
+// segments of 2 .. kShortCap entries, in static shared memory.
+__global__ void __launch_bounds__(256) det_segsort_kernel(const int* gbeg, const int* ngroups_p, int* ent) {
+  __shared__ int buf[kSortWarps][kShortCap];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ngroups = *ngroups_p;
   for (int k = blockIdx.x * kSortWarps + warp; k < ngroups; k += gridDim.x * kSortWarps) {
     const int b = gbeg[k], n = gbeg[k + 1] - b;
-    if (n <= 1 || (n > kShortCap) != LONG) continue;
+    if (n <= 1 || n > kShortCap) continue;
     int np = 1;
     while (np < n) np <<= 1;
-    int* a;
-    if constexpr (LONG) a = np <= kLongCap ? long_buf + warp * kLongCap : scratch + 2 * (size_t)b;
-    else a = short_buf[warp];
+    int* a = buf[warp];
     for (int i = lane; i < np; i += 32) a[i] = i < n ? ent[b + i] : INT_MAX;
     __syncwarp();
     warp_bitonic(a, np, lane);
     for (int i = lane; i < n; i += 32) ent[b + i] = a[i];
     __syncwarp();
+  }
+}
+
+// One block per longer segment (many occurrences of one key in the chunk):
+// an ascending bitonic sort by 256 threads, in shared memory up to kLongCap
+// entries, beyond that in a padded copy at scratch + 2 * begin, which never
+// overlaps another segment's copy.
+__global__ void __launch_bounds__(256) det_segsort_long_kernel(const int* gbeg, const int* ngroups_p, int* ent,
+                                                               int* scratch) {
+  __shared__ int buf[kLongCap];
+  const int tid = threadIdx.x;
+  const int ngroups = *ngroups_p;
+  for (int k = blockIdx.x; k < ngroups; k += gridDim.x) {
+    const int b = gbeg[k], n = gbeg[k + 1] - b;
+    if (n <= kShortCap) continue;
+    int np = 1;
+    while (np < n) np <<= 1;
+    int* a = np <= kLongCap ? buf : scratch + 2 * (size_t)b;
+    for (int i = tid; i < np; i += 256) a[i] = i < n ? ent[b + i] : INT_MAX;
+    __syncthreads();
+    for (int kk = 2; kk <= np; kk <<= 1) {
+      for (int j = kk >> 1; j > 0; j >>= 1) {
+        for (int i = tid; i < np; i += 256) {
+          const int ixj = i ^ j;
+          if (ixj > i) {
+            const int x = a[i], y = a[ixj];
+            if ((x > y) == ((i & kk) == 0)) {
+              a[i] = y;
+              a[ixj] = x;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    }
+    for (int i = tid; i < n; i += 256) ent[b + i] = a[i];
+    __syncthreads();
   }
 }
 
@@ -157,12 +185,10 @@ cudaError_t launch_det_sort(const Prob& p, const int* gbeg, const int* ngroups, 
   if (p.ntok <= 0 || p.T2 <= 0) return cudaSuccess;
   if (!long_segs) {
     const int grid = (p.T2 + 7) / 8 < 4096 ? (p.T2 + 7) / 8 : 4096;
-    det_segsort_kernel<false><<<grid, 256, 0, st>>>(gbeg, ngroups, ent, scratch);
-    return cudaGetLastError();
+    det_segsort_kernel<<<grid, 256, 0, st>>>(gbeg, ngroups, ent);
+  } else {
+    det_segsort_long_kernel<<<4 * 152, 256, 0, st>>>(gbeg, ngroups, ent, scratch);
   }
-  cudaError_t e = cudaFuncSetAttribute(det_segsort_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLongSmem);
-  if (e != cudaSuccess) return e;
-  det_segsort_kernel<true><<<152, 256, kLongSmem, st>>>(gbeg, ngroups, ent, scratch);
   return cudaGetLastError();
 }
 
