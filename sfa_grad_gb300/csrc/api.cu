@@ -299,9 +299,9 @@ int kvq_tile_group(const Plan& P) {
 const char* const kChunkDet[] = {"rowtab", "sdp", "det_count", "det_scan", "det_scatter", "det_sort",
                                  "det_sort_long", "kvq", "det_reduce"};
 const char* const kChunkKvq[] = {"rowtab", "sdp", "kvq"};
-const char* const kChunkKvb[] = {"rowtab", "sdp", "blk_count", "blk_scan", "blk_scatter", "kvb", "kvq"};
-const char* const kChunkKvbDetHead[] = {"rowtab", "sdp", "blk_count", "blk_scan", "blk_scatter", "blk_sort",
-                                        "blk_sort_long"};
+const char* const kChunkKvb[] = {"rowtab", "blk_count", "blk_scan", "blk_scatter", "sdpb", "kvb", "kvq"};
+const char* const kChunkKvbDetHead[] = {"rowtab", "blk_count", "blk_scan", "blk_scatter", "blk_sort",
+                                        "blk_sort_long", "sdpb"};
 
 int64_t plan_names(const Plan& P, const char** out, int64_t cap) {
   int64_t n = 0;
@@ -432,8 +432,10 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
     void* dSst = ws + P.off_dS;
     SFA_CK(launch_rowtab(pr, st));
     SFA_CK(mk.mark(st));
-    SFA_CK(launch_sdp<T>(maps, pr, kModeBwd, Pst, dSst, nullptr, gerr, nsm, st));
-    SFA_CK(mk.mark(st));
+    if (!P.kvb) {   // block indices that many tokens select: scores per block below
+      SFA_CK(launch_sdp<T>(maps, pr, kModeBwd, Pst, dSst, nullptr, gerr, nsm, st));
+      SFA_CK(mk.mark(st));
+    }
     if (P.det && !P.kvb) {
       int* bcnt = reinterpret_cast<int*>(ws + P.off_bcnt);
       int* bcur = reinterpret_cast<int*>(ws + P.off_bcur);
@@ -467,7 +469,7 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
       int* bbeg = reinterpret_cast<int*>(ws + P.off_bbeg);
       int* bng = reinterpret_cast<int*>(ws + P.off_bng);
       int* bent = reinterpret_cast<int*>(ws + P.off_bent);
-      SFA_CK(launch_blk_count(pr, bcnt, st));
+      SFA_CK(launch_blk_count(pr, bcnt, Pst, dSst, st));
       SFA_CK(mk.mark(st));
       SFA_CK(launch_blk_scan(bcnt, P.T2 + P.bs, bcur, bgrp, bbeg, bng, st));
       SFA_CK(mk.mark(st));
@@ -475,13 +477,19 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
       SFA_CK(mk.mark(st));
       if (P.det) {
         // each group's pairs in ascending (token, index) order, so that the
-        // tensor-memory accumulation of a block has one fixed order; then the
-        // groups in bs launches by start residue, so that no two tiles added
-        // in one launch share a key row
+        // tensor-memory accumulation of a block has one fixed order
         SFA_CK(launch_det_sort(pr, bbeg, bng, bent, reinterpret_cast<int*>(ws + P.off_dscr), false, st));
         SFA_CK(mk.mark(st));
         SFA_CK(launch_det_sort(pr, bbeg, bng, bent, reinterpret_cast<int*>(ws + P.off_dscr), true, st));
         SFA_CK(mk.mark(st));
+      }
+      // scores per block: each block's key / value rows loaded once for all
+      // the tokens that select it
+      SFA_CK(launch_sdpb<T>(maps, pr, bgrp, bbeg, bng, bent, Pst, dSst, gerr, nsm, st));
+      SFA_CK(mk.mark(st));
+      if (P.det) {
+        // the groups in bs launches by start residue, so that no two tiles
+        // added in one launch share a key row
         for (int r = 0; r < P.bs; ++r) {
           SFA_CK(launch_kvb<T>(bmaps, pr, P.bs, bgrp, bbeg, bng, bent, acc, r, gerr, nsm, st));
           SFA_CK(mk.mark(st));

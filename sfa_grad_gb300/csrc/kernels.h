@@ -18,7 +18,9 @@ cudaError_t launch_sdp(const Maps& maps, const Prob& p, int mode, void* out_p, v
 // every group's block in tensor memory and add it to acc once.  res >= 0
 // (deterministic mode; entries sorted within each group): only the groups
 // whose start is res modulo bs, whose blocks share no key row.
-cudaError_t launch_blk_count(const Prob& p, int* cnt, cudaStream_t st);
+// pst / dsst (optional): the staged P^T / dS^T; the rows no group covers
+// (pairs left out, padding slots) are zeroed.
+cudaError_t launch_blk_count(const Prob& p, int* cnt, void* pst, void* dsst, cudaStream_t st);
 cudaError_t launch_blk_scan(const int* cnt, int nbins, int* cursor, int* groups, int* gbeg, int* ngroups,
                             cudaStream_t st);
 cudaError_t launch_blk_scatter(const Prob& p, int* cursor, int* entries, cudaStream_t st);
@@ -26,6 +28,13 @@ template <typename T>
 cudaError_t launch_kvb(const BlkMaps& maps, const Prob& p, int bs, const int* groups, const int* gbeg,
                        const int* ngroups, const int* entries, float* acc, int res, int* gerr, int nsm,
                        cudaStream_t st);
+
+// Key-major scores for block-sparse indices (sdpb.cu): per group of pairs
+// sharing a block start, S and dP of packs of 128 / GK tokens against the
+// block's resident key / value rows; writes the pairs' staged P^T / dS^T rows.
+template <typename T>
+cudaError_t launch_sdpb(const Maps& maps, const Prob& p, const int* groups, const int* gbeg, const int* ngroups,
+                        const int* entries, void* pst, void* dsst, int* gerr, int nsm, cudaStream_t st);
 
 // Key-side and query-side contractions in one launch, two pipelines per CTA
 // (kvq.cu): key-side reductions into acc, dQ / dQRope out.  tile_group: key
