@@ -167,6 +167,14 @@ __global__ void __launch_bounds__(kThreads, 1) sdpb_kernel(const __grid_constant
           for (int pn = 0; pn < 8; ++pn) tma_2d(smem_u32(kv + (9 + pn) * kPanel), &maps.v, pn * 64, y0, &kv_full);
         }
         for (int j = 0; j < npk && ok; ++j) {
+          // the pack's first head rows, once per pack (a missing token of the
+          // last pack: rows below row 0)
+          int ys[TPK];
+#pragma unroll
+          for (int jt = 0; jt < TPK; ++jt) {
+            const int e = e0 + j * TPK + jt;
+            ys[jt] = e < e1 ? (p.tok0 + __ldg(entries + e) / p.Kidx) * p.G : -2 * GK;
+          }
           for (int c = 0; c < nc && ok; ++c, ++g) {
             const int slot = g % kStages;
             if (slot != me) continue;
@@ -177,15 +185,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpb_kernel(const __grid_constant
             const CUtensorMap* mq = c < 8 ? &maps.qg : c < nS ? &maps.qrg : &maps.dOg;
             const int x = c < 8 ? c * 64 : c < nS ? 0 : (c - nS) * 64;
             const uint32_t dst = smem_u32(ring + slot * kStageBytes);
-            for (int jt = 0; jt < TPK; ++jt) {
-              const int e = e0 + j * TPK + jt;
-              int y = -2 * GK;
-              if (e < e1) {
-                const int pr = __ldg(entries + e);
-                y = (p.tok0 + pr / p.Kidx) * p.G;
-              }
-              tma_2d(dst + jt * GK * 128, mq, x, y, &a_full[slot]);
-            }
+#pragma unroll
+            for (int jt = 0; jt < TPK; ++jt) tma_2d(dst + jt * GK * 128, mq, x, ys[jt], &a_full[slot]);
           }
         }
       }
