@@ -12,9 +12,12 @@
 //     P  = exp(S * scale - softmaxMax) / softmaxSum  (masked keys -> 0)
 //     dS = P * (dP - Dsum) * scale
 // and writes each pair's bs staged P^T / dS^T rows (slots index*bs .. +bs-1,
-// rows of Gs heads) with one bulk copy per pair and tensor.  The per-token
-// score kernel (sdp.cu) instead loads a block's key and value rows once per
-// selecting token; here they are loaded once per group.
+// rows of Gs heads; neighbouring heads paired into 4-byte stores).  The
+// per-token score kernel (sdp.cu) instead loads a block's key and value rows
+// once per selecting token; here they are loaded once per group.  The pack
+// stream is bound by the bytes in flight, so the ring takes the shared
+// memory the resident block leaves: five 16 KB stages, one producer warp
+// each.
 //
 // aclnnSparseFlashAttentionGrad doc, 功能说明 (selected blocks of
 // sparseBlockSize keys) and 阶段1/阶段2 (dP, dS); MindSpore
@@ -26,25 +29,16 @@ namespace sfa {
 
 namespace {
 
-constexpr int kThreads = 256;   // warp 0: MMA issuer, warps 1-3: TMA producers, warps 4-7: epilogue
-constexpr int kStages = 3;      // pack operand ring (one stage per producer warp)
+constexpr int kStages = 5;      // pack operand ring, one producer warp per stage slot
+// warp 0: MMA issuer, warps 1-5: TMA producers, warps 6-9: epilogue
+constexpr int kThreads = (1 + kStages + 4) * 32;
+constexpr int kEpi0 = 1 + kStages;        // first epilogue warp
 constexpr int kRows = 128;      // MMA M: token-head rows of a pack
 constexpr int kStageBytes = kRows * 128;   // one 64-feature panel of the pack
 
-// dynamic shared memory: KV panels (17 x bs rows), ring, epilogue P and dS tiles
+// dynamic shared memory: KV panels (17 x bs rows), then the ring
 __host__ __device__ constexpr int kv_bytes(int bs) { return 17 * bs * 128; }
-__host__ __device__ constexpr int epi_bytes(int bs) { return kRows * bs * 2; }
-__host__ __device__ constexpr int smem_bytes(int bs) {
-  return kv_bytes(bs) + kStages * kStageBytes + 2 * epi_bytes(bs) + 1024;
-}
-
-__device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__host__ __device__ constexpr int smem_bytes(int bs) { return kv_bytes(bs) + kStages * kStageBytes + 1024; }
 
 template <typename T, int BS, int GK>
 __global__ void __launch_bounds__(kThreads, 1) sdpb_kernel(const __grid_constant__ Maps maps, Prob p, const int* groups,
@@ -57,8 +51,6 @@ __global__ void __launch_bounds__(kThreads, 1) sdpb_kernel(const __grid_constant
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* kv = smem;
   uint8_t* ring = smem + kv_bytes(BS);
-  T* epi_p = reinterpret_cast<T*>(ring + kStages * kStageBytes);
-  T* epi_ds = epi_p + kRows * BS;
   __shared__ uint64_t kv_full, kv_empty, a_full[kStages], a_empty[kStages], t_full[2], t_empty[2], done_bar;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
@@ -144,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpb_kernel(const __grid_constant
     __syncwarp();
   } else if (warp <= kStages) {
     // ---------------------------------------------------------------- TMA producers
-    // Producer w (warps 1-3) fills ring slot w-1 for every third stage: the
+    // Producer w (warps 1-5) fills ring slot w-1 for every fifth stage: the
     // pack's tokens' head rows of one 64-feature panel, one box of GK rows per
     // token (a missing token of the last pack reads rows below row 0: zeros).
     // Producer 0 also loads each group's key / value panels.
@@ -195,35 +187,33 @@ __global__ void __launch_bounds__(kThreads, 1) sdpb_kernel(const __grid_constant
       klog.settle(&kv_full, gerr);
     }
     __syncwarp();
-  } else {
+  } else if (warp >= kEpi0) {
     // ---------------------------------------------------------------- epilogue
-    // Thread r = TMEM lane r = token-head row: token jt = r / GK of the pack,
-    // head h = r % GK.  P and dS go to shared memory as [token][key][Gs
-    // heads] (each pair's bs rows contiguous, as in the staging), then thread
-    // jt < TPK copies token jt's two tiles with bulk copies.  Named barriers
-    // run once per pack whatever happens, so their trip counts never depend
-    // on the abort flag.
-    const int r = threadIdx.x - 128;
+    // Warp w reads TMEM lane quadrant w % 4; thread r = TMEM lane = token-head
+    // row: token jt = r / GK of the pack, head h = r % GK.  For each key u the
+    // even head of a neighbouring pair stores both heads' bf16 values as one
+    // 4-byte word into the pair's staged row (tl * Kpad + index * bs + u).
+    const int r = (warp & 3) * 32 + lane;
     const int jt = r / GK, h = r - jt * GK;
     const float sl2 = p.scale * kLog2e;
     int it = 0;
-    bool pending = false;   // this thread has bulk copies reading the tiles
-    for (int k = blockIdx.x; k < ngroups; k += gridDim.x) {
+    for (int k = blockIdx.x; k < ngroups && !abort_flag; k += gridDim.x) {
       const int e0 = gbeg[k], e1 = gbeg[k + 1];
       const int npk = (e1 - e0 + TPK - 1) / TPK;
       for (int j = 0; j < npk; ++j, ++it) {
         const int set = it & 1;
         const int e = e0 + j * TPK + jt;
         const bool has = jt < TPK && e < e1;
-        int tl = 0, ii = 0, ridx = 0, lim = -1;
+        int ridx = 0, lim = -1;
+        size_t row0 = 0;
         float m = 0.f, linv = 0.f, dsc = 0.f;
         if (has) {
           const int pr = __ldg(entries + e);
-          tl = pr / p.Kidx;
-          ii = pr - tl * p.Kidx;
+          const int tl = pr / p.Kidx, ii = pr - tl * p.Kidx;
           const int t = p.tok0 + tl;
           ridx = __ldg(p.idx + (size_t)t * p.Kidx + ii);
           lim = p.meta[t].limit;
+          row0 = (size_t)tl * p.Kpad + (size_t)ii * BS;
           if (h < p.G) {
             const float l = __ldg(p.ssum + (size_t)t * p.G + h);
             m = l > 0.f ? __ldg(p.smax + (size_t)t * p.G + h) * kLog2e : 0.f;
@@ -231,63 +221,42 @@ __global__ void __launch_bounds__(kThreads, 1) sdpb_kernel(const __grid_constant
             dsc = __ldg(p.dsum + (size_t)t * p.G + h) * p.scale;
           }
         }
-        const bool ok = __all_sync(0xffffffffu, !abort_flag && mbar_wait(&t_full[set], (it >> 1) & 1, wt));
-        // the previous pack's copies must have read the tiles before they are rewritten
-        if (pending) {
-          bulk_wait_read();
-          pending = false;
-        }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (ok) {
-          tc_fence_after();
-          const uint32_t td = tbase + set * (2 * BS) + ((uint32_t)((warp - 4) * 32) << 16);
-          constexpr int CH = BS < 32 ? BS : 32;   // key columns per TMEM load
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&t_full[set], (it >> 1) & 1, wt));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t td = tbase + set * (2 * BS) + ((uint32_t)((warp & 3) * 32) << 16);
+        const bool store = has && (h & 1) == 0 && h < Gs;
+        uint32_t* op = reinterpret_cast<uint32_t*>(pst + row0 * Gs + h);
+        uint32_t* od = reinterpret_cast<uint32_t*>(dsst + row0 * Gs + h);
+        constexpr int CH = BS < 32 ? BS : 32;   // key columns per TMEM load
 #pragma unroll 1
-          for (int u0 = 0; u0 < BS; u0 += CH) {
-            float s[CH], dp[CH];
-            if constexpr (CH == 32) {
-              tmem_ld32(td + u0, s);
-              tmem_ld32(td + BS + u0, dp);
-            } else {
-              tmem_ld16(td + u0, s);
-              tmem_ld16(td + BS + u0, dp);
-            }
-            if (jt < TPK && h < Gs) {
-              T* op = epi_p + ((size_t)jt * BS + u0) * Gs + h;
-              T* od = epi_ds + ((size_t)jt * BS + u0) * Gs + h;
+        for (int u0 = 0; u0 < BS; u0 += CH) {
+          float s[CH], dp[CH];
+          if constexpr (CH == 32) {
+            tmem_ld32(td + u0, s);
+            tmem_ld32(td + BS + u0, dp);
+          } else {
+            tmem_ld16(td + u0, s);
+            tmem_ld16(td + BS + u0, dp);
+          }
 #pragma unroll
-              for (int u = 0; u < CH; ++u) {
-                const int key = ridx + u0 + u;
-                const bool valid = has && key >= 0 && key <= lim;
-                const float pp = valid ? ex2(fmaf(s[u], sl2, -m)) * linv : 0.f;
-                const float dd = pp != 0.f ? pp * fmaf(dp[u], p.scale, -dsc) : 0.f;
-                op[u * Gs] = E::from_f(pp);
-                od[u * Gs] = E::from_f(dd);
-              }
+          for (int u = 0; u < CH; ++u) {
+            const int key = ridx + u0 + u;
+            const bool valid = has && key >= 0 && key <= lim;
+            const float pp = valid ? ex2(fmaf(s[u], sl2, -m)) * linv : 0.f;
+            const float dd = pp != 0.f ? pp * fmaf(dp[u], p.scale, -dsc) : 0.f;
+            const float pp1 = __shfl_down_sync(0xffffffffu, pp, 1);
+            const float dd1 = __shfl_down_sync(0xffffffffu, dd, 1);
+            if (store) {
+              op[(size_t)(u0 + u) * Gs / 2] = E::pack(pp, pp1);
+              od[(size_t)(u0 + u) * Gs / 2] = E::pack(dd, dd1);
             }
           }
-          tc_fence_before();
         }
+        tc_fence_before();
         mbar_arrive(&t_empty[set]);
-        fence_async_smem();
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        // thread r < TPK copies token r's tiles of the pack
-        if (ok && r < TPK) {
-          const int e2 = e0 + j * TPK + r;
-          if (e2 < e1) {
-            const int pr = __ldg(entries + e2);
-            const int tl2 = pr / p.Kidx, ii2 = pr - tl2 * p.Kidx;
-            const size_t row0 = ((size_t)tl2 * p.Kpad + (size_t)ii2 * BS) * Gs;
-            const uint32_t bytes = (uint32_t)(BS * Gs * sizeof(T));
-            bulk_store(pst + row0, smem_u32(epi_p + (size_t)r * BS * Gs), bytes);
-            bulk_store(dsst + row0, smem_u32(epi_ds + (size_t)r * BS * Gs), bytes);
-            bulk_commit();
-            pending = true;
-          }
-        }
       }
     }
-    if (pending) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
