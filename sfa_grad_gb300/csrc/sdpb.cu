@@ -12,7 +12,7 @@
 //     P  = exp(S * scale - softmaxMax) / softmaxSum  (masked keys -> 0)
 //     dS = P * (dP - Dsum) * scale
 // and writes each pair's bs staged P^T / dS^T rows (slots index*bs .. +bs-1,
-// rows of Gs heads; neighbouring heads paired into 4-byte stores).  The
+// rows of Gs heads).  The
 // per-token score kernel (sdp.cu) instead loads a block's key and value rows
 // once per selecting token; here they are loaded once per group.  The pack
 // stream is bound by the bytes in flight, so the ring takes the shared
@@ -191,71 +191,113 @@ __global__ void __launch_bounds__(kThreads, 1) sdpb_kernel(const __grid_constant
     // ---------------------------------------------------------------- epilogue
     // Warp w reads TMEM lane quadrant w % 4; thread r = TMEM lane = token-head
     // row: token jt = r / GK of the pack, head h = r % GK.  For each key u the
-    // even head of a neighbouring pair stores both heads' bf16 values as one
-    // 4-byte word into the pair's staged row (tl * Kpad + index * bs + u).
+    // 16-bit P and dS values go straight to the pair's staged row (tl * Kpad
+    // + index * bs + u, column h): a token's heads are contiguous, so a warp
+    // store covers 32 contiguous bytes per token.  The pair data a pack needs
+    // (entry -> index and token metadata -> statistics) is a chain of
+    // dependent loads, so it is fetched two packs ahead: the entry of pack
+    // n + 2 and the rest of pack n + 1 while pack n is processed.
     const int r = (warp & 3) * 32 + lane;
     const int jt = r / GK, h = r - jt * GK;
     const float sl2 = p.scale * kLog2e;
-    int it = 0;
-    for (int k = blockIdx.x; k < ngroups && !abort_flag; k += gridDim.x) {
-      const int e0 = gbeg[k], e1 = gbeg[k + 1];
-      const int npk = (e1 - e0 + TPK - 1) / TPK;
-      for (int j = 0; j < npk; ++j, ++it) {
-        const int set = it & 1;
-        const int e = e0 + j * TPK + jt;
-        const bool has = jt < TPK && e < e1;
-        int ridx = 0, lim = -1;
-        size_t row0 = 0;
-        float m = 0.f, linv = 0.f, dsc = 0.f;
-        if (has) {
-          const int pr = __ldg(entries + e);
-          const int tl = pr / p.Kidx, ii = pr - tl * p.Kidx;
-          const int t = p.tok0 + tl;
-          ridx = __ldg(p.idx + (size_t)t * p.Kidx + ii);
-          lim = p.meta[t].limit;
-          row0 = (size_t)tl * p.Kpad + (size_t)ii * BS;
-          if (h < p.G) {
-            const float l = __ldg(p.ssum + (size_t)t * p.G + h);
-            m = l > 0.f ? __ldg(p.smax + (size_t)t * p.G + h) * kLog2e : 0.f;
-            linv = l > 0.f ? 1.f / l : 0.f;
-            dsc = __ldg(p.dsum + (size_t)t * p.G + h) * p.scale;
-          }
+    // walk of this CTA's packs in order: group k (strided), pack j
+    struct Pos {
+      int k, j, e0, e1;
+    };
+    auto first = [&]() {
+      Pos q{(int)blockIdx.x, 0, 0, 0};
+      if (q.k < ngroups) {
+        q.e0 = gbeg[q.k];
+        q.e1 = gbeg[q.k + 1];
+      }
+      return q;
+    };
+    auto next = [&](Pos q) {
+      if (q.k >= ngroups) return q;
+      if ((++q.j) * TPK >= q.e1 - q.e0) {
+        q.k += gridDim.x;
+        q.j = 0;
+        if (q.k < ngroups) {
+          q.e0 = gbeg[q.k];
+          q.e1 = gbeg[q.k + 1];
         }
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(&t_full[set], (it >> 1) & 1, wt));
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t td = tbase + set * (2 * BS) + ((uint32_t)((warp & 3) * 32) << 16);
-        const bool store = has && (h & 1) == 0 && h < Gs;
-        uint32_t* op = reinterpret_cast<uint32_t*>(pst + row0 * Gs + h);
-        uint32_t* od = reinterpret_cast<uint32_t*>(dsst + row0 * Gs + h);
-        constexpr int CH = BS < 32 ? BS : 32;   // key columns per TMEM load
+      }
+      return q;
+    };
+    // this thread's pair of a pack position, -1 if none
+    auto pair_of = [&](const Pos& q) {
+      const int e = q.e0 + q.j * TPK + jt;
+      return (q.k < ngroups && jt < TPK && e < q.e1) ? __ldg(entries + e) : -1;
+    };
+    struct Meta {
+      int ridx, lim;
+      size_t row0;
+      float m, linv, dsc;
+    };
+    auto meta_of = [&](int pr) {
+      Meta d{0, -1, 0, 0.f, 0.f, 0.f};
+      if (pr < 0) return d;
+      const int tl = pr / p.Kidx, ii = pr - tl * p.Kidx;
+      const int t = p.tok0 + tl;
+      d.ridx = __ldg(p.idx + (size_t)t * p.Kidx + ii);
+      d.lim = p.meta[t].limit;
+      d.row0 = (size_t)tl * p.Kpad + (size_t)ii * BS;
+      if (h < p.G) {
+        const float l = __ldg(p.ssum + (size_t)t * p.G + h);
+        d.m = l > 0.f ? __ldg(p.smax + (size_t)t * p.G + h) * kLog2e : 0.f;
+        d.linv = l > 0.f ? 1.f / l : 0.f;
+        d.dsc = __ldg(p.dsum + (size_t)t * p.G + h) * p.scale;
+      }
+      return d;
+    };
+    Pos cur = first();
+    Pos nx1 = next(cur);
+    int pr_cur = pair_of(cur), pr1 = pair_of(nx1);
+    Meta mc = meta_of(pr_cur);
+    int it = 0;
+    for (; cur.k < ngroups && !abort_flag; ++it) {
+      const int set = it & 1;
+      const Pos nx2 = next(nx1);
+      const int pr2 = pair_of(nx2);      // entry two packs ahead
+      const Meta mn = meta_of(pr1);      // data one pack ahead
+      const bool has = pr_cur >= 0;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&t_full[set], (it >> 1) & 1, wt));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t td = tbase + set * (2 * BS) + ((uint32_t)((warp & 3) * 32) << 16);
+      const bool store = has && h < Gs;
+      T* op = pst + mc.row0 * Gs + h;
+      T* od = dsst + mc.row0 * Gs + h;
+      constexpr int CH = BS < 32 ? BS : 32;   // key columns per TMEM load
 #pragma unroll 1
-        for (int u0 = 0; u0 < BS; u0 += CH) {
-          float s[CH], dp[CH];
-          if constexpr (CH == 32) {
-            tmem_ld32(td + u0, s);
-            tmem_ld32(td + BS + u0, dp);
-          } else {
-            tmem_ld16(td + u0, s);
-            tmem_ld16(td + BS + u0, dp);
-          }
+      for (int u0 = 0; u0 < BS; u0 += CH) {
+        float s[CH], dp[CH];
+        if constexpr (CH == 32) {
+          tmem_ld32(td + u0, s);
+          tmem_ld32(td + BS + u0, dp);
+        } else {
+          tmem_ld16(td + u0, s);
+          tmem_ld16(td + BS + u0, dp);
+        }
+        if (store) {
 #pragma unroll
           for (int u = 0; u < CH; ++u) {
-            const int key = ridx + u0 + u;
-            const bool valid = has && key >= 0 && key <= lim;
-            const float pp = valid ? ex2(fmaf(s[u], sl2, -m)) * linv : 0.f;
-            const float dd = pp != 0.f ? pp * fmaf(dp[u], p.scale, -dsc) : 0.f;
-            const float pp1 = __shfl_down_sync(0xffffffffu, pp, 1);
-            const float dd1 = __shfl_down_sync(0xffffffffu, dd, 1);
-            if (store) {
-              op[(size_t)(u0 + u) * Gs / 2] = E::pack(pp, pp1);
-              od[(size_t)(u0 + u) * Gs / 2] = E::pack(dd, dd1);
-            }
+            const int key = mc.ridx + u0 + u;
+            const bool valid = key >= 0 && key <= mc.lim;
+            const float pp = valid ? ex2(fmaf(s[u], sl2, -mc.m)) * mc.linv : 0.f;
+            const float dd = pp != 0.f ? pp * fmaf(dp[u], p.scale, -mc.dsc) : 0.f;
+            op[(size_t)(u0 + u) * Gs] = E::from_f(pp);
+            od[(size_t)(u0 + u) * Gs] = E::from_f(dd);
           }
         }
-        tc_fence_before();
-        mbar_arrive(&t_empty[set]);
       }
+      tc_fence_before();
+      mbar_arrive(&t_empty[set]);
+      cur = nx1;
+      nx1 = nx2;
+      pr_cur = pr1;
+      pr1 = pr2;
+      mc = mn;
     }
   }
   tc_fence_before();
