@@ -33,7 +33,7 @@ struct Plan {
   unsigned long long wait_ns;   // limit of every pipeline wait in the kernels
   int chunk;
   size_t off_err, off_batch, off_meta, off_dsum, off_acc, off_P, off_dS, off_rows, off_part, off_dscr, off_tstats;
-  size_t off_bcnt, off_bcur, off_bgrp, off_bbeg, off_bng, off_bent;
+  size_t off_bcnt, off_bcur, off_bgrp, off_bbeg, off_bng, off_bent, off_bres;
   size_t total;
 };
 
@@ -101,6 +101,13 @@ sfa_status validate(const sfa_params* p, bool fwd, Plan* out) {
     const size_t c2 = kPartCap / part_per_tok;
     if (c2 < chunk) chunk = c2;
   }
+  if (P.kvb) {
+    // the key-major block kernels read every pair's head rows (q, qRope, dO):
+    // chunks of about 64 MB of them stay resident in L2
+    const size_t c3 = (size_t(64) << 20) / ((size_t)P.G * (512 + 64 + 512) * 2);
+    const size_t c3c = c3 < 256 ? 256 : c3;
+    if (c3c < chunk) chunk = c3c;
+  }
   if (chunk < 1) chunk = 1;
   if (chunk > (size_t)P.T1) chunk = P.T1 > 0 ? P.T1 : 1;
   P.chunk = (int)chunk;
@@ -127,6 +134,7 @@ sfa_status validate(const sfa_params* p, bool fwd, Plan* out) {
   P.off_bbeg = o; o += bins ? up((nb + 1) * 4) : 0;
   P.off_bng = o; o += bins ? up(4) : 0;
   P.off_bent = o; o += bins ? up(ents * 4) : 0;
+  P.off_bres = o; o += P.kvb ? up(64 * 4) : 0;
   P.total = o;
   return SFA_OK;
 }
@@ -447,7 +455,7 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
       uint16_t* part = reinterpret_cast<uint16_t*>(ws + P.off_part);
       SFA_CK(launch_det_count(pr, bcnt, st));
       SFA_CK(mk.mark(st));
-      SFA_CK(launch_blk_scan(bcnt, P.T2, bcur, bgrp, bbeg, bng, st));
+      SFA_CK(launch_blk_scan(bcnt, P.T2, bcur, bgrp, bbeg, bng, 0, nullptr, st));
       SFA_CK(mk.mark(st));
       SFA_CK(launch_det_scatter(pr, bcur, bent, st));
       SFA_CK(mk.mark(st));
@@ -471,7 +479,8 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
       int* bent = reinterpret_cast<int*>(ws + P.off_bent);
       SFA_CK(launch_blk_count(pr, bcnt, Pst, dSst, st));
       SFA_CK(mk.mark(st));
-      SFA_CK(launch_blk_scan(bcnt, P.T2 + P.bs, bcur, bgrp, bbeg, bng, st));
+      int* bres = reinterpret_cast<int*>(ws + P.off_bres);
+      SFA_CK(launch_blk_scan(bcnt, P.T2 + P.bs, bcur, bgrp, bbeg, bng, P.bs, bres, st));
       SFA_CK(mk.mark(st));
       SFA_CK(launch_blk_scatter(pr, bcur, bent, st));
       SFA_CK(mk.mark(st));
@@ -491,11 +500,11 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
         // the groups in bs launches by start residue, so that no two tiles
         // added in one launch share a key row
         for (int r = 0; r < P.bs; ++r) {
-          SFA_CK(launch_kvb<T>(bmaps, pr, P.bs, bgrp, bbeg, bng, bent, acc, r, gerr, nsm, st));
+          SFA_CK(launch_kvb<T>(bmaps, pr, P.bs, bgrp, bbeg, bng, bent, acc, r, bres, gerr, nsm, st));
           SFA_CK(mk.mark(st));
         }
       } else {
-        SFA_CK(launch_kvb<T>(bmaps, pr, P.bs, bgrp, bbeg, bng, bent, acc, -1, gerr, nsm, st));
+        SFA_CK(launch_kvb<T>(bmaps, pr, P.bs, bgrp, bbeg, bng, bent, acc, -1, bres, gerr, nsm, st));
         SFA_CK(mk.mark(st));
       }
       SFA_CK(launch_kvq<T>(maps, pr, acc, dq, P.has_rope ? dqr : nullptr, 0, false, gerr, nsm, st));   // query side only

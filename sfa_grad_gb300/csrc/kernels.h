@@ -21,13 +21,14 @@ cudaError_t launch_sdp(const Maps& maps, const Prob& p, int mode, void* out_p, v
 // pst / dsst (optional): the staged P^T / dS^T; the rows no group covers
 // (pairs left out, padding slots) are zeroed.
 cudaError_t launch_blk_count(const Prob& p, int* cnt, void* pst, void* dsst, cudaStream_t st);
-cudaError_t launch_blk_scan(const int* cnt, int nbins, int* cursor, int* groups, int* gbeg, int* ngroups,
-                            cudaStream_t st);
+// nres (optional, bs entries): non-empty bins per residue modulo bs.
+cudaError_t launch_blk_scan(const int* cnt, int nbins, int* cursor, int* groups, int* gbeg, int* ngroups, int bs,
+                            int* nres, cudaStream_t st);
 cudaError_t launch_blk_scatter(const Prob& p, int* cursor, int* entries, cudaStream_t st);
 template <typename T>
 cudaError_t launch_kvb(const BlkMaps& maps, const Prob& p, int bs, const int* groups, const int* gbeg,
-                       const int* ngroups, const int* entries, float* acc, int res, int* gerr, int nsm,
-                       cudaStream_t st);
+                       const int* ngroups, const int* entries, float* acc, int res, const int* nres, int* gerr,
+                       int nsm, cudaStream_t st);
 
 // Key-major scores for block-sparse indices (sdpb.cu): per group of pairs
 // sharing a block start, S and dP of packs of 128 / GK tokens against the

@@ -75,12 +75,16 @@ __global__ void blk_count_kernel(Prob p, int* cnt, uint8_t* pst, uint8_t* dsst, 
 // gbeg[ngroups] = total entries.  The block walks the bins 4096 at a time
 // (four consecutive bins per thread, coalesced), scanning each tile with warp
 // shuffles and carrying the running totals.
+// With nres given (key-major blocks, bins = start + bs), also the number of
+// non-empty bins per residue bin % bs (nres[0 .. bs)).
 __global__ void __launch_bounds__(1024) blk_scan_kernel(const int* cnt, int nbins, int* cursor, int* groups, int* gbeg,
-                                                        int* ngroups) {
+                                                        int* ngroups, int bs, int* nres) {
   __shared__ int ex_sum[32], ex_nz[32];
   __shared__ int carry[2];
+  __shared__ int res_cnt[64];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) carry[0] = carry[1] = 0;
+  if (tid < 64) res_cnt[tid] = 0;
   __syncthreads();
   for (int base = 0; base < nbins; base += 4096) {
     const int b0 = base + tid * 4;
@@ -129,6 +133,7 @@ __global__ void __launch_bounds__(1024) blk_scan_kernel(const int* cnt, int nbin
           groups[k] = b0 + u;
           gbeg[k] = off;
           ++k;
+          if (nres) atomicAdd(&res_cnt[(b0 + u) % bs], 1);
         }
         off += c[u];
       }
@@ -144,6 +149,7 @@ __global__ void __launch_bounds__(1024) blk_scan_kernel(const int* cnt, int nbin
     *ngroups = carry[1];
     gbeg[carry[1]] = carry[0];
   }
+  if (nres && tid < bs) nres[tid] = res_cnt[tid];
 }
 
 __global__ void blk_scatter_kernel(Prob p, int* cursor, int* entries) {
@@ -172,7 +178,8 @@ template <typename T, int GK>
 __global__ void __launch_bounds__(kThreads, 1) kvb_kernel(const __grid_constant__ BlkMaps maps, Prob p, int bs,
                                                           int nstages, int nprod, const int* groups, const int* gbeg,
                                                           const int* ngroups_p, const int* entries, float* acc,
-                                                          int res, int* gerr) {
+                                                          int res, const int* nres, int* gerr) {
+  if (res >= 0 && nres[res] == 0) return;   // no group with this start residue
   using E = Elt<T>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -351,10 +358,10 @@ cudaError_t launch_blk_count(const Prob& p, int* cnt, void* pst, void* dsst, cud
   return cudaGetLastError();
 }
 
-cudaError_t launch_blk_scan(const int* cnt, int nbins, int* cursor, int* groups, int* gbeg, int* ngroups,
-                            cudaStream_t st) {
+cudaError_t launch_blk_scan(const int* cnt, int nbins, int* cursor, int* groups, int* gbeg, int* ngroups, int bs,
+                            int* nres, cudaStream_t st) {
   if (nbins <= 0) return cudaSuccess;
-  blk_scan_kernel<<<1, 1024, 0, st>>>(cnt, nbins, cursor, groups, gbeg, ngroups);
+  blk_scan_kernel<<<1, 1024, 0, st>>>(cnt, nbins, cursor, groups, gbeg, ngroups, bs, nres);
   return cudaGetLastError();
 }
 
@@ -375,8 +382,8 @@ int kvb_stages(int gk) {
 
 template <typename T>
 cudaError_t launch_kvb(const BlkMaps& maps, const Prob& p, int bs, const int* groups, const int* gbeg,
-                       const int* ngroups, const int* entries, float* acc, int res, int* gerr, int nsm,
-                       cudaStream_t st) {
+                       const int* ngroups, const int* entries, float* acc, int res, const int* nres, int* gerr,
+                       int nsm, cudaStream_t st) {
   if (p.ntok <= 0 || p.T2 <= 0) return cudaSuccess;
   const int gk = (p.G + 15) / 16 * 16;
   const int nst = kvb_stages(gk);
@@ -386,13 +393,13 @@ cudaError_t launch_kvb(const BlkMaps& maps, const Prob& p, int bs, const int* gr
   auto kern = gk == 16 ? kvb_kernel<T, 16> : gk == 32 ? kvb_kernel<T, 32> : gk == 48 ? kvb_kernel<T, 48> : kvb_kernel<T, 64>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<nsm, kThreads, smem, st>>>(maps, p, bs, nst, nprod, groups, gbeg, ngroups, entries, acc, res, gerr);
+  kern<<<nsm, kThreads, smem, st>>>(maps, p, bs, nst, nprod, groups, gbeg, ngroups, entries, acc, res, nres, gerr);
   return cudaGetLastError();
 }
 
 template cudaError_t launch_kvb<__nv_bfloat16>(const BlkMaps&, const Prob&, int, const int*, const int*, const int*,
-                                               const int*, float*, int, int*, int, cudaStream_t);
+                                               const int*, float*, int, const int*, int*, int, cudaStream_t);
 template cudaError_t launch_kvb<__half>(const BlkMaps&, const Prob&, int, const int*, const int*, const int*,
-                                        const int*, float*, int, int*, int, cudaStream_t);
+                                        const int*, float*, int, const int*, int*, int, cudaStream_t);
 
 }  // namespace sfa
