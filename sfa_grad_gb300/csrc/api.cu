@@ -101,13 +101,6 @@ sfa_status validate(const sfa_params* p, bool fwd, Plan* out) {
     const size_t c2 = kPartCap / part_per_tok;
     if (c2 < chunk) chunk = c2;
   }
-  if (P.kvb) {
-    // the key-major block kernels read every pair's head rows (q, qRope, dO):
-    // chunks of about 64 MB of them stay resident in L2
-    const size_t c3 = (size_t(64) << 20) / ((size_t)P.G * (512 + 64 + 512) * 2);
-    const size_t c3c = c3 < 256 ? 256 : c3;
-    if (c3c < chunk) chunk = c3c;
-  }
   if (chunk < 1) chunk = 1;
   if (chunk > (size_t)P.T1) chunk = P.T1 > 0 ? P.T1 : 1;
   P.chunk = (int)chunk;
