@@ -27,7 +27,8 @@ constexpr int kThreads = 640;   // 20 warps, roles below
 // warp 0: key-side MMA issuer          warp 1: key-side TMA producer
 // warp 2: query-side MMA issuer        warp 3: idle
 // warps 4-11: key-side drain           warps 12-15: query-side epilogue
-// warps 16-17: query-side gather producers, warps 18-19: idle
+// warps 16-17: query-side gather producers, warps 18-19: idle (query side
+// alone: warps 16-19 are its producers)
 constexpr int kDrainThreads = 256;
 
 constexpr int kKeys = 128;        // key-side tile (MMA M)
@@ -35,7 +36,8 @@ constexpr int kKvStages = 3;      // key-side A stages: 128 slots x 64 heads
 constexpr int kKvChunks = 9;      // dK 4 x 128 + dKRope 64, dV 4 x 128
 constexpr int kAccRow = 1088;
 constexpr int kQSlots = 64;       // query-side keys per stage (MMA K extent)
-constexpr int kQStages = 2;
+constexpr int kQStages = 2;       // query-side stages next to the key side
+constexpr int kQStagesQO = 4;     // query side alone: its stages take the key side's shared memory
 constexpr int kQCol = 192;        // query-side features per item (MMA N)
 constexpr int kQParts = 3;
 
@@ -48,6 +50,7 @@ constexpr int kQ = kKvStg + 8 * 32 * 32 * 4;              // 2 stages x (A 16 KB
 constexpr int kQA = 2 * kQSlots * 128;
 constexpr int kQStage = kQA + (kQCol / 64) * kQSlots * 128;
 constexpr int kSmemBytes = kQ + kQStages * kQStage + 1024;
+constexpr int kSmemBytesQO = kQStagesQO * kQStage + 1024;
 
 // TMEM columns: key-side accumulators [0,128) and [128,256), query side [256,448)
 constexpr uint32_t kQCol0 = 256;
@@ -93,17 +96,22 @@ __device__ __forceinline__ void red_add_v4(float* dst, float4 x) {
 // bf16, as element (token_local * Kpad + slot) * 1088 of the bf16 array at
 // acc (the partial rows the fixed-order reduction of det.cu sums in fp32);
 // masked slots are not written.
-template <typename T, int GP, bool BLK, bool PART>
+// QO: query side only (tile_group = 0): the key side's shared memory goes to
+// kQStagesQO query-side stages instead of kQStages, fed by as many producer
+// warps (16 ..).
+template <typename T, int GP, bool BLK, bool PART, bool QO>
 __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant__ Maps maps, Prob p, float* acc,
                                                           T* dq, T* dqr, int tg, int* gerr) {
   using E = Elt<T>;
+  constexpr int QST = QO ? kQStagesQO : kQStages;   // query-side stages
+  constexpr int QOFF = QO ? 0 : kQ;                 // offset of the query-side stages
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t kv_full[kKvStages], kv_empty[kKvStages], kv_tfull[2], kv_tempty[2], kv_bfull, kv_bempty;
-  __shared__ uint64_t q_full[kQStages], q_empty[kQStages], q_tfull, q_tempty, kv_done, q_done;
+  __shared__ uint64_t q_full[QST], q_empty[QST], q_tfull, q_tempty, kv_done, q_done;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
-  __shared__ __align__(16) int q_rows[kQStages][kQSlots];   // read and written as int2
+  __shared__ __align__(16) int q_rows[QST][kQSlots];   // read and written as int2
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntiles = p.Kpad / kKeys;
@@ -113,8 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
 
   if (GP == 64) {
     // query side: heads 64-127 do not exist, their A panel stays zero
-    for (int s = 0; s < kQStages; ++s) {
-      uint4* z = reinterpret_cast<uint4*>(smem + kQ + s * kQStage + kQSlots * 128);
+    for (int s = 0; s < QST; ++s) {
+      uint4* z = reinterpret_cast<uint4*>(smem + QOFF + s * kQStage + kQSlots * 128);
       for (int i = threadIdx.x; i < kQSlots * 128 / 16; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
     }
     fence_async_smem();
@@ -130,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
     }
     mbar_init(&kv_bfull, 1);
     mbar_init(&kv_bempty, 1);
-    for (int i = 0; i < kQStages; ++i) {
+    for (int i = 0; i < QST; ++i) {
       mbar_init(&q_full[i], 32 + 1);   // the owning warp's lanes + the TMA transaction arrive
       mbar_init(&q_empty[i], 1);
     }
@@ -319,8 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
     // ================================================================ query side: MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(128, kQCol, E::is_f16, true, true);
-      const uint64_t dqa0 = sdesc_mnmajor(smem_u32(smem + kQ), 0, kQSlots);
-      const uint64_t dqb0 = sdesc_mnmajor(smem_u32(smem + kQ + kQA), 0, kQSlots);
+      const uint64_t dqa0 = sdesc_mnmajor(smem_u32(smem + QOFF), 0, kQSlots);
+      const uint64_t dqb0 = sdesc_mnmajor(smem_u32(smem + QOFF + kQA), 0, kQSlots);
       const uint32_t d = tbase + kQCol0;
       int it = 0, g = 0;
       bool ok = true;
@@ -329,8 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
         if (!ok) break;
         tc_fence_after();
         for (int c = 0; c < qchunks; ++c, ++g) {
-          const int slot = g % kQStages;
-          ok = mbar_wait_poll(&q_full[slot], (g / kQStages) & 1, wt);
+          const int slot = g % QST;
+          ok = mbar_wait_poll(&q_full[slot], (g / QST) & 1, wt);
           if (!ok) break;
           tc_fence_after();
           static_assert(kQSlots == 64, "four K steps per stage");
@@ -343,9 +351,9 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
       mma_settle(&q_done, gerr);   // no MMA still writing tensor memory at exit
     }
     __syncwarp();
-  } else if (warp == 16 || warp == 17) {
+  } else if (warp >= 16 && warp < 16 + QST) {
     // ================================================================ query side: gather producers
-    // Warp 16 + s owns stage slot s and takes every second stage of 64 keys:
+    // Warp 16 + s owns stage slot s and takes every QST-th stage of 64 keys:
     // the staged dS^T rows as one TMA box per 64-head panel and the keys'
     // feature rows by cp.async; it waits only for its own copies, then fences
     // them for the tensor core and arrives.
@@ -354,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
     const int me = warp - 16;
     const T* kmain = static_cast<const T*>(p.k);
     const T* krope = static_cast<const T*>(p.kr);
-    const uint32_t a = smem_u32(smem + kQ + me * kQStage);
+    const uint32_t a = smem_u32(smem + QOFF + me * kQStage);
     const uint32_t b = a + kQA;
     int* rows = q_rows[me];
     int g = 0;
@@ -364,9 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
       const int tl = item / kQParts, part = item % kQParts;
       const int f0 = part * kQCol;
       for (int c = 0; c < qchunks; ++c, ++g) {
-        if (g % kQStages != me) continue;
+        if (g % QST != me) continue;
         const int2 r2 = *reinterpret_cast<const int2*>(p.rowtab + (size_t)tl * p.Kpad + c * kQSlots + 2 * lane);
-        if (lane == 0) ok = mbar_wait(&q_empty[me], ((g / kQStages) & 1) ^ 1, wt);
+        if (lane == 0) ok = mbar_wait(&q_empty[me], ((g / QST) & 1) ^ 1, wt);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         *reinterpret_cast<int2*>(rows + 2 * lane) = r2;
         __syncwarp();
@@ -374,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
         constexpr bool blk = BLK;
         if (lane == 0) {
           mbar_expect_tx(&q_full[me], kHP * kQSlots * 128 + (blk ? (kQCol / 64) * kQSlots * 128 : 0));
-          alog.arm(me, (uint32_t)(g / kQStages));
+          alog.arm(me, (uint32_t)(g / QST));
           for (int hp = 0; hp < kHP; ++hp)
             tma_2d(a + hp * (kQSlots * 128), &maps.dS, hp * 64, tl * p.Kpad + c * kQSlots, &q_full[me]);
         }
@@ -470,15 +478,18 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
 template <typename T, int GP>
 cudaError_t launch_gp(const Maps& maps, const Prob& p, float* acc, void* dq, void* dqr, int tile_group, bool part,
                       int* gerr, int nsm, cudaStream_t st) {
-  auto kern = p.bs >= 8 ? (part ? kvq_kernel<T, GP, true, true> : kvq_kernel<T, GP, true, false>)
-                        : (part ? kvq_kernel<T, GP, false, true> : kvq_kernel<T, GP, false, false>);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  const int tg = tile_group < 0 ? 0 : tile_group;
+  const bool qo = tg == 0;
+  auto kern = qo ? (p.bs >= 8 ? kvq_kernel<T, GP, true, false, true> : kvq_kernel<T, GP, false, false, true>)
+          : p.bs >= 8 ? (part ? kvq_kernel<T, GP, true, true, false> : kvq_kernel<T, GP, true, false, false>)
+                      : (part ? kvq_kernel<T, GP, false, true, false> : kvq_kernel<T, GP, false, false, false>);
+  const int smem = qo ? kSmemBytesQO : kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int nitems = p.ntok * kKvChunks;
   const int grid = nitems < nsm ? nitems : nsm;
   if (grid <= 0) return cudaSuccess;
-  const int tg = tile_group < 0 ? 0 : tile_group;
-  kern<<<grid, kThreads, kSmemBytes, st>>>(maps, p, acc, static_cast<T*>(dq), static_cast<T*>(dqr), tg, gerr);
+  kern<<<grid, kThreads, smem, st>>>(maps, p, acc, static_cast<T*>(dq), static_cast<T*>(dqr), tg, gerr);
   return cudaGetLastError();
 }
 
