@@ -221,10 +221,10 @@ def workload_desc(w, det, shared_kv=False):
 # token counts.  Reported only while the kernel source still hashes to the
 # value it had when the counters were taken.
 TRAFFIC = {
-    # ncu capture of the 512-token MLA profiling workload: 912.1 MB read + 81.7 MB written per launch
+    # not yet captured on the current source
     "kvq": {"sources": ["kvq.cu", "common.cuh"],
-             "sha256": "2fa6e2c8a39697e825dacc1801f3b7548e74743fa92c86089e72b65abc86c8ed",
-             "bytes_per_token": 993.8e6 / 512},
+             "sha256": None,
+             "bytes_per_token": None},
 }
 
 
@@ -247,13 +247,14 @@ def kernel_traffic(name, tokens):
 
 
 # Contraction work per valid (query, head, key) of each tensor-core kernel,
-# in flops: sdp recomputes S (576-deep) and dP (512-deep); kvq forms dV (512
-# features), [dK | dKRope] (576) and [dQ | dQRope] (576), only the last when
-# kvb has taken the key side; kvb forms dV and [dK | dKRope] per block.
-TENSOR_FLOPS = {"sdp": 2 * (576 + 512), "kvq": 2 * (512 + 576 + 576), "kvb": 2 * (512 + 576)}
+# in flops: sdp and sdpb recompute S (576-deep) and dP (512-deep); kvq forms
+# dV (512 features), [dK | dKRope] (576) and [dQ | dQRope] (576); kvb forms dV
+# and [dK | dKRope] per block; dqb forms [dQ | dQRope].
+TENSOR_FLOPS = {"sdp": 2 * (576 + 512), "sdpb": 2 * (576 + 512), "kvq": 2 * (512 + 576 + 576),
+                "kvb": 2 * (512 + 576), "dqb": 2 * 576}
 # Bytes a streaming kernel must move per valid (query, key) pair: det_reduce
-# reads each pair's 1088-float partial row once.
-STREAM_BYTES = {"det_reduce": 1088 * 4}
+# reads each pair's 1088-element bf16 partial row once.
+STREAM_BYTES = {"det_reduce": 1088 * 2}
 # L2-resident fp32 vector reductions (red.global.add.v4.f32, four key rows x
 # 128 B per warp instruction) measured on this GPU by a microbenchmark: the
 # ceiling of the key-side scatter, which never reaches DRAM.
@@ -269,13 +270,11 @@ def roofline(dname, names, qhk, pairs, k_ms, peaks, det):
     t = k_ms * 1e-3
     if dname in TENSOR_FLOPS:
         per = TENSOR_FLOPS[dname]
-        if dname == "kvq" and "kvb" in names:
-            per = 2 * 576
         achieved = qhk * per / t / 1e12
         peak = peaks["bf16_tflops"]
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "flops_per_query_head_key": per}
-        if dname == "kvq" and "kvb" not in names and not det:
+        if dname == "kvq" and not det:
             # the key side's scatter: 1088 fp32 reductions (4352 B) per pair
             gbs = pairs * 4352 / t / 1e9
             roof["l2_red"] = {"achieved_gbs": gbs, "ceiling_gbs": L2_RED_CEILING_GBS,

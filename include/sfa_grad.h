@@ -164,10 +164,10 @@ sfa_status sfa_grad_plan_info(const sfa_params* p, int64_t* chunk_tokens, int64_
  * intervals the events of sfa_grad_profile delimit): "batch_prefix" (TND),
  * "meta", "dsum", then per token chunk "rowtab" and either "sdp", "kvq"
  * (scores per token, then combined key-side and query-side contractions), or
- * "blk_count", "blk_scan", "blk_scatter", "sdpb", "kvb", "kvq" (block-sparse
+ * "blk_count", "blk_scan", "blk_scatter", "sdpb", "kvb", "dqb" (block-sparse
  * indices whose blocks many tokens select: pairs grouped by block start,
  * scores per block for packs of its tokens, key side accumulated per block,
- * then the query side alone; with deterministic = 1 the grouping is followed
+ * then dQ per token with the features on the MMA's rows; with deterministic = 1 the grouping is followed
  * by "blk_sort" and "blk_sort_long", each group's pairs in ascending (token,
  * index) order (groups of up to 1024 pairs, then longer ones), and "kvb" is
  * launched sparse_block_size times, once per block-start residue modulo the

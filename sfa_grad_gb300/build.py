@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "libsfa.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["api.cu", "sdp.cu", "sdpb.cu", "dq.cu", "prep.cu", "det.cu", "noalloc.cu", "kvq.cu", "kvb.cu"]
+SOURCES = ["api.cu", "sdp.cu", "sdpb.cu", "dq.cu", "prep.cu", "det.cu", "noalloc.cu", "kvq.cu", "kvb.cu", "dqb.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

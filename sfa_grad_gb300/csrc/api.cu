@@ -300,7 +300,7 @@ int kvq_tile_group(const Plan& P) {
 const char* const kChunkDet[] = {"rowtab", "sdp", "det_count", "det_scan", "det_scatter", "det_sort",
                                  "det_sort_long", "kvq", "det_reduce"};
 const char* const kChunkKvq[] = {"rowtab", "sdp", "kvq"};
-const char* const kChunkKvb[] = {"rowtab", "blk_count", "blk_scan", "blk_scatter", "sdpb", "kvb", "kvq"};
+const char* const kChunkKvb[] = {"rowtab", "blk_count", "blk_scan", "blk_scatter", "sdpb", "kvb", "dqb"};
 const char* const kChunkKvbDetHead[] = {"rowtab", "blk_count", "blk_scan", "blk_scatter", "blk_sort",
                                         "blk_sort_long", "sdpb"};
 
@@ -319,7 +319,7 @@ int64_t plan_names(const Plan& P, const char** out, int64_t cap) {
     if (P.kvb && P.det) {
       for (const char* s : kChunkKvbDetHead) put(s);
       for (int r = 0; r < P.bs; ++r) put("kvb");   // one launch per start residue
-      put("kvq");
+      put("dqb");
     } else if (P.det) {
       for (const char* s : kChunkDet) put(s);
     } else if (P.kvb) {
@@ -500,7 +500,8 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
         SFA_CK(launch_kvb<T>(bmaps, pr, P.bs, bgrp, bbeg, bng, bent, acc, -1, bres, gerr, nsm, st));
         SFA_CK(mk.mark(st));
       }
-      SFA_CK(launch_kvq<T>(maps, pr, acc, dq, P.has_rope ? dqr : nullptr, 0, false, gerr, nsm, st));   // query side only
+      // dQ with the features on the MMA's M (at most 64 heads here)
+      SFA_CK(launch_dqb<T>(maps, pr, dq, P.has_rope ? dqr : nullptr, gerr, nsm, st));
       SFA_CK(mk.mark(st));
     } else {
       SFA_CK(launch_kvq<T>(maps, pr, acc, dq, P.has_rope ? dqr : nullptr, kvq_tile_group(P), false, gerr, nsm, st));

@@ -1,0 +1,224 @@
+// dQ for block-sparse indices with at most 64 heads, features on the MMA's M:
+//     [dQ || dQRope](t)^T = [K || KRope]_sel(t)^T . dS(t)^T
+// (M = 128 features per tile, N = GN = G rounded up to 16 heads, K = keys),
+// accumulated in tensor memory over all of the token's selected keys.
+//
+// With heads on M (the query side of kvq.cu) a token of G = 16 heads fills
+// 16 of the MMA's 128 rows; here the 576 features fill M (four tiles of the
+// 512-wide part, a fifth for the 64 rope features) and the heads are N, so
+// no MMA row is padding.  The kernel is then bound by the L2-to-SM loads of
+// the selected key rows (1152 B per key), so a stage carries all 576
+// features of 64 keys and the token's staged dS rows once, and the ring is
+// as deep as shared memory allows (two stages of 80 KB).
+//
+// aclnnSparseFlashAttentionGrad doc, 功能说明 (selected blocks of
+// sparseBlockSize keys) and 阶段3 (dQ = dS . K * scale, with the scale folded
+// into dS); MindSpore flash_attention_bwd.py, update_dQi.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace sfa {
+
+namespace {
+
+constexpr int kKeys = 64;                  // keys per stage (MMA K extent)
+constexpr int kStages = 2;
+constexpr int kPanel = kKeys * 128;        // 64 keys x 64 features (or heads), 8 KB
+// stage layout, one panel each: [kRope | k 0-63 | ... | k 448-511 | dS].
+// Feature tile m < 4 is panels 2m+1, 2m+2; the rope tile is panels 0, 1, so
+// its rows 64-127 read k 0-63 (finite data whose results are never stored).
+constexpr int kStageBytes = 10 * kPanel;
+constexpr int kDsOff = 9 * kPanel;
+// warp 0: MMA issuer, warps 1-2: TMA producers (one per stage slot),
+// warps 3-6: epilogue (one per TMEM lane quadrant)
+constexpr int kThreads = (1 + kStages + 4) * 32;
+constexpr int kEpi0 = 1 + kStages;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+
+__device__ __forceinline__ uint32_t tile_off(int m) { return m < 4 ? (uint32_t)(2 * m + 1) * kPanel : 0u; }
+
+template <typename T, int GN>
+__global__ void __launch_bounds__(kThreads, 1) dqb_kernel(const __grid_constant__ Maps maps, Prob p, T* dq, T* dqr,
+                                                          int* gerr) {
+  using E = Elt<T>;
+  // five feature tiles per accumulator, each at a 32-column boundary
+  constexpr int TS = (GN + 31) / 32 * 32;
+  constexpr int kBufCols = 5 * TS;
+  constexpr int NBUF = 2 * kBufCols <= 512 ? 2 : 1;        // accumulator buffers
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t a_full[kStages], a_empty[kStages], t_full[NBUF], t_empty[NBUF], done_bar;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nst = p.Kpad / kKeys;          // stages per token
+  const int nt = p.has_rope ? 5 : 4;       // feature tiles
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&a_full[i], 1);
+      mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < NBUF; ++i) {
+      mbar_init(&t_full[i], 1);
+      mbar_init(&t_empty[i], 128);
+    }
+    mbar_init(&done_bar, 1);
+    abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0) tmem_alloc(&tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base;
+  const Waiter wt{&abort_flag, gerr, p.wait_ns};
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(128, GN, E::is_f16, true, true);
+      const uint64_t d0 = sdesc_mnmajor(smem_u32(smem), 0, kKeys);
+      int g = 0, it = 0;
+      bool ok = true;
+      for (int tl = blockIdx.x; tl < p.ntok && ok; tl += gridDim.x, ++it) {
+        const int buf = it % NBUF;
+        ok = mbar_wait_poll(&t_empty[buf], ((it / NBUF) & 1) ^ 1, wt);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d = tbase + buf * kBufCols;
+        for (int c = 0; c < nst; ++c, ++g) {
+          const int slot = g % kStages;
+          ok = mbar_wait_poll(&a_full[slot], (g / kStages) & 1, wt);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t so = slot * kStageBytes;
+          const uint64_t db = d0 + desc_off(so + kDsOff);
+          for (int m = 0; m < nt; ++m)
+            mma_ss_k64<128, 128>(d + m * TS, d0 + desc_off(so + tile_off(m)), db, idesc, c == 0 ? 0u : 1u);
+          mma_commit(&a_empty[slot]);
+        }
+        if (ok) mma_commit(&t_full[buf]);
+      }
+      mma_settle(&done_bar, gerr);   // no MMA still writing tensor memory at exit
+    }
+    __syncwarp();
+  } else if (warp < kEpi0) {
+    // ---------------------------------------------------------------- TMA producers
+    // Producer w (warps 1-2) fills slot w-1 for every second stage: the
+    // token's staged dS rows of 64 slots (one box; heads past Gs read as
+    // zeros) and, per selected block of the stage, one box of bs key rows per
+    // 64-feature panel.  An index with no key at or above 0, past the last
+    // row or past the index list reads rows below row 0: zeros.
+    if (lane == 0) {
+      const int me = warp - 1;
+      const int nidx = kKeys / p.bs;
+      const uint32_t tx = kPanel * (p.has_rope ? 10u : 9u);
+      int g = 0;
+      bool ok = true;
+      ArmLog alog;
+      for (int tl = blockIdx.x; tl < p.ntok && ok; tl += gridDim.x) {
+        const int t = p.tok0 + tl;
+        const long long kv0 = p.meta[t].kv_start;
+        for (int c = 0; c < nst && ok; ++c, ++g) {
+          const int slot = g % kStages;
+          if (slot != me) continue;
+          ok = mbar_wait(&a_empty[slot], ((g / kStages) & 1) ^ 1, wt);
+          if (!ok) break;
+          mbar_expect_tx(&a_full[slot], tx);
+          alog.arm(slot, (uint32_t)(g / kStages));
+          const uint32_t st = smem_u32(smem + slot * kStageBytes);
+          tma_2d(st + kDsOff, &maps.dS, 0, tl * p.Kpad + c * kKeys, &a_full[slot]);
+          for (int i = 0; i < nidx; ++i) {
+            const int ii = c * nidx + i;
+            int y = -p.bs;
+            if (ii < p.Kidx) {
+              const int r = __ldg(p.idx + (size_t)t * p.Kidx + ii);
+              const long long yy = kv0 + r;
+              if ((long long)r + p.bs > 0 && yy < p.T2) y = (int)yy;
+            }
+            const uint32_t dst = st + (uint32_t)(i * p.bs) * 128;
+            for (int pn = 0; pn < 8; ++pn) tma_2d(dst + (1 + pn) * kPanel, &maps.k, pn * 64, y, &a_full[slot]);
+            if (p.has_rope) tma_2d(dst, &maps.kr, 0, y, &a_full[slot]);
+          }
+        }
+      }
+      alog.settle(a_full, gerr);   // no copy still landing in shared memory at exit
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    // Warp w reads TMEM lane quadrant w % 4: thread = feature row f of a
+    // tile, GN head columns; a warp store covers 32 consecutive features of
+    // one head row (64 contiguous bytes).
+    const int qd = warp & 3;
+    int it = 0;
+    for (int tl = blockIdx.x; tl < p.ntok && !abort_flag; tl += gridDim.x, ++it) {
+      const int buf = it % NBUF;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&t_full[buf], (it / NBUF) & 1, wt));
+      if (!ok) break;
+      tc_fence_after();
+      const size_t t = (size_t)(p.tok0 + tl);
+      const uint32_t td = tbase + buf * kBufCols + ((uint32_t)(qd * 32) << 16);
+      for (int m = 0; m < nt; ++m) {
+        const int f = m * 128 + qd * 32 + lane;
+        float v[GN];
+#pragma unroll
+        for (int c0 = 0; c0 + 32 <= GN; c0 += 32) tmem_ld32(td + m * TS + c0, v + c0);
+        if constexpr (GN % 32 != 0) tmem_ld16(td + m * TS + (GN - 16), v + (GN - 16));
+        T* dst = nullptr;
+        size_t hs = 0;
+        if (f < 512) {
+          dst = dq + t * p.G * 512 + f;
+          hs = 512;
+        } else if (f < 576 && dqr) {
+          dst = dqr + t * p.G * 64 + (f - 512);
+          hs = 64;
+        }
+        if (dst) {
+#pragma unroll
+          for (int h = 0; h < GN; ++h)
+            if (h < p.G) dst[h * hs] = E::from_f(v[h]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&t_empty[buf]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <typename T, int GN>
+cudaError_t launch_g(const Maps& maps, const Prob& p, void* dq, void* dqr, int* gerr, int nsm, cudaStream_t st) {
+  auto kern = dqb_kernel<T, GN>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int grid = p.ntok < nsm ? p.ntok : nsm;
+  kern<<<grid, kThreads, kSmemBytes, st>>>(maps, p, static_cast<T*>(dq), static_cast<T*>(dqr), gerr);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+template <typename T>
+cudaError_t launch_dqb(const Maps& maps, const Prob& p, void* dq, void* dqr, int* gerr, int nsm, cudaStream_t st) {
+  if (p.ntok <= 0) return cudaSuccess;
+  if (p.bs < 16 || p.bs > kKeys || kKeys % p.bs != 0 || p.Kpad % kKeys != 0 || p.G > 64) return cudaErrorInvalidValue;
+  switch (p.Gs) {
+    case 16: return launch_g<T, 16>(maps, p, dq, dqr, gerr, nsm, st);
+    case 32: return launch_g<T, 32>(maps, p, dq, dqr, gerr, nsm, st);
+    case 48: return launch_g<T, 48>(maps, p, dq, dqr, gerr, nsm, st);
+    default: return launch_g<T, 64>(maps, p, dq, dqr, gerr, nsm, st);
+  }
+}
+
+template cudaError_t launch_dqb<__nv_bfloat16>(const Maps&, const Prob&, void*, void*, int*, int, cudaStream_t);
+template cudaError_t launch_dqb<__half>(const Maps&, const Prob&, void*, void*, int*, int, cudaStream_t);
+
+}  // namespace sfa

@@ -39,14 +39,19 @@ cudaError_t launch_sdpb(const Maps& maps, const Prob& p, const int* groups, cons
 
 // Key-side and query-side contractions in one launch, two pipelines per CTA
 // (kvq.cu): key-side reductions into acc, dQ / dQRope out.  tile_group: key
-// tiles per key-side work item (items run tile-group major; a group of all
-// tiles gives token-major order); 0 runs the query side only.  part:
+// tiles per key-side work item, at least 1 (items run tile-group major; a
+// group of all tiles gives token-major order).  part:
 // deterministic mode; acc is then the chunk's partial-row buffer (bf16
 // elements) and every valid (token, slot) row is stored there instead of
 // reduced.
 template <typename T>
 cudaError_t launch_kvq(const Maps& maps, const Prob& p, float* acc, void* dq, void* dqr, int tile_group, bool part,
                        int* gerr, int nsm, cudaStream_t st);
+
+// dQ / dQRope for block-sparse indices with at most 64 heads (dqb.cu):
+// features on the MMA's M, heads on N, over each token's selected blocks.
+template <typename T>
+cudaError_t launch_dqb(const Maps& maps, const Prob& p, void* dq, void* dqr, int* gerr, int nsm, cudaStream_t st);
 
 // Companion forward's output O = P V over each token's selected keys (dq.cu).
 template <typename T>

@@ -11,8 +11,8 @@
 // pipe mostly idle; the query side is bound by gathers and the tensor pipe.
 // Running both in the same CTA overlaps the two.  Key-side items run
 // token-major, or tile-group major when the accumulator rows a batch touches
-// exceed L2; with tile_group = 0 only the query side runs (the key side of
-// block indices is then done per block, kvb.cu).
+// exceed L2.  (Block indices that many tokens select take kvb.cu for the key
+// side and dqb.cu for dQ instead.)
 //
 // aclnnSparseFlashAttentionGrad doc, 阶段1 (dV = P^T dO) and 阶段3 (dQ, dK);
 // MindSpore flash_attention_bwd.py, update_dVj / update_dQi / update_dKj.
@@ -27,8 +27,7 @@ constexpr int kThreads = 640;   // 20 warps, roles below
 // warp 0: key-side MMA issuer          warp 1: key-side TMA producer
 // warp 2: query-side MMA issuer        warp 3: idle
 // warps 4-11: key-side drain           warps 12-15: query-side epilogue
-// warps 16-17: query-side gather producers, warps 18-19: idle (query side
-// alone: warps 16-19 are its producers)
+// warps 16-17: query-side gather producers, warps 18-19: idle
 constexpr int kDrainThreads = 256;
 
 constexpr int kKeys = 128;        // key-side tile (MMA M)
@@ -37,7 +36,6 @@ constexpr int kKvChunks = 9;      // dK 4 x 128 + dKRope 64, dV 4 x 128
 constexpr int kAccRow = 1088;
 constexpr int kQSlots = 64;       // query-side keys per stage (MMA K extent)
 constexpr int kQStages = 2;       // query-side stages next to the key side
-constexpr int kQStagesQO = 4;     // query side alone: its stages take the key side's shared memory
 constexpr int kQCol = 192;        // query-side features per item (MMA N)
 constexpr int kQParts = 3;
 
@@ -50,7 +48,6 @@ constexpr int kQ = kKvStg + 8 * 32 * 32 * 4;              // 2 stages x (A 16 KB
 constexpr int kQA = 2 * kQSlots * 128;
 constexpr int kQStage = kQA + (kQCol / 64) * kQSlots * 128;
 constexpr int kSmemBytes = kQ + kQStages * kQStage + 1024;
-constexpr int kSmemBytesQO = kQStagesQO * kQStage + 1024;
 
 // TMEM columns: key-side accumulators [0,128) and [128,256), query side [256,448)
 constexpr uint32_t kQCol0 = 256;
@@ -96,15 +93,12 @@ __device__ __forceinline__ void red_add_v4(float* dst, float4 x) {
 // bf16, as element (token_local * Kpad + slot) * 1088 of the bf16 array at
 // acc (the partial rows the fixed-order reduction of det.cu sums in fp32);
 // masked slots are not written.
-// QO: query side only (tile_group = 0): the key side's shared memory goes to
-// kQStagesQO query-side stages instead of kQStages, fed by as many producer
-// warps (16 ..).
-template <typename T, int GP, bool BLK, bool PART, bool QO>
+template <typename T, int GP, bool BLK, bool PART>
 __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant__ Maps maps, Prob p, float* acc,
                                                           T* dq, T* dqr, int tg, int* gerr) {
   using E = Elt<T>;
-  constexpr int QST = QO ? kQStagesQO : kQStages;   // query-side stages
-  constexpr int QOFF = QO ? 0 : kQ;                 // offset of the query-side stages
+  constexpr int QST = kQStages;   // query-side stages
+  constexpr int QOFF = kQ;        // offset of the query-side stages
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t kv_full[kKvStages], kv_empty[kKvStages], kv_tfull[2], kv_tempty[2], kv_bfull, kv_bempty;
@@ -115,7 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntiles = p.Kpad / kKeys;
-  const int nkv = tg > 0 ? (ntiles + tg - 1) / tg * p.ntok * kKvChunks : 0;   // tg = 0: query side only
+  const int nkv = (ntiles + tg - 1) / tg * p.ntok * kKvChunks;
   const int qchunks = p.Kpad / kQSlots;
   const int nq = p.ntok * kQParts;
 
@@ -478,18 +472,16 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
 template <typename T, int GP>
 cudaError_t launch_gp(const Maps& maps, const Prob& p, float* acc, void* dq, void* dqr, int tile_group, bool part,
                       int* gerr, int nsm, cudaStream_t st) {
-  const int tg = tile_group < 0 ? 0 : tile_group;
-  const bool qo = tg == 0;
-  auto kern = qo ? (p.bs >= 8 ? kvq_kernel<T, GP, true, false, true> : kvq_kernel<T, GP, false, false, true>)
-          : p.bs >= 8 ? (part ? kvq_kernel<T, GP, true, true, false> : kvq_kernel<T, GP, true, false, false>)
-                      : (part ? kvq_kernel<T, GP, false, true, false> : kvq_kernel<T, GP, false, false, false>);
-  const int smem = qo ? kSmemBytesQO : kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (tile_group < 1) return cudaErrorInvalidValue;
+  auto kern = p.bs >= 8 ? (part ? kvq_kernel<T, GP, true, true> : kvq_kernel<T, GP, true, false>)
+                        : (part ? kvq_kernel<T, GP, false, true> : kvq_kernel<T, GP, false, false>);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const int nitems = p.ntok * kKvChunks;
   const int grid = nitems < nsm ? nitems : nsm;
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, kThreads, smem, st>>>(maps, p, acc, static_cast<T*>(dq), static_cast<T*>(dqr), tg, gerr);
+  kern<<<grid, kThreads, kSmemBytes, st>>>(maps, p, acc, static_cast<T*>(dq), static_cast<T*>(dqr), tile_group,
+                                           gerr);
   return cudaGetLastError();
 }
 

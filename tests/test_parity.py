@@ -36,6 +36,7 @@ SMALL = {
     "g12_kvb_tnd_causal": small_workload(name="tnd_kvb", layout="TND", B=2, N1=12, K=6, block_size=16, mode=3,
                                          index_kind="causal", kv_extra=64, T1=40, act_q=(24, 16), seed=27),
     "g16_kvb_padding_dups": small_workload(N1=16, S1=32, S2=256, K=8, block_size=16, index_kind="random_any", seed=28),
+    "g64_kvb_bs32": small_workload(N1=64, S1=32, S2=512, K=8, block_size=32, index_kind="block", seed=38),
     # edge cases: a single index per token; a KV sequence shorter than one key tile, every key selected
     "g8_single_index": small_workload(N1=8, S1=6, S2=300, K=1, seed=29),
     "g32_short_kv_all": small_workload(N1=32, S1=5, S2=64, K=64, index_kind="all", seed=30),
