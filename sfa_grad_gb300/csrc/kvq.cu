@@ -119,8 +119,11 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
       uint4* z = reinterpret_cast<uint4*>(smem + QOFF + s * kQStage + kQSlots * 128);
       for (int i = threadIdx.x; i < kQSlots * 128 / 16; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
     }
-    fence_async_smem();
   }
+  // key side: the head-row panels start as zeros (the rope chunk loads one)
+  for (int i = threadIdx.x; i < 2 * GP * 128 / 16; i += kThreads)
+    reinterpret_cast<uint4*>(smem + kKvB)[i] = make_uint4(0, 0, 0, 0);
+  fence_async_smem();
   if (threadIdx.x == 0) {
     for (int i = 0; i < kKvStages; ++i) {
       mbar_init(&kv_full[i], 1);
@@ -158,11 +161,18 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
       bool ok = true;
       const uint64_t da0 = sdesc_kmajor(smem_u32(smem + kKvA), 0);
       const uint64_t db0 = sdesc_mnmajor(smem_u32(smem + kKvB), 0, GP);
+      // Reductions: [key slots x features] = [dS | P]^T (K-major, slots on M)
+      // . [q | qRope | dO] (MN-major, features on N).  Partial rows (PART):
+      // the transpose, [features x key slots] with features on M, so that
+      // the drain needs no shared-memory transposition; the rope chunk's
+      // second feature panel then holds no data (zeros or an earlier item's
+      // rows) and its rows of the result are not drained.
       for (int item = blockIdx.x; item < nkv && ok; item += gridDim.x, ++icount) {
         const KvItem ki = kv_item(item, p.ntok, ntiles, tg);
         int ncol, col0;
         kv_chunk(ki.ch, ncol, col0);
-        const uint32_t idesc = idesc_f16(kKeys, ncol, E::is_f16, false, true);
+        const uint32_t idesc = PART ? idesc_f16(128, kKeys, E::is_f16, true, false)
+                                    : idesc_f16(kKeys, ncol, E::is_f16, false, true);
         ok = mbar_wait_poll(&kv_bfull, icount & 1, wt);
         if (!ok) break;
         for (int kt = ki.kt0; kt < ki.kt1 && ok; ++kt, ++tcount) {
@@ -175,7 +185,10 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
             ok = mbar_wait_poll(&kv_full[stage], phase, wt);
             if (!ok) break;
             tc_fence_after();
-            mma_ss_k64<2, 128>(d, da0 + desc_off(stage * kKvAStage), db0 + (uint64_t)(hp * 512), idesc, hp > 0 ? 1u : 0u);
+            if constexpr (PART)
+              mma_ss_k64<128, 2>(d, db0 + (uint64_t)(hp * 512), da0 + desc_off(stage * kKvAStage), idesc, hp > 0 ? 1u : 0u);
+            else
+              mma_ss_k64<2, 128>(d, da0 + desc_off(stage * kKvAStage), db0 + (uint64_t)(hp * 512), idesc, hp > 0 ? 1u : 0u);
             mma_commit(&kv_empty[stage]);
             if (++stage == kKvStages) { stage = 0; phase ^= 1; }
           }
@@ -237,8 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
       alog_b.settle(&kv_bfull, gerr);
     }
     __syncwarp();
-  } else if (warp >= 4 && warp < 12) {
-    // ================================================================ key side: drain
+  } else if (!PART && warp >= 4 && warp < 12) {
+    // ================================================================ key side: reduction drain
     // Two groups of four warps take alternate tiles (group g drains TMEM
     // set g), so one group's reductions overlap the other group's TMEM loads
     // and staging instead of all eight warps pausing together.  Warp w of a
@@ -294,23 +307,85 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
             const int rl = rr * 4 + (lane >> 3), c4 = lane & 7;
             const float4 x = reinterpret_cast<const float4*>(stg + rl * 32)[c4 ^ (rl & 7)];
             const int grow = __shfl_sync(0xffffffffu, row, rl);
-            if constexpr (PART) {
-              // streaming store of the pair's row rounded to bf16 (read back
-              // once, after this kernel, and summed in fp32)
-              if (grow >= 0) {
-                uint2 h;
-                h.x = Elt<__nv_bfloat16>::pack(x.x, x.y);
-                h.y = Elt<__nv_bfloat16>::pack(x.z, x.w);
-                __stcs(reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(acc) +
-                                                ((size_t)ki.tl * p.Kpad + kt * kKeys + qd * 32 + rl) * kAccRow + col0 +
-                                                c + c4 * 4),
-                       h);
-              }
-            } else if (grow >= 0) {
-              red_add_v4(acc + (size_t)grow * kAccRow + col0 + c + c4 * 4, x);
-            }
+            if (grow >= 0) red_add_v4(acc + (size_t)grow * kAccRow + col0 + c + c4 * 4, x);
           }
           __syncwarp();
+        }
+        tc_fence_before();
+        mbar_arrive(&kv_tempty[set]);
+      }
+      if (!ok) break;
+    }
+  } else if (PART && warp >= 4 && warp < 12) {
+    // ================================================================ key side: partial-row drain
+    // Two groups of four warps take alternate tiles (group g drains TMEM
+    // set g), so one group's reductions overlap the other group's TMEM loads
+    // instead of all eight warps pausing together.  A tile is [features x
+    // key slots]: warp w of a group reads TMEM lanes (features) 32*(w%4) ..
+    // +31 and all 128 slot columns.  Adjacent lanes swap one value, so that
+    // each lane holds two consecutive features of one pair's row and one
+    // store instruction covers two rows x 64 contiguous bytes.
+    const int qd = warp & 3;
+    const int grp = (warp - 4) >> 2;
+    const int odd = lane & 1;
+    int tcount = 0;
+    // row ids of slots 32*s + lane of the group's next tile, loaded one tile ahead
+    auto rows_of = [&](int item, int kt, int* r) {
+      const int* rt = item < nkv ? p.rowtab + (size_t)kv_item(item, p.ntok, ntiles, tg).tl * p.Kpad + kt * kKeys : nullptr;
+#pragma unroll
+      for (int s = 0; s < 4; ++s) r[s] = rt ? rt[32 * s + lane] : -1;
+    };
+    auto advance = [&](int& item, int& kt) {
+      if (++kt == kv_item(item, p.ntok, ntiles, tg).kt1) {
+        item += gridDim.x;
+        kt = kv_item(item, p.ntok, ntiles, tg).kt0;
+      }
+    };
+    int nitem = blockIdx.x, nkt = kv_item(blockIdx.x, p.ntok, ntiles, tg).kt0;
+    if (grp) advance(nitem, nkt);
+    int next_rows[4];
+    rows_of(nitem, nkt, next_rows);
+    for (int item = blockIdx.x; item < nkv && !abort_flag; item += gridDim.x) {
+      const KvItem ki = kv_item(item, p.ntok, ntiles, tg);
+      const int ch = ki.ch;
+      int ncol, col0;
+      kv_chunk(ch, ncol, col0);
+      // first feature of this lane's pair
+      const int f = col0 + qd * 32 + lane - odd;
+      bool ok = true;
+      for (int kt = ki.kt0; kt < ki.kt1; ++kt, ++tcount) {
+        const int set = tcount & 1;
+        if (set != grp) continue;
+        int rows[4];
+#pragma unroll
+        for (int s = 0; s < 4; ++s) rows[s] = next_rows[s];
+        advance(nitem, nkt);
+        advance(nitem, nkt);
+        rows_of(nitem, nkt, next_rows);
+        ok = __all_sync(0xffffffffu, mbar_wait(&kv_tfull[set], (tcount >> 1) & 1, wt));
+        if (!ok) break;
+        tc_fence_after();
+        if (qd * 32 < ncol) {   // the rope chunk has 64 features: lanes 64-127 hold no result
+          const uint32_t td = tbase + set * 128 + ((uint32_t)(qd * 32) << 16);
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            float v[32];
+            tmem_ld32(td + 32 * s, v);
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              // even lane: features f, f+1 of slot j; odd lane: of slot j+1
+              const float x = __shfl_xor_sync(0xffffffffu, odd ? v[j] : v[j + 1], 1);
+              const float a = odd ? x : v[j], b = odd ? v[j + 1] : x;
+              const int grow = __shfl_sync(0xffffffffu, rows[s], j + odd);
+              // streaming store of the pair's row rounded to bf16 (read back
+              // once, after this kernel, and summed in fp32)
+              if (grow >= 0)
+                __stcs(reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(acc) +
+                                                   ((size_t)ki.tl * p.Kpad + kt * kKeys + 32 * s + j + odd) * kAccRow +
+                                                   f),
+                       Elt<__nv_bfloat16>::pack(a, b));
+            }
+          }
         }
         tc_fence_before();
         mbar_arrive(&kv_tempty[set]);
