@@ -221,10 +221,10 @@ def workload_desc(w, det, shared_kv=False):
 # token counts.  Reported only while the kernel source still hashes to the
 # value it had when the counters were taken.
 TRAFFIC = {
-    # not yet captured on the current source
+    # ncu capture of the 512-token MLA profiling workload: 913.7 MB read + 81.7 MB written per launch
     "kvq": {"sources": ["kvq.cu", "common.cuh"],
-             "sha256": None,
-             "bytes_per_token": None},
+             "sha256": "fc523270ca66ec1cafb7db7b79a5f9d6e0824fe6c5a3b1927afc36276ae77511",
+             "bytes_per_token": 995.4e6 / 512},
 }
 
 
@@ -256,9 +256,10 @@ TENSOR_FLOPS = {"sdp": 2 * (576 + 512), "sdpb": 2 * (576 + 512), "kvq": 2 * (512
 # reads each pair's 1088-element bf16 partial row once.
 STREAM_BYTES = {"det_reduce": 1088 * 2}
 # L2-resident fp32 vector reductions (red.global.add.v4.f32, four key rows x
-# 128 B per warp instruction) measured on this GPU by a microbenchmark: the
-# ceiling of the key-side scatter, which never reaches DRAM.
-L2_RED_CEILING_GBS = 6350.0
+# 128 B per warp instruction) measured on this GPU by bench_l2_red.cu
+# (`bench.py --l2-red-ceiling`): the ceiling of the key-side scatter, which
+# never reaches DRAM.
+L2_RED_CEILING_GBS = 7040.0
 
 
 def roofline(dname, names, qhk, pairs, k_ms, peaks, det):
@@ -279,7 +280,7 @@ def roofline(dname, names, qhk, pairs, k_ms, peaks, det):
             gbs = pairs * 4352 / t / 1e9
             roof["l2_red"] = {"achieved_gbs": gbs, "ceiling_gbs": L2_RED_CEILING_GBS,
                               "frac": gbs / L2_RED_CEILING_GBS,
-                              "ceiling_source": "red.global.add.v4.f32 microbenchmark on GB300 (152 SMs)"}
+                              "ceiling_source": "bench_l2_red.cu: red.global.add.v4.f32, 4 rows x 128 B per warp instruction, 152 SMs"}
         return roof
     per_b = STREAM_BYTES.get(dname)
     if per_b is None:
@@ -531,6 +532,20 @@ def run_forward(args):
     return 0
 
 
+def run_l2_red_ceiling():
+    """Builds and runs bench_l2_red.cu (L2-resident fp32 reduction rates by
+    instruction shape) and prints its JSON line."""
+    import tempfile
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "bench_l2_red.cu")
+    with tempfile.TemporaryDirectory() as d:
+        exe = os.path.join(d, "bench_l2_red")
+        nvcc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
+        subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-o", exe, src], check=True)
+        r = subprocess.run([exe], capture_output=True, text=True)
+        print(r.stdout.strip(), flush=True)
+        return r.returncode
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -545,7 +560,11 @@ def main():
     ap.add_argument("--forward", action="store_true", help="time the companion forward sfa_fwd instead")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per launch of the dominant kernel from an ncu capture")
+    ap.add_argument("--l2-red-ceiling", action="store_true",
+                    help="measure the L2 fp32 reduction ceiling (bench_l2_red.cu) and exit")
     args = ap.parse_args()
+    if args.l2_red_ceiling:
+        return run_l2_red_ceiling()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
