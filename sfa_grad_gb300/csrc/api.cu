@@ -91,8 +91,10 @@ sfa_status validate(const sfa_params* p, bool fwd, Plan* out) {
   // Used when blocks hold >= 16 keys, at most 64 heads, and the average kv
   // row is selected by >= 8 query tokens.  Deterministic mode sorts each
   // group's pairs and adds the groups in bs launches (one per start residue
-  // modulo bs, whose blocks share no key row).
-  P.kvb = !fwd && P.bs >= 16 && P.Gp == 64 && T2 > 0 && T1 * keff >= 8 * T2;
+  // modulo bs, whose blocks share no key row).  The companion forward scores
+  // the same groups per block (statistics, then P) and forms O per token with
+  // the features on the MMA's rows.
+  P.kvb = P.bs >= 16 && P.Gp == 64 && T2 > 0 && T1 * keff >= 8 * T2;
   // token chunking keeps the per-chunk staging bounded
   const size_t pds_per_tok = (size_t)P.Kpad * P.Gs * 2 * (fwd ? 1 : 2);
   size_t chunk = kPdsCap / pds_per_tok;
@@ -116,7 +118,8 @@ sfa_status validate(const sfa_params* p, bool fwd, Plan* out) {
   const size_t ents = chunk * (P.kvb ? P.Kidx : P.Kpad);   // sorted entries per chunk
   P.off_part = o; o += P.det && !P.kvb ? up(chunk * P.Kpad * kAccRow * 2) : 0;
   P.off_dscr = o; o += P.det ? up(2 * ents * 4) : 0;   // padded copies of long segments
-  P.off_tstats = o; o += fwd ? up(chunk * (P.Kpad / 128) * P.G * 2 * 4) : 0;
+  // forward partial statistics: per key tile of 128, or per block index
+  P.off_tstats = o; o += fwd ? up(chunk * (P.kvb ? P.Kidx : P.Kpad / 128) * P.G * 2 * 4) : 0;
   // counting-sort bins: block starts + bs (key-major blocks) or kv rows
   // (deterministic reduction), and the sorted entries
   const bool bins = P.kvb || P.det;
@@ -470,7 +473,7 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
       int* bbeg = reinterpret_cast<int*>(ws + P.off_bbeg);
       int* bng = reinterpret_cast<int*>(ws + P.off_bng);
       int* bent = reinterpret_cast<int*>(ws + P.off_bent);
-      SFA_CK(launch_blk_count(pr, bcnt, Pst, dSst, st));
+      SFA_CK(launch_blk_count(pr, bcnt, Pst, dSst, nullptr, st));
       SFA_CK(mk.mark(st));
       int* bres = reinterpret_cast<int*>(ws + P.off_bres);
       SFA_CK(launch_blk_scan(bcnt, P.T2 + P.bs, bcur, bgrp, bbeg, bng, P.bs, bres, st));
@@ -487,7 +490,7 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
       }
       // scores per block: each block's key / value rows loaded once for all
       // the tokens that select it
-      SFA_CK(launch_sdpb<T>(maps, pr, bgrp, bbeg, bng, bent, Pst, dSst, gerr, nsm, st));
+      SFA_CK(launch_sdpb<T>(maps, pr, kModeBwd, bgrp, bbeg, bng, bent, Pst, dSst, nullptr, gerr, nsm, st));
       SFA_CK(mk.mark(st));
       if (P.det) {
         // the groups in bs launches by start residue, so that no two tiles
@@ -501,7 +504,7 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
         SFA_CK(mk.mark(st));
       }
       // dQ with the features on the MMA's M (at most 64 heads here)
-      SFA_CK(launch_dqb<T>(maps, pr, dq, P.has_rope ? dqr : nullptr, gerr, nsm, st));
+      SFA_CK(launch_dqb<T>(maps, pr, false, dq, P.has_rope ? dqr : nullptr, gerr, nsm, st));
       SFA_CK(mk.mark(st));
     } else {
       SFA_CK(launch_kvq<T>(maps, pr, acc, dq, P.has_rope ? dqr : nullptr, kvq_tile_group(P), false, gerr, nsm, st));
@@ -652,10 +655,28 @@ sfa_status run_fwd(const Plan& P, const void* q, const void* k, const void* v, c
     pr.tok0 = t0;
     pr.ntok = (P.T1 - t0) < P.chunk ? (P.T1 - t0) : P.chunk;
     SFA_CK(launch_rowtab(pr, st));
-    SFA_CK(launch_sdp<T>(maps, pr, kModeFwdStats, nullptr, nullptr, ts, gerr, nsm, st));
-    SFA_CK(launch_stats_combine(pr, ts, smax, ssum, st));
-    SFA_CK(launch_sdp<T>(maps, pr, kModeFwdP, ws + P.off_P, nullptr, nullptr, gerr, nsm, st));
-    SFA_CK(launch_pv<T>(maps, pr, out, gerr, nsm, st));
+    if (P.kvb) {
+      // block indices that many tokens select: the pairs grouped by block
+      // start, statistics and P per block, O per token (features on M)
+      int* bcnt = reinterpret_cast<int*>(ws + P.off_bcnt);
+      int* bcur = reinterpret_cast<int*>(ws + P.off_bcur);
+      int* bgrp = reinterpret_cast<int*>(ws + P.off_bgrp);
+      int* bbeg = reinterpret_cast<int*>(ws + P.off_bbeg);
+      int* bng = reinterpret_cast<int*>(ws + P.off_bng);
+      int* bent = reinterpret_cast<int*>(ws + P.off_bent);
+      SFA_CK(launch_blk_count(pr, bcnt, ws + P.off_P, nullptr, ts, st));
+      SFA_CK(launch_blk_scan(bcnt, P.T2 + P.bs, bcur, bgrp, bbeg, bng, P.bs, nullptr, st));
+      SFA_CK(launch_blk_scatter(pr, bcur, bent, st));
+      SFA_CK(launch_sdpb<T>(maps, pr, kModeFwdStats, bgrp, bbeg, bng, bent, nullptr, nullptr, ts, gerr, nsm, st));
+      SFA_CK(launch_stats_combine(pr, ts, P.Kidx, smax, ssum, st));
+      SFA_CK(launch_sdpb<T>(maps, pr, kModeFwdP, bgrp, bbeg, bng, bent, ws + P.off_P, nullptr, nullptr, gerr, nsm, st));
+      SFA_CK(launch_dqb<T>(maps, pr, true, out, nullptr, gerr, nsm, st));
+    } else {
+      SFA_CK(launch_sdp<T>(maps, pr, kModeFwdStats, nullptr, nullptr, ts, gerr, nsm, st));
+      SFA_CK(launch_stats_combine(pr, ts, P.Kpad / 128, smax, ssum, st));
+      SFA_CK(launch_sdp<T>(maps, pr, kModeFwdP, ws + P.off_P, nullptr, nullptr, gerr, nsm, st));
+      SFA_CK(launch_pv<T>(maps, pr, out, gerr, nsm, st));
+    }
   }
   return SFA_OK;
 }

@@ -11,6 +11,9 @@
 // features of 64 keys and the token's staged dS rows once, and the ring is
 // as deep as shared memory allows (two stages of 80 KB).
 //
+// PV: the companion forward's O(t)^T = V_sel(t)^T . P(t)^T with the same
+// pipeline (value rows, the staged P rows, four feature tiles).
+//
 // aclnnSparseFlashAttentionGrad doc, 功能说明 (selected blocks of
 // sparseBlockSize keys) and 阶段3 (dQ = dS . K * scale, with the scale folded
 // into dS); MindSpore flash_attention_bwd.py, update_dQi.
@@ -37,7 +40,7 @@ constexpr int kSmemBytes = kStages * kStageBytes + 1024;
 
 __device__ __forceinline__ uint32_t tile_off(int m) { return m < 4 ? (uint32_t)(2 * m + 1) * kPanel : 0u; }
 
-template <typename T, int GN>
+template <typename T, int GN, bool PV>
 __global__ void __launch_bounds__(kThreads, 1) dqb_kernel(const __grid_constant__ Maps maps, Prob p, T* dq, T* dqr,
                                                           int* gerr) {
   using E = Elt<T>;
@@ -53,7 +56,8 @@ __global__ void __launch_bounds__(kThreads, 1) dqb_kernel(const __grid_constant_
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nst = p.Kpad / kKeys;          // stages per token
-  const int nt = p.has_rope ? 5 : 4;       // feature tiles
+  const bool rope = !PV && p.has_rope;
+  const int nt = rope ? 5 : 4;             // feature tiles
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -114,7 +118,9 @@ __global__ void __launch_bounds__(kThreads, 1) dqb_kernel(const __grid_constant_
     if (lane == 0) {
       const int me = warp - 1;
       const int nidx = kKeys / p.bs;
-      const uint32_t tx = kPanel * (p.has_rope ? 10u : 9u);
+      const uint32_t tx = kPanel * (rope ? 10u : 9u);
+      const CUtensorMap* mrow = PV ? &maps.v : &maps.k;
+      const CUtensorMap* mcol = PV ? &maps.P : &maps.dS;
       int g = 0;
       bool ok = true;
       ArmLog alog;
@@ -129,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1) dqb_kernel(const __grid_constant_
           mbar_expect_tx(&a_full[slot], tx);
           alog.arm(slot, (uint32_t)(g / kStages));
           const uint32_t st = smem_u32(smem + slot * kStageBytes);
-          tma_2d(st + kDsOff, &maps.dS, 0, tl * p.Kpad + c * kKeys, &a_full[slot]);
+          tma_2d(st + kDsOff, mcol, 0, tl * p.Kpad + c * kKeys, &a_full[slot]);
           for (int i = 0; i < nidx; ++i) {
             const int ii = c * nidx + i;
             int y = -p.bs;
@@ -139,8 +145,8 @@ __global__ void __launch_bounds__(kThreads, 1) dqb_kernel(const __grid_constant_
               if ((long long)r + p.bs > 0 && yy < p.T2) y = (int)yy;
             }
             const uint32_t dst = st + (uint32_t)(i * p.bs) * 128;
-            for (int pn = 0; pn < 8; ++pn) tma_2d(dst + (1 + pn) * kPanel, &maps.k, pn * 64, y, &a_full[slot]);
-            if (p.has_rope) tma_2d(dst, &maps.kr, 0, y, &a_full[slot]);
+            for (int pn = 0; pn < 8; ++pn) tma_2d(dst + (1 + pn) * kPanel, mrow, pn * 64, y, &a_full[slot]);
+            if (rope) tma_2d(dst, &maps.kr, 0, y, &a_full[slot]);
           }
         }
       }
@@ -195,8 +201,9 @@ __global__ void __launch_bounds__(kThreads, 1) dqb_kernel(const __grid_constant_
 }
 
 template <typename T, int GN>
-cudaError_t launch_g(const Maps& maps, const Prob& p, void* dq, void* dqr, int* gerr, int nsm, cudaStream_t st) {
-  auto kern = dqb_kernel<T, GN>;
+cudaError_t launch_g(const Maps& maps, const Prob& p, bool pv, void* dq, void* dqr, int* gerr, int nsm,
+                     cudaStream_t st) {
+  auto kern = pv ? dqb_kernel<T, GN, true> : dqb_kernel<T, GN, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = p.ntok < nsm ? p.ntok : nsm;
@@ -207,18 +214,19 @@ cudaError_t launch_g(const Maps& maps, const Prob& p, void* dq, void* dqr, int* 
 }  // namespace
 
 template <typename T>
-cudaError_t launch_dqb(const Maps& maps, const Prob& p, void* dq, void* dqr, int* gerr, int nsm, cudaStream_t st) {
+cudaError_t launch_dqb(const Maps& maps, const Prob& p, bool pv, void* dq, void* dqr, int* gerr, int nsm,
+                       cudaStream_t st) {
   if (p.ntok <= 0) return cudaSuccess;
   if (p.bs < 16 || p.bs > kKeys || kKeys % p.bs != 0 || p.Kpad % kKeys != 0 || p.G > 64) return cudaErrorInvalidValue;
   switch (p.Gs) {
-    case 16: return launch_g<T, 16>(maps, p, dq, dqr, gerr, nsm, st);
-    case 32: return launch_g<T, 32>(maps, p, dq, dqr, gerr, nsm, st);
-    case 48: return launch_g<T, 48>(maps, p, dq, dqr, gerr, nsm, st);
-    default: return launch_g<T, 64>(maps, p, dq, dqr, gerr, nsm, st);
+    case 16: return launch_g<T, 16>(maps, p, pv, dq, dqr, gerr, nsm, st);
+    case 32: return launch_g<T, 32>(maps, p, pv, dq, dqr, gerr, nsm, st);
+    case 48: return launch_g<T, 48>(maps, p, pv, dq, dqr, gerr, nsm, st);
+    default: return launch_g<T, 64>(maps, p, pv, dq, dqr, gerr, nsm, st);
   }
 }
 
-template cudaError_t launch_dqb<__nv_bfloat16>(const Maps&, const Prob&, void*, void*, int*, int, cudaStream_t);
-template cudaError_t launch_dqb<__half>(const Maps&, const Prob&, void*, void*, int*, int, cudaStream_t);
+template cudaError_t launch_dqb<__nv_bfloat16>(const Maps&, const Prob&, bool, void*, void*, int*, int, cudaStream_t);
+template cudaError_t launch_dqb<__half>(const Maps&, const Prob&, bool, void*, void*, int*, int, cudaStream_t);
 
 }  // namespace sfa

@@ -19,8 +19,10 @@ cudaError_t launch_sdp(const Maps& maps, const Prob& p, int mode, void* out_p, v
 // (deterministic mode; entries sorted within each group): only the groups
 // whose start is res modulo bs, whose blocks share no key row.
 // pst / dsst (optional): the staged P^T / dS^T; the rows no group covers
-// (pairs left out, padding slots) are zeroed.
-cudaError_t launch_blk_count(const Prob& p, int* cnt, void* pst, void* dsst, cudaStream_t st);
+// (pairs left out, padding slots) are zeroed.  tile_stats (optional, the
+// forward's per-pair statistics): a left-out pair's entries are set to
+// {-inf, 0}.
+cudaError_t launch_blk_count(const Prob& p, int* cnt, void* pst, void* dsst, float* tile_stats, cudaStream_t st);
 // nres (optional, bs entries): non-empty bins per residue modulo bs.
 cudaError_t launch_blk_scan(const int* cnt, int nbins, int* cursor, int* groups, int* gbeg, int* ngroups, int bs,
                             int* nres, cudaStream_t st);
@@ -31,11 +33,15 @@ cudaError_t launch_kvb(const BlkMaps& maps, const Prob& p, int bs, const int* gr
                        int nsm, cudaStream_t st);
 
 // Key-major scores for block-sparse indices (sdpb.cu): per group of pairs
-// sharing a block start, S and dP of packs of 128 / GK tokens against the
-// block's resident key / value rows; writes the pairs' staged P^T / dS^T rows.
+// sharing a block start, S (and dP) of packs of 128 / GK tokens against the
+// block's resident key (and value) rows.  mode kModeBwd writes the pairs'
+// staged P^T / dS^T rows; kModeFwdStats the pairs' partial statistics
+// (tile_stats, (token, index, head) x {max, sum}); kModeFwdP the staged P^T
+// rows from the final statistics.
 template <typename T>
-cudaError_t launch_sdpb(const Maps& maps, const Prob& p, const int* groups, const int* gbeg, const int* ngroups,
-                        const int* entries, void* pst, void* dsst, int* gerr, int nsm, cudaStream_t st);
+cudaError_t launch_sdpb(const Maps& maps, const Prob& p, int mode, const int* groups, const int* gbeg,
+                        const int* ngroups, const int* entries, void* pst, void* dsst, float* tile_stats, int* gerr,
+                        int nsm, cudaStream_t st);
 
 // Key-side and query-side contractions in one launch, two pipelines per CTA
 // (kvq.cu): key-side reductions into acc, dQ / dQRope out.  tile_group: key
@@ -50,8 +56,11 @@ cudaError_t launch_kvq(const Maps& maps, const Prob& p, float* acc, void* dq, vo
 
 // dQ / dQRope for block-sparse indices with at most 64 heads (dqb.cu):
 // features on the MMA's M, heads on N, over each token's selected blocks.
+// pv: the companion forward's O = P V instead (value rows, staged P; dq is
+// the output, dqr unused).
 template <typename T>
-cudaError_t launch_dqb(const Maps& maps, const Prob& p, void* dq, void* dqr, int* gerr, int nsm, cudaStream_t st);
+cudaError_t launch_dqb(const Maps& maps, const Prob& p, bool pv, void* dq, void* dqr, int* gerr, int nsm,
+                       cudaStream_t st);
 
 // Companion forward's output O = P V over each token's selected keys (dq.cu).
 template <typename T>
@@ -68,7 +77,9 @@ template <typename T>
 cudaError_t launch_dsum(const Prob& p, int tok0, int ntok, float* dsum, cudaStream_t st);
 template <typename T>
 cudaError_t launch_cast(const float* acc, int T2, void* dk, void* dkr, void* dv, int has_rope, cudaStream_t st);
-cudaError_t launch_stats_combine(const Prob& p, const float* tile_stats, float* smax, float* ssum, cudaStream_t st);
+// ntiles: partial statistics per token (key tiles of 128, or block indices).
+cudaError_t launch_stats_combine(const Prob& p, const float* tile_stats, int ntiles, float* smax, float* ssum,
+                                 cudaStream_t st);
 
 // Records a message for sfa_last_error_message on the calling thread (api.cu).
 void set_last_error(const char* msg);

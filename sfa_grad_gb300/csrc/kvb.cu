@@ -52,7 +52,7 @@ __device__ __forceinline__ bool pair_start(const Prob& p, long long i, int& bin)
 // zeroes the staged P^T / dS^T rows that the key-major score kernel (sdpb.cu)
 // does not write: those of pairs left out of every group and of the padding
 // slots past K * bs, which the query-side contraction still reads.
-__global__ void blk_count_kernel(Prob p, int* cnt, uint8_t* pst, uint8_t* dsst, int rowbytes) {
+__global__ void blk_count_kernel(Prob p, int* cnt, uint8_t* pst, uint8_t* dsst, float* ts, int rowbytes) {
   const int nb = p.Kpad / p.bs;   // index positions per token, padding included
   const long long n = (long long)p.ntok * nb;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
@@ -60,11 +60,16 @@ __global__ void blk_count_kernel(Prob p, int* cnt, uint8_t* pst, uint8_t* dsst, 
     int bin;
     if (ii < p.Kidx && pair_start(p, (long long)tl * p.Kidx + ii, bin)) {
       atomicAdd(cnt + bin, 1);
-    } else if (pst) {
-      const size_t off = ((size_t)tl * p.Kpad + (size_t)ii * p.bs) * rowbytes;
-      uint4* a = reinterpret_cast<uint4*>(pst + off);
-      uint4* b = reinterpret_cast<uint4*>(dsst + off);
-      for (int k = 0; k < p.bs * rowbytes / 16; ++k) a[k] = b[k] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const size_t off = ((size_t)tl * p.Kpad + (size_t)ii * p.bs) * rowbytes;
+    for (int k = 0; k < p.bs * rowbytes / 16; ++k) {
+      if (pst) reinterpret_cast<uint4*>(pst + off)[k] = make_uint4(0, 0, 0, 0);
+      if (dsst) reinterpret_cast<uint4*>(dsst + off)[k] = make_uint4(0, 0, 0, 0);
+    }
+    if (ts && ii < p.Kidx) {
+      float2* e = reinterpret_cast<float2*>(ts) + ((size_t)tl * p.Kidx + ii) * p.G;
+      for (int h = 0; h < p.G; ++h) e[h] = make_float2(-INFINITY, 0.f);
     }
   }
 }
@@ -348,13 +353,14 @@ __global__ void __launch_bounds__(kThreads, 1) kvb_kernel(const __grid_constant_
 
 }  // namespace
 
-cudaError_t launch_blk_count(const Prob& p, int* cnt, void* pst, void* dsst, cudaStream_t st) {
+cudaError_t launch_blk_count(const Prob& p, int* cnt, void* pst, void* dsst, float* tile_stats, cudaStream_t st) {
   if (p.ntok <= 0 || p.T2 <= 0) return cudaSuccess;
   cudaError_t e = cudaMemsetAsync(cnt, 0, (size_t)(p.T2 + p.bs) * sizeof(int), st);
   if (e != cudaSuccess) return e;
   const long long n = (long long)p.ntok * (p.Kpad / p.bs);
   const int grid = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
-  blk_count_kernel<<<grid, 256, 0, st>>>(p, cnt, static_cast<uint8_t*>(pst), static_cast<uint8_t*>(dsst), p.Gs * 2);
+  blk_count_kernel<<<grid, 256, 0, st>>>(p, cnt, static_cast<uint8_t*>(pst), static_cast<uint8_t*>(dsst), tile_stats,
+                                         p.Gs * 2);
   return cudaGetLastError();
 }
 

@@ -200,11 +200,11 @@ cudaError_t launch_cast(const float* acc, int T2, void* dk, void* dkr, void* dv,
   return cudaGetLastError();
 }
 
-cudaError_t launch_stats_combine(const Prob& p, const float* tile_stats, float* smax, float* ssum, cudaStream_t st) {
+cudaError_t launch_stats_combine(const Prob& p, const float* tile_stats, int ntiles, float* smax, float* ssum,
+                                 cudaStream_t st) {
   const int n = p.ntok * p.G;
   if (n == 0) return cudaSuccess;
-  stats_combine_kernel<<<(n + 255) / 256, 256, 0, st>>>(tile_stats, p.ntok, p.Kpad / 128, p.G, p.tok0, p.scale, smax,
-                                                        ssum);
+  stats_combine_kernel<<<(n + 255) / 256, 256, 0, st>>>(tile_stats, p.ntok, ntiles, p.G, p.tok0, p.scale, smax, ssum);
   return cudaGetLastError();
 }
 

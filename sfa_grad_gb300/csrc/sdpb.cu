@@ -19,6 +19,11 @@
 // memory the resident block leaves: five 16 KB stages, one producer warp
 // each.
 //
+// The companion forward's two score passes use the same kernel without dP:
+// MODE kModeFwdStats writes per pair and head the max of the raw scores over
+// the block's valid keys and the sum of exp((s - max) * scale) (combined per
+// token afterwards), MODE kModeFwdP writes P from the final statistics.
+//
 // aclnnSparseFlashAttentionGrad doc, 功能说明 (selected blocks of
 // sparseBlockSize keys) and 阶段1/阶段2 (dP, dS); MindSpore
 // flash_attention_bwd.py, compute_Pij and compute_dSij.
@@ -40,10 +45,11 @@ constexpr int kStageBytes = kRows * 128;   // one 64-feature panel of the pack
 __host__ __device__ constexpr int kv_bytes(int bs) { return 17 * bs * 128; }
 __host__ __device__ constexpr int smem_bytes(int bs) { return kv_bytes(bs) + kStages * kStageBytes + 1024; }
 
-template <typename T, int BS, int GK>
+template <typename T, int BS, int GK, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) sdpb_kernel(const __grid_constant__ Maps maps, Prob p, const int* groups,
                                                            const int* gbeg, const int* ngroups_p, const int* entries,
-                                                           T* pst, T* dsst, int* gerr) {
+                                                           T* pst, T* dsst, float* tile_stats, int* gerr) {
+  constexpr bool bwd = MODE == kModeBwd;
   using E = Elt<T>;
   constexpr int TPK = kRows / GK;          // tokens per pack
   constexpr int kPanel = BS * 128;         // one 64-feature panel of the block's rows
@@ -58,7 +64,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpb_kernel(const __grid_constant
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ngroups = *ngroups_p;
   const int nS = p.has_rope ? 9 : 8;       // stages of the score contraction
-  const int nc = nS + 8;                    // + 8 of dP
+  const int nc = bwd ? nS + 8 : nS;        // + 8 of dP
   const int Gs = p.Gs;
 
   // pack rows past TPK * GK (GK = 48) never receive a box: zero them once
@@ -152,11 +158,12 @@ __global__ void __launch_bounds__(kThreads, 1) sdpb_kernel(const __grid_constant
           if (kvn > 0) ok = mbar_wait(&kv_empty, (kvn - 1) & 1, wt);
           if (!ok) break;
           const int y0 = __ldg(groups + k) - BS;   // first key row (may be below 0: zeros)
-          mbar_expect_tx(&kv_full, (uint32_t)(nS + 8) * kPanel);
+          mbar_expect_tx(&kv_full, (uint32_t)(bwd ? nS + 8 : nS) * kPanel);
           klog.arm(0, (uint32_t)kvn);
           for (int pn = 0; pn < 8; ++pn) tma_2d(smem_u32(kv + pn * kPanel), &maps.k, pn * 64, y0, &kv_full);
           if (p.has_rope) tma_2d(smem_u32(kv + 8 * kPanel), &maps.kr, 0, y0, &kv_full);
-          for (int pn = 0; pn < 8; ++pn) tma_2d(smem_u32(kv + (9 + pn) * kPanel), &maps.v, pn * 64, y0, &kv_full);
+          if (bwd)
+            for (int pn = 0; pn < 8; ++pn) tma_2d(smem_u32(kv + (9 + pn) * kPanel), &maps.v, pn * 64, y0, &kv_full);
         }
         for (int j = 0; j < npk && ok; ++j) {
           // the pack's first head rows, once per pack (a missing token of the
@@ -231,22 +238,23 @@ __global__ void __launch_bounds__(kThreads, 1) sdpb_kernel(const __grid_constant
     };
     struct Meta {
       int ridx, lim;
-      size_t row0;
+      size_t row0, sidx;
       float m, linv, dsc;
     };
     auto meta_of = [&](int pr) {
-      Meta d{0, -1, 0, 0.f, 0.f, 0.f};
+      Meta d{0, -1, 0, 0, 0.f, 0.f, 0.f};
       if (pr < 0) return d;
       const int tl = pr / p.Kidx, ii = pr - tl * p.Kidx;
       const int t = p.tok0 + tl;
       d.ridx = __ldg(p.idx + (size_t)t * p.Kidx + ii);
       d.lim = p.meta[t].limit;
       d.row0 = (size_t)tl * p.Kpad + (size_t)ii * BS;
-      if (h < p.G) {
+      d.sidx = (size_t)pr * p.G + h;
+      if (MODE != kModeFwdStats && h < p.G) {
         const float l = __ldg(p.ssum + (size_t)t * p.G + h);
         d.m = l > 0.f ? __ldg(p.smax + (size_t)t * p.G + h) * kLog2e : 0.f;
         d.linv = l > 0.f ? 1.f / l : 0.f;
-        d.dsc = __ldg(p.dsum + (size_t)t * p.G + h) * p.scale;
+        if (bwd) d.dsc = __ldg(p.dsum + (size_t)t * p.G + h) * p.scale;
       }
       return d;
     };
@@ -265,29 +273,59 @@ __global__ void __launch_bounds__(kThreads, 1) sdpb_kernel(const __grid_constant
       if (!ok) break;
       tc_fence_after();
       const uint32_t td = tbase + set * (2 * BS) + ((uint32_t)((warp & 3) * 32) << 16);
-      const bool store = has && h < Gs;
-      T* op = pst + mc.row0 * Gs + h;
-      T* od = dsst + mc.row0 * Gs + h;
       constexpr int CH = BS < 32 ? BS : 32;   // key columns per TMEM load
-#pragma unroll 1
-      for (int u0 = 0; u0 < BS; u0 += CH) {
-        float s[CH], dp[CH];
-        if constexpr (CH == 32) {
-          tmem_ld32(td + u0, s);
-          tmem_ld32(td + BS + u0, dp);
-        } else {
-          tmem_ld16(td + u0, s);
-          tmem_ld16(td + BS + u0, dp);
-        }
-        if (store) {
+      if constexpr (MODE == kModeFwdStats) {
+        // the pair's partial statistics per (token, head) row: max of the raw
+        // scores over the block's valid keys and the sum of exp((s - max) * scale)
+        float sv[BS];
 #pragma unroll
-          for (int u = 0; u < CH; ++u) {
-            const int key = mc.ridx + u0 + u;
-            const bool valid = key >= 0 && key <= mc.lim;
-            const float pp = valid ? ex2(fmaf(s[u], sl2, -mc.m)) * mc.linv : 0.f;
-            const float dd = pp != 0.f ? pp * fmaf(dp[u], p.scale, -mc.dsc) : 0.f;
-            op[(size_t)(u0 + u) * Gs] = E::from_f(pp);
-            od[(size_t)(u0 + u) * Gs] = E::from_f(dd);
+        for (int u0 = 0; u0 < BS; u0 += CH) {
+          if constexpr (CH == 32) tmem_ld32(td + u0, sv + u0);
+          else tmem_ld16(td + u0, sv + u0);
+        }
+        if (has && h < p.G) {
+          float mx = -INFINITY;
+#pragma unroll
+          for (int u = 0; u < BS; ++u) {
+            const int key = mc.ridx + u;
+            if (key >= 0 && key <= mc.lim) mx = fmaxf(mx, sv[u]);
+          }
+          float l = 0.f;
+          if (mx != -INFINITY) {
+#pragma unroll
+            for (int u = 0; u < BS; ++u) {
+              const int key = mc.ridx + u;
+              if (key >= 0 && key <= mc.lim) l += ex2((sv[u] - mx) * sl2);
+            }
+          }
+          reinterpret_cast<float2*>(tile_stats)[mc.sidx] = make_float2(mx, l);
+        }
+      } else {
+        const bool store = has && h < Gs;
+        T* op = pst + mc.row0 * Gs + h;
+        T* od = bwd ? dsst + mc.row0 * Gs + h : nullptr;
+#pragma unroll 1
+        for (int u0 = 0; u0 < BS; u0 += CH) {
+          float s[CH], dp[CH];
+          if constexpr (CH == 32) {
+            tmem_ld32(td + u0, s);
+            if (bwd) tmem_ld32(td + BS + u0, dp);
+          } else {
+            tmem_ld16(td + u0, s);
+            if (bwd) tmem_ld16(td + BS + u0, dp);
+          }
+          if (store) {
+#pragma unroll
+            for (int u = 0; u < CH; ++u) {
+              const int key = mc.ridx + u0 + u;
+              const bool valid = key >= 0 && key <= mc.lim;
+              const float pp = valid ? ex2(fmaf(s[u], sl2, -mc.m)) * mc.linv : 0.f;
+              op[(size_t)(u0 + u) * Gs] = E::from_f(pp);
+              if (bwd) {
+                const float dd = pp != 0.f ? pp * fmaf(dp[u], p.scale, -mc.dsc) : 0.f;
+                od[(size_t)(u0 + u) * Gs] = E::from_f(dd);
+              }
+            }
           }
         }
       }
@@ -309,41 +347,51 @@ __global__ void __launch_bounds__(kThreads, 1) sdpb_kernel(const __grid_constant
 }
 
 template <typename T, int BS, int GK>
-cudaError_t launch_bg(const Maps& maps, const Prob& p, const int* groups, const int* gbeg, const int* ngroups,
-                      const int* entries, void* pst, void* dsst, int* gerr, int nsm, cudaStream_t st) {
-  auto kern = sdpb_kernel<T, BS, GK>;
+cudaError_t launch_bg(const Maps& maps, const Prob& p, int mode, const int* groups, const int* gbeg, const int* ngroups,
+                      const int* entries, void* pst, void* dsst, float* tile_stats, int* gerr, int nsm,
+                      cudaStream_t st) {
+  auto kern = mode == kModeFwdStats ? sdpb_kernel<T, BS, GK, kModeFwdStats>
+              : mode == kModeFwdP   ? sdpb_kernel<T, BS, GK, kModeFwdP>
+                                    : sdpb_kernel<T, BS, GK, kModeBwd>;
   const int smem = smem_bytes(BS) > kOneCtaSmem ? smem_bytes(BS) : kOneCtaSmem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   kern<<<nsm, kThreads, smem, st>>>(maps, p, groups, gbeg, ngroups, entries, static_cast<T*>(pst),
-                                    static_cast<T*>(dsst), gerr);
+                                    static_cast<T*>(dsst), tile_stats, gerr);
   return cudaGetLastError();
 }
 
 template <typename T, int BS>
-cudaError_t launch_b(const Maps& maps, const Prob& p, const int* groups, const int* gbeg, const int* ngroups,
-                     const int* entries, void* pst, void* dsst, int* gerr, int nsm, cudaStream_t st) {
+cudaError_t launch_b(const Maps& maps, const Prob& p, int mode, const int* groups, const int* gbeg, const int* ngroups,
+                     const int* entries, void* pst, void* dsst, float* tile_stats, int* gerr, int nsm,
+                     cudaStream_t st) {
   const int gk = (p.G + 15) / 16 * 16;
-  if (gk == 16) return launch_bg<T, BS, 16>(maps, p, groups, gbeg, ngroups, entries, pst, dsst, gerr, nsm, st);
-  if (gk == 32) return launch_bg<T, BS, 32>(maps, p, groups, gbeg, ngroups, entries, pst, dsst, gerr, nsm, st);
-  if (gk == 48) return launch_bg<T, BS, 48>(maps, p, groups, gbeg, ngroups, entries, pst, dsst, gerr, nsm, st);
-  return launch_bg<T, BS, 64>(maps, p, groups, gbeg, ngroups, entries, pst, dsst, gerr, nsm, st);
+  if (gk == 16)
+    return launch_bg<T, BS, 16>(maps, p, mode, groups, gbeg, ngroups, entries, pst, dsst, tile_stats, gerr, nsm, st);
+  if (gk == 32)
+    return launch_bg<T, BS, 32>(maps, p, mode, groups, gbeg, ngroups, entries, pst, dsst, tile_stats, gerr, nsm, st);
+  if (gk == 48)
+    return launch_bg<T, BS, 48>(maps, p, mode, groups, gbeg, ngroups, entries, pst, dsst, tile_stats, gerr, nsm, st);
+  return launch_bg<T, BS, 64>(maps, p, mode, groups, gbeg, ngroups, entries, pst, dsst, tile_stats, gerr, nsm, st);
 }
 
 }  // namespace
 
 template <typename T>
-cudaError_t launch_sdpb(const Maps& maps, const Prob& p, const int* groups, const int* gbeg, const int* ngroups,
-                        const int* entries, void* pst, void* dsst, int* gerr, int nsm, cudaStream_t st) {
+cudaError_t launch_sdpb(const Maps& maps, const Prob& p, int mode, const int* groups, const int* gbeg,
+                        const int* ngroups, const int* entries, void* pst, void* dsst, float* tile_stats, int* gerr,
+                        int nsm, cudaStream_t st) {
   if (p.ntok <= 0 || p.T2 <= 0) return cudaSuccess;
-  if (p.bs == 16) return launch_b<T, 16>(maps, p, groups, gbeg, ngroups, entries, pst, dsst, gerr, nsm, st);
-  if (p.bs == 32) return launch_b<T, 32>(maps, p, groups, gbeg, ngroups, entries, pst, dsst, gerr, nsm, st);
-  return launch_b<T, 64>(maps, p, groups, gbeg, ngroups, entries, pst, dsst, gerr, nsm, st);
+  if (p.bs == 16)
+    return launch_b<T, 16>(maps, p, mode, groups, gbeg, ngroups, entries, pst, dsst, tile_stats, gerr, nsm, st);
+  if (p.bs == 32)
+    return launch_b<T, 32>(maps, p, mode, groups, gbeg, ngroups, entries, pst, dsst, tile_stats, gerr, nsm, st);
+  return launch_b<T, 64>(maps, p, mode, groups, gbeg, ngroups, entries, pst, dsst, tile_stats, gerr, nsm, st);
 }
 
-template cudaError_t launch_sdpb<__nv_bfloat16>(const Maps&, const Prob&, const int*, const int*, const int*,
-                                                const int*, void*, void*, int*, int, cudaStream_t);
-template cudaError_t launch_sdpb<__half>(const Maps&, const Prob&, const int*, const int*, const int*, const int*,
-                                         void*, void*, int*, int, cudaStream_t);
+template cudaError_t launch_sdpb<__nv_bfloat16>(const Maps&, const Prob&, int, const int*, const int*, const int*,
+                                                const int*, void*, void*, float*, int*, int, cudaStream_t);
+template cudaError_t launch_sdpb<__half>(const Maps&, const Prob&, int, const int*, const int*, const int*,
+                                         const int*, void*, void*, float*, int*, int, cudaStream_t);
 
 }  // namespace sfa
