@@ -5,6 +5,8 @@ No GPU."""
 import os
 import sys
 
+import pytest
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
 import bench  # noqa: E402
@@ -27,3 +29,17 @@ def test_traffic_null_when_source_differs(monkeypatch):
     monkeypatch.setitem(bench.TRAFFIC, "kvq", ent)
     assert bench.kernel_traffic("kvq", 4096) is None
     assert bench.kernel_traffic("sdp", 4096) is None
+
+
+def test_l2_red_microbenchmark_compiles(tmp_path):
+    """bench.py --l2-red-ceiling builds bench_l2_red.cu for sm_103a; the
+    source must compile (nvcc cross-compiles without a GPU)."""
+    import shutil
+    import subprocess
+    nvcc = shutil.which("nvcc") or os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not available")
+    src = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "bench_l2_red.cu")
+    r = subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-o", str(tmp_path / "b"), src],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr

@@ -64,12 +64,16 @@ def test_backward_wait_timeout_then_recovery(name):
         compare(f"{name}/{n}", x, ref[n], w.dtype)
 
 
-def test_forward_wait_timeout_then_recovery():
-    w, _ = CASES["atomic"]
+# the per-token forward (score statistics, P, P.V) and the per-block one
+# (statistics and P per block start, O with the features on the MMA's rows)
+@pytest.mark.parametrize("name", ["atomic", "kvb"])
+def test_forward_wait_timeout_then_recovery(name):
+    w, _ = CASES[name]
     inp = make_inputs_cached(w)
     dev = {k: to_cuda(v) for k, v in inp.items()}
     kw = gpu_call_kwargs(w, dev)
-    p = sfa.make_params(dev["q"], dev["k"], dev["indices"], w.scale_value, sparse_mode=w.mode)
+    p = sfa.make_params(dev["q"], dev["k"], dev["indices"], w.scale_value, sparse_mode=w.mode,
+                        sparse_block_size=w.block_size)
     ws = torch.empty(max(sfa.fwd_workspace_size(p), 256), dtype=torch.uint8, device="cuda")
     sfa.fwd(dev["q"], dev["k"], dev["v"], dev["indices"], w.scale_value, workspace=ws, wait_limit_us=1, **kw)
     torch.cuda.synchronize()
@@ -78,7 +82,7 @@ def test_forward_wait_timeout_then_recovery():
     torch.cuda.synchronize()
     assert sfa.read_device_error(ws) == 0
     ro, _, _ = oracle.sfa_fwd(**oracle_kwargs(w, inp))
-    compare("fwd/out", o, ro, w.dtype)
+    compare(f"fwd_{name}/out", o, ro, w.dtype)
 
 
 _CACHE = {}
