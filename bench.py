@@ -216,15 +216,20 @@ def workload_desc(w, det, shared_kv=False):
             + (" value=key" if shared_kv else ""))
 
 
-# DRAM bytes (read + write) per query token of one launch, from an ncu capture
-# of the MLA-shaped 512-token profiling workload, scaled by tokens for other
-# token counts.  Reported only while the kernel source still hashes to the
-# value it had when the counters were taken.
+# DRAM bytes (read + write) per query token of one launch, from ncu captures
+# of 512-token profiling workloads, scaled by tokens for other token counts of
+# the same shape (heads, indices per token, block size, mode): the per-token
+# traffic of another shape differs.  Reported only while the kernel source
+# still hashes to the value it had when the counters were taken.
 TRAFFIC = {
-    # ncu capture of the 512-token MLA profiling workload: 913.7 MB read + 81.7 MB written per launch
     "kvq": {"sources": ["kvq.cu", "common.cuh"],
-             "sha256": "fc523270ca66ec1cafb7db7b79a5f9d6e0824fe6c5a3b1927afc36276ae77511",
-             "bytes_per_token": 995.4e6 / 512},
+            "sha256": "fc523270ca66ec1cafb7db7b79a5f9d6e0824fe6c5a3b1927afc36276ae77511",
+            "shapes": [
+                # mla_q512: 913.7 MB read + 81.7 MB written per launch
+                {"N1": 128, "K": 2048, "bs": 1, "det": False, "bytes_per_token": 995.4e6 / 512},
+                # mla_q512 --deterministic: 926.8 MB read + 2313.8 MB written (bf16 partial rows)
+                {"N1": 128, "K": 2048, "bs": 1, "det": True, "bytes_per_token": 3240.6e6 / 512},
+            ]},
 }
 
 
@@ -237,13 +242,19 @@ def _source_hash(files):
     return h.hexdigest()
 
 
-def kernel_traffic(name, tokens):
+def kernel_traffic(name, tokens, shape):
+    """Recorded DRAM bytes of `name` for `tokens` query tokens of `shape`
+    (dict with N1, K, bs, det), or None when no capture of that shape on the
+    current source exists."""
     ent = TRAFFIC.get(name)
-    if not ent or ent["sha256"] is None or ent["bytes_per_token"] is None:
+    if not ent or ent["sha256"] is None:
         return None
     if _source_hash(ent["sources"]) != ent["sha256"]:
         return None
-    return ent["bytes_per_token"] * tokens
+    for sh in ent["shapes"]:
+        if all(sh[k] == shape.get(k) for k in ("N1", "K", "bs", "det")):
+            return sh["bytes_per_token"] * tokens
+    return None
 
 
 # Contraction work per valid (query, head, key) of each tensor-core kernel,
@@ -439,7 +450,8 @@ def run_sfa(args):
     if args.traffic is not None:
         roof["traffic"] = args.traffic                        # given per launch
     else:
-        tr = kernel_traffic(dname, p.T1)                      # all tokens of the step
+        shape = {"N1": w.N1, "K": w.K, "bs": w.block_size, "det": bool(det)}
+        tr = kernel_traffic(dname, p.T1, shape)               # all tokens of the step
         roof["traffic"] = None if tr is None else tr / k_n    # per launch
     if roof["traffic"] is not None:
         # the kernel's measured DRAM traffic over its mean launch time, against

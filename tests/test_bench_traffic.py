@@ -18,17 +18,24 @@ def test_recorded_traffic_matches_committed_source():
     changed and was not recaptured yet) reports no traffic."""
     for name, ent in bench.TRAFFIC.items():
         if ent["sha256"] is None:
-            assert bench.kernel_traffic(name, 4096) is None
+            for sh in ent["shapes"]:
+                assert bench.kernel_traffic(name, 4096, sh) is None
             continue
         assert bench._source_hash(ent["sources"]) == ent["sha256"], f"{name} changed since its ncu capture: recapture"
-        assert bench.kernel_traffic(name, 4096) == ent["bytes_per_token"] * 4096
+        for sh in ent["shapes"]:
+            assert bench.kernel_traffic(name, 4096, sh) == sh["bytes_per_token"] * 4096
 
 
-def test_traffic_null_when_source_differs(monkeypatch):
+def test_traffic_only_for_the_captured_shape(monkeypatch):
+    """Another head count, index count, block size or mode has another
+    per-token traffic: no figure is reported for it."""
+    sh = dict(bench.TRAFFIC["kvq"]["shapes"][0])
+    for k, v in (("N1", 64), ("K", 8192), ("bs", 64)):
+        assert bench.kernel_traffic("kvq", 4096, dict(sh, **{k: v})) is None
     ent = dict(bench.TRAFFIC["kvq"], sha256="0" * 64)
     monkeypatch.setitem(bench.TRAFFIC, "kvq", ent)
-    assert bench.kernel_traffic("kvq", 4096) is None
-    assert bench.kernel_traffic("sdp", 4096) is None
+    assert bench.kernel_traffic("kvq", 4096, sh) is None
+    assert bench.kernel_traffic("sdp", 4096, sh) is None
 
 
 def test_l2_red_microbenchmark_compiles(tmp_path):
