@@ -162,23 +162,27 @@ sfa_status sfa_grad_plan_info(const sfa_params* p, int64_t* chunk_tokens, int64_
 /*
  * Names of the kernels one sfa_grad call launches, in launch order (the
  * intervals the events of sfa_grad_profile delimit): "batch_prefix" (TND),
- * "meta", "dsum", then per token chunk "rowtab" and either "sdp", "kvq"
- * (scores per token, then combined key-side and query-side contractions), or
- * "blk_count", "blk_scan", "blk_scatter", "sdpb", "kvb", "dqb" (block-sparse
- * indices whose blocks many tokens select: pairs grouped by block start,
- * scores per block for packs of its tokens, key side accumulated per block,
- * then dQ per token with the features on the MMA's rows; with deterministic = 1 the grouping is followed
- * by "blk_sort" and "blk_sort_long", each group's pairs in ascending (token,
- * index) order (groups of up to 1024 pairs, then longer ones), and "kvb" is
- * launched sparse_block_size times, once per block-start residue modulo the
- * block size), or with deterministic = 1 and single-key or rarely shared
- * indices "sdp", "det_count", "det_scan", "det_scatter", "det_sort",
- * "det_sort_long" (entries sorted by kv row, then token and slot), "kvq" (the
- * key side stored as per-pair partial rows, with the query side),
- * "det_reduce"; finally "cast".  Writes at most `capacity`
- * pointers to static strings into names[] (names may be null when capacity
- * is 0) and the total count into *count (may be null).  Host only; validates
- * *p like sfa_grad_workspace_size.
+ * "meta", "dsum", then per token chunk either
+ *   "rowtab", "sdp", "kvq" (row table of the chunk's slots, scores per token,
+ *   then combined key-side and query-side contractions), or
+ *   "blk_count", "blk_scan", "blk_scatter", "sdpb", "kvb", "dqb" (block-sparse
+ *   indices whose blocks many tokens select: pairs grouped by block start,
+ *   scores per block for packs of its tokens, key side accumulated per block,
+ *   then dQ per token with the features on the MMA's rows; with
+ *   deterministic = 1 the grouping is followed by "blk_sort" and
+ *   "blk_sort_long", each group's pairs in ascending (token, index) order
+ *   (groups of up to 1024 pairs, then longer ones), and "kvb" is launched
+ *   sparse_block_size times, once per block-start residue modulo the block
+ *   size), or
+ *   with deterministic = 1 and single-key or rarely shared indices "rowtab",
+ *   "sdp", "det_count", "det_scan", "det_scatter", "det_sort",
+ *   "det_sort_long" (entries sorted by kv row, then token and slot), "kvq"
+ *   (the key side stored as per-pair partial rows, with the query side),
+ *   "det_reduce";
+ * finally "cast".  Writes at most `capacity` pointers to static strings into
+ * names[] (names may be null when capacity is 0) and the total count into
+ * *count (may be null).  Host only; validates *p like
+ * sfa_grad_workspace_size.
  */
 sfa_status sfa_grad_plan_names(const sfa_params* p, const char** names, int32_t capacity, int32_t* count);
 

@@ -114,7 +114,7 @@ sfa_status validate(const sfa_params* p, bool fwd, Plan* out) {
   P.off_acc = o; o += fwd ? 0 : up((size_t)P.T2 * kAccRow * 4);
   P.off_P = o; o += up(chunk * P.Kpad * P.Gs * 2);
   P.off_dS = o; o += fwd ? 0 : up(chunk * P.Kpad * P.Gs * 2);
-  P.off_rows = o; o += up(chunk * P.Kpad * 4);
+  P.off_rows = o; o += P.kvb ? 0 : up(chunk * P.Kpad * 4);   // the key-major block plan reads no row table
   const size_t ents = chunk * (P.kvb ? P.Kidx : P.Kpad);   // sorted entries per chunk
   P.off_part = o; o += P.det && !P.kvb ? up(chunk * P.Kpad * kAccRow * 2) : 0;
   P.off_dscr = o; o += P.det ? up(2 * ents * 4) : 0;   // padded copies of long segments
@@ -303,9 +303,8 @@ int kvq_tile_group(const Plan& P) {
 const char* const kChunkDet[] = {"rowtab", "sdp", "det_count", "det_scan", "det_scatter", "det_sort",
                                  "det_sort_long", "kvq", "det_reduce"};
 const char* const kChunkKvq[] = {"rowtab", "sdp", "kvq"};
-const char* const kChunkKvb[] = {"rowtab", "blk_count", "blk_scan", "blk_scatter", "sdpb", "kvb", "dqb"};
-const char* const kChunkKvbDetHead[] = {"rowtab", "blk_count", "blk_scan", "blk_scatter", "blk_sort",
-                                        "blk_sort_long", "sdpb"};
+const char* const kChunkKvb[] = {"blk_count", "blk_scan", "blk_scatter", "sdpb", "kvb", "dqb"};
+const char* const kChunkKvbDetHead[] = {"blk_count", "blk_scan", "blk_scatter", "blk_sort", "blk_sort_long", "sdpb"};
 
 int64_t plan_names(const Plan& P, const char** out, int64_t cap) {
   int64_t n = 0;
@@ -434,9 +433,9 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
     }
     void* Pst = ws + P.off_P;
     void* dSst = ws + P.off_dS;
-    SFA_CK(launch_rowtab(pr, st));
-    SFA_CK(mk.mark(st));
-    if (!P.kvb) {   // block indices that many tokens select: scores per block below
+    if (!P.kvb) {   // block indices that many tokens select: no row table, scores per block below
+      SFA_CK(launch_rowtab(pr, st));
+      SFA_CK(mk.mark(st));
       SFA_CK(launch_sdp<T>(maps, pr, kModeBwd, Pst, dSst, nullptr, gerr, nsm, st));
       SFA_CK(mk.mark(st));
     }
@@ -654,7 +653,6 @@ sfa_status run_fwd(const Plan& P, const void* q, const void* k, const void* v, c
   for (int t0 = 0; t0 < P.T1; t0 += P.chunk) {
     pr.tok0 = t0;
     pr.ntok = (P.T1 - t0) < P.chunk ? (P.T1 - t0) : P.chunk;
-    SFA_CK(launch_rowtab(pr, st));
     if (P.kvb) {
       // block indices that many tokens select: the pairs grouped by block
       // start, statistics and P per block, O per token (features on M)
@@ -672,6 +670,7 @@ sfa_status run_fwd(const Plan& P, const void* q, const void* k, const void* v, c
       SFA_CK(launch_sdpb<T>(maps, pr, kModeFwdP, bgrp, bbeg, bng, bent, ws + P.off_P, nullptr, nullptr, gerr, nsm, st));
       SFA_CK(launch_dqb<T>(maps, pr, true, out, nullptr, gerr, nsm, st));
     } else {
+      SFA_CK(launch_rowtab(pr, st));
       SFA_CK(launch_sdp<T>(maps, pr, kModeFwdStats, nullptr, nullptr, ts, gerr, nsm, st));
       SFA_CK(launch_stats_combine(pr, ts, P.Kpad / 128, smax, ssum, st));
       SFA_CK(launch_sdp<T>(maps, pr, kModeFwdP, ws + P.off_P, nullptr, nullptr, gerr, nsm, st));

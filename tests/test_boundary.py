@@ -121,7 +121,7 @@ def test_plan_names(sfa):
     assert mla == ["meta", "dsum", "rowtab", "sdp", "kvq", "cast"]
     assert sfa.plan_info(_p(sfa, S1=4096, S2=4096, N1=128, K=2048))[1] == len(mla)
     blk = sfa.plan_names(_p(sfa, dtype=1, B=2, S1=8192, S2=32768, N1=16, K=64, sparse_block_size=64))
-    chunk = ["rowtab", "blk_count", "blk_scan", "blk_scatter", "sdpb", "kvb", "dqb"]
+    chunk = ["blk_count", "blk_scan", "blk_scatter", "sdpb", "kvb", "dqb"]
     assert blk[:2] == ["meta", "dsum"] and blk[-1] == "cast"
     ctok, nl = sfa.plan_info(_p(sfa, dtype=1, B=2, S1=8192, S2=32768, N1=16, K=64, sparse_block_size=64))
     nchunks = (2 * 8192 + ctok - 1) // ctok
@@ -138,7 +138,7 @@ def test_plan_names(sfa):
     # kvb launch per block-start residue
     bdet = sfa.plan_names(_p(sfa, dtype=1, B=2, S1=8192, S2=32768, N1=16, K=64, sparse_block_size=64,
                              deterministic=1))
-    cdet = (["rowtab", "blk_count", "blk_scan", "blk_scatter", "blk_sort", "blk_sort_long", "sdpb"] + ["kvb"] * 64
+    cdet = (["blk_count", "blk_scan", "blk_scatter", "blk_sort", "blk_sort_long", "sdpb"] + ["kvb"] * 64
             + ["dqb"])
     assert bdet[2:2 + len(cdet)] == cdet and "det_reduce" not in bdet
     assert sfa.plan_info(_p(sfa, dtype=1, B=2, S1=8192, S2=32768, N1=16, K=64, sparse_block_size=64,
