@@ -588,18 +588,18 @@ std::vector<int> host_bounds(int T1, int cap, double ratio, int tmin) {
 }
 
 // Schedule parameters from the problem shape.  Kernel time per query token
-// ~ Kpad x Gp x 9 ps (measured on GB300: MLA 10.3, long context 10.5,
-// block-sparse 8.0 ps per slot and padded head); copy time per token = its
-// input bytes at 200 GB/s (pinned host memory measured at 211 GB/s).  The
-// ratio is 0.9 of that estimate, kept within [1.25, 8] (causal TND runs
-// slower per slot than the estimate, which only makes its ramp cautious).
-// The tail stops halving at the chunk whose dQ readback takes ~0.1 ms at
-// 190 GB/s, and at 128 tokens at least.  On MLA the ramp (x1.25) beat even
-// splits into 4, 8 or 16 chunks and ramps of x1.5 and x1.15; on the
-// block-sparse workload the shape-derived ramp (x8, tail 1000 tokens) took
-// 36.8 against 39.0 ms for x1.25.
+// ~ Kpad x Gp x 9 ps (measured on GB300: MLA 10.3, long context 10.5 ps per
+// slot and padded head), or 4 ps on the key-major block plan (block-sparse
+// workload 3.9 ps); copy time per token = its input bytes at 200 GB/s
+// (pinned host memory measured at 211 GB/s).  The ratio is 0.9 of that
+// estimate, kept within [1.25, 8] (causal TND runs slower per slot than the
+// estimate, which only makes its ramp cautious).  The tail stops halving at
+// the chunk whose dQ readback takes ~0.1 ms at 190 GB/s, and at 128 tokens
+// at least.  On MLA the ramp (x1.25) beat even splits into 4, 8 or 16 chunks
+// and ramps of x1.5 and x1.15; on the block-sparse workload ramps of x2, x4
+// and x8 took 21.2, 20.6 and 20.9 ms end to end (the estimate gives x3.7).
 void host_schedule(const Plan& P, double* ratio, int* tmin) {
-  const double g = P.G, kernel_s = (double)P.Kpad * P.Gp * 9e-12;
+  const double g = P.G, kernel_s = (double)P.Kpad * P.Gp * (P.kvb ? 4e-12 : 9e-12);
   const double copy_s = (g * (3 * 512 + (P.has_rope ? 64 : 0)) * 2 + (double)P.Kidx * 4 + 2 * g * 4) / 200e9;
   double r = 0.9 * kernel_s / copy_s;
   *ratio = r < 1.25 ? 1.25 : r > 8.0 ? 8.0 : r;
