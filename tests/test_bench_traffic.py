@@ -50,3 +50,22 @@ def test_l2_red_microbenchmark_compiles(tmp_path):
     r = subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-o", str(tmp_path / "b"), src],
                        capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_roofline_arithmetic():
+    """The bench's roofline object: algorithmic flops (or bytes) per unit of
+    the dominant kernel over its time, against the measured peak."""
+    peaks = {"bf16_tflops": 2000.0, "hbm_gbs": 7000.0}
+    qhk, pairs, ms = 1 << 30, (1 << 30) // 128, 7.5
+    r = bench.roofline("kvq", [], qhk, pairs, ms, peaks, False)
+    assert r["bound"] == "tensor" and r["flops_per_query_head_key"] == 3328
+    assert abs(r["achieved"] - qhk * 3328 / 7.5e-3 / 1e12) < 1e-9
+    assert abs(r["frac"] - r["achieved"] / 2000.0) < 1e-12
+    # the key-side scatter's rate against the reduction ceiling, atomic mode only
+    assert abs(r["l2_red"]["achieved_gbs"] - pairs * 4352 / 7.5e-3 / 1e9) < 1e-6
+    assert "l2_red" not in bench.roofline("kvq", [], qhk, pairs, ms, peaks, True)
+    for name, per in (("sdp", 2176), ("sdpb", 2176), ("kvb", 2176), ("dqb", 1152)):
+        assert bench.roofline(name, [], qhk, pairs, ms, peaks, False)["flops_per_query_head_key"] == per
+    d = bench.roofline("det_reduce", [], qhk, pairs, ms, peaks, True)
+    assert d["bound"] == "hbm" and d["bytes_per_pair"] == 2176
+    assert abs(d["frac"] - pairs * 2176 / 7.5e-3 / 1e9 / 7000.0) < 1e-12
