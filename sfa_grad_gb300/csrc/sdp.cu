@@ -11,10 +11,11 @@
 //
 // Pipeline: the contraction runs in stages of 128 features (64 for the rope
 // part).  The gathered key/value rows (A) and the token's head rows (B) have
-// separate rings.  A: four slots, each owned by a producer warp that takes
-// every fourth stage, copies 256 contiguous bytes per gathered row by cp.async
-// (scattered 128-byte pieces halve the achievable gather rate) and waits only
-// for its own copies, so up to four gathers are in flight.  B: two slots
+// separate rings.  A: four slots (five with 64 heads), each owned by a
+// producer warp that takes every fourth (fifth) stage, copies 256 contiguous
+// bytes per gathered row by cp.async (scattered 128-byte pieces halve the
+// achievable gather rate) and waits only for its own copies, so up to four
+// (five) gathers are in flight.  B: two slots
 // filled by TMA from one thread.  Both operands of a stage complete on one
 // barrier, so the MMA issuer waits once per stage.  Compile-time variants:
 // value = key (one gathered stage feeds both contractions) and block indices
@@ -31,14 +32,19 @@ namespace sfa {
 namespace {
 
 constexpr int kKeys = 128;           // keys per work item (MMA M)
-constexpr int kSlots = 4;            // gathered-operand slots = gather producer warps
 constexpr int kBSlots = 2;           // head-row operand slots (TMA)
-constexpr int kMaxSlots = 4;         // barrier arrays sized for either ring layout
+constexpr int kGatherWarps = 5;
+constexpr int kMaxSlots = 5;         // barrier arrays sized for every ring layout
 constexpr int kEpiThreads = 256;     // warps 4-11
-// warp 0: MMA issuer; warps 1-3 and 12: gather producers (slots 0-2, 3);
-// warps 4-11: epilogue; warp 13: TMA producer of the head-row operand
-constexpr int kThreads = 14 * 32;
+// warp 0: MMA issuer; warps 1-3, 12 and 14: gather producers (slots 0-2, 3,
+// 4; a warp without a slot of the layout idles); warps 4-11: epilogue;
+// warp 13: TMA producer of the head-row operand
+constexpr int kThreads = 15 * 32;
 
+// The gathered rows are the stream that sets the kernel's pace (their bytes
+// in flight per SM over the L2 latency), so they get the shared memory the
+// head rows leave: four 32 KB slots with 128 heads, five with 64 (the head-row
+// slots are half as large).
 // SH: key and value are the same tensor.  A gathered stage of key rows then
 // serves both the score and the dP contraction, so half as many rows are
 // gathered; the rings become two gathered slots (two producer warps each,
@@ -46,7 +52,7 @@ constexpr int kThreads = 14 * 32;
 // stage are both resident).
 template <int GP, bool SH>
 struct SdpSmem {
-  static constexpr int kNA = SH ? 2 : kSlots;            // gathered slots
+  static constexpr int kNA = SH ? 2 : (GP == 64 ? 5 : 4);   // gathered slots
   static constexpr int kNB = SH ? 4 : kBSlots;           // head-row slots
   static constexpr int kPanelA = kKeys * 128;   // 64 features x 128 key rows
   static constexpr int kPanelB = GP * 128;      // 64 features x GP head rows
@@ -86,10 +92,10 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
   // arrivals each producer made on full_bar (head-row TMA thread per slot;
   // gather warps), for the wind-down that completes every phase one of them
   // started
-  __shared__ int arr_tma[kMaxSlots], arr_gat[4];
+  __shared__ int arr_tma[kMaxSlots], arr_gat[kGatherWarps];
   __shared__ float red_buf[4][GP][2];
   __shared__ float stats_s[2][3 * GP];
-  __shared__ __align__(16) int rows_s[4][kKeys];        // one per gather warp; read and written as int4
+  __shared__ __align__(16) int rows_s[kGatherWarps][kKeys];   // one per gather warp; read and written as int4
   __shared__ uint4 epi_stage[8][32 * 4];                 // epilogue row transposition, 2 KB per warp
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -120,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
     }
     mbar_init(&done_bar, 1);
     for (int i = 0; i < kMaxSlots; ++i) arr_tma[i] = 0;
-    for (int i = 0; i < 4; ++i) arr_gat[i] = 0;
+    for (int i = 0; i < kGatherWarps; ++i) arr_gat[i] = 0;
     abort_flag = 0;
     mbar_fence_init();
   }
@@ -244,11 +250,11 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
       }
     }
     __syncwarp();
-  } else if (warp <= 3 || warp == 12) {
+  } else if (warp <= 3 || warp == 12 || warp == 14) {
     // ---------------------------------------------------------------- gather producers
     // Without SH warp me owns slot me and all 128 rows of its stages; with SH
     // warps 2s and 2s+1 share slot s, one half of the rows each.
-    const int me = warp == 12 ? 3 : warp - 1;
+    const int me = warp == 12 ? 3 : warp == 14 ? 4 : warp - 1;
     const int slot = SH ? (me >> 1) : me;
     const int r0 = SH ? (me & 1) * (kKeys / 2) : 0;
     const int r1 = SH ? r0 + kKeys / 2 : kKeys;
@@ -503,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
       constexpr int kTShare = SH ? 2 : 1;                // head-row arrivals per phase
       int n[3], sh[3], nr = 0;
       n[nr] = arr_tma[s], sh[nr++] = kTShare;
-      for (int w = 0; w < 4; ++w)
+      for (int w = 0; w < kGatherWarps; ++w)
         if ((SH ? (w >> 1) : w) == s) n[nr] = arr_gat[w], sh[nr++] = 32;
       int klo = 1 << 30, khi = 0;
       for (int r = 0; r < nr; ++r) {
