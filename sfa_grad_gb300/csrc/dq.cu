@@ -18,8 +18,10 @@ namespace sfa {
 namespace {
 
 constexpr int kSlots = 64;         // keys per pipeline stage (MMA K extent)
-constexpr int kStages = 3;        // stage slots = producer warps 1-3
-constexpr int kThreads = 256;
+constexpr int kStages = 4;        // stage slots = producer warps 1-4
+// warp 0: MMA issuer, warps 1-4: producers, warps 5-8: epilogue (TMEM lane
+// quadrant = warp % 4)
+constexpr int kThreads = (1 + kStages + 4) * 32;
 
 template <int NCOL>
 struct DqSmem {
@@ -189,9 +191,9 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
       }
     }
     alog.settle(full_bar, gerr);   // no copy still landing in shared memory at exit
-  } else if (warp >= 4) {
+  } else if (warp > kStages) {
     // ---------------------------------------------------------------- epilogue (thread = head)
-    const int ew = warp - 4;
+    const int ew = warp & 3;   // the TMEM lane quadrant this warp may read
     const int h = ew * 32 + lane;
     int it = 0;
     for (int item = blockIdx.x; item < nitems && !abort_flag; item += gridDim.x, ++it) {
