@@ -18,28 +18,34 @@ namespace sfa {
 namespace {
 
 constexpr int kSlots = 64;         // keys per pipeline stage (MMA K extent)
-constexpr int kStages = 4;        // stage slots = producer warps 1-4
-// warp 0: MMA issuer, warps 1-4: producers, warps 5-8: epilogue (TMEM lane
-// quadrant = warp % 4)
-constexpr int kThreads = (1 + kStages + 4) * 32;
-
-template <int NCOL>
+// A stage: the staged P / dS of 64 keys (one 64-head panel per 64 heads),
+// then the gathered rows' feature panels.  With 64 heads the MMA's rows
+// 64-127 read the stage's first feature panel (the A operand's second
+// 64-row atom lies one panel further on): finite data whose results are
+// never stored; the stage is smaller and one more fits.
+// warp 0: MMA issuer, warps 1..NST: producers (one per stage slot), then four
+// epilogue warps (TMEM lane quadrant = warp % 4)
+template <int NCOL, int GP>
 struct DqSmem {
-  static constexpr int kA = 2 * kSlots * 128;            // two 64-head panels (heads 0-63, 64-127)
+  static constexpr int kA = (GP / 64) * kSlots * 128;    // head panels
   static constexpr int kB = (NCOL / 64) * kSlots * 128;  // feature panels
   static constexpr int kStage = kA + kB;
-  static constexpr int kBytes = kStages * kStage + 1024;
+  static constexpr int NST = GP == 64 ? 5 : 4;
+  static constexpr int kBytes = NST * kStage + 1024;
+  static constexpr int kThreads = (1 + NST + 4) * 32;
 };
 
 // BLK: block-sparse indices (sparseBlockSize >= 8): the key / value rows of a
 // stage arrive as one TMA box per selected block and feature panel.
 template <typename T, int GP, int MODE, bool BLK>
-__global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__ Maps maps, Prob p, T* out_main, T* out_rope,
-                                                         int* gerr) {
+__global__ void __launch_bounds__(DqSmem<MODE == 0 ? 192 : 256, GP>::kThreads, 1)
+    dq_kernel(const __grid_constant__ Maps maps, Prob p, T* out_main, T* out_rope, int* gerr) {
   using E = Elt<T>;
   constexpr int NCOL = MODE == 0 ? 192 : 256;
   constexpr int NPART = MODE == 0 ? 3 : 2;
-  using S = DqSmem<NCOL>;
+  using S = DqSmem<NCOL, GP>;
+  constexpr int kStages = S::NST;
+  constexpr int kThreads = S::kThreads;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t full_bar[kStages], empty_bar[kStages], tfull_bar[2], tempty_bar[2], done_bar;
@@ -51,14 +57,6 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
   const int nchunks = p.Kpad / kSlots;
   const int nitems = p.ntok * NPART;
 
-  if (GP == 64) {
-    // heads 64-127 do not exist: their A panel stays zero for the whole kernel
-    for (int s = 0; s < kStages; ++s) {
-      uint4* z = reinterpret_cast<uint4*>(smem + s * S::kStage + kSlots * 128);
-      for (int i = threadIdx.x; i < kSlots * 128 / 16; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
-    }
-    fence_async_smem();
-  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full_bar[i], 32 + 1);   // the owning warp's lanes + the TMA transaction arrive
@@ -238,14 +236,15 @@ template <typename T, int GP, int MODE>
 cudaError_t launch_one(const Maps& maps, const Prob& p, void* o1, void* o2, int* gerr, int nsm, cudaStream_t st) {
   constexpr int NCOL = MODE == 0 ? 192 : 256;
   constexpr int NPART = MODE == 0 ? 3 : 2;
+  using S = DqSmem<NCOL, GP>;
   auto kern = p.bs >= 8 ? dq_kernel<T, GP, MODE, true> : dq_kernel<T, GP, MODE, false>;
-  const int smem = DqSmem<NCOL>::kBytes > kOneCtaSmem ? DqSmem<NCOL>::kBytes : kOneCtaSmem;
+  const int smem = S::kBytes > kOneCtaSmem ? S::kBytes : kOneCtaSmem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int nitems = p.ntok * NPART;
   const int grid = nitems < nsm ? nitems : nsm;
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, kThreads, smem, st>>>(maps, p, static_cast<T*>(o1), static_cast<T*>(o2), gerr);
+  kern<<<grid, S::kThreads, smem, st>>>(maps, p, static_cast<T*>(o1), static_cast<T*>(o2), gerr);
   return cudaGetLastError();
 }
 
