@@ -1,15 +1,13 @@
-// Query-side contraction over a token's selected keys, on the tensor cores:
-//   mode 0:  [dQ || dQRope](t) = dS(t) . [K || KRope]_sel   (3 chunks of 192 features;
-//            the softmax scale is already folded into the stored dS)
-//   mode 1:  O(t) = P(t) . V_sel                              (2 chunks of 256 features)
-// Only mode 1 is launched (the companion forward's output); the backward
-// forms dQ in kvq.cu, next to the key side.
-// Heads on M (padded to 128), features on N, keys (64 per pipeline stage) on K;
-// the accumulator stays in tensor memory for the whole key loop and is written
-// once, so dQ needs no atomics.
+// The companion forward's output over a token's selected keys, on the tensor
+// cores:  O(t) = P(t) . V_sel  (2 items of 256 features per token), with P
+// staged by the score kernel's P mode (sdp.cu) from the final statistics.
+// Heads on M (padded to 128), features on N, keys (64 per pipeline stage) on
+// K; the accumulator stays in tensor memory for the whole key loop and is
+// written once.  (The backward's dQ has the same shape and runs in kvq.cu,
+// next to the key side; block indices use dqb.cu for both.)
 //
-// aclnnSparseFlashAttentionGrad doc, 阶段3 (dQ = dS K[u] / sqrt(d)); MindSpore
-// flash_attention_bwd.py, update_dQi.
+// aclnnSparseFlashAttentionGrad doc, 功能说明 (selectedValue gathered by
+// topkIndices); MindSpore flash_attention_bwd.py, the forward's O = P V.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -18,7 +16,7 @@ namespace sfa {
 namespace {
 
 constexpr int kSlots = 64;         // keys per pipeline stage (MMA K extent)
-// A stage: the staged P / dS of 64 keys (one 64-head panel per 64 heads),
+// A stage: the staged P of 64 keys (one 64-head panel per 64 heads),
 // then the gathered rows' feature panels.  With 64 heads the MMA's rows
 // 64-127 read the stage's first feature panel (the A operand's second
 // 64-row atom lies one panel further on): finite data whose results are
@@ -37,15 +35,15 @@ struct DqSmem {
 
 // BLK: block-sparse indices (sparseBlockSize >= 8): the key / value rows of a
 // stage arrive as one TMA box per selected block and feature panel.
-template <typename T, int GP, int MODE, bool BLK>
-__global__ void __launch_bounds__(DqSmem<MODE == 0 ? 192 : 256, GP>::kThreads, 1)
-    dq_kernel(const __grid_constant__ Maps maps, Prob p, T* out_main, T* out_rope, int* gerr) {
+constexpr int NCOL = 256;     // features per item (MMA N)
+constexpr int NPART = 2;      // items per token
+
+template <typename T, int GP, bool BLK>
+__global__ void __launch_bounds__(DqSmem<NCOL, GP>::kThreads, 1)
+    dq_kernel(const __grid_constant__ Maps maps, Prob p, T* out, int* gerr) {
   using E = Elt<T>;
-  constexpr int NCOL = MODE == 0 ? 192 : 256;
-  constexpr int NPART = MODE == 0 ? 3 : 2;
   using S = DqSmem<NCOL, GP>;
   constexpr int kStages = S::NST;
-  constexpr int kThreads = S::kThreads;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t full_bar[kStages], empty_bar[kStages], tfull_bar[2], tempty_bar[2], done_bar;
@@ -108,17 +106,16 @@ __global__ void __launch_bounds__(DqSmem<MODE == 0 ? 192 : 256, GP>::kThreads, 1
     __syncwarp();
   } else if (warp <= kStages) {
     // ---------------------------------------------------------------- producers
-    // Warp w owns stage slot w-1 and takes every third stage of 64 keys: the
-    // staged dS^T (or P^T) rows as one TMA box per 64-head panel, and the
-    // keys' feature rows gathered by cp.async (NCOL contiguous features per
-    // row).  The warp waits only for its own copies, then fences them for the
-    // tensor core and arrives.
+    // Warp w owns stage slot w-1 and takes every NST-th stage of 64 keys: the
+    // staged P^T rows as one TMA box per 64-head panel, and the keys' value
+    // rows gathered by cp.async (NCOL contiguous features per row).  The warp
+    // waits only for its own copies, then fences them for the tensor core and
+    // arrives.
     constexpr int kHP = GP / 64;
     constexpr int kCpr = NCOL / 8;            // 16-byte pieces per gathered row
     const int me = warp - 1;
-    const CUtensorMap* mA = MODE == 0 ? &maps.dS : &maps.P;
-    const T* kmain = static_cast<const T*>(MODE == 0 ? p.k : p.v);
-    const T* krope = static_cast<const T*>(p.kr);
+    const CUtensorMap* mA = &maps.P;
+    const T* vrow = static_cast<const T*>(p.v);
     const uint32_t a = smem_u32(smem + me * S::kStage);
     const uint32_t b = a + S::kA;
     int* rows = rows_s[me];
@@ -160,25 +157,18 @@ __global__ void __launch_bounds__(DqSmem<MODE == 0 ? 192 : 256, GP>::kThreads, 1
             for (int pn = 0; pn < NCOL / 64; ++pn) {
               const int f = f0 + pn * 64;
               const uint32_t dst = b + pn * (kSlots * 128) + lane * p.bs * 128;
-              if (MODE == 1) tma_2d(dst, &maps.v, f, y, &full_bar[me]);
-              else if (f < 512) tma_2d(dst, &maps.k, f, y, &full_bar[me]);
-              else tma_2d(dst, p.has_rope ? &maps.kr : &maps.k, p.has_rope ? f - 512 : 0, p.has_rope ? y : -p.bs,
-                          &full_bar[me]);
+              tma_2d(dst, &maps.v, f, y, &full_bar[me]);
             }
           }
         } else if (lane < kCpr) {   // lane < kCpr owns 16-byte piece `lane` of every gathered row
-          const int f = f0 + lane * 8;
-          const bool rope = MODE == 0 && f >= 512;
-          const T* base = rope ? (p.has_rope ? krope + (f - 512) : kmain) : kmain + f;
-          const int rlen = rope ? 64 : 512;
-          const bool zero = rope && !p.has_rope;
+          const T* base = vrow + f0 + lane * 8;
           const uint32_t dst0 = b + (lane >> 3) * (kSlots * 128);
           const uint32_t c = lane & 7;
 #pragma unroll 8
           for (int r = 0; r < kSlots; ++r) {
             const int row = rows[r];
-            cp_async16(dst0 + r * 128 + ((c ^ (r & 7)) << 4), base + (size_t)(row < 0 ? 0 : row) * rlen,
-                       (row < 0 || zero) ? 0u : 16u);
+            cp_async16(dst0 + r * 128 + ((c ^ (r & 7)) << 4), base + (size_t)(row < 0 ? 0 : row) * 512,
+                       row < 0 ? 0u : 16u);
           }
         }
         cp_async_commit();
@@ -206,11 +196,7 @@ __global__ void __launch_bounds__(DqSmem<MODE == 0 ? 192 : 256, GP>::kThreads, 1
         float v[32];
         tmem_ld32(td + c, v);
         const int f = part * NCOL + c;
-        T* dst = nullptr;
-        if (h < p.G) {
-          if (MODE == 1 || f < 512) dst = out_main + ((size_t)t * p.G + h) * 512 + f;
-          else if (p.has_rope) dst = out_rope + ((size_t)t * p.G + h) * 64 + (f - 512);
-        }
+        T* dst = h < p.G ? out + ((size_t)t * p.G + h) * 512 + f : nullptr;
         if (dst) {
           uint32_t pk[16];
 #pragma unroll
@@ -232,19 +218,17 @@ __global__ void __launch_bounds__(DqSmem<MODE == 0 ? 192 : 256, GP>::kThreads, 1
   }
 }
 
-template <typename T, int GP, int MODE>
-cudaError_t launch_one(const Maps& maps, const Prob& p, void* o1, void* o2, int* gerr, int nsm, cudaStream_t st) {
-  constexpr int NCOL = MODE == 0 ? 192 : 256;
-  constexpr int NPART = MODE == 0 ? 3 : 2;
+template <typename T, int GP>
+cudaError_t launch_one(const Maps& maps, const Prob& p, void* out, int* gerr, int nsm, cudaStream_t st) {
   using S = DqSmem<NCOL, GP>;
-  auto kern = p.bs >= 8 ? dq_kernel<T, GP, MODE, true> : dq_kernel<T, GP, MODE, false>;
+  auto kern = p.bs >= 8 ? dq_kernel<T, GP, true> : dq_kernel<T, GP, false>;
   const int smem = S::kBytes > kOneCtaSmem ? S::kBytes : kOneCtaSmem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int nitems = p.ntok * NPART;
   const int grid = nitems < nsm ? nitems : nsm;
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, S::kThreads, smem, st>>>(maps, p, static_cast<T*>(o1), static_cast<T*>(o2), gerr);
+  kern<<<grid, S::kThreads, smem, st>>>(maps, p, static_cast<T*>(out), gerr);
   return cudaGetLastError();
 }
 
@@ -252,8 +236,8 @@ cudaError_t launch_one(const Maps& maps, const Prob& p, void* o1, void* o2, int*
 
 template <typename T>
 cudaError_t launch_pv(const Maps& maps, const Prob& p, void* out, int* gerr, int nsm, cudaStream_t st) {
-  if (p.Gp == 64) return launch_one<T, 64, 1>(maps, p, out, nullptr, gerr, nsm, st);
-  return launch_one<T, 128, 1>(maps, p, out, nullptr, gerr, nsm, st);
+  if (p.Gp == 64) return launch_one<T, 64>(maps, p, out, gerr, nsm, st);
+  return launch_one<T, 128>(maps, p, out, gerr, nsm, st);
 }
 
 template cudaError_t launch_pv<__nv_bfloat16>(const Maps&, const Prob&, void*, int*, int, cudaStream_t);
