@@ -224,17 +224,6 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int
       "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
-// Four one-row boxes (rows r0..r3, columns x .. x+63) into four consecutive
-// 128-byte rows at `dst`.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int r0, int r1, int r2, int r3,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
-      "%5, %6}], [%7];" ::"r"(dst),
-      "l"(map), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // ------------------------------------------------------------------ operand layouts
 // All tensor-core operands live in shared memory as 128-byte swizzled rows:
 // a "panel" holds R rows of 64 consecutive 16-bit elements (128 B per row),
@@ -242,10 +231,6 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map
 // stored at chunk position c ^ (r & 7).  A K-major operand (K contiguous) with
 // K > 64 is a sequence of panels along K; an MN-major operand (M or N
 // contiguous) is a sequence of panels along MN whose rows are indexed by K.
-__host__ __device__ __forceinline__ uint32_t swz_chunk(uint32_t row, uint32_t chunk16) {
-  return row * 128u + (((chunk16 ^ (row & 7u)) & 7u) << 4);
-}
-
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading and
 // stride byte offsets (16-byte units), descriptor version 1, 128-byte swizzle.
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
