@@ -24,6 +24,9 @@ SMALL = {
     "g32_padding_dups": small_workload(N1=32, S1=5, S2=300, K=160, index_kind="random_any", seed=15),
     "g64_norope": small_workload(N1=64, S1=4, S2=700, K=256, Dr=0, seed=16),
     "g128_fp16": small_workload(N1=128, S1=3, S2=600, K=384, dtype="fp16", seed=17),
+    # 128 heads and an even number of 128-key tiles (a ragged last tile; no rope part)
+    "g128_pair_ragged": small_workload(N1=128, S1=5, S2=1024, K=500, mode=3, seed=39),
+    "g128_pair_norope_fp16": small_workload(N1=128, S1=3, S2=700, K=256, Dr=0, dtype="fp16", seed=40),
     "g4_bs64": small_workload(N1=4, S1=4, S2=4096, K=5, block_size=64, index_kind="block", seed=18),
     # KV extent past 64 MB of fp32 key rows: key-side items run tile-group major
     "g64_wide_kv": small_workload(N1=64, S1=4, S2=16384, K=640, seed=23),
@@ -132,7 +135,8 @@ def test_decode_bit_exact(name):
 
 # the last seven: block indices that many tokens select, which the forward
 # scores per block start (statistics and P) and multiplies by V per token
-@pytest.mark.parametrize("name", ["tiny", "g128_causal", "g64_tnd", "g16_block_fp16", "g64_norope", "g16_kvb_bs16",
+@pytest.mark.parametrize("name", ["tiny", "g128_causal", "g128_pair_ragged", "g128_pair_norope_fp16", "g64_tnd",
+                                  "g16_block_fp16", "g64_norope", "g16_kvb_bs16",
                                   "g16_kvb_bs32_unaligned", "g32_kvb_bs64_norope_fp16", "g12_kvb_tnd_causal",
                                   "g16_kvb_padding_dups", "g64_kvb_bs32", "g48_bs16"])
 def test_fwd_small(name):
