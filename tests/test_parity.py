@@ -53,6 +53,11 @@ SMALL = {
     "g48_bs16": small_workload(N1=48, S1=24, S2=512, K=12, block_size=16, index_kind="block", seed=36),
     "g12_tnd": small_workload(name="tnd_g12", layout="TND", B=2, N1=12, K=150, mode=3, index_kind="causal",
                               kv_extra=100, T1=9, act_q=(4, 5), seed=37),
+    # one and two heads (the smallest N1 of the page's list) over many batches;
+    # the TND lengths are random cuts of T1
+    "g1_many_batches": small_workload(B=40, N1=1, S1=2, S2=256, K=96, seed=41),
+    "g2_tnd_many_batches": small_workload(name="tnd_many", layout="TND", B=24, N1=2, K=64, mode=3,
+                                          index_kind="causal", kv_extra=40, T1=60, seed=42),
     # ~5100 occurrences of each of two keys in one token chunk: the deterministic
     # sort takes its path for row segments longer than one warp sorts in shared memory
     "g4_pile_dups": small_workload(N1=4, S1=160, S2=512, K=128, index_kind="pile", std=0.15, seed=32),
@@ -136,7 +141,7 @@ def test_decode_bit_exact(name):
 # the last seven: block indices that many tokens select, which the forward
 # scores per block start (statistics and P) and multiplies by V per token
 @pytest.mark.parametrize("name", ["tiny", "g128_causal", "g128_pair_ragged", "g128_pair_norope_fp16", "g64_tnd",
-                                  "g16_block_fp16", "g64_norope", "g16_kvb_bs16",
+                                  "g1_many_batches", "g2_tnd_many_batches", "g16_block_fp16", "g64_norope", "g16_kvb_bs16",
                                   "g16_kvb_bs32_unaligned", "g32_kvb_bs64_norope_fp16", "g12_kvb_tnd_causal",
                                   "g16_kvb_padding_dups", "g64_kvb_bs32", "g48_bs16"])
 def test_fwd_small(name):
