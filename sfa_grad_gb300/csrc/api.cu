@@ -119,7 +119,7 @@ sfa_status validate(const sfa_params* p, bool fwd, Plan* out) {
   P.off_part = o; o += P.det && !P.kvb ? up(chunk * P.Kpad * kAccRow * 2) : 0;
   P.off_dscr = o; o += P.det ? up(2 * ents * 4) : 0;   // padded copies of long segments
   // forward partial statistics: per key tile of 128, or per block index
-  P.off_tstats = o; o += fwd ? up(chunk * (P.kvb ? P.Kidx : P.Kpad / 128) * P.G * 2 * 4) : 0;
+  P.off_tstats = o; o += fwd ? up(chunk * (P.kvb ? P.Kidx : P.Kpad / 32) * P.G * 2 * 4) : 0;
   // counting-sort bins: block starts + bs (key-major blocks) or kv rows
   // (deterministic reduction), and the sorted entries
   const bool bins = P.kvb || P.det;
@@ -670,11 +670,12 @@ sfa_status run_fwd(const Plan& P, const void* q, const void* k, const void* v, c
       SFA_CK(launch_sdpb<T>(maps, pr, kModeFwdP, bgrp, bbeg, bng, bent, ws + P.off_P, nullptr, nullptr, gerr, nsm, st));
       SFA_CK(launch_dqb<T>(maps, pr, true, out, nullptr, gerr, nsm, st));
     } else {
+      // statistics per 32 slots with P staged relative to each group's max,
+      // the final statistics, then O = P V (P rescaled per group)
       SFA_CK(launch_rowtab(pr, st));
-      SFA_CK(launch_sdp<T>(maps, pr, kModeFwdStats, nullptr, nullptr, ts, gerr, nsm, st));
-      SFA_CK(launch_stats_combine(pr, ts, P.Kpad / 128, smax, ssum, st));
-      SFA_CK(launch_sdp<T>(maps, pr, kModeFwdP, ws + P.off_P, nullptr, nullptr, gerr, nsm, st));
-      SFA_CK(launch_pv<T>(maps, pr, out, gerr, nsm, st));
+      SFA_CK(launch_sdp<T>(maps, pr, kModeFwdStats, ws + P.off_P, nullptr, ts, gerr, nsm, st));
+      SFA_CK(launch_stats_combine(pr, ts, P.Kpad / 32, smax, ssum, st));
+      SFA_CK(launch_pv<T>(maps, pr, ts, out, gerr, nsm, st));
     }
   }
   return SFA_OK;

@@ -168,6 +168,16 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // tensor core (async proxy).
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// 16-byte shared-memory load and store at a shared-window address.
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 // Tensor maps of one call (2-D, 16-bit elements, 64-element = 128-byte inner
 // box, 128-byte swizzle, so a box lands in shared memory exactly in the panel
@@ -358,6 +368,12 @@ struct Elt<__nv_bfloat16> {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
   }
+  // the two values pack() put in a word: a from the low half, b from the high
+  // the two values of w times those of f, rounded once
+  __device__ static __forceinline__ uint32_t mul2(uint32_t w, uint32_t f) {
+    __nv_bfloat162 r = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&w), *reinterpret_cast<const __nv_bfloat162*>(&f));
+    return *reinterpret_cast<uint32_t*>(&r);
+  }
   __device__ static __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
   __device__ static __forceinline__ __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
 };
@@ -367,6 +383,10 @@ struct Elt<__half> {
   __device__ static __forceinline__ uint32_t pack(float a, float b) {
     __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __device__ static __forceinline__ uint32_t mul2(uint32_t w, uint32_t f) {
+    __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&w), *reinterpret_cast<const __half2*>(&f));
+    return *reinterpret_cast<uint32_t*>(&r);
   }
   __device__ static __forceinline__ float to_f(__half x) { return __half2float(x); }
   __device__ static __forceinline__ __half from_f(float x) { return __float2half_rn(x); }

@@ -1,6 +1,10 @@
 // The companion forward's output over a token's selected keys, on the tensor
-// cores:  O(t) = P(t) . V_sel  (2 items of 256 features per token), with P
-// staged by the score kernel's P mode (sdp.cu) from the final statistics.
+// cores:  O(t) = P(t) . V_sel  (2 items of 256 features per token).  The
+// score kernel's statistics pass (sdp.cu) staged P~ = exp((s - m_g) * scale)
+// relative to the max m_g of each group of 32 of the token's slots; the
+// producers rescale every stage's P~ in shared memory by the group's factor
+// exp((m_g - m) * scale) / l, which gives P for the final statistics m, l
+// (softmaxMax = m * scale, softmaxSum = l) without a second score pass.
 // Heads on M (padded to 128), features on N, keys (64 per pipeline stage) on
 // K; the accumulator stays in tensor memory for the whole key loop and is
 // written once.  (The backward's dQ has the same shape and runs in kvq.cu,
@@ -40,13 +44,15 @@ constexpr int NPART = 2;      // items per token
 
 template <typename T, int GP, bool BLK>
 __global__ void __launch_bounds__(DqSmem<NCOL, GP>::kThreads, 1)
-    dq_kernel(const __grid_constant__ Maps maps, Prob p, T* out, int* gerr) {
+    dq_kernel(const __grid_constant__ Maps maps, Prob p, const float* part_stats, T* out, int* gerr) {
   using E = Elt<T>;
   using S = DqSmem<NCOL, GP>;
   constexpr int kStages = S::NST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t full_bar[kStages], empty_bar[kStages], tfull_bar[2], tempty_bar[2], done_bar;
+  // pfull_bar: the stage's staged P~ has landed (to be rescaled); full_bar:
+  // the whole stage is ready for the MMA
+  __shared__ uint64_t full_bar[kStages], pfull_bar[kStages], empty_bar[kStages], tfull_bar[2], tempty_bar[2], done_bar;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ __align__(16) int rows_s[kStages][kSlots];   // read and written as int2
@@ -57,7 +63,8 @@ __global__ void __launch_bounds__(DqSmem<NCOL, GP>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&full_bar[i], 32 + 1);   // the owning warp's lanes + the TMA transaction arrive
+      mbar_init(&full_bar[i], 32 + 1);   // the owning warp's lanes + one arrival with the value boxes' bytes
+      mbar_init(&pfull_bar[i], 1);
       mbar_init(&empty_bar[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -107,12 +114,20 @@ __global__ void __launch_bounds__(DqSmem<NCOL, GP>::kThreads, 1)
   } else if (warp <= kStages) {
     // ---------------------------------------------------------------- producers
     // Warp w owns stage slot w-1 and takes every NST-th stage of 64 keys: the
-    // staged P^T rows as one TMA box per 64-head panel, and the keys' value
-    // rows gathered by cp.async (NCOL contiguous features per row).  The warp
-    // waits only for its own copies, then fences them for the tensor core and
-    // arrives.
+    // staged P~^T rows as one TMA box per 64-head panel, and the keys' value
+    // rows gathered by cp.async (NCOL contiguous features per row).  While the
+    // value rows are in flight the warp rescales the landed P~ in place (lane:
+    // one 16-byte piece of 8 heads in kRPL consecutive rows, all in one group
+    // of 32 slots), then waits for its own copies, fences them and its stores
+    // for the tensor core and arrives.
     constexpr int kHP = GP / 64;
     constexpr int kCpr = NCOL / 8;            // 16-byte pieces per gathered row
+    constexpr int kCPR = 8 * kHP;             // 16-byte pieces per staged P~ row
+    constexpr int kRPL = kSlots * kCPR / 32;  // P~ rows per lane
+    static_assert(kRPL == 16 || kRPL == 32, "a lane's rows lie in one group of 32 slots");
+    const int pc = lane % kCPR, rs = lane / kCPR;
+    const int hb = (pc >> 3) * 64 + (pc & 7) * 8;   // the lane's first head
+    const int ngroups = p.Kpad / 32;
     const int me = warp - 1;
     const CUtensorMap* mA = &maps.P;
     const T* vrow = static_cast<const T*>(p.v);
@@ -121,10 +136,21 @@ __global__ void __launch_bounds__(DqSmem<NCOL, GP>::kThreads, 1)
     int* rows = rows_s[me];
     int g = 0;
     bool ok = true;
-    ArmLog alog;
+    ArmLog alog, plog;
     for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
       const int tl = item / NPART, part = item % NPART;
       const int f0 = part * NCOL;
+      // the final statistics of the lane's 8 heads: softmaxMax in log2 units
+      // and 1 / softmaxSum (0 for a head past G or without a valid key)
+      float nm[8], il[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int h = hb + u;
+        const size_t o = (size_t)(p.tok0 + tl) * p.G + h;
+        const float l = h < p.G ? __ldg(p.ssum + o) : 0.f;
+        nm[u] = h < p.G ? __ldg(p.smax + o) * kLog2e : 0.f;
+        il[u] = l > 0.f ? 1.f / l : 0.f;
+      }
       for (int c = 0; c < nchunks; ++c, ++g) {
         if (g % kStages != me) continue;
         const int2 r2 = *reinterpret_cast<const int2*>(p.rowtab + (size_t)tl * p.Kpad + c * kSlots + 2 * lane);
@@ -133,11 +159,23 @@ __global__ void __launch_bounds__(DqSmem<NCOL, GP>::kThreads, 1)
         *reinterpret_cast<int2*>(rows + 2 * lane) = r2;
         __syncwarp();
         if (!ok) break;
+        const uint32_t ph = (uint32_t)(g / kStages);
         if (lane == 0) {
-          mbar_expect_tx(&full_bar[me], kHP * kSlots * 128 + (BLK ? (NCOL / 64) * kSlots * 128 : 0));
-          alog.arm(me, (uint32_t)(g / kStages));
+          mbar_expect_tx(&pfull_bar[me], kHP * kSlots * 128);
+          plog.arm(me, ph);
           for (int hp = 0; hp < kHP; ++hp)
-            tma_2d(a + hp * (kSlots * 128), mA, hp * 64, tl * p.Kpad + c * kSlots, &full_bar[me]);
+            tma_2d(a + hp * (kSlots * 128), mA, hp * 64, tl * p.Kpad + c * kSlots, &pfull_bar[me]);
+          mbar_expect_tx(&full_bar[me], BLK ? (NCOL / 64) * kSlots * 128 : 0);
+          alog.arm(me, ph);
+        }
+        // the group maxima of the lane's 8 heads (-inf past the heads), loaded
+        // now and used once the value rows are in flight
+        float mg[8];
+        {
+          const int grp = (c * kSlots + rs * kRPL) / 32;
+          const float* ps = part_stats + ((size_t)tl * ngroups + grp) * p.G * 2;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) mg[u] = hb + u < p.G ? __ldg(ps + 2 * (hb + u)) : -INFINITY;
         }
         if constexpr (BLK) {
           // lane i < 64/bs owns the stage's i-th index: one box of bs rows per
@@ -172,13 +210,48 @@ __global__ void __launch_bounds__(DqSmem<NCOL, GP>::kThreads, 1)
           }
         }
         cp_async_commit();
+        // the factors exp((m_g - m) * scale) / l, as pairs in the input type
+        // (0 past the heads, or for a group without a valid key, whose P~ is 0)
+        uint32_t fac[4];
+        {
+          const float sl2 = p.scale * kLog2e;
+          float f[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) f[u] = mg[u] == -INFINITY ? 0.f : ex2(fmaf(mg[u], sl2, -nm[u])) * il[u];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) fac[u] = E::pack(f[2 * u], f[2 * u + 1]);
+        }
+        // P = P~ x factor, in place, once the staged rows have landed
+        const bool pok = __all_sync(0xffffffffu, mbar_wait(&pfull_bar[me], ph & 1u, wt));
+        if (pok) {
+          // eight rows at a time: all loads, then all stores, so that the
+          // loads overlap instead of each waiting behind the previous store
+          const uint32_t pb = a + (pc >> 3) * (kSlots * 128) + (uint32_t)(rs * kRPL) * 128;
+#pragma unroll
+          for (int i0 = 0; i0 < kRPL; i0 += 8) {
+            uint4 w[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) w[j] = lds128(pb + (i0 + j) * 128 + (((pc & 7) ^ ((i0 + j) & 7)) << 4));
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              sts128(pb + (i0 + j) * 128 + (((pc & 7) ^ ((i0 + j) & 7)) << 4),
+                     make_uint4(E::mul2(w[j].x, fac[0]), E::mul2(w[j].y, fac[1]), E::mul2(w[j].z, fac[2]),
+                                E::mul2(w[j].w, fac[3])));
+          }
+        }
         cp_async_wait<0>();
         fence_async_smem();
         mbar_arrive(&full_bar[me]);
         __syncwarp();
+        if (!pok) {
+          ok = false;
+          break;
+        }
       }
     }
-    alog.settle(full_bar, gerr);   // no copy still landing in shared memory at exit
+    // no copy still landing in shared memory at exit
+    plog.settle(pfull_bar, gerr);
+    alog.settle(full_bar, gerr);
   } else if (warp > kStages) {
     // ---------------------------------------------------------------- epilogue (thread = head)
     const int ew = warp & 3;   // the TMEM lane quadrant this warp may read
@@ -219,7 +292,8 @@ __global__ void __launch_bounds__(DqSmem<NCOL, GP>::kThreads, 1)
 }
 
 template <typename T, int GP>
-cudaError_t launch_one(const Maps& maps, const Prob& p, void* out, int* gerr, int nsm, cudaStream_t st) {
+cudaError_t launch_one(const Maps& maps, const Prob& p, const float* part_stats, void* out, int* gerr, int nsm,
+                       cudaStream_t st) {
   using S = DqSmem<NCOL, GP>;
   auto kern = p.bs >= 8 ? dq_kernel<T, GP, true> : dq_kernel<T, GP, false>;
   const int smem = S::kBytes > kOneCtaSmem ? S::kBytes : kOneCtaSmem;
@@ -228,19 +302,20 @@ cudaError_t launch_one(const Maps& maps, const Prob& p, void* out, int* gerr, in
   const int nitems = p.ntok * NPART;
   const int grid = nitems < nsm ? nitems : nsm;
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, S::kThreads, smem, st>>>(maps, p, static_cast<T*>(out), gerr);
+  kern<<<grid, S::kThreads, smem, st>>>(maps, p, part_stats, static_cast<T*>(out), gerr);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 template <typename T>
-cudaError_t launch_pv(const Maps& maps, const Prob& p, void* out, int* gerr, int nsm, cudaStream_t st) {
-  if (p.Gp == 64) return launch_one<T, 64>(maps, p, out, gerr, nsm, st);
-  return launch_one<T, 128>(maps, p, out, gerr, nsm, st);
+cudaError_t launch_pv(const Maps& maps, const Prob& p, const float* part_stats, void* out, int* gerr, int nsm,
+                      cudaStream_t st) {
+  if (p.Gp == 64) return launch_one<T, 64>(maps, p, part_stats, out, gerr, nsm, st);
+  return launch_one<T, 128>(maps, p, part_stats, out, gerr, nsm, st);
 }
 
-template cudaError_t launch_pv<__nv_bfloat16>(const Maps&, const Prob&, void*, int*, int, cudaStream_t);
-template cudaError_t launch_pv<__half>(const Maps&, const Prob&, void*, int*, int, cudaStream_t);
+template cudaError_t launch_pv<__nv_bfloat16>(const Maps&, const Prob&, const float*, void*, int*, int, cudaStream_t);
+template cudaError_t launch_pv<__half>(const Maps&, const Prob&, const float*, void*, int*, int, cudaStream_t);
 
 }  // namespace sfa

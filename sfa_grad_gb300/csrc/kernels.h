@@ -5,7 +5,9 @@
 namespace sfa {
 
 constexpr int kModeBwd = 0;       // S and dP -> P, dS
-constexpr int kModeFwdStats = 1;  // S -> per-tile max / sum partials
+// S -> partial max / sum statistics; the per-token kernel (sdp.cu) also
+// stages P relative to each partial max (one partial per 32 keys)
+constexpr int kModeFwdStats = 1;
 constexpr int kModeFwdP = 2;      // S -> P from final statistics
 
 // Score / softmax-gradient kernel (sdp.cu).
@@ -62,9 +64,14 @@ template <typename T>
 cudaError_t launch_dqb(const Maps& maps, const Prob& p, bool pv, void* dq, void* dqr, int* gerr, int nsm,
                        cudaStream_t st);
 
-// Companion forward's output O = P V over each token's selected keys (dq.cu).
+// Companion forward's output O = P V over each token's selected keys (dq.cu),
+// from the P staged by sdp.cu's statistics pass relative to each 32-key
+// group's max, rescaled per (group, head) to the final statistics p.smax,
+// p.ssum.  part_stats: that pass's (token, Kpad / 32 groups, head) x {max of
+// the raw score, sum}.
 template <typename T>
-cudaError_t launch_pv(const Maps& maps, const Prob& p, void* out, int* gerr, int nsm, cudaStream_t st);
+cudaError_t launch_pv(const Maps& maps, const Prob& p, const float* part_stats, void* out, int* gerr, int nsm,
+                      cudaStream_t st);
 
 // Small kernels (prep.cu).
 cudaError_t launch_rowtab(const Prob& p, cudaStream_t st);
@@ -77,7 +84,7 @@ template <typename T>
 cudaError_t launch_dsum(const Prob& p, int tok0, int ntok, float* dsum, cudaStream_t st);
 template <typename T>
 cudaError_t launch_cast(const float* acc, int T2, void* dk, void* dkr, void* dv, int has_rope, cudaStream_t st);
-// ntiles: partial statistics per token (key tiles of 128, or block indices).
+// ntiles: partial statistics per token (32-key groups, or block indices).
 cudaError_t launch_stats_combine(const Prob& p, const float* tile_stats, int ntiles, float* smax, float* ssum,
                                  cudaStream_t st);
 

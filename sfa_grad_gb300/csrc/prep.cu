@@ -134,20 +134,24 @@ __global__ void cast_kernel(const float* acc, long long n4, T* dk, T* dkr, T* dv
   }
 }
 
-// Per (token, head): combine per-tile (max of raw score, sum of exp) partials.
+// Per (token, head): combine the partial (max of raw score, sum of exp) pairs
+// in one pass, rescaling the running sum whenever the running max grows.
 __global__ void stats_combine_kernel(const float* ts, int ntok, int ntiles, int G, int tok0, float scale, float* smax,
                                      float* ssum) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= ntok * G) return;
   const int tl = i / G, h = i - tl * G;
   const float sl2 = scale * 1.4426950408889634f;
-  float mx = -INFINITY;
-  for (int kt = 0; kt < ntiles; ++kt) mx = fmaxf(mx, ts[(((size_t)tl * ntiles + kt) * G + h) * 2]);
-  float l = 0.f;
-  if (mx != -INFINITY) {
-    for (int kt = 0; kt < ntiles; ++kt) {
-      const float m = ts[(((size_t)tl * ntiles + kt) * G + h) * 2];
-      if (m != -INFINITY) l += ts[(((size_t)tl * ntiles + kt) * G + h) * 2 + 1] * exp2f((m - mx) * sl2);
+  const float2* e = reinterpret_cast<const float2*>(ts) + (size_t)tl * ntiles * G + h;
+  float mx = -INFINITY, l = 0.f;
+  for (int kt = 0; kt < ntiles; ++kt) {
+    const float2 pr = e[(size_t)kt * G];
+    if (pr.x == -INFINITY) continue;   // no valid key in the partial
+    if (pr.x > mx) {
+      l = l * exp2f((mx - pr.x) * sl2) + pr.y;
+      mx = pr.x;
+    } else {
+      l += pr.y * exp2f((pr.x - mx) * sl2);
     }
   }
   const size_t o = (size_t)(tok0 + tl) * G + h;

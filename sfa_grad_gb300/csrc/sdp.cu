@@ -6,8 +6,9 @@
 //     P  = exp(S - softmaxMax) / softmaxSum                (masked keys -> 0)
 //     dS = P * (dP - Dsum) * scale
 // and writes P^T and dS^T (input dtype, heads contiguous, rows of G rounded
-// up to 16 heads) for the later contractions.  Forward modes reuse the score half: per-tile max/sum partials,
-// or P from final statistics.
+// up to 16 heads) for the later contractions.  The forward's one score pass
+// reuses the score half: max/sum partials per 32 keys, with P staged relative
+// to each partial's max.
 //
 // Pipeline: the contraction runs in stages of 128 features (64 for the rope
 // part).  The gathered key/value rows (A) and the token's head rows (B) have
@@ -74,6 +75,26 @@ __device__ __forceinline__ Chunk chunk_of(int c, int nS) {
   return Chunk{(c - nS) * 128, 2, 2};
 }
 
+// Reduce-scatter across the warp: on entry each lane holds 32 values (one
+// per column j); on exit a[0] of lane j holds the max (MAX) or the sum of
+// column j over all 32 lanes.  Five exchange steps, each lane keeping the half
+// of its columns that its lane bit selects: 31 shuffles instead of 5 per
+// column.
+template <bool MAX>
+__device__ __forceinline__ void butterfly_reduce(float (&a)[32], int lane) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool up = (lane & w) != 0;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float send = up ? a[i] : a[i + w];
+      const float keep = up ? a[i + w] : a[i];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, w);
+      a[i] = MAX ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+}
+
 // BLK: block-sparse indices (sparseBlockSize >= 8), key/value rows by TMA boxes.
 template <typename T, int GP, int MODE, bool SH, bool BLK>
 __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant__ Maps maps, Prob p, void* out_p, void* out_ds,
@@ -93,7 +114,6 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
   // gather warps), for the wind-down that completes every phase one of them
   // started
   __shared__ int arr_tma[kMaxSlots], arr_gat[kGatherWarps];
-  __shared__ float red_buf[4][GP][2];
   __shared__ float stats_s[2][3 * GP];
   __shared__ __align__(16) int rows_s[kGatherWarps][kKeys];   // one per gather warp; read and written as int4
   __shared__ uint4 epi_stage[8][32 * 4];                 // epilogue row transposition, 2 KB per warp
@@ -423,43 +443,52 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
       const uint32_t tS = tbase + set * (2 * GP) + ((uint32_t)(q * 32) << 16);
       const uint32_t tP = tS + GP;
       if (MODE == kModeFwdStats) {
-        // per head over the tile's valid keys: max of the raw score s and
-        // sum of exp((s - max) * scale)
+        // Per head over the warp's 32 keys (one group of the token's slots):
+        // m = max of the raw score s over the valid keys, l = sum of
+        // exp((s - m) * scale), and P~ = exp((s - m) * scale) staged in the P
+        // rows (0 for a masked key).  The P.V kernel rescales each group's P~
+        // to the final statistics, so no second score pass is needed.
+        T* ptile = static_cast<T*>(out_p) + ((size_t)tl * p.Kpad + kt * kKeys + q * 32) * Gs;
+        float2* tsg = reinterpret_cast<float2*>(tile_stats) + ((size_t)tl * (ntiles * 4) + kt * 4 + q) * p.G;
 #pragma unroll 1
         for (int c = 0; c < HH / 32; ++c) {
           const int h0 = half * HH + c * 32;
-          float s[32];
-          if (ok) tmem_ld32(tS + h0, s);
+          if (h0 >= Gs) break;                       // padded heads only: nothing is staged
+          const int npc = Gs - h0 >= 32 ? 4 : (Gs - h0) / 8;
+          // per-head max over the 32 lanes (keys): lane j ends with head j's;
+          // every lane then reads all 32 from the warp's staging buffer.  The
+          // scores are read from tensor memory twice (for the max, then for
+          // the exponentials) so that one 32-value array is live at a time.
+          float a[32];
+          if (ok) tmem_ld32(tS + h0, a);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float x = (valid && ok) ? s[j] : -INFINITY;
-            float mx = x;
+          for (int j = 0; j < 32; ++j) a[j] = (valid && ok) ? a[j] : -INFINITY;
+          butterfly_reduce<true>(a, lane);
+          const float gm = a[0];
+          float* mrow = reinterpret_cast<float*>(stg);
+          mrow[lane] = gm;
+          __syncwarp();
+          if (ok) tmem_ld32(tS + h0, a);
+          uint32_t pk[16];
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            float e = (x == -INFINITY) ? 0.f : ex2((x - mx) * sl2);
+          for (int j = 0; j < 32; j += 4) {
+            const float4 m4 = *reinterpret_cast<const float4*>(mrow + j);
+            const float mj[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
-            if (lane == 0) {
-              red_buf[q][h0 + j][0] = mx;
-              red_buf[q][h0 + j][1] = e;
-            }
+            for (int u = 0; u < 4; ++u) a[j + u] = (valid && ok) ? ex2((a[j + u] - mj[u]) * sl2) : 0.f;
+            pk[j / 2] = E::pack(a[j], a[j + 1]);
+            pk[j / 2 + 1] = E::pack(a[j + 2], a[j + 3]);
+          }
+          __syncwarp();
+          butterfly_reduce<false>(a, lane);
+          const float gl = a[0];
+          if (ok) {
+            if (h0 + lane < p.G) tsg[h0 + lane] = make_float2(gm, gl);   // raw score (unscaled), sum
+            put_rows(pk, ptile + h0, npc);
           }
         }
         tc_fence_before();
         if (ok) mbar_arrive(&tempty_bar[set]);
-        asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-        if (etid < p.G) {
-          float mx = -INFINITY;
-          for (int w = 0; w < 4; ++w) mx = fmaxf(mx, red_buf[w][etid][0]);
-          float l = 0.f;
-          if (mx != -INFINITY)
-            for (int w = 0; w < 4; ++w)
-              if (red_buf[w][etid][0] != -INFINITY) l += red_buf[w][etid][1] * ex2((red_buf[w][etid][0] - mx) * sl2);
-          float* ts = tile_stats + (((size_t)tl * ntiles + kt) * p.G + etid) * 2;
-          ts[0] = mx;   // raw score (unscaled)
-          ts[1] = l;
-        }
-        asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
         continue;
       }
       if (!ok) continue;
@@ -559,12 +588,12 @@ cudaError_t launch_sdp(const Maps& maps, const Prob& p, int mode, void* out_p, v
     if (mode == kModeBwd && shared_kv) return launch_one<T, 64, kModeBwd, true>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
     if (mode == kModeBwd) return launch_one<T, 64, kModeBwd>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
     if (mode == kModeFwdStats) return launch_one<T, 64, kModeFwdStats>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
-    return launch_one<T, 64, kModeFwdP>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
+    return cudaErrorInvalidValue;
   }
   if (mode == kModeBwd && shared_kv) return launch_one<T, 128, kModeBwd, true>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
   if (mode == kModeBwd) return launch_one<T, 128, kModeBwd>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
   if (mode == kModeFwdStats) return launch_one<T, 128, kModeFwdStats>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
-  return launch_one<T, 128, kModeFwdP>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
+  return cudaErrorInvalidValue;   // P from final statistics: the block kernel's mode (sdpb.cu)
 }
 
 template cudaError_t launch_sdp<__nv_bfloat16>(const Maps&, const Prob&, int, void*, void*, float*, int*, int, cudaStream_t);
