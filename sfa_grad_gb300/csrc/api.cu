@@ -503,7 +503,7 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
         SFA_CK(mk.mark(st));
       }
       // dQ with the features on the MMA's M (at most 64 heads here)
-      SFA_CK(launch_dqb<T>(maps, pr, false, dq, P.has_rope ? dqr : nullptr, gerr, nsm, st));
+      SFA_CK(launch_dqb<T>(maps, pr, false, dq, P.has_rope ? dqr : nullptr, nullptr, gerr, nsm, st));
       SFA_CK(mk.mark(st));
     } else {
       SFA_CK(launch_kvq<T>(maps, pr, acc, dq, P.has_rope ? dqr : nullptr, kvq_tile_group(P), false, gerr, nsm, st));
@@ -655,7 +655,8 @@ sfa_status run_fwd(const Plan& P, const void* q, const void* k, const void* v, c
     pr.ntok = (P.T1 - t0) < P.chunk ? (P.T1 - t0) : P.chunk;
     if (P.kvb) {
       // block indices that many tokens select: the pairs grouped by block
-      // start, statistics and P per block, O per token (features on M)
+      // start, statistics per pair with P staged relative to each pair's max,
+      // the final statistics, then O per token (features on M, P rescaled)
       int* bcnt = reinterpret_cast<int*>(ws + P.off_bcnt);
       int* bcur = reinterpret_cast<int*>(ws + P.off_bcur);
       int* bgrp = reinterpret_cast<int*>(ws + P.off_bgrp);
@@ -665,10 +666,9 @@ sfa_status run_fwd(const Plan& P, const void* q, const void* k, const void* v, c
       SFA_CK(launch_blk_count(pr, bcnt, ws + P.off_P, nullptr, ts, st));
       SFA_CK(launch_blk_scan(bcnt, P.T2 + P.bs, bcur, bgrp, bbeg, bng, P.bs, nullptr, st));
       SFA_CK(launch_blk_scatter(pr, bcur, bent, st));
-      SFA_CK(launch_sdpb<T>(maps, pr, kModeFwdStats, bgrp, bbeg, bng, bent, nullptr, nullptr, ts, gerr, nsm, st));
+      SFA_CK(launch_sdpb<T>(maps, pr, kModeFwdStats, bgrp, bbeg, bng, bent, ws + P.off_P, nullptr, ts, gerr, nsm, st));
       SFA_CK(launch_stats_combine(pr, ts, P.Kidx, smax, ssum, st));
-      SFA_CK(launch_sdpb<T>(maps, pr, kModeFwdP, bgrp, bbeg, bng, bent, ws + P.off_P, nullptr, nullptr, gerr, nsm, st));
-      SFA_CK(launch_dqb<T>(maps, pr, true, out, nullptr, gerr, nsm, st));
+      SFA_CK(launch_dqb<T>(maps, pr, true, out, nullptr, ts, gerr, nsm, st));
     } else {
       // statistics per 32 slots with P staged relative to each group's max,
       // the final statistics, then O = P V (P rescaled per group)

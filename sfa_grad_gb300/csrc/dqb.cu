@@ -12,7 +12,8 @@
 // as deep as shared memory allows (two stages of 80 KB).
 //
 // PV: the companion forward's O(t)^T = V_sel(t)^T . P(t)^T with the same
-// pipeline (value rows, the staged P rows, four feature tiles).
+// pipeline (value rows, the staged P rows, four feature tiles); P is staged
+// relative to each (token, block) pair's max and rescaled here.
 //
 // aclnnSparseFlashAttentionGrad doc, 功能说明 (selected blocks of
 // sparseBlockSize keys) and 阶段3 (dQ = dS . K * scale, with the scale folded
@@ -42,7 +43,7 @@ __device__ __forceinline__ uint32_t tile_off(int m) { return m < 4 ? (uint32_t)(
 
 template <typename T, int GN, bool PV>
 __global__ void __launch_bounds__(kThreads, 1) dqb_kernel(const __grid_constant__ Maps maps, Prob p, T* dq, T* dqr,
-                                                          int* gerr) {
+                                                          const float* part_stats, int* gerr) {
   using E = Elt<T>;
   // five feature tiles per accumulator, each at a 32-column boundary
   constexpr int TS = (GN + 31) / 32 * 32;
@@ -50,7 +51,10 @@ __global__ void __launch_bounds__(kThreads, 1) dqb_kernel(const __grid_constant_
   constexpr int NBUF = 2 * kBufCols <= 512 ? 2 : 1;        // accumulator buffers
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t a_full[kStages], a_empty[kStages], t_full[NBUF], t_empty[NBUF], done_bar;
+  // PV: p_full (the stage's P box has landed, to be rescaled) and each
+  // producer's factor table (blocks of the stage x heads)
+  __shared__ uint64_t a_full[kStages], p_full[kStages], a_empty[kStages], t_full[NBUF], t_empty[NBUF], done_bar;
+  __shared__ __align__(16) float fac_s[kStages][(kKeys / 16) * 64];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
@@ -61,7 +65,8 @@ __global__ void __launch_bounds__(kThreads, 1) dqb_kernel(const __grid_constant_
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&a_full[i], 1);
+      mbar_init(&a_full[i], PV ? 1 + 32 : 1);   // PV: the arming lane + the rescaling lanes
+      mbar_init(&p_full[i], 1);
       mbar_init(&a_empty[i], 1);
     }
     for (int i = 0; i < NBUF; ++i) {
@@ -115,44 +120,149 @@ __global__ void __launch_bounds__(kThreads, 1) dqb_kernel(const __grid_constant_
     // zeros) and, per selected block of the stage, one box of bs key rows per
     // 64-feature panel.  An index with no key at or above 0, past the last
     // row or past the index list reads rows below row 0: zeros.
-    if (lane == 0) {
-      const int me = warp - 1;
-      const int nidx = kKeys / p.bs;
-      const uint32_t tx = kPanel * (rope ? 10u : 9u);
-      const CUtensorMap* mrow = PV ? &maps.v : &maps.k;
-      const CUtensorMap* mcol = PV ? &maps.P : &maps.dS;
+    const int me = warp - 1;
+    const int nidx = kKeys / p.bs;
+    const uint32_t tx = kPanel * (rope ? 10u : 9u);
+    const CUtensorMap* mrow = PV ? &maps.v : &maps.k;
+    const CUtensorMap* mcol = PV ? &maps.P : &maps.dS;
+    // the stage's key (or value) rows: nidx blocks x (8 + rope) panel boxes
+    auto issue_rows = [&](uint32_t st, int t, long long kv0, int c, uint64_t* bar) {
+      for (int i = 0; i < nidx; ++i) {
+        const int ii = c * nidx + i;
+        int y = -p.bs;
+        if (ii < p.Kidx) {
+          const int r = __ldg(p.idx + (size_t)t * p.Kidx + ii);
+          const long long yy = kv0 + r;
+          if ((long long)r + p.bs > 0 && yy < p.T2) y = (int)yy;
+        }
+        const uint32_t dst = st + (uint32_t)(i * p.bs) * 128;
+        for (int pn = 0; pn < 8; ++pn) tma_2d(dst + (1 + pn) * kPanel, mrow, pn * 64, y, bar);
+        if (rope) tma_2d(dst, &maps.kr, 0, y, bar);
+      }
+    };
+    if constexpr (!PV) {
+      if (lane == 0) {
+        int g = 0;
+        bool ok = true;
+        ArmLog alog;
+        for (int tl = blockIdx.x; tl < p.ntok && ok; tl += gridDim.x) {
+          const int t = p.tok0 + tl;
+          const long long kv0 = p.meta[t].kv_start;
+          for (int c = 0; c < nst && ok; ++c, ++g) {
+            const int slot = g % kStages;
+            if (slot != me) continue;
+            ok = mbar_wait(&a_empty[slot], ((g / kStages) & 1) ^ 1, wt);
+            if (!ok) break;
+            mbar_expect_tx(&a_full[slot], tx);
+            alog.arm(slot, (uint32_t)(g / kStages));
+            const uint32_t st = smem_u32(smem + slot * kStageBytes);
+            tma_2d(st + kDsOff, mcol, 0, tl * p.Kpad + c * kKeys, &a_full[slot]);
+            issue_rows(st, t, kv0, c, &a_full[slot]);
+          }
+        }
+        alog.settle(a_full, gerr);   // no copy still landing in shared memory at exit
+      }
+      __syncwarp();
+    } else {
+      // PV: the staged rows hold P~ relative to each (token, block) pair's max
+      // (sdpb.cu's statistics pass).  The P box lands on its own barrier; the
+      // warp builds the stage's factor table exp((m_pair - m) * scale) / l
+      // (blocks x heads) meanwhile, rescales the box in place once it has
+      // landed, fences its stores and arrives (one arrival per lane).
+      constexpr int CPR = GN / 8;        // 16-byte pieces of a staged row that hold heads
+      constexpr int NPL = kKeys * CPR / 32;
+      constexpr int kFacPerLane = (kKeys / 16) * GN / 32;   // table entries per lane at bs = 16
+      float* ft = fac_s[me];
+      const float sl2 = p.scale * kLog2e;
       int g = 0;
       bool ok = true;
-      ArmLog alog;
+      ArmLog alog, plog;
       for (int tl = blockIdx.x; tl < p.ntok && ok; tl += gridDim.x) {
         const int t = p.tok0 + tl;
         const long long kv0 = p.meta[t].kv_start;
         for (int c = 0; c < nst && ok; ++c, ++g) {
           const int slot = g % kStages;
           if (slot != me) continue;
-          ok = mbar_wait(&a_empty[slot], ((g / kStages) & 1) ^ 1, wt);
-          if (!ok) break;
-          mbar_expect_tx(&a_full[slot], tx);
-          alog.arm(slot, (uint32_t)(g / kStages));
-          const uint32_t st = smem_u32(smem + slot * kStageBytes);
-          tma_2d(st + kDsOff, mcol, 0, tl * p.Kpad + c * kKeys, &a_full[slot]);
-          for (int i = 0; i < nidx; ++i) {
+          const uint32_t ph = (uint32_t)(g / kStages);
+          // the statistics behind the stage's factors (entry e = lane + 32 j:
+          // block e / GN, head e % GN), loaded before the slot wait so that
+          // their latency hides behind it
+          float em[kFacPerLane], el[kFacPerLane], ex[kFacPerLane];
+#pragma unroll
+          for (int j = 0; j < kFacPerLane; ++j) {
+            const int e = lane + 32 * j;
+            const int i = e / GN, h = e - i * GN;
             const int ii = c * nidx + i;
-            int y = -p.bs;
-            if (ii < p.Kidx) {
-              const int r = __ldg(p.idx + (size_t)t * p.Kidx + ii);
-              const long long yy = kv0 + r;
-              if ((long long)r + p.bs > 0 && yy < p.T2) y = (int)yy;
+            em[j] = -INFINITY;
+            el[j] = 0.f;
+            ex[j] = 0.f;
+            if (e < nidx * GN && h < p.G && ii < p.Kidx) {
+              const size_t o = (size_t)t * p.G + h;
+              em[j] = __ldg(part_stats + (((size_t)tl * p.Kidx + ii) * p.G + h) * 2);
+              el[j] = __ldg(p.ssum + o);
+              ex[j] = __ldg(p.smax + o);
             }
-            const uint32_t dst = st + (uint32_t)(i * p.bs) * 128;
-            for (int pn = 0; pn < 8; ++pn) tma_2d(dst + (1 + pn) * kPanel, mrow, pn * 64, y, &a_full[slot]);
-            if (rope) tma_2d(dst, &maps.kr, 0, y, &a_full[slot]);
+          }
+          bool w = true;
+          if (lane == 0) w = mbar_wait(&a_empty[slot], (ph & 1u) ^ 1u, wt);
+          ok = __shfl_sync(0xffffffffu, w, 0);
+          if (!ok) break;
+          const uint32_t st = smem_u32(smem + slot * kStageBytes);
+          if (lane == 0) {
+            mbar_expect_tx(&p_full[slot], kPanel);
+            plog.arm(slot, ph);
+            tma_2d(st + kDsOff, mcol, 0, tl * p.Kpad + c * kKeys, &p_full[slot]);
+            mbar_expect_tx(&a_full[slot], tx - kPanel);
+            alog.arm(slot, ph);
+            issue_rows(st, t, kv0, c, &a_full[slot]);
+            // the P box of this warp's next stage (kStages on), from HBM into
+            // L2 now: the rescale waits on its copy, which then comes from L2
+            int nc = c + kStages, ntl = tl;
+            if (nc >= nst) {
+              nc -= nst;
+              ntl += gridDim.x;
+            }
+            if (nc < nst && ntl < p.ntok) tma_prefetch_2d(mcol, 0, ntl * p.Kpad + nc * kKeys);
+          }
+#pragma unroll
+          for (int j = 0; j < kFacPerLane; ++j) {
+            const int e = lane + 32 * j;
+            if (e < nidx * GN)
+              ft[e] = (em[j] != -INFINITY && el[j] > 0.f) ? ex2(fmaf(em[j], sl2, -ex[j] * kLog2e)) / el[j] : 0.f;
+          }
+          __syncwarp();
+          const bool pok = __all_sync(0xffffffffu, mbar_wait(&p_full[slot], ph & 1u, wt));
+          if (pok) {
+            uint4 v[NPL];
+#pragma unroll
+            for (int j = 0; j < NPL; ++j) {
+              const int e = lane + 32 * j, r = e / CPR, k = e - r * CPR;
+              v[j] = lds128(st + kDsOff + r * 128 + ((k ^ (r & 7)) << 4));
+            }
+#pragma unroll
+            for (int j = 0; j < NPL; ++j) {
+              const int e = lane + 32 * j, r = e / CPR, k = e - r * CPR;
+              const float* f = ft + (r / p.bs) * GN + 8 * k;
+              const float4 f0 = *reinterpret_cast<const float4*>(f);
+              const float4 f1 = *reinterpret_cast<const float4*>(f + 4);
+              sts128(st + kDsOff + r * 128 + ((k ^ (r & 7)) << 4),
+                     make_uint4(E::mul2(v[j].x, E::pack(f0.x, f0.y)), E::mul2(v[j].y, E::pack(f0.z, f0.w)),
+                                E::mul2(v[j].z, E::pack(f1.x, f1.y)), E::mul2(v[j].w, E::pack(f1.z, f1.w))));
+            }
+          }
+          fence_async_smem();
+          mbar_arrive(&a_full[slot]);
+          __syncwarp();
+          if (!pok) {
+            ok = false;
+            break;
           }
         }
       }
-      alog.settle(a_full, gerr);   // no copy still landing in shared memory at exit
+      // no copy still landing in shared memory at exit
+      plog.settle(p_full, gerr);
+      alog.settle(a_full, gerr);
     }
-    __syncwarp();
   } else {
     // ---------------------------------------------------------------- epilogue
     // Warp w reads TMEM lane quadrant w % 4: thread = feature row f of a
@@ -201,32 +311,35 @@ __global__ void __launch_bounds__(kThreads, 1) dqb_kernel(const __grid_constant_
 }
 
 template <typename T, int GN>
-cudaError_t launch_g(const Maps& maps, const Prob& p, bool pv, void* dq, void* dqr, int* gerr, int nsm,
-                     cudaStream_t st) {
+cudaError_t launch_g(const Maps& maps, const Prob& p, bool pv, void* dq, void* dqr, const float* part_stats, int* gerr,
+                     int nsm, cudaStream_t st) {
   auto kern = pv ? dqb_kernel<T, GN, true> : dqb_kernel<T, GN, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = p.ntok < nsm ? p.ntok : nsm;
-  kern<<<grid, kThreads, kSmemBytes, st>>>(maps, p, static_cast<T*>(dq), static_cast<T*>(dqr), gerr);
+  kern<<<grid, kThreads, kSmemBytes, st>>>(maps, p, static_cast<T*>(dq), static_cast<T*>(dqr), part_stats, gerr);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 template <typename T>
-cudaError_t launch_dqb(const Maps& maps, const Prob& p, bool pv, void* dq, void* dqr, int* gerr, int nsm,
-                       cudaStream_t st) {
+cudaError_t launch_dqb(const Maps& maps, const Prob& p, bool pv, void* dq, void* dqr, const float* part_stats,
+                       int* gerr, int nsm, cudaStream_t st) {
   if (p.ntok <= 0) return cudaSuccess;
   if (p.bs < 16 || p.bs > kKeys || kKeys % p.bs != 0 || p.Kpad % kKeys != 0 || p.G > 64) return cudaErrorInvalidValue;
+  if (pv && !part_stats) return cudaErrorInvalidValue;
   switch (p.Gs) {
-    case 16: return launch_g<T, 16>(maps, p, pv, dq, dqr, gerr, nsm, st);
-    case 32: return launch_g<T, 32>(maps, p, pv, dq, dqr, gerr, nsm, st);
-    case 48: return launch_g<T, 48>(maps, p, pv, dq, dqr, gerr, nsm, st);
-    default: return launch_g<T, 64>(maps, p, pv, dq, dqr, gerr, nsm, st);
+    case 16: return launch_g<T, 16>(maps, p, pv, dq, dqr, part_stats, gerr, nsm, st);
+    case 32: return launch_g<T, 32>(maps, p, pv, dq, dqr, part_stats, gerr, nsm, st);
+    case 48: return launch_g<T, 48>(maps, p, pv, dq, dqr, part_stats, gerr, nsm, st);
+    default: return launch_g<T, 64>(maps, p, pv, dq, dqr, part_stats, gerr, nsm, st);
   }
 }
 
-template cudaError_t launch_dqb<__nv_bfloat16>(const Maps&, const Prob&, bool, void*, void*, int*, int, cudaStream_t);
-template cudaError_t launch_dqb<__half>(const Maps&, const Prob&, bool, void*, void*, int*, int, cudaStream_t);
+template cudaError_t launch_dqb<__nv_bfloat16>(const Maps&, const Prob&, bool, void*, void*, const float*, int*, int,
+                                               cudaStream_t);
+template cudaError_t launch_dqb<__half>(const Maps&, const Prob&, bool, void*, void*, const float*, int*, int,
+                                        cudaStream_t);
 
 }  // namespace sfa

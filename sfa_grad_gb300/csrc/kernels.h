@@ -8,7 +8,6 @@ constexpr int kModeBwd = 0;       // S and dP -> P, dS
 // S -> partial max / sum statistics; the per-token kernel (sdp.cu) also
 // stages P relative to each partial max (one partial per 32 keys)
 constexpr int kModeFwdStats = 1;
-constexpr int kModeFwdP = 2;      // S -> P from final statistics
 
 // Score / softmax-gradient kernel (sdp.cu).
 template <typename T>
@@ -38,8 +37,8 @@ cudaError_t launch_kvb(const BlkMaps& maps, const Prob& p, int bs, const int* gr
 // sharing a block start, S (and dP) of packs of 128 / GK tokens against the
 // block's resident key (and value) rows.  mode kModeBwd writes the pairs'
 // staged P^T / dS^T rows; kModeFwdStats the pairs' partial statistics
-// (tile_stats, (token, index, head) x {max, sum}); kModeFwdP the staged P^T
-// rows from the final statistics.
+// (tile_stats, (token, index, head) x {max, sum}) and their P^T rows relative
+// to each pair's max.
 template <typename T>
 cudaError_t launch_sdpb(const Maps& maps, const Prob& p, int mode, const int* groups, const int* gbeg,
                         const int* ngroups, const int* entries, void* pst, void* dsst, float* tile_stats, int* gerr,
@@ -58,11 +57,13 @@ cudaError_t launch_kvq(const Maps& maps, const Prob& p, float* acc, void* dq, vo
 
 // dQ / dQRope for block-sparse indices with at most 64 heads (dqb.cu):
 // features on the MMA's M, heads on N, over each token's selected blocks.
-// pv: the companion forward's O = P V instead (value rows, staged P; dq is
-// the output, dqr unused).
+// pv: the companion forward's O = P V instead (value rows; dq is the
+// output, dqr unused), from P staged by sdpb's statistics pass relative to
+// each (token, block) pair's max and rescaled to the final statistics
+// p.smax, p.ssum; part_stats: that pass's (pair, head) x {max, sum}.
 template <typename T>
-cudaError_t launch_dqb(const Maps& maps, const Prob& p, bool pv, void* dq, void* dqr, int* gerr, int nsm,
-                       cudaStream_t st);
+cudaError_t launch_dqb(const Maps& maps, const Prob& p, bool pv, void* dq, void* dqr, const float* part_stats,
+                       int* gerr, int nsm, cudaStream_t st);
 
 // Companion forward's output O = P V over each token's selected keys (dq.cu),
 // from the P staged by sdp.cu's statistics pass relative to each 32-key

@@ -593,7 +593,7 @@ cudaError_t launch_sdp(const Maps& maps, const Prob& p, int mode, void* out_p, v
   if (mode == kModeBwd && shared_kv) return launch_one<T, 128, kModeBwd, true>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
   if (mode == kModeBwd) return launch_one<T, 128, kModeBwd>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
   if (mode == kModeFwdStats) return launch_one<T, 128, kModeFwdStats>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
-  return cudaErrorInvalidValue;   // P from final statistics: the block kernel's mode (sdpb.cu)
+  return cudaErrorInvalidValue;
 }
 
 template cudaError_t launch_sdp<__nv_bfloat16>(const Maps&, const Prob&, int, void*, void*, float*, int*, int, cudaStream_t);

@@ -19,10 +19,11 @@
 // memory the resident block leaves: five 16 KB stages, one producer warp
 // each.
 //
-// The companion forward's two score passes use the same kernel without dP:
-// MODE kModeFwdStats writes per pair and head the max of the raw scores over
-// the block's valid keys and the sum of exp((s - max) * scale) (combined per
-// token afterwards), MODE kModeFwdP writes P from the final statistics.
+// The companion forward's score pass uses the same kernel without dP: MODE
+// kModeFwdStats writes per pair and head the max of the raw scores over the
+// block's valid keys and the sum of exp((s - max) * scale) (combined per
+// token afterwards), and stages P~ = exp((s - max) * scale), which the P.V
+// kernel (dqb.cu) rescales per pair to the final statistics.
 //
 // aclnnSparseFlashAttentionGrad doc, 功能说明 (selected blocks of
 // sparseBlockSize keys) and 阶段1/阶段2 (dP, dS); MindSpore
@@ -276,29 +277,34 @@ __global__ void __launch_bounds__(kThreads, 1) sdpb_kernel(const __grid_constant
       constexpr int CH = BS < 32 ? BS : 32;   // key columns per TMEM load
       if constexpr (MODE == kModeFwdStats) {
         // the pair's partial statistics per (token, head) row: max of the raw
-        // scores over the block's valid keys and the sum of exp((s - max) * scale)
+        // scores over the block's valid keys and the sum of exp((s - max) *
+        // scale); P~ = exp((s - max) * scale) staged (0 for a masked key or a
+        // padded head)
         float sv[BS];
 #pragma unroll
         for (int u0 = 0; u0 < BS; u0 += CH) {
           if constexpr (CH == 32) tmem_ld32(td + u0, sv + u0);
           else tmem_ld16(td + u0, sv + u0);
         }
+        float mx = -INFINITY;
         if (has && h < p.G) {
-          float mx = -INFINITY;
 #pragma unroll
           for (int u = 0; u < BS; ++u) {
             const int key = mc.ridx + u;
             if (key >= 0 && key <= mc.lim) mx = fmaxf(mx, sv[u]);
           }
+        }
+        if (has && h < Gs) {
+          T* op = pst + mc.row0 * Gs + h;
           float l = 0.f;
-          if (mx != -INFINITY) {
 #pragma unroll
-            for (int u = 0; u < BS; ++u) {
-              const int key = mc.ridx + u;
-              if (key >= 0 && key <= mc.lim) l += ex2((sv[u] - mx) * sl2);
-            }
+          for (int u = 0; u < BS; ++u) {
+            const int key = mc.ridx + u;
+            const float e = (mx != -INFINITY && key >= 0 && key <= mc.lim) ? ex2((sv[u] - mx) * sl2) : 0.f;
+            l += e;
+            op[(size_t)u * Gs] = E::from_f(e);
           }
-          reinterpret_cast<float2*>(tile_stats)[mc.sidx] = make_float2(mx, l);
+          if (h < p.G) reinterpret_cast<float2*>(tile_stats)[mc.sidx] = make_float2(mx, l);
         }
       } else {
         const bool store = has && h < Gs;
@@ -350,9 +356,8 @@ template <typename T, int BS, int GK>
 cudaError_t launch_bg(const Maps& maps, const Prob& p, int mode, const int* groups, const int* gbeg, const int* ngroups,
                       const int* entries, void* pst, void* dsst, float* tile_stats, int* gerr, int nsm,
                       cudaStream_t st) {
-  auto kern = mode == kModeFwdStats ? sdpb_kernel<T, BS, GK, kModeFwdStats>
-              : mode == kModeFwdP   ? sdpb_kernel<T, BS, GK, kModeFwdP>
-                                    : sdpb_kernel<T, BS, GK, kModeBwd>;
+  if (mode != kModeFwdStats && mode != kModeBwd) return cudaErrorInvalidValue;
+  auto kern = mode == kModeFwdStats ? sdpb_kernel<T, BS, GK, kModeFwdStats> : sdpb_kernel<T, BS, GK, kModeBwd>;
   const int smem = smem_bytes(BS) > kOneCtaSmem ? smem_bytes(BS) : kOneCtaSmem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
