@@ -64,8 +64,9 @@ def test_backward_wait_timeout_then_recovery(name):
         compare(f"{name}/{n}", x, ref[n], w.dtype)
 
 
-# the per-token forward (score statistics, P, P.V) and the per-block one
-# (statistics and P per block start, O with the features on the MMA's rows)
+# the per-token forward (one score pass, P.V with the per-group rescale) and
+# the per-block one (scores per block start, O with the features on the MMA's
+# rows)
 @pytest.mark.parametrize("name", ["atomic", "kvb"])
 def test_forward_wait_timeout_then_recovery(name):
     w, _ = CASES[name]
