@@ -142,7 +142,8 @@ def test_decode_bit_exact(name):
 # scores per block start (statistics and P) and multiplies by V per token
 @pytest.mark.parametrize("name", ["tiny", "g128_causal", "g128_pair_ragged", "g128_pair_norope_fp16", "g64_tnd",
                                   "g1_many_batches", "g2_tnd_many_batches", "g3_odd_heads", "g6_causal", "g24_fp16",
-                                  "g32_padding_dups", "g16_block_fp16", "g64_norope", "g16_kvb_bs16",
+                                  "g32_padding_dups", "g16_block_fp16", "g4_bs64", "g16_bs8_edges", "g64_norope",
+                                  "g16_kvb_bs16",
                                   "g16_kvb_bs32_unaligned", "g32_kvb_bs64_norope_fp16", "g12_kvb_tnd_causal",
                                   "g16_kvb_padding_dups", "g64_kvb_bs32", "g48_bs16"])
 def test_fwd_small(name):
