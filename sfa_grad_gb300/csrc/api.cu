@@ -172,18 +172,21 @@ EncodeTiled encoder() {
   return fn;
 }
 
-// 2-D row-major map over `rows` x `cols` 16-bit elements, 128-byte swizzle,
-// box of 64 columns x box_rows rows.
-bool encode2d(CUtensorMap* m, bool f16, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+// 2-D row-major map over `rows` x `cols` 16-bit elements, box of box_cols
+// columns x box_rows rows: 64 columns with 128-byte swizzle, or 32 columns
+// with 64-byte swizzle.
+bool encode2d(CUtensorMap* m, bool f16, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows,
+              uint32_t box_cols = 64) {
   EncodeTiled fn = encoder();
   if (!fn) return false;
   if (rows == 0) rows = 1;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t es[2] = {1, 1};
+  const CUtensorMapSwizzle sw = box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   return fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-            strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -234,6 +237,8 @@ bool make_maps(Maps* M, const Plan& P, const void* q, const void* qr, const void
   ok = ok && encode2d(&M->v, f, v, 512, T2, kb);
   ok = ok && encode2d(&M->P, f, Pst, P.Gs, R, 64);
   ok = ok && encode2d(&M->dS, f, dSst ? dSst : Pst, P.Gs, R, 64);
+  ok = ok && encode2d(&M->Pw, f, Pst, P.Gs, R, 32, 32);
+  ok = ok && encode2d(&M->dSw, f, dSst ? dSst : Pst, P.Gs, R, 32, 32);
   const uint32_t gk = (uint32_t)((P.G + 15) / 16 * 16);
   ok = ok && encode2d(&M->qg, f, q, 512, TG, gk);
   ok = ok && encode2d(&M->qrg, f, qr ? qr : q, qr ? 64 : 512, TG, gk);
@@ -436,7 +441,7 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
     if (!P.kvb) {   // block indices that many tokens select: no row table, scores per block below
       SFA_CK(launch_rowtab(pr, st));
       SFA_CK(mk.mark(st));
-      SFA_CK(launch_sdp<T>(maps, pr, kModeBwd, Pst, dSst, nullptr, gerr, nsm, st));
+      SFA_CK(launch_sdp<T>(maps, pr, kModeBwd, nullptr, gerr, nsm, st));
       SFA_CK(mk.mark(st));
     }
     if (P.det && !P.kvb) {
@@ -673,7 +678,7 @@ sfa_status run_fwd(const Plan& P, const void* q, const void* k, const void* v, c
       // statistics per 32 slots with P staged relative to each group's max,
       // the final statistics, then O = P V (P rescaled per group)
       SFA_CK(launch_rowtab(pr, st));
-      SFA_CK(launch_sdp<T>(maps, pr, kModeFwdStats, ws + P.off_P, nullptr, ts, gerr, nsm, st));
+      SFA_CK(launch_sdp<T>(maps, pr, kModeFwdStats, ts, gerr, nsm, st));
       SFA_CK(launch_stats_combine(pr, ts, P.Kpad / 32, smax, ssum, st));
       SFA_CK(launch_pv<T>(maps, pr, ts, out, gerr, nsm, st));
     }

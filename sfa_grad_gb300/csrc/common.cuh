@@ -198,6 +198,9 @@ struct Maps {
   // kernel loads only a token's own head rows (the padded rows up to GP stay
   // zero in its shared memory)
   CUtensorMap qg, qrg, dOg;
+  // staged P^T / dS^T for the score kernel's stores: box 32 heads x 32 rows,
+  // 64-byte swizzle (heads past Gs are outside the map and not written)
+  CUtensorMap Pw, dSw;
 };
 
 // Tensor maps of the key-major block kernel (kvb.cu).
@@ -226,6 +229,18 @@ __device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int
       "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
 }
+// Store of the box at (x, y) from shared memory at `src` (bulk group of the
+// issuing thread); x, y >= 0.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(x), "r"(y),
+               "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// The issuing thread's bulk stores have read their shared-memory sources.
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// The issuing thread's bulk stores are complete.
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Prefetch of the box at (x, y) into L2 (no shared memory, no completion).
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y) : "memory");

@@ -9,9 +9,10 @@ constexpr int kModeBwd = 0;       // S and dP -> P, dS
 // stages P relative to each partial max (one partial per 32 keys)
 constexpr int kModeFwdStats = 1;
 
-// Score / softmax-gradient kernel (sdp.cu).
+// Score / softmax-gradient kernel (sdp.cu).  The staged P^T / dS^T rows go
+// through the store maps maps.Pw / maps.dSw.
 template <typename T>
-cudaError_t launch_sdp(const Maps& maps, const Prob& p, int mode, void* out_p, void* out_ds, float* tile_stats, int* gerr, int nsm,
+cudaError_t launch_sdp(const Maps& maps, const Prob& p, int mode, float* tile_stats, int* gerr, int nsm,
                        cudaStream_t st);
 
 // Key-major dK / dV for block-sparse indices (kvb.cu): group the chunk's

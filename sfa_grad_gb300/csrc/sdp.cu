@@ -97,8 +97,8 @@ __device__ __forceinline__ void butterfly_reduce(float (&a)[32], int lane) {
 
 // BLK: block-sparse indices (sparseBlockSize >= 8), key/value rows by TMA boxes.
 template <typename T, int GP, int MODE, bool SH, bool BLK>
-__global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant__ Maps maps, Prob p, void* out_p, void* out_ds,
-                                                          float* tile_stats, int* gerr) {
+__global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant__ Maps maps, Prob p, float* tile_stats,
+                                                          int* gerr) {
   using E = Elt<T>;
   using S = SdpSmem<GP, SH>;
   static_assert(!SH || MODE == kModeBwd, "the shared key/value layout serves the backward only");
@@ -116,7 +116,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
   __shared__ int arr_tma[kMaxSlots], arr_gat[kGatherWarps];
   __shared__ float stats_s[2][3 * GP];
   __shared__ __align__(16) int rows_s[kGatherWarps][kKeys];   // one per gather warp; read and written as int4
-  __shared__ uint4 epi_stage[8][32 * 4];                 // epilogue row transposition, 2 KB per warp
+  // epilogue row transposition, 2 KB per warp, in the 64-byte swizzle of its TMA stores
+  __shared__ __align__(1024) uint4 epi_stage[8][32 * 4];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool bwd = (MODE == kModeBwd);
@@ -401,23 +402,29 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
       }
     };
     // A lane holds 32 heads (64 bytes) of its own key row.  The warp's 32
-    // rows pass through a private shared buffer (16-byte pieces XOR-swizzled
-    // by row) so that each global store instruction writes eight rows x 64
-    // contiguous bytes instead of 32 scattered 16-byte pieces.  Staged rows
-    // hold Gs heads (G rounded up to 16); the pieces past Gs are not written.
+    // rows go to a private shared buffer (16-byte piece u of row r at
+    // position u ^ ((r >> 1) & 3): the 64-byte swizzle) and leave as one TMA
+    // store of 32 rows x 32 heads, so the warp does not wait for them.
+    // Staged rows hold Gs heads (G rounded up to 16); the store map ends at
+    // Gs, so heads past it are not written.
     const int Gs = p.Gs;
     uint4* stg = epi_stage[warp - 4];
-    auto put_rows = [&](const uint32_t* pk, T* dst, int npc) {
+    // the buffer may be written once this warp's last store has read it
+    auto stg_free = [&]() {
+      if (lane == 0) bulk_wait_read0();
+      __syncwarp();
+    };
+    auto put_rows = [&](const uint32_t* pk, const CUtensorMap* map, int x, int y) {
+      stg_free();
 #pragma unroll
       for (int u = 0; u < 4; ++u)
         stg[lane * 4 + (u ^ ((lane >> 1) & 3))] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      fence_async_smem();
       __syncwarp();
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = i * 8 + (lane >> 2), pc = lane & 3;
-        if (pc < npc) *reinterpret_cast<uint4*>(dst + (size_t)r * Gs + pc * 8) = stg[r * 4 + (pc ^ ((r >> 1) & 3))];
+      if (lane == 0) {
+        tma_store_2d(map, x, y, smem_u32(stg));
+        bulk_commit();
       }
-      __syncwarp();
     };
     int nrow;
     float nmax, nsum, ndsum;
@@ -448,13 +455,12 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
         // exp((s - m) * scale), and P~ = exp((s - m) * scale) staged in the P
         // rows (0 for a masked key).  The P.V kernel rescales each group's P~
         // to the final statistics, so no second score pass is needed.
-        T* ptile = static_cast<T*>(out_p) + ((size_t)tl * p.Kpad + kt * kKeys + q * 32) * Gs;
+        const int row0 = tl * p.Kpad + kt * kKeys + q * 32;   // the warp's 32 staged rows
         float2* tsg = reinterpret_cast<float2*>(tile_stats) + ((size_t)tl * (ntiles * 4) + kt * 4 + q) * p.G;
 #pragma unroll 1
         for (int c = 0; c < HH / 32; ++c) {
           const int h0 = half * HH + c * 32;
           if (h0 >= Gs) break;                       // padded heads only: nothing is staged
-          const int npc = Gs - h0 >= 32 ? 4 : (Gs - h0) / 8;
           // per-head max over the 32 lanes (keys): lane j ends with head j's;
           // every lane then reads all 32 from the warp's staging buffer.  The
           // scores are read from tensor memory twice (for the max, then for
@@ -466,6 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
           butterfly_reduce<true>(a, lane);
           const float gm = a[0];
           float* mrow = reinterpret_cast<float*>(stg);
+          stg_free();
           mrow[lane] = gm;
           __syncwarp();
           if (ok) tmem_ld32(tS + h0, a);
@@ -484,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
           const float gl = a[0];
           if (ok) {
             if (h0 + lane < p.G) tsg[h0 + lane] = make_float2(gm, gl);   // raw score (unscaled), sum
-            put_rows(pk, ptile + h0, npc);
+            put_rows(pk, &maps.Pw, h0, row0);
           }
         }
         tc_fence_before();
@@ -492,13 +499,11 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
         continue;
       }
       if (!ok) continue;
-      T* ptile = static_cast<T*>(out_p) + ((size_t)tl * p.Kpad + kt * kKeys + q * 32) * Gs;
-      T* dstile = bwd ? static_cast<T*>(out_ds) + ((size_t)tl * p.Kpad + kt * kKeys + q * 32) * Gs : nullptr;
+      const int row0 = tl * p.Kpad + kt * kKeys + q * 32;   // the warp's 32 staged rows
 #pragma unroll 1
       for (int c = 0; c < HH / 32; ++c) {
         const int h0 = half * HH + c * 32;
         if (h0 >= Gs) break;                       // padded heads only: nothing is staged
-        const int npc = Gs - h0 >= 32 ? 4 : (Gs - h0) / 8;
         float s[32], dp[32];
         tmem_ld32(tS + h0, s);
         if (bwd) tmem_ld32(tP + h0, dp);
@@ -519,12 +524,15 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
           pk[j / 2] = E::pack(pv[0], pv[1]);
           dk[j / 2] = E::pack(dv[0], dv[1]);
         }
-        put_rows(pk, ptile + h0, npc);
-        if (bwd) put_rows(dk, dstile + h0, npc);
+        put_rows(pk, &maps.Pw, h0, row0);
+        if (bwd) put_rows(dk, &maps.dSw, h0, row0);
       }
       tc_fence_before();
       mbar_arrive(&tempty_bar[set]);
     }
+    // the warp's stores are complete before the CTA exits
+    if (lane == 0) bulk_wait0();
+    __syncwarp();
   }
   // Wind-down.  A stage barrier collects arrivals from two producers (the
   // gather warps and the head-row TMA thread); after an abandoned wait one of
@@ -563,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdp_kernel(const __grid_constant_
 }
 
 template <typename T, int GP, int MODE, bool SH = false>
-cudaError_t launch_one(const Maps& maps, const Prob& p, void* out_p, void* out_ds, float* tile_stats, int* gerr, int nsm,
+cudaError_t launch_one(const Maps& maps, const Prob& p, float* tile_stats, int* gerr, int nsm,
                        cudaStream_t st) {
   auto kern = p.bs >= 8 ? sdp_kernel<T, GP, MODE, SH, true> : sdp_kernel<T, GP, MODE, SH, false>;
   using S = SdpSmem<GP, SH>;
@@ -573,30 +581,30 @@ cudaError_t launch_one(const Maps& maps, const Prob& p, void* out_p, void* out_d
   const int nitems = p.ntok * (p.Kpad / kKeys);
   const int grid = nitems < nsm ? nitems : nsm;
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, kThreads, smem, st>>>(maps, p, out_p, out_ds, tile_stats, gerr);
+  kern<<<grid, kThreads, smem, st>>>(maps, p, tile_stats, gerr);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 template <typename T>
-cudaError_t launch_sdp(const Maps& maps, const Prob& p, int mode, void* out_p, void* out_ds, float* tile_stats, int* gerr, int nsm,
+cudaError_t launch_sdp(const Maps& maps, const Prob& p, int mode, float* tile_stats, int* gerr, int nsm,
                        cudaStream_t st) {
   // key and value given as the same tensor: gather the rows once per stage
   const bool shared_kv = p.k == p.v;
   if (p.Gp == 64) {
-    if (mode == kModeBwd && shared_kv) return launch_one<T, 64, kModeBwd, true>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
-    if (mode == kModeBwd) return launch_one<T, 64, kModeBwd>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
-    if (mode == kModeFwdStats) return launch_one<T, 64, kModeFwdStats>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
+    if (mode == kModeBwd && shared_kv) return launch_one<T, 64, kModeBwd, true>(maps, p, tile_stats, gerr, nsm, st);
+    if (mode == kModeBwd) return launch_one<T, 64, kModeBwd>(maps, p, tile_stats, gerr, nsm, st);
+    if (mode == kModeFwdStats) return launch_one<T, 64, kModeFwdStats>(maps, p, tile_stats, gerr, nsm, st);
     return cudaErrorInvalidValue;
   }
-  if (mode == kModeBwd && shared_kv) return launch_one<T, 128, kModeBwd, true>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
-  if (mode == kModeBwd) return launch_one<T, 128, kModeBwd>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
-  if (mode == kModeFwdStats) return launch_one<T, 128, kModeFwdStats>(maps, p, out_p, out_ds, tile_stats, gerr, nsm, st);
+  if (mode == kModeBwd && shared_kv) return launch_one<T, 128, kModeBwd, true>(maps, p, tile_stats, gerr, nsm, st);
+  if (mode == kModeBwd) return launch_one<T, 128, kModeBwd>(maps, p, tile_stats, gerr, nsm, st);
+  if (mode == kModeFwdStats) return launch_one<T, 128, kModeFwdStats>(maps, p, tile_stats, gerr, nsm, st);
   return cudaErrorInvalidValue;
 }
 
-template cudaError_t launch_sdp<__nv_bfloat16>(const Maps&, const Prob&, int, void*, void*, float*, int*, int, cudaStream_t);
-template cudaError_t launch_sdp<__half>(const Maps&, const Prob&, int, void*, void*, float*, int*, int, cudaStream_t);
+template cudaError_t launch_sdp<__nv_bfloat16>(const Maps&, const Prob&, int, float*, int*, int, cudaStream_t);
+template cudaError_t launch_sdp<__half>(const Maps&, const Prob&, int, float*, int*, int, cudaStream_t);
 
 }  // namespace sfa
