@@ -223,7 +223,8 @@ bool make_blk_maps(BlkMaps* M, const Plan& P, const void* q, const void* qr, con
 // Maps of one call.  Tensors a call does not use (dO and dS in the forward,
 // the rope pair without rope) alias a used tensor and are never read.
 bool make_maps(Maps* M, const Plan& P, const void* q, const void* qr, const void* dO, const void* k, const void* kr,
-               const void* v, const void* Pst, const void* dSst) {
+               const void* v, const void* Pst, const void* dSst, const void* dq = nullptr,
+               const void* dqr = nullptr) {
   const bool f = P.is_f16;
   const uint64_t TG = (uint64_t)P.T1 * P.G, T2 = (uint64_t)P.T2, R = (uint64_t)P.chunk * P.Kpad;
   bool ok = encode2d(&M->q, f, q, 512, TG, P.Gp);
@@ -239,6 +240,9 @@ bool make_maps(Maps* M, const Plan& P, const void* q, const void* qr, const void
   ok = ok && encode2d(&M->dS, f, dSst ? dSst : Pst, P.Gs, R, 64);
   ok = ok && encode2d(&M->Pw, f, Pst, P.Gs, R, 32, 32);
   ok = ok && encode2d(&M->dSw, f, dSst ? dSst : Pst, P.Gs, R, 32, 32);
+  // the backward's dQ / dQRope outputs (the forward has none: aliases, unused)
+  ok = ok && encode2d(&M->dQw, f, dq ? dq : q, 512, TG, 32, 32);
+  ok = ok && encode2d(&M->dQRw, f, dqr ? dqr : (dq ? dq : q), dqr ? 64 : 512, TG, 32, 32);
   const uint32_t gk = (uint32_t)((P.G + 15) / 16 * 16);
   ok = ok && encode2d(&M->qg, f, q, 512, TG, gk);
   ok = ok && encode2d(&M->qrg, f, qr ? qr : q, qr ? 64 : 512, TG, gk);
@@ -404,7 +408,7 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
   const int nsm = sm_count();
   Maps maps;
   BlkMaps bmaps;
-  if (!make_maps(&maps, P, q, pr.qr, dO, k, pr.kr, v, ws + P.off_P, ws + P.off_dS) ||
+  if (!make_maps(&maps, P, q, pr.qr, dO, k, pr.kr, v, ws + P.off_P, ws + P.off_dS, dq, P.has_rope ? dqr : nullptr) ||
       (P.kvb && !make_blk_maps(&bmaps, P, q, pr.qr, dO, ws + P.off_P, ws + P.off_dS))) {
     snprintf(g_last_error, sizeof(g_last_error), "tensor map encoding failed");
     return SFA_ERR_RUNTIME;
