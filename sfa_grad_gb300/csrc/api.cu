@@ -649,7 +649,7 @@ sfa_status run_fwd(const Plan& P, const void* q, const void* k, const void* v, c
   pr.smax = smax; pr.ssum = ssum;
   const int nsm = sm_count();
   Maps maps;
-  if (!make_maps(&maps, P, q, pr.qr, nullptr, k, pr.kr, v, ws + P.off_P, nullptr)) {
+  if (!make_maps(&maps, P, q, pr.qr, nullptr, k, pr.kr, v, ws + P.off_P, nullptr, out)) {
     snprintf(g_last_error, sizeof(g_last_error), "tensor map encoding failed");
     return SFA_ERR_RUNTIME;
   }

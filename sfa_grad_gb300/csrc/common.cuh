@@ -201,8 +201,9 @@ struct Maps {
   // staged P^T / dS^T for the score kernel's stores: box 32 heads x 32 rows,
   // 64-byte swizzle (heads past Gs are outside the map and not written)
   CUtensorMap Pw, dSw;
-  // dQ (T1*G, 512) and dQRope (T1*G, 64) for the stores of kvq's query side:
-  // box 32 features x 32 head rows, 64-byte swizzle
+  // dQ (T1*G, 512) and dQRope (T1*G, 64) for the stores of kvq's query side
+  // (in the forward, dQw maps the output O for dq.cu's stores): box 32
+  // features x 32 head rows, 64-byte swizzle
   CUtensorMap dQw, dQRw;
 };
 

@@ -56,6 +56,8 @@ __global__ void __launch_bounds__(DqSmem<NCOL, GP>::kThreads, 1)
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ __align__(16) int rows_s[kStages][kSlots];   // read and written as int2
+  // epilogue staging, 2 KB per warp, in the 64-byte swizzle of its TMA stores
+  __shared__ __align__(1024) uint4 o_stage[4][32 * 4];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nchunks = p.Kpad / kSlots;
@@ -254,8 +256,13 @@ __global__ void __launch_bounds__(DqSmem<NCOL, GP>::kThreads, 1)
     alog.settle(full_bar, gerr);
   } else if (warp > kStages) {
     // ---------------------------------------------------------------- epilogue (thread = head)
+    // A warp whose 32 heads all exist stages each 32-feature piece of its
+    // head rows in a private 2 KB buffer (the 64-byte swizzle) and sends it
+    // with one TMA store; a warp with heads past G stores from registers.
     const int ew = warp & 3;   // the TMEM lane quadrant this warp may read
     const int h = ew * 32 + lane;
+    const bool tma_rows = ew * 32 + 32 <= p.G;
+    uint4* stg = o_stage[ew];
     int it = 0;
     for (int item = blockIdx.x; item < nitems && !abort_flag; item += gridDim.x, ++it) {
       const int set = it & 1;
@@ -269,11 +276,25 @@ __global__ void __launch_bounds__(DqSmem<NCOL, GP>::kThreads, 1)
         float v[32];
         tmem_ld32(td + c, v);
         const int f = part * NCOL + c;
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) pk[j] = E::pack(v[2 * j], v[2 * j + 1]);
+        if (tma_rows) {
+          if (lane == 0) bulk_wait_read0();   // the buffer's previous store has read it
+          __syncwarp();
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            stg[lane * 4 + (u ^ ((lane >> 1) & 3))] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&maps.dQw, f, t * p.G + ew * 32, smem_u32(stg));
+            bulk_commit();
+          }
+          continue;
+        }
         T* dst = h < p.G ? out + ((size_t)t * p.G + h) * 512 + f : nullptr;
         if (dst) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) pk[j] = E::pack(v[2 * j], v[2 * j + 1]);
           uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
           for (int u = 0; u < 4; ++u) d4[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
@@ -282,6 +303,9 @@ __global__ void __launch_bounds__(DqSmem<NCOL, GP>::kThreads, 1)
       tc_fence_before();
       mbar_arrive(&tempty_bar[set]);
     }
+    // the warp's stores are complete before the CTA exits
+    if (lane == 0) bulk_wait0();
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
