@@ -224,7 +224,7 @@ bool make_blk_maps(BlkMaps* M, const Plan& P, const void* q, const void* qr, con
 // the rope pair without rope) alias a used tensor and are never read.
 bool make_maps(Maps* M, const Plan& P, const void* q, const void* qr, const void* dO, const void* k, const void* kr,
                const void* v, const void* Pst, const void* dSst, const void* dq = nullptr,
-               const void* dqr = nullptr) {
+               const void* dqr = nullptr, const void* part = nullptr) {
   const bool f = P.is_f16;
   const uint64_t TG = (uint64_t)P.T1 * P.G, T2 = (uint64_t)P.T2, R = (uint64_t)P.chunk * P.Kpad;
   bool ok = encode2d(&M->q, f, q, 512, TG, P.Gp);
@@ -243,6 +243,20 @@ bool make_maps(Maps* M, const Plan& P, const void* q, const void* qr, const void
   // the backward's dQ / dQRope outputs (the forward has none: aliases, unused)
   ok = ok && encode2d(&M->dQw, f, dq ? dq : q, 512, TG, 32, 32);
   ok = ok && encode2d(&M->dQRw, f, dqr ? dqr : (dq ? dq : q), dqr ? 64 : 512, TG, 32, 32);
+  // deterministic partial rows (bf16 whatever the input type; the unused
+  // map of the other plans aliases q)
+  if (part) {
+    EncodeTiled fn = encoder();
+    cuuint64_t dims[2] = {(cuuint64_t)kAccRow, R == 0 ? 1 : R};
+    cuuint64_t strides[1] = {(cuuint64_t)kAccRow * 2};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t es[2] = {1, 1};
+    ok = ok && fn && fn(&M->partw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(part), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  } else {
+    ok = ok && encode2d(&M->partw, f, q, 512, TG, 32, 32);
+  }
   const uint32_t gk = (uint32_t)((P.G + 15) / 16 * 16);
   ok = ok && encode2d(&M->qg, f, q, 512, TG, gk);
   ok = ok && encode2d(&M->qrg, f, qr ? qr : q, qr ? 64 : 512, TG, gk);
@@ -408,7 +422,8 @@ sfa_status run_grad(const Plan& P, const sfa_params* prm, const void* q, const v
   const int nsm = sm_count();
   Maps maps;
   BlkMaps bmaps;
-  if (!make_maps(&maps, P, q, pr.qr, dO, k, pr.kr, v, ws + P.off_P, ws + P.off_dS, dq, P.has_rope ? dqr : nullptr) ||
+  if (!make_maps(&maps, P, q, pr.qr, dO, k, pr.kr, v, ws + P.off_P, ws + P.off_dS, dq, P.has_rope ? dqr : nullptr,
+                 P.det && !P.kvb ? ws + P.off_part : nullptr) ||
       (P.kvb && !make_blk_maps(&bmaps, P, q, pr.qr, dO, ws + P.off_P, ws + P.off_dS))) {
     snprintf(g_last_error, sizeof(g_last_error), "tensor map encoding failed");
     return SFA_ERR_RUNTIME;

@@ -205,6 +205,9 @@ struct Maps {
   // (in the forward, dQw maps the output O for dq.cu's stores): box 32
   // features x 32 head rows, 64-byte swizzle
   CUtensorMap dQw, dQRw;
+  // deterministic mode's bf16 partial rows (chunk*Kpad, 1088) for kvq's
+  // drain stores: box 32 features x 32 slot rows, 64-byte swizzle
+  CUtensorMap partw;
 };
 
 // Tensor maps of the key-major block kernel (kvb.cu).

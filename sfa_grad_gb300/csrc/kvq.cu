@@ -106,8 +106,10 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ __align__(16) int q_rows[QST][kQSlots];   // read and written as int2
-  // query-side epilogue staging, 2 KB per warp, in the 64-byte swizzle of its TMA stores
+  // query-side epilogue staging, 2 KB per warp, in the 64-byte swizzle of its
+  // TMA stores; PART: the same for each partial-row drain warp
   __shared__ __align__(1024) uint4 q_stage[4][32 * 4];
+  __shared__ __align__(1024) uint4 part_stage[PART ? 8 : 1][32 * 4];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntiles = p.Kpad / kKeys;
@@ -325,45 +327,26 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
     // instead of all eight warps pausing together.  A tile is [features x
     // key slots]: warp w of a group reads TMEM lanes (features) 32*(w%4) ..
     // +31 and all 128 slot columns.  Adjacent lanes swap one value, so that
-    // each lane holds two consecutive features of one pair's row and one
-    // store instruction covers two rows x 64 contiguous bytes.
+    // each lane holds two consecutive features of one pair's row; per 32
+    // slots the warp stages its 32 rows x 32 features in a 2 KB buffer (the
+    // 64-byte swizzle) and sends them with one TMA store.  Rows of masked
+    // slots are written too; the fixed-order sum reads only valid pairs.
     const int qd = warp & 3;
     const int grp = (warp - 4) >> 2;
     const int odd = lane & 1;
+    uint32_t* pst = reinterpret_cast<uint32_t*>(part_stage[PART ? warp - 4 : 0]);
     int tcount = 0;
-    // row ids of slots 32*s + lane of the group's next tile, loaded one tile ahead
-    auto rows_of = [&](int item, int kt, int* r) {
-      const int* rt = item < nkv ? p.rowtab + (size_t)kv_item(item, p.ntok, ntiles, tg).tl * p.Kpad + kt * kKeys : nullptr;
-#pragma unroll
-      for (int s = 0; s < 4; ++s) r[s] = rt ? rt[32 * s + lane] : -1;
-    };
-    auto advance = [&](int& item, int& kt) {
-      if (++kt == kv_item(item, p.ntok, ntiles, tg).kt1) {
-        item += gridDim.x;
-        kt = kv_item(item, p.ntok, ntiles, tg).kt0;
-      }
-    };
-    int nitem = blockIdx.x, nkt = kv_item(blockIdx.x, p.ntok, ntiles, tg).kt0;
-    if (grp) advance(nitem, nkt);
-    int next_rows[4];
-    rows_of(nitem, nkt, next_rows);
     for (int item = blockIdx.x; item < nkv && !abort_flag; item += gridDim.x) {
       const KvItem ki = kv_item(item, p.ntok, ntiles, tg);
       const int ch = ki.ch;
       int ncol, col0;
       kv_chunk(ch, ncol, col0);
-      // first feature of this lane's pair
-      const int f = col0 + qd * 32 + lane - odd;
+      // this lane's pair of features within the warp's 32
+      const int fl = lane - odd;
       bool ok = true;
       for (int kt = ki.kt0; kt < ki.kt1; ++kt, ++tcount) {
         const int set = tcount & 1;
         if (set != grp) continue;
-        int rows[4];
-#pragma unroll
-        for (int s = 0; s < 4; ++s) rows[s] = next_rows[s];
-        advance(nitem, nkt);
-        advance(nitem, nkt);
-        rows_of(nitem, nkt, next_rows);
         ok = __all_sync(0xffffffffu, mbar_wait(&kv_tfull[set], (tcount >> 1) & 1, wt));
         if (!ok) break;
         tc_fence_after();
@@ -373,19 +356,24 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
           for (int s = 0; s < 4; ++s) {
             float v[32];
             tmem_ld32(td + 32 * s, v);
+            if (lane == 0) bulk_wait_read0();   // the buffer's previous store has read it
+            __syncwarp();
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
-              // even lane: features f, f+1 of slot j; odd lane: of slot j+1
+              // even lane: features fl, fl+1 of slot j; odd lane: of slot j+1
               const float x = __shfl_xor_sync(0xffffffffu, odd ? v[j] : v[j + 1], 1);
               const float a = odd ? x : v[j], b = odd ? v[j + 1] : x;
-              const int grow = __shfl_sync(0xffffffffu, rows[s], j + odd);
-              // streaming store of the pair's row rounded to bf16 (read back
-              // once, after this kernel, and summed in fp32)
-              if (grow >= 0)
-                __stcs(reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(acc) +
-                                                   ((size_t)ki.tl * p.Kpad + kt * kKeys + 32 * s + j + odd) * kAccRow +
-                                                   f),
-                       Elt<__nv_bfloat16>::pack(a, b));
+              const int row = j + odd;
+              pst[row * 16 + ((((fl >> 3) ^ ((row >> 1) & 3))) << 2) + ((fl & 7) >> 1)] =
+                  Elt<__nv_bfloat16>::pack(a, b);
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              // the pairs' rows rounded to bf16 (read back once, after this
+              // kernel, and summed in fp32)
+              tma_store_2d(&maps.partw, col0 + qd * 32, ki.tl * p.Kpad + kt * kKeys + 32 * s, smem_u32(pst));
+              bulk_commit();
             }
           }
         }
@@ -394,6 +382,9 @@ __global__ void __launch_bounds__(kThreads, 1) kvq_kernel(const __grid_constant_
       }
       if (!ok) break;
     }
+    // the warp's stores are complete before the CTA exits
+    if (lane == 0) bulk_wait0();
+    __syncwarp();
   } else if (warp == 2) {
     // ================================================================ query side: MMA issuer
     if (lane == 0) {
