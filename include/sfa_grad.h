@@ -192,7 +192,12 @@ sfa_status sfa_grad_plan_names(const sfa_params* p, const char** names, int32_t 
  * specify the forward).  out = sum_j P_j v_j with P and the statistics defined
  * as above; a row with no valid key gets out = 0, softmaxMax = -inf,
  * softmaxSum = 0.  Same conventions, shapes and error codes as sfa_grad
- * (p->deterministic is ignored: the forward is always deterministic).
+ * (p->deterministic is ignored: the forward is always deterministic).  The
+ * keys are scored once: P is formed relative to the max of each group of 32
+ * selected slots (or of each selected block) and rescaled to the final
+ * statistics in the input type, so each P entry carries up to three roundings
+ * to the input type before the P.V product (accumulated in fp32); the
+ * statistics are fp32.
  */
 sfa_status sfa_fwd_workspace_size(const sfa_params* p, size_t* bytes);
 sfa_status sfa_fwd(const sfa_params* p, const void* q, const void* k, const void* v, const int32_t* indices,
