@@ -223,12 +223,12 @@ def workload_desc(w, det, shared_kv=False):
 # still hashes to the value it had when the counters were taken.
 TRAFFIC = {
     "kvq": {"sources": ["kvq.cu", "common.cuh"],
-            "sha256": "82a0d73f54363475ef84241767fc4340120c2095735167501bb0fe061ddcde5d",
+            "sha256": "f54b31958027f5a265f0752651eca38ce939c0eec7c8ad81aa04bf232718526b",
             "shapes": [
-                # mla_q512: 916.5 MB read + 83.5 MB written per launch
-                {"N1": 128, "K": 2048, "bs": 1, "det": False, "bytes_per_token": 1000.0e6 / 512},
-                # mla_q512 --deterministic: 935.8 MB read + 2313.8 MB written (bf16 partial rows)
-                {"N1": 128, "K": 2048, "bs": 1, "det": True, "bytes_per_token": 3249.5e6 / 512},
+                # mla_q512: 915.9 MB read + 83.0 MB written per launch
+                {"N1": 128, "K": 2048, "bs": 1, "det": False, "bytes_per_token": 998.9e6 / 512},
+                # mla_q512 --deterministic: 935.0 MB read + 2313.0 MB written (bf16 partial rows)
+                {"N1": 128, "K": 2048, "bs": 1, "det": True, "bytes_per_token": 3248.0e6 / 512},
             ]},
 }
 

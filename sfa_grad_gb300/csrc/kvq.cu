@@ -9,7 +9,10 @@
 //               accumulated in tensor memory over all the token's keys.
 // The key side is bound by the SM-to-L2 reduction path and leaves the tensor
 // pipe mostly idle; the query side is bound by gathers and the tensor pipe.
-// Running both in the same CTA overlaps the two.  Key-side items run
+// Running both in the same CTA overlaps the two.  The stores (dQ rows; in
+// deterministic mode the partial rows) leave as TMA stores of 2 KB tiles
+// staged in shared memory, which keeps them off the request path the
+// reductions use.  Key-side items run
 // token-major, or tile-group major when the accumulator rows a batch touches
 // exceed L2.  (Block indices that many tokens select take kvb.cu for the key
 // side and dqb.cu for dQ instead.)
